@@ -1,0 +1,437 @@
+"""Benchmark of one paged decode step on GB300.
+
+A step = the whole hot path over one batch: copy-on-write block copies (when
+the workload has any), write_cache of one new token per sequence, then decode
+attention (partition kernel + reduce kernel).  Default workload: the 8B-class
+GQA decode layer (64 sequences, 32 query / 8 KV heads, head_dim 128, bf16,
+context lengths uniform in [128, 2048], blocks scattered over a pool 1.25x
+the need).  Inputs are synthetic, seeded, N(0,1).
+
+Metric: decode KV bytes per second (GB/s) over the step, its fraction of the
+HBM peak, and sequences*layers per second.  `value` counts the algorithmic
+bytes of the step (K+V history read, block-table entries, queries, outputs,
+context lengths, new-token rows read and written, copy-on-write block bytes)
+divided by the device time of exactly K steps.  Between timed steps the K/V
+pools rotate over R device replicas whose total exceeds L2 several times.
+
+`--impl reference` times the fp64 CPU oracle instead (a deliberately slow
+statement of the same computation) on a bounded sample of the workload.
+
+Multi-GPU (torchrun): every rank runs the same per-GPU workload (replicas,
+weak scaling); time is the max over ranks, value the sum of bytes / that time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode paged-attention KV GB/s and % of GB300 HBM peak; sequences·layers/sec"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ----------------------------------------------------------- byte accounting
+
+def step_bytes(wl, out_bytes_per_elem=4):
+    """Algorithmic bytes of one step, split into the partition kernel's share and the rest."""
+    S, Hq, Hkv, D = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    L = wl.context_lens.astype(np.int64)
+    kv = int(L.sum()) * Hkv * D * 2 * 2
+    tables = int(np.sum((L + 15) // 16)) * 4
+    q = S * Hq * D * 2
+    out = S * Hq * D * out_bytes_per_elem
+    lens = S * 4
+    attn = kv + tables + q + out + lens
+    T = wl.slot_mapping.shape[0]
+    write = 2 * T * Hkv * D * 2 * 2 + T * 4  # read new rows + write pool rows, K and V; slots
+    cow = wl.copy_pairs.shape[0] * (2 * 16 * Hkv * D * 2 * 2 + 8)
+    return {"attention": attn, "kv": kv, "write": write, "copy": cow, "step": attn + write + cow}
+
+
+# -------------------------------------------------------------- clock sampler
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+
+        fd, self.path = tempfile.mkstemp(prefix="pkv_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.15)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_112_gb300 as pkv
+    import pkv_inputs as P
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    pkv.load()
+
+    wl = P.make_workload(args.config, poison=False)
+    ps = wl.partition_size if args.partition_size is None else args.partition_size
+    dt = {"f16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(dt)
+
+    q = to_dev(wl.q)
+    k_new, v_new = to_dev(wl.k_new), to_dev(wl.v_new)
+    k0, v0 = to_dev(wl.k_pool), to_dev(wl.v_pool)
+    bt = torch.from_numpy(wl.block_tables).to(dev)
+    cl = torch.from_numpy(wl.context_lens).to(dev)
+    sm = torch.from_numpy(wl.slot_mapping).to(dev)
+    pairs = torch.from_numpy(np.ascontiguousarray(wl.copy_pairs, dtype=np.int32)).to(dev)
+    out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    ws_bytes = pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, wl.max_context_len, ps)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    pool_bytes = 2 * k0.numel() * k0.element_size()
+    replicas = args.replicas or max(1, math.ceil(4 * l2 / pool_bytes))
+    pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(replicas - 1)]
+    max_len = wl.max_context_len
+    n_launch = 1 + 1 + (1 if pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, max_len, ps)
+                        else 0) + (1 if pairs.shape[0] else 0)
+
+    def step(i, ev=None):
+        kp, vp = pools[i % replicas]
+        if pairs.shape[0]:
+            pkv.copy_blocks(kp, vp, pairs, status=status)
+        pkv.write_cache(k_new, v_new, kp, vp, sm, status=status)
+        if ev is not None:
+            ev[0].record()
+        pkv.decode_partitions(out, q, kp, vp, bt, cl, wl.scale, partition_size=ps, max_context_len=max_len,
+                              workspace=ws, status=status)
+        if ev is not None:
+            ev[1].record()
+        if ws is not None:
+            pkv.decode_reduce(out, cl, num_q_heads=wl.num_q_heads, head_dim=wl.head_dim, partition_size=ps,
+                              max_context_len=max_len, workspace=ws, status=status)
+
+    nb = step_bytes(wl)
+    K, W = args.steps, args.warmup
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.start()
+    barrier()
+    t_start.record()
+    for i in range(K):
+        step(W + i, evs[i])
+    t_end.record()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    elapsed_ms = t_start.elapsed_time(t_end)
+    kern_ms = [a.elapsed_time(b) for a, b in evs]
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed steps")
+
+    # end to end through the public API: pinned host inputs in, host output out, every step
+    e2e = None
+    if rank == 0 or world > 1:
+        host_in = {n: t.cpu().pin_memory() for n, t in
+                   dict(q=q, k_new=k_new, v_new=v_new, bt=bt, cl=cl, sm=sm, pairs=pairs).items()}
+        dev_in = dict(q=q, k_new=k_new, v_new=v_new, bt=bt, cl=cl, sm=sm, pairs=pairs)
+        host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = host_out.numel() * host_out.element_size()
+        Ke = max(1, min(K, args.e2e_steps))
+        for i in range(2):
+            for n in dev_in:
+                dev_in[n].copy_(host_in[n], non_blocking=True)
+            step(i)
+            host_out.copy_(out, non_blocking=True)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(Ke):
+            for n in dev_in:
+                dev_in[n].copy_(host_in[n], non_blocking=True)
+            step(i)
+            host_out.copy_(out, non_blocking=True)
+        e1.record()
+        barrier()
+        e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": round(world * nb["step"] * Ke / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": Ke,
+               "ms_per_step": round(e_ms / Ke, 5)}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+
+    peak, peak_kind = _peaks()
+    ms = elapsed_ms / K
+    value = world * nb["step"] / (ms * 1e-3) / 1e9
+    kern_avg_ms = statistics.mean(kern_ms)
+    achieved = nb["attention"] / (kern_avg_ms * 1e-3) / 1e9
+    traffic = _recorded_traffic(args.config)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
+                   "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": 16,
+                   "partition_size": ps, "max_context_len": max_len, "total_context_tokens":
+                   int(wl.context_lens.astype(np.int64).sum()), "num_blocks": wl.num_blocks,
+                   "cow_pairs": int(wl.copy_pairs.shape[0]), "out_dtype": "f32",
+                   "l2": f"inputs larger than L2: {replicas} pool replicas of {pool_bytes / 1e6:.0f} MB rotated "
+                         f"(L2 {l2 / 1e6:.0f} MB)", "parallelism": f"replicas x{world}"},
+        "pct_of_hbm_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_hbm_measured": round(100 * value / world / peak, 2),
+        "seq_layers_per_s": round(world * wl.num_seqs / (ms * 1e-3), 1),
+        "kv_bytes_per_step": nb["kv"], "step_bytes": nb["step"],
+        "roofline": {"bound": "hbm", "kernel": "decode_partitions_kernel", "achieved": round(achieved, 2),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "bytes_per_launch": nb["attention"],
+                     "avg_launch_ms": round(kern_avg_ms, 5)},
+        "gpu_launches": n_launch * K,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
+def _recorded_traffic(cfg):
+    """DRAM bytes per launch of the partition kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    import hashlib
+
+    summ = os.path.join(ROOT, "profiles", f"decode_partitions_config{cfg}_traffic.txt")
+    src = os.path.join(ROOT, "paged_kv_cache_112_gb300", "csrc", "pkv_decode.cu")
+    if not os.path.exists(summ):
+        return None
+    vals = {}
+    with open(summ) as f:
+        for line in f:
+            if "=" in line and not line.lstrip().startswith("#"):
+                k, v = line.split("=", 1)
+                vals[k.strip()] = v.strip()
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    if vals.get("kernel_source_sha256_16") != sha:
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------ CPU oracle arm
+
+def _oracle_pass(wl, seqs, k_pool, v_pool, threads):
+    import oracle
+
+    rows = [(s, h) for s in seqs for h in range(wl.num_q_heads)]
+    oracle.decode_attention(wl.q, k_pool, v_pool, wl.block_tables, wl.context_lens, wl.scale, wl.dtype,
+                            rows=rows, num_threads=threads)
+
+
+def _sample_bytes(wl, seqs):
+    L = wl.context_lens.astype(np.int64)[list(seqs)]
+    return int(L.sum()) * wl.num_kv_heads * wl.head_dim * 2 * 2
+
+
+def cpu_baseline(wl, seconds):
+    """The oracle, as it stands, on whole sequences of the workload, repeated
+    for about `seconds` of wall time on all host cores."""
+    import oracle
+
+    threads = oracle.hardware_threads()
+    k, v, _ = oracle.apply_step(wl, attention=False)
+    order = list(range(wl.num_seqs))
+    t0 = time.perf_counter()
+    _oracle_pass(wl, order[:1], k, v, threads)
+    per_seq = max(time.perf_counter() - t0, 1e-4)
+    n = max(1, min(wl.num_seqs, int(seconds / 3 / per_seq)))
+    seqs = order[:n]
+    done_bytes, t0, reps = 0, time.perf_counter(), 0
+    while True:
+        _oracle_pass(wl, seqs, k, v, threads)
+        done_bytes += _sample_bytes(wl, seqs)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds or reps >= 1000:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(done_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"fp64 oracle over the first {n} of {wl.num_seqs} sequences (all query heads), "
+                      f"{reps} passes, {dt:.1f} s wall"}
+
+
+def run_reference(args):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return None
+    import oracle
+    import pkv_inputs as P
+
+    wl = P.make_workload(args.config, poison=False)
+    threads = oracle.hardware_threads()
+    k, v, _ = oracle.apply_step(wl, attention=False)
+    K, W = args.steps, args.warmup
+    # size one step's sample so that W + K steps take about args.ref_seconds
+    rows_all = [(s, h) for s in range(wl.num_seqs) for h in range(wl.num_q_heads)]
+    t0 = time.perf_counter()
+    oracle.decode_attention(wl.q, k, v, wl.block_tables, wl.context_lens, wl.scale, wl.dtype,
+                            rows=rows_all[: wl.num_q_heads], num_threads=threads)
+    per_row = max((time.perf_counter() - t0) / wl.num_q_heads, 1e-6)
+    budget = args.ref_seconds / max(1, K + W)
+    n_rows = int(max(1, min(len(rows_all), budget / per_row)))
+    rows = rows_all[:n_rows]
+    G = wl.num_q_heads // wl.num_kv_heads
+    L = wl.context_lens.astype(np.int64)
+    # KV bytes the sampled rows account for (a row reads 1/G of its KV head's bytes)
+    sample_bytes = sum(int(L[s]) * wl.head_dim * 2 * 2 for s, _ in rows) / G
+
+    def one():
+        oracle.decode_attention(wl.q, k, v, wl.block_tables, wl.context_lens, wl.scale, wl.dtype, rows=rows,
+                                num_threads=threads)
+
+    for _ in range(W):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        one()
+    dt = time.perf_counter() - t0
+    ms = dt / K * 1e3
+    value = sample_bytes / (ms * 1e-3) / 1e9
+    sample = (f"fp64 oracle, {n_rows} (sequence, query head) rows of {len(rows_all)} per step, "
+              f"{threads} threads")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "sample_rows": n_rows},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--partition-size", type=int, default=None)
+    ap.add_argument("--replicas", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.steps is None:
+        args.steps = 5000 if args.impl == "ours" else 20
+    if args.warmup is None:
+        args.warmup = 20 if args.impl == "ours" else 3
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

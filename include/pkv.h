@@ -1,0 +1,183 @@
+/*
+ * pkv.h -- C ABI of libpkv: the paged KV-cache decode hot path on one GPU
+ * (NVIDIA GB300, sm_103a).
+ *
+ * The operations follow four web pages on paged KV caches (vLLM's
+ * PagedAttention):
+ *   [P1] "gpu_paged_kv_cache" (aicassindra.com)
+ *   [P2] "PagedAttention internals: blocks, copy-on-write" (manishklach)
+ *   [P3] "tm_paged_attention" (aicassindra.com)
+ *   [P4] "KV Cache & PagedAttention" (lattice-ai-eng)
+ *
+ * Common conventions
+ *   - Every pointer argument is a DEVICE pointer unless its comment says host.
+ *   - The caller owns all memory.  The library allocates nothing, keeps no
+ *     pointer after a call returns, never synchronises the device, and
+ *     launches its kernels only on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  Calls are asynchronous: a PKV_OK return means
+ *     the arguments were valid and the kernels were launched.
+ *   - KV pools are one K and one V tensor per layer [P1 "Sizing the pool"],
+ *     laid out [num_blocks][block_size][num_kv_heads][head_dim], head_dim
+ *     innermost and contiguous [P1 "The write path"], block-major as in the
+ *     numpy sketch of [P4 section 4] without its layer axis.  A "slot" is
+ *     one row of num_kv_heads * head_dim elements; slot = block * block_size
+ *     + offset [P1 "The write path"].
+ *   - block_size must be 16 [P1 "Fixed-size blocks"; P2 section 02].
+ *   - Elements are IEEE binary16 (PKV_F16) or bfloat16 (PKV_BF16).  Queries
+ *     have the pools' type.
+ *   - dev_status, when not NULL, is a device int32 into which kernels OR the
+ *     PKV_DEV_ERR_* bits below when they meet an out-of-range index or a
+ *     timed-out wait.  The offending element is skipped (nothing outside the
+ *     caller's buffers is read or written).  The caller zeroes it and reads
+ *     it after synchronising.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned pointer */
+  PKV_ERR_UNSUPPORTED = 2,   /* block_size != 16, head_dim not 64/128, group > 8 ... */
+  PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than pkv_decode_workspace_bytes */
+  PKV_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed */
+} pkv_status;
+
+typedef enum pkv_dtype { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 } pkv_dtype;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define PKV_DEV_ERR_SLOT 1u     /* write_cache: slot >= num_blocks * block_size or < -1 */
+#define PKV_DEV_ERR_PAIR 2u     /* copy_blocks: src or dst outside [0, num_blocks) */
+#define PKV_DEV_ERR_BLOCK 4u    /* decode: block-table entry outside [0, num_blocks) */
+#define PKV_DEV_ERR_LENGTH 8u   /* decode: context length < 0 or > the table / max_context_len */
+#define PKV_DEV_ERR_TIMEOUT 16u /* decode: a wait for a tile copy exceeded its time limit */
+
+/*
+ * pkv_write_cache -- the write path [P1 "The write path: slot mapping and
+ * scatter"]: for every token i in [0, num_tokens) with slot_mapping[i] >= 0,
+ *     k_pool[slot / B][slot % B][:][:] = k_new[i][:][:]
+ *     v_pool[slot / B][slot % B][:][:] = v_new[i][:][:]
+ * as a bitwise copy.  slot_mapping[i] == -1 marks a padding token (no write;
+ * the pages leave padding open, this is the library's convention).  Slots
+ * must be distinct within a call.
+ *   k_new, v_new : [num_tokens][num_kv_heads][head_dim]; consecutive tokens
+ *                  are new_row_stride elements apart (0 = dense, i.e.
+ *                  num_kv_heads*head_dim), so rows of a fused QKV projection
+ *                  can be passed directly.  Rows must be 16-byte aligned.
+ *   k_pool, v_pool : pools as above, 16-byte aligned.
+ *   slot_mapping : int32[num_tokens].
+ * num_tokens == 0 is a no-op.  Out-of-range slots set PKV_DEV_ERR_SLOT.
+ */
+pkv_status pkv_write_cache(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                           const int32_t* slot_mapping, int num_tokens, int64_t new_row_stride,
+                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                           pkv_dtype kv_dtype, int32_t* dev_status, void* stream);
+
+/*
+ * pkv_copy_blocks -- the copy-on-write block copy [P1 "Prefix sharing,
+ * reference counts, and copy-on-write"; P2 section 03; P3 "The
+ * architecture"]: for each pair i, block pairs[2i+1] := block pairs[2i] in
+ * both pools, bitwise, device to device.
+ *   pairs : int32[num_pairs][2] = (src, dst).  dsts must be distinct and no
+ *           dst may also be a src in the same call (a copy-on-write target is
+ *           always a freshly allocated block).
+ * num_pairs == 0 is a no-op.  Out-of-range pairs set PKV_DEV_ERR_PAIR and are
+ * skipped.
+ */
+pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int num_pairs,
+                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                           pkv_dtype kv_dtype, int32_t* dev_status, void* stream);
+
+/*
+ * Bytes of workspace pkv_decode_attention needs for split-K partial results
+ * (0 when every sequence fits one partition).  Host function, no GPU use.
+ * partition_size 0 means "no split".  Returns 0 for invalid sizes.
+ */
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_context_len,
+                                  int partition_size);
+
+/*
+ * pkv_decode_attention -- single-query (decode) grouped-query attention
+ * through block tables [P1 "Inside the paged attention kernel"; P2 section
+ * 02; P3 "End-to-end flow"].  For each sequence s and query head h, with
+ * G = num_q_heads / num_kv_heads, g = h / G (contiguous groups: each KV head
+ * serves its group of query heads [P2 section 02]) and L = context_lens[s]
+ * (the history including the token written this step [P3]):
+ *     k_t = k_pool[block_tables[s][t / 16]][t % 16][g],  v_t likewise,
+ *     out[s][h] = sum_t softmax_t(scale * q[s][h] . k_t) v_t,  t in [0, L).
+ * L == 0 gives a zero row.  Sequences longer than partition_size tokens
+ * are split into partitions of partition_size tokens that run on separate
+ * thread blocks and are merged by a second reduce kernel (the split-K
+ * restructuring of [P1 "Inside the paged attention kernel"]).
+ *   out          : [num_seqs][num_q_heads][head_dim], out_dtype F32/F16/BF16.
+ *   q            : [num_seqs][num_q_heads][head_dim], kv_dtype, 4-byte aligned.
+ *   k_pool, v_pool : pools as above (16-byte aligned).
+ *   block_tables : int32[num_seqs][max_blocks_per_seq], row-major; entries at
+ *                  and past ceil(L/16) are never read.
+ *   context_lens : int32[num_seqs].
+ *   scale        : softmax scale (typically 1/sqrt(head_dim)).
+ *   partition_size : tokens per split-K partition, a multiple of 16, or 0 for
+ *                  one partition per sequence.
+ *   max_context_len : host-side upper bound on every context_lens[s]; it
+ *                  sizes the grid and the workspace (no device read is made
+ *                  on the host).  Longer sequences set PKV_DEV_ERR_LENGTH and
+ *                  are truncated.
+ *   workspace    : device scratch of at least pkv_decode_workspace_bytes()
+ *                  bytes, 16-byte aligned (may be NULL when that is 0).
+ * Supported: head_dim 64 or 128, block_size 16, 1 <= G <= 8.
+ * The two kernels run back to back on `stream`; pkv_decode_partitions and
+ * pkv_decode_reduce below expose them separately.
+ */
+pkv_status pkv_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                const int32_t* block_tables, int max_blocks_per_seq,
+                                const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                float scale, int partition_size, int max_context_len,
+                                void* workspace, size_t workspace_bytes, pkv_dtype kv_dtype,
+                                pkv_dtype out_dtype, int32_t* dev_status, void* stream);
+
+/*
+ * pkv_decode_partitions -- the first of the two kernels of
+ * pkv_decode_attention (same arguments and meaning).  Sequences that fit one
+ * partition get their final output row; longer ones leave per-partition
+ * (running max, running sum, unnormalised accumulator) in the workspace for
+ * pkv_decode_reduce.
+ */
+pkv_status pkv_decode_partitions(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                 float scale, int partition_size, int max_context_len,
+                                 void* workspace, size_t workspace_bytes, pkv_dtype kv_dtype,
+                                 pkv_dtype out_dtype, int32_t* dev_status, void* stream);
+
+/*
+ * pkv_decode_reduce -- the second kernel: merges the partial softmax states of
+ * every sequence with more than one partition ("the cheap reduction" of [P1
+ * "Inside the paged attention kernel"]):  M = max_p m_p,
+ *     out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p.
+ * Arguments as in pkv_decode_attention; it must follow pkv_decode_partitions
+ * with the same sizes, workspace and stream.  A no-op when no sequence is split.
+ */
+pkv_status pkv_decode_reduce(void* out, const int32_t* context_lens, int num_seqs, int num_q_heads,
+                             int head_dim, int partition_size, int max_context_len,
+                             const void* workspace, size_t workspace_bytes, pkv_dtype out_dtype,
+                             int32_t* dev_status, void* stream);
+
+/* Static string naming a status code.  Host function. */
+const char* pkv_status_string(pkv_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch.  Host function. */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

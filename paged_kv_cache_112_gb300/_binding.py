@@ -1,0 +1,172 @@
+"""ctypes binding of libpkv (include/pkv.h): argument marshalling only.
+
+Every function takes torch tensors that already live on the GPU, checks
+their dtype, shape, device and contiguity, and forwards raw pointers, sizes
+and the current CUDA stream to the C ABI.  All computation happens in the
+library's kernels; there is no fallback path, and the library must be built
+(see build.py) or calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA = range(5)
+PKV_F32, PKV_F16, PKV_BF16 = 0, 1, 2
+DEV_ERR_SLOT, DEV_ERR_PAIR, DEV_ERR_BLOCK, DEV_ERR_LENGTH, DEV_ERR_TIMEOUT = 1, 2, 4, 8, 16
+
+_DTYPES = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
+_KV_DTYPES = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
+
+_c_void_p, _c_int, _c_int64, _c_size_t, _c_float = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                                    ctypes.c_size_t, ctypes.c_float)
+_SIGS = {
+    "pkv_write_cache": [_c_void_p] * 5 + [_c_int, _c_int64] + [_c_int] * 5 + [_c_void_p, _c_void_p],
+    "pkv_copy_blocks": [_c_void_p] * 3 + [_c_int] * 6 + [_c_void_p, _c_void_p],
+    "pkv_decode_workspace_bytes": [_c_int] * 5,
+    "pkv_decode_attention": [_c_void_p] * 5 + [_c_int, _c_void_p] + [_c_int] * 6 + [_c_float, _c_int, _c_int,
+                                                                                      _c_void_p, _c_size_t,
+                                                                                      _c_int, _c_int, _c_void_p,
+                                                                                      _c_void_p],
+    "pkv_decode_reduce": [_c_void_p, _c_void_p] + [_c_int] * 5 + [_c_void_p, _c_size_t, _c_int, _c_void_p,
+                                                                  _c_void_p],
+    "pkv_status_string": [_c_int],
+    "pkv_version": [],
+}
+_SIGS["pkv_decode_partitions"] = _SIGS["pkv_decode_attention"]
+
+_LIB = None
+
+
+class PkvError(RuntimeError):
+    pass
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """Loads libpkv.so (building it first if asked).  Raises when it is absent."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if build_if_missing:
+        _build.build()
+    if not os.path.exists(_build.LIB):
+        raise PkvError(f"libpkv is not built ({_build.LIB} missing); run "
+                       "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(_build.LIB)
+    for name, argtypes in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = argtypes
+        fn.restype = ctypes.c_size_t if name == "pkv_decode_workspace_bytes" else (
+            ctypes.c_char_p if name == "pkv_status_string" else ctypes.c_int)
+    _LIB = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load().pkv_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str):
+    if code != PKV_OK:
+        raise PkvError(f"{what}: {status_string(code)}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else int(t.data_ptr())
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise PkvError("tensors must be contiguous CUDA tensors")
+
+
+def _kv_dtype(t) -> int:
+    if t.dtype not in _KV_DTYPES:
+        raise PkvError(f"KV dtype must be float16 or bfloat16, got {t.dtype}")
+    return _KV_DTYPES[t.dtype]
+
+
+def write_cache(k_new, v_new, k_pool, v_pool, slot_mapping, *, status=None, stream=None):
+    """pkv_write_cache: k_new/v_new [T, H_kv, D] (rows may be strided), pools [NB, 16, H_kv, D]."""
+    _need_cuda(k_pool, v_pool, slot_mapping, status)
+    NB, B, Hkv, D = k_pool.shape
+    T = k_new.shape[0]
+    for t in (k_new, v_new):
+        if not t.is_cuda or t.dim() != 3 or t.shape[1:] != (Hkv, D) or t.stride(2) != 1 or t.stride(1) != D:
+            raise PkvError("k_new/v_new must be CUDA [T, H_kv, D] with dense rows")
+    if k_new.stride(0) != v_new.stride(0):
+        raise PkvError("k_new and v_new must share a row stride")
+    _check(load().pkv_write_cache(_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(slot_mapping), T,
+                                  int(k_new.stride(0)), Hkv, D, B, NB, _kv_dtype(k_pool), _ptr(status),
+                                  _stream(stream)), "pkv_write_cache")
+
+
+def copy_blocks(k_pool, v_pool, pairs, *, status=None, stream=None):
+    """pkv_copy_blocks: pairs int32 [P, 2] (src, dst)."""
+    _need_cuda(k_pool, v_pool, pairs, status)
+    NB, B, Hkv, D = k_pool.shape
+    _check(load().pkv_copy_blocks(_ptr(k_pool), _ptr(v_pool), _ptr(pairs), int(pairs.shape[0]), Hkv, D, B, NB,
+                                  _kv_dtype(k_pool), _ptr(status), _stream(stream)), "pkv_copy_blocks")
+
+
+def decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len, partition_size) -> int:
+    return int(load().pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len, partition_size))
+
+
+def _decode_args(out, q, k_pool, v_pool, block_tables, context_lens, scale, partition_size, max_context_len,
+                 workspace, status, stream):
+    _need_cuda(out, q, k_pool, v_pool, block_tables, context_lens, workspace, status)
+    S, Hq, D = q.shape
+    NB, B, Hkv, D2 = k_pool.shape
+    if D2 != D or v_pool.shape != k_pool.shape or q.dtype != k_pool.dtype or v_pool.dtype != k_pool.dtype:
+        raise PkvError("q, k_pool, v_pool shapes/dtypes disagree")
+    if out.shape != q.shape or out.dtype not in _DTYPES:
+        raise PkvError("out must be [S, H_q, D] float32/float16/bfloat16")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise PkvError("block_tables and context_lens must be int32")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return (_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), int(block_tables.shape[1]),
+            _ptr(context_lens), S, Hq, Hkv, D, B, NB, float(scale), int(partition_size), int(max_context_len),
+            _ptr(workspace), ws_bytes, _kv_dtype(k_pool), _DTYPES[out.dtype], _ptr(status), _stream(stream))
+
+
+def decode_attention(out, q, k_pool, v_pool, block_tables, context_lens, scale, *, partition_size=0,
+                     max_context_len, workspace=None, status=None, stream=None):
+    """pkv_decode_attention (partition kernel + reduce kernel)."""
+    _check(load().pkv_decode_attention(*_decode_args(out, q, k_pool, v_pool, block_tables, context_lens, scale,
+                                                     partition_size, max_context_len, workspace, status, stream)),
+           "pkv_decode_attention")
+
+
+def decode_partitions(out, q, k_pool, v_pool, block_tables, context_lens, scale, *, partition_size=0,
+                      max_context_len, workspace=None, status=None, stream=None):
+    """pkv_decode_partitions: the first kernel of decode_attention alone."""
+    _check(load().pkv_decode_partitions(*_decode_args(out, q, k_pool, v_pool, block_tables, context_lens, scale,
+                                                      partition_size, max_context_len, workspace, status,
+                                                      stream)), "pkv_decode_partitions")
+
+
+def decode_reduce(out, context_lens, *, num_q_heads, head_dim, partition_size, max_context_len, workspace=None,
+                  status=None, stream=None):
+    """pkv_decode_reduce: the second kernel of decode_attention alone."""
+    _need_cuda(out, context_lens, workspace, status)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().pkv_decode_reduce(_ptr(out), _ptr(context_lens), int(context_lens.shape[0]), num_q_heads,
+                                    head_dim, int(partition_size), int(max_context_len), _ptr(workspace),
+                                    ws_bytes, _DTYPES[out.dtype], _ptr(status), _stream(stream)),
+           "pkv_decode_reduce")

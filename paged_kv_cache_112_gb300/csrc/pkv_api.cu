@@ -1,0 +1,286 @@
+// Host side of the libpkv C ABI: argument validation, TMA descriptor
+// encoding and kernel launches.  No allocation, no device synchronisation.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "../../include/pkv.h"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_parts) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  WorkspaceLayout w{};
+  if (max_parts <= 1) return w;
+  const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_parts;
+  w.acc_offset = 0;
+  w.acc_bytes = rows * head_dim * sizeof(float);
+  w.ml_offset = up(w.acc_bytes);
+  w.ml_bytes = rows * 2 * sizeof(float);
+  w.total = w.ml_offset + up(w.ml_bytes);
+  return w;
+}
+
+namespace {
+
+constexpr long long kWaitTimeoutNs = 2000000000LL;  // 2 s per bounded wait
+
+bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+bool kv_dtype_ok(pkv_dtype d) { return d == PKV_F16 || d == PKV_BF16; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Describes a pool [num_blocks * 16 rows][num_kv_heads * head_dim / 64 lines][64 elements]
+// so that one box {64, 1, 16} is the 16 token rows of one 128-byte line of
+// one head: half of a (block, head) tile at head_dim 128, all of it at 64.
+bool encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, int head_dim) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(num_kv_heads) * (head_dim / 64),
+                              static_cast<cuuint64_t>(num_blocks) * kBlockSize};
+  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
+  const cuuint32_t box[3] = {64, 1, kBlockSize};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        head_dim >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int parts_for(int max_context_len, int partition_size, int* ps_out) {
+  int ps = partition_size;
+  if (ps == 0) {
+    const int len = max_context_len > 0 ? max_context_len : 1;
+    ps = ((len + kBlockSize - 1) / kBlockSize) * kBlockSize;
+  }
+  *ps_out = ps;
+  const int len = max_context_len > 0 ? max_context_len : 1;
+  return (len + ps - 1) / ps;
+}
+
+struct DecodeCall {
+  DecodeArgs args;
+  CUtensorMap tmap_k, tmap_v;
+};
+
+pkv_status prepare_decode(DecodeCall* c, void* out, const void* q, const void* k_pool, const void* v_pool,
+                          const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                          int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                          int num_blocks, float scale, int partition_size, int max_context_len, void* workspace,
+                          size_t workspace_bytes, pkv_dtype kv_dtype, pkv_dtype out_dtype, int32_t* dev_status,
+                          bool need_maps) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq < 0 || num_blocks <= 0 ||
+      max_context_len < 0 || partition_size < 0 || !std::isfinite(scale))
+    return PKV_ERR_INVALID_ARG;
+  if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (num_q_heads % num_kv_heads != 0) return PKV_ERR_UNSUPPORTED;
+  const int group = num_q_heads / num_kv_heads;
+  if (group > 8) return PKV_ERR_UNSUPPORTED;
+  if (partition_size % kBlockSize != 0) return PKV_ERR_UNSUPPORTED;
+  if (!kv_dtype_ok(kv_dtype) || (out_dtype != PKV_F32 && out_dtype != PKV_F16 && out_dtype != PKV_BF16))
+    return PKV_ERR_INVALID_ARG;
+  if (num_seqs > 0 && (!out || !q || !k_pool || !v_pool || !context_lens || (!block_tables && max_blocks_per_seq)))
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(q, 4) ||
+      !aligned(out, out_dtype == PKV_F32 ? 4 : 2) || !aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return PKV_ERR_INVALID_ARG;
+  int ps = 0;
+  const int max_parts = parts_for(max_context_len, partition_size, &ps);
+  const WorkspaceLayout ws = workspace_layout(num_seqs, num_q_heads, head_dim, max_parts);
+  if (ws.total > 0 && (!workspace || workspace_bytes < ws.total || !aligned(workspace, 16)))
+    return PKV_ERR_WORKSPACE;
+
+  DecodeArgs& a = c->args;
+  a.out = out;
+  a.q = static_cast<const uint16_t*>(q);
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.ws_acc = ws.total ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws.acc_offset) : nullptr;
+  a.ws_ml = ws.total ? reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + ws.ml_offset) : nullptr;
+  a.dev_status = dev_status;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.group = group;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.partition_size = ps;
+  a.max_parts = max_parts;
+  a.max_context_len = max_context_len;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.out_dtype = static_cast<int>(out_dtype);
+  a.timeout_ns = kWaitTimeoutNs;
+  if (need_maps && num_seqs > 0) {
+    if (!encode_pool_map(&c->tmap_k, k_pool, num_blocks, num_kv_heads, head_dim) ||
+        !encode_pool_map(&c->tmap_v, v_pool, num_blocks, num_kv_heads, head_dim))
+      return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+pkv_status pkv_write_cache(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                           const int32_t* slot_mapping, int num_tokens, int64_t new_row_stride, int num_kv_heads,
+                           int head_dim, int block_size, int num_blocks, pkv_dtype kv_dtype, int32_t* dev_status,
+                           void* stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || new_row_stride < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (!kv_dtype_ok(kv_dtype)) return PKV_ERR_INVALID_ARG;
+  if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  const int row = num_kv_heads * head_dim;
+  if (row % 8 != 0) return PKV_ERR_UNSUPPORTED;  // 16-byte vectors
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !k_pool || !v_pool || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  const int64_t stride = new_row_stride ? new_row_stride : row;
+  if (stride < row || stride % 8 != 0) return PKV_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+      !aligned(slot_mapping, 4))
+    return PKV_ERR_INVALID_ARG;
+  WriteCacheArgs a;
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.k_pool = static_cast<uint16_t*>(k_pool);
+  a.v_pool = static_cast<uint16_t*>(v_pool);
+  a.slot_mapping = slot_mapping;
+  a.dev_status = dev_status;
+  a.k_stride = stride;
+  a.v_stride = stride;
+  a.num_slots = static_cast<int64_t>(num_blocks) * kBlockSize;
+  a.num_tokens = num_tokens;
+  a.row_elems = row;
+  return launch_write_cache(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int num_pairs, int num_kv_heads,
+                           int head_dim, int block_size, int num_blocks, pkv_dtype kv_dtype, int32_t* dev_status,
+                           void* stream) {
+  if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+  if (!kv_dtype_ok(kv_dtype)) return PKV_ERR_INVALID_ARG;
+  if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  if ((num_kv_heads * head_dim) % 8 != 0) return PKV_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PKV_OK;
+  if (!k_pool || !v_pool || !pairs) return PKV_ERR_INVALID_ARG;
+  if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(pairs, 4)) return PKV_ERR_INVALID_ARG;
+  CopyBlocksArgs a;
+  a.k_pool = static_cast<uint16_t*>(k_pool);
+  a.v_pool = static_cast<uint16_t*>(v_pool);
+  a.pairs = pairs;
+  a.dev_status = dev_status;
+  a.block_elems = static_cast<int64_t>(kBlockSize) * num_kv_heads * head_dim;
+  a.num_pairs = num_pairs;
+  a.num_blocks = num_blocks;
+  return launch_copy_blocks(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_context_len,
+                                  int partition_size) {
+  if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 || partition_size < 0 ||
+      partition_size % kBlockSize != 0)
+    return 0;
+  int ps = 0;
+  const int parts = parts_for(max_context_len, partition_size, &ps);
+  return workspace_layout(num_seqs, num_q_heads, head_dim, parts).total;
+}
+
+pkv_status pkv_decode_partitions(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                 const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                 int num_blocks, float scale, int partition_size, int max_context_len,
+                                 void* workspace, size_t workspace_bytes, pkv_dtype kv_dtype, pkv_dtype out_dtype,
+                                 int32_t* dev_status, void* stream) {
+  DecodeCall c;
+  pkv_status st = prepare_decode(&c, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+                                 num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                                 partition_size, max_context_len, workspace, workspace_bytes, kv_dtype, out_dtype,
+                                 dev_status, true);
+  if (st != PKV_OK || num_seqs == 0) return st;
+  return launch_decode_partitions(c.args, c.tmap_k, c.tmap_v, head_dim, kv_dtype == PKV_BF16,
+                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_decode_reduce(void* out, const int32_t* context_lens, int num_seqs, int num_q_heads, int head_dim,
+                             int partition_size, int max_context_len, const void* workspace, size_t workspace_bytes,
+                             pkv_dtype out_dtype, int32_t* dev_status, void* stream) {
+  if (num_seqs < 0 || num_q_heads <= 0 || max_context_len < 0 || partition_size < 0) return PKV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (partition_size % kBlockSize != 0) return PKV_ERR_UNSUPPORTED;
+  if (out_dtype != PKV_F32 && out_dtype != PKV_F16 && out_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  int ps = 0;
+  const int max_parts = parts_for(max_context_len, partition_size, &ps);
+  const WorkspaceLayout ws = workspace_layout(num_seqs, num_q_heads, head_dim, max_parts);
+  if (ws.total == 0 || num_seqs == 0) return PKV_OK;
+  if (!out || !context_lens) return PKV_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < ws.total || !aligned(workspace, 16)) return PKV_ERR_WORKSPACE;
+  DecodeArgs a{};
+  a.out = out;
+  a.context_lens = context_lens;
+  a.ws_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(const_cast<void*>(workspace)) + ws.acc_offset);
+  a.ws_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(const_cast<void*>(workspace)) + ws.ml_offset);
+  a.dev_status = dev_status;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.partition_size = ps;
+  a.max_parts = max_parts;
+  a.max_context_len = max_context_len;
+  // The reduce clamps lengths the same way the partition kernel does; the
+  // table width is not needed for that beyond max_context_len.
+  a.max_blocks_per_seq = (max_context_len + kBlockSize - 1) / kBlockSize;
+  a.out_dtype = static_cast<int>(out_dtype);
+  return launch_decode_reduce(a, head_dim, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK
+                                                                                              : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                                int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                int num_blocks, float scale, int partition_size, int max_context_len, void* workspace,
+                                size_t workspace_bytes, pkv_dtype kv_dtype, pkv_dtype out_dtype, int32_t* dev_status,
+                                void* stream) {
+  pkv_status st = pkv_decode_partitions(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+                                        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                                        partition_size, max_context_len, workspace, workspace_bytes, kv_dtype,
+                                        out_dtype, dev_status, stream);
+  if (st != PKV_OK) return st;
+  return pkv_decode_reduce(out, context_lens, num_seqs, num_q_heads, head_dim, partition_size, max_context_len,
+                           workspace, workspace_bytes, out_dtype, dev_status, stream);
+}
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+    case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+  }
+  return "PKV_ERR_UNKNOWN";
+}
+
+int pkv_version(void) { return 100; }
+
+}  // extern "C"

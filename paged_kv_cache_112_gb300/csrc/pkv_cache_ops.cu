@@ -1,0 +1,95 @@
+// Write path and copy-on-write block copy.
+//
+//  * write_cache: "a small scatter kernel copies the new K and V into the
+//    pool, driven by a slot mapping ... block_index x B + offset"; head_dim
+//    innermost "so each store stays vectorized despite scattered
+//    destinations" ("gpu_paged_kv_cache", section "The write path: slot
+//    mapping and scatter").
+//  * copy_blocks: copy-on-write "allocate a fresh block, device-to-device copy
+//    it" (same page, "Prefix sharing, reference counts, and copy-on-write";
+//    "PagedAttention internals", section 03).
+//
+// Both are pure byte movers: every thread moves one 16-byte vector, adjacent
+// threads move adjacent vectors of the same row (coalesced 128-byte lines on
+// both sides).  Grids are capped at a multiple of the SM count and
+// grid-stride over the work.
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+__device__ __forceinline__ void flag(int32_t* status, unsigned bit) {
+  if (status) atomicOr(reinterpret_cast<unsigned*>(status), bit);
+}
+
+__global__ void __launch_bounds__(256) write_cache_kernel(WriteCacheArgs a) {
+  const int vec_per_row = a.row_elems / 8;  // 16-byte vectors per K (or V) row
+  const int64_t total = static_cast<int64_t>(a.num_tokens) * 2 * vec_per_row;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int v = static_cast<int>(idx % vec_per_row);
+    const int64_t r = idx / vec_per_row;
+    const int which = static_cast<int>(r & 1);  // 0 = K, 1 = V
+    const int64_t tok = r >> 1;
+    const int64_t slot = a.slot_mapping[tok];
+    if (slot < 0) {
+      if (slot != -1 && v == 0 && which == 0) flag(a.dev_status, 1u);  // PKV_DEV_ERR_SLOT
+      continue;
+    }
+    if (slot >= a.num_slots) {
+      if (v == 0 && which == 0) flag(a.dev_status, 1u);
+      continue;
+    }
+    const uint16_t* src = which ? a.v_new + tok * a.v_stride : a.k_new + tok * a.k_stride;
+    uint16_t* dst = (which ? a.v_pool : a.k_pool) + slot * a.row_elems;
+    const uint4 val = __ldg(reinterpret_cast<const uint4*>(src) + v);
+    reinterpret_cast<uint4*>(dst)[v] = val;
+  }
+}
+
+__global__ void __launch_bounds__(256) copy_blocks_kernel(CopyBlocksArgs a) {
+  const int64_t vec_per_block = a.block_elems / 8;
+  const int64_t total = static_cast<int64_t>(a.num_pairs) * 2 * vec_per_block;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t v = idx % vec_per_block;
+    const int64_t r = idx / vec_per_block;
+    const int which = static_cast<int>(r & 1);
+    const int64_t pair = r >> 1;
+    const int src = a.pairs[2 * pair];
+    const int dst = a.pairs[2 * pair + 1];
+    if (src < 0 || src >= a.num_blocks || dst < 0 || dst >= a.num_blocks) {
+      if (v == 0 && which == 0) flag(a.dev_status, 2u);  // PKV_DEV_ERR_PAIR
+      continue;
+    }
+    uint16_t* pool = which ? a.v_pool : a.k_pool;
+    const uint4 val = reinterpret_cast<const uint4*>(pool + src * a.block_elems)[v];
+    reinterpret_cast<uint4*>(pool + dst * a.block_elems)[v] = val;
+  }
+}
+
+int grid_for(int64_t work_items, int threads) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (work_items + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(sms) * 16;  // 16 resident 256-thread CTAs per SM at most
+  return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_write_cache(const WriteCacheArgs& a, cudaStream_t stream) {
+  const int64_t work = static_cast<int64_t>(a.num_tokens) * 2 * (a.row_elems / 8);
+  if (work == 0) return cudaSuccess;
+  write_cache_kernel<<<grid_for(work, 256), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream) {
+  const int64_t work = static_cast<int64_t>(a.num_pairs) * 2 * (a.block_elems / 8);
+  if (work == 0) return cudaSuccess;
+  copy_blocks_kernel<<<grid_for(work, 256), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

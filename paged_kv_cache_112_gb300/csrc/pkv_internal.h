@@ -1,0 +1,73 @@
+// Internal declarations shared by the host entry points and the kernel
+// translation units of libpkv.  Not part of the public C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+constexpr int kBlockSize = 16;  // tokens per KV block
+
+struct WriteCacheArgs {
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  uint16_t* k_pool;
+  uint16_t* v_pool;
+  const int32_t* slot_mapping;
+  int32_t* dev_status;
+  int64_t k_stride;   // elements between consecutive new tokens
+  int64_t v_stride;
+  int64_t num_slots;  // num_blocks * block_size
+  int num_tokens;
+  int row_elems;      // num_kv_heads * head_dim
+};
+
+struct CopyBlocksArgs {
+  uint16_t* k_pool;
+  uint16_t* v_pool;
+  const int32_t* pairs;
+  int32_t* dev_status;
+  int64_t block_elems;  // block_size * num_kv_heads * head_dim
+  int num_pairs;
+  int num_blocks;
+};
+
+struct DecodeArgs {
+  void* out;
+  const uint16_t* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float* ws_acc;     // [S][H_q][max_parts][D] unnormalised partial outputs
+  float2* ws_ml;     // [S][H_q][max_parts] (running max in log2 units, running sum)
+  int32_t* dev_status;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;
+  int max_blocks_per_seq;
+  int num_blocks;
+  int partition_size;  // tokens, multiple of 16
+  int max_parts;
+  int max_context_len;
+  float scale_log2;    // scale * log2(e)
+  int out_dtype;       // pkv_dtype
+  long long timeout_ns;
+};
+
+// Split-K workspace layout (both regions 256-byte aligned).
+struct WorkspaceLayout {
+  size_t acc_offset, acc_bytes, ml_offset, ml_bytes, total;
+};
+WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_parts);
+
+cudaError_t launch_write_cache(const WriteCacheArgs& a, cudaStream_t stream);
+cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream);
+// kv_bf16: 0 = f16, 1 = bf16.  Tensor maps describe the K and V pools.
+cudaError_t launch_decode_partitions(const DecodeArgs& a, const CUtensorMap& tmap_k,
+                                     const CUtensorMap& tmap_v, int head_dim, int kv_bf16,
+                                     cudaStream_t stream);
+cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,116 @@
+"""The C ABI library loads and exports every declared symbol; host-side checks
+work without a GPU (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_112_gb300 as pkv
+from paged_kv_cache_112_gb300 import build as pkv_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    try:
+        pkv_build.build()
+    except RuntimeError as e:  # no nvcc on this machine
+        pytest.skip(str(e))
+    return pkv.load()
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ["pkv_write_cache", "pkv_copy_blocks", "pkv_decode_attention", "pkv_decode_partitions",
+              "pkv_decode_reduce", "pkv_decode_workspace_bytes", "pkv_status_string", "pkv_version"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(pkv.library_path())
+    for name in _declared():
+        assert hasattr(raw, name), name
+
+
+def test_status_strings_and_version(lib):
+    assert pkv.status_string(pkv.PKV_OK) == "PKV_OK"
+    assert pkv.status_string(pkv.PKV_ERR_WORKSPACE) == "PKV_ERR_WORKSPACE"
+    assert lib.pkv_version() >= 100
+
+
+def test_workspace_bytes(lib):
+    # no split -> nothing needed
+    assert pkv.decode_workspace_bytes(64, 32, 128, 2048, 0) == 0
+    assert pkv.decode_workspace_bytes(64, 32, 128, 512, 512) == 0
+    # 8 seqs x 32 heads x 256 partitions: acc fp32 [.., 128] + (m, l) pairs, each 256-B aligned
+    rows = 8 * 32 * 256
+    acc = rows * 128 * 4
+    ml = rows * 8
+    up = lambda x: (x + 255) // 256 * 256
+    assert pkv.decode_workspace_bytes(8, 32, 128, 131072, 512) == up(acc) + up(ml)
+    assert pkv.decode_workspace_bytes(8, 32, 128, 100, 24) == 0  # not a multiple of 16 -> invalid
+
+
+FAKE = 0x10000  # never dereferenced: validation fails before any device work
+
+
+def _decode(lib, **kw):
+    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, maxb=4, cl=FAKE, S=2, Hq=8, Hkv=2, D=128, B=16, NB=10,
+             scale=0.1, ps=0, maxlen=64, ws=None, wsb=0, kvd=pkv.PKV_BF16, od=pkv.PKV_F32)
+    a.update(kw)
+    return lib.pkv_decode_attention(a["out"], a["q"], a["k"], a["v"], a["bt"], a["maxb"], a["cl"], a["S"], a["Hq"],
+                                    a["Hkv"], a["D"], a["B"], a["NB"], a["scale"], a["ps"], a["maxlen"], a["ws"],
+                                    a["wsb"], a["kvd"], a["od"], None, None)
+
+
+def test_decode_argument_validation(lib):
+    assert _decode(lib, B=8) == pkv.PKV_ERR_UNSUPPORTED
+    assert _decode(lib, D=96) == pkv.PKV_ERR_UNSUPPORTED
+    assert _decode(lib, Hq=6, Hkv=4) == pkv.PKV_ERR_UNSUPPORTED  # not a whole group
+    assert _decode(lib, Hq=32, Hkv=2) == pkv.PKV_ERR_UNSUPPORTED  # group 16 > 8
+    assert _decode(lib, ps=24) == pkv.PKV_ERR_UNSUPPORTED
+    assert _decode(lib, q=None) == pkv.PKV_ERR_INVALID_ARG
+    assert _decode(lib, k=FAKE + 8) == pkv.PKV_ERR_INVALID_ARG  # pool not 16-byte aligned
+    assert _decode(lib, kvd=pkv.PKV_F32) == pkv.PKV_ERR_INVALID_ARG
+    assert _decode(lib, S=-1) == pkv.PKV_ERR_INVALID_ARG
+    assert _decode(lib, scale=float("nan")) == pkv.PKV_ERR_INVALID_ARG
+    # split needs a workspace
+    assert _decode(lib, ps=16, maxlen=64) == pkv.PKV_ERR_WORKSPACE
+    need = pkv.decode_workspace_bytes(2, 8, 128, 64, 16)
+    assert _decode(lib, ps=16, maxlen=64, ws=FAKE, wsb=need - 1) == pkv.PKV_ERR_WORKSPACE
+
+
+def test_write_and_copy_argument_validation(lib):
+    w = lambda **kw: lib.pkv_write_cache(kw.get("kn", FAKE), kw.get("vn", FAKE), FAKE, FAKE, FAKE, kw.get("T", 4),
+                                         kw.get("stride", 0), kw.get("Hkv", 8), kw.get("D", 128), kw.get("B", 16),
+                                         100, kw.get("dt", pkv.PKV_F16), None, None)
+    assert w(B=32) == pkv.PKV_ERR_UNSUPPORTED
+    assert w(T=-1) == pkv.PKV_ERR_INVALID_ARG
+    assert w(kn=None) == pkv.PKV_ERR_INVALID_ARG
+    assert w(kn=FAKE + 2) == pkv.PKV_ERR_INVALID_ARG  # rows must be 16-byte aligned
+    assert w(stride=100) == pkv.PKV_ERR_INVALID_ARG  # stride below a row
+    assert w(Hkv=1, D=4) == pkv.PKV_ERR_UNSUPPORTED  # row not a whole 16-byte vector
+    assert w(T=0) == pkv.PKV_OK  # no-op, no launch
+    c = lambda **kw: lib.pkv_copy_blocks(FAKE, FAKE, kw.get("pairs", FAKE), kw.get("P", 3), 8, 128,
+                                         kw.get("B", 16), 100, pkv.PKV_BF16, None, None)
+    assert c(B=8) == pkv.PKV_ERR_UNSUPPORTED
+    assert c(pairs=None) == pkv.PKV_ERR_INVALID_ARG
+    assert c(P=0) == pkv.PKV_OK
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from paged_kv_cache_112_gb300 import _binding
+
+    monkeypatch.setattr(_binding, "_LIB", None)
+    monkeypatch.setattr(_binding._build, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(pkv.PkvError):
+        _binding.load()
