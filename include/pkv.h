@@ -170,6 +170,33 @@ pkv_status pkv_decode_reduce(void* out, const int32_t* context_lens, int num_seq
                              const void* workspace, size_t workspace_bytes, pkv_dtype out_dtype,
                              int32_t* dev_status, void* stream);
 
+/*
+ * pkv_decode_attention_static_workspace -- pkv_decode_attention for callers
+ * that cannot allocate device memory when they run decode (for example
+ * plugins whose host framework owns all device memory and forbids
+ * cudaMalloc during execution, or loops that cannot take the device-wide
+ * synchronisation an allocation may cause).  The caller passes the same
+ * inputs and outputs as for pkv_decode_attention but no workspace; the
+ * split-K partials go to a fixed device array inside the library.
+ * The paged-attention pages have no counterpart of this entry point.
+ *   - The array holds PKV_STATIC_WORKSPACE_BYTES bytes on every GPU where the
+ *     library is loaded, until the process exits.  A call whose
+ *     pkv_decode_workspace_bytes() exceeds it returns PKV_ERR_WORKSPACE and
+ *     launches nothing.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address; make that first call before any stream capture.
+ *   - Every call shares the array and it keeps the last call's contents;
+ *     nothing in it needs to start at zero.  Calls whose kernels overlap on
+ *     the GPU race on it: order them (one stream, or explicit events).
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define PKV_STATIC_WORKSPACE_BYTES (16u << 20)
+pkv_status pkv_decode_attention_static_workspace(
+    void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+    int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+    int head_dim, int block_size, int num_blocks, float scale, int partition_size, int max_context_len,
+    pkv_dtype kv_dtype, pkv_dtype out_dtype, int32_t* dev_status, void* stream);
+
 /* Static string naming a status code.  Host function. */
 const char* pkv_status_string(pkv_status status);
 
