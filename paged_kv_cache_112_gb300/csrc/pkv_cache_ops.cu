@@ -23,6 +23,8 @@ __device__ __forceinline__ void flag(int32_t* status, unsigned bit) {
 }
 
 __global__ void __launch_bounds__(256) write_cache_kernel(WriteCacheArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // inputs may come from the previous grid
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int vec_per_row = a.row_elems / 8;  // 16-byte vectors per K (or V) row
   const int64_t total = static_cast<int64_t>(a.num_tokens) * 2 * vec_per_row;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
@@ -48,6 +50,8 @@ __global__ void __launch_bounds__(256) write_cache_kernel(WriteCacheArgs a) {
 }
 
 __global__ void __launch_bounds__(256) copy_blocks_kernel(CopyBlocksArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t vec_per_block = a.block_elems / 8;
   const int64_t total = static_cast<int64_t>(a.num_pairs) * 2 * vec_per_block;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
@@ -81,15 +85,13 @@ int grid_for(int64_t work_items, int threads) {
 cudaError_t launch_write_cache(const WriteCacheArgs& a, cudaStream_t stream) {
   const int64_t work = static_cast<int64_t>(a.num_tokens) * 2 * (a.row_elems / 8);
   if (work == 0) return cudaSuccess;
-  write_cache_kernel<<<grid_for(work, 256), 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(write_cache_kernel, dim3(grid_for(work, 256)), dim3(256), 0, stream, a);
 }
 
 cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream) {
   const int64_t work = static_cast<int64_t>(a.num_pairs) * 2 * (a.block_elems / 8);
   if (work == 0) return cudaSuccess;
-  copy_blocks_kernel<<<grid_for(work, 256), 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(copy_blocks_kernel, dim3(grid_for(work, 256)), dim3(256), 0, stream, a);
 }
 
 }  // namespace pkv

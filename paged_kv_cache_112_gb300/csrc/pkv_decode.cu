@@ -103,6 +103,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Programmatic dependent launch: wait until the previous grid on the stream
+// has completed and its writes are visible; allow the next grid to launch.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -192,6 +199,9 @@ __global__ void __launch_bounds__(NW * 32) decode_partitions_kernel(
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
 
+  // Every input may come from the kernel just before this one on the stream.
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int Hkv = a.num_kv_heads;
@@ -316,15 +326,22 @@ __global__ void __launch_bounds__(NW * 32) decode_partitions_kernel(
     const int nv = ((bad_stage >> st) & 1) ? 0 : min(kBlockSize, ntok - i * kBlockSize);
 
     // S^T = K Q^T : lane holds tokens gr, gr+8 for heads 2tq, 2tq+1.
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    // Two independent accumulation chains (even / odd k-steps) halve the
+    // dependent MMA latency of the score computation.
+    float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int kk = 0; kk < KT; ++kk) {
       const int chunk = ((kk & 3) << 1) + colK;
       const uint32_t addr = sK + (kk >> 2) * 2048 + rowK * 128 + ((chunk ^ (rowK & 7)) << 4);
       uint32_t ka[4];
       ldsm_x4(ka, addr);
-      mma_16816<BF16>(c, ka, qf[kk][0], qf[kk][1]);
+      if (kk & 1)
+        mma_16816<BF16>(c2, ka, qf[kk][0], qf[kk][1]);
+      else
+        mma_16816<BF16>(c, ka, qf[kk][0], qf[kk][1]);
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) c[e] += c2[e];
     float s0 = c[0] * sl2, s1 = c[1] * sl2, s2 = c[2] * sl2, s3 = c[3] * sl2;
     if (gr >= nv) s0 = s1 = kNegInf;
     if (gr + 8 >= nv) s2 = s3 = kNegInf;
@@ -442,61 +459,133 @@ __global__ void __launch_bounds__(NW * 32) decode_partitions_kernel(
 
 // --------------------------------------------------------------- reduce kernel
 
-// One CTA of D threads per (query head, sequence) that was split: thread d
-// owns output element d.
+// Merging the partition states of one (sequence, query head) row:
+//     M' = max(M, m_p),  O' = O 2^(M-M') + acc_p 2^(m_p-M'),  l' likewise,
+// lane j of a warp owning output elements [EPL*j, EPL*j + EPL).  Partitions
+// are loaded in batches of U whose loads are issued together.
 template <int D>
-__global__ void __launch_bounds__(D) decode_reduce_kernel(const DecodeArgs a) {
-  extern __shared__ float w_sm[];  // [max_parts] merge weights, then [D/32] scratch
-  float* red = w_sm + a.max_parts;
-  const int h = blockIdx.x;
-  const int s = blockIdx.y;
+struct RowMerge {
+  static constexpr int EPL = D / 32;
+  static constexpr int U = 8;
+  float M = -__builtin_huge_valf(), den = 0.f, o[EPL] = {};
+
+  // Merges partitions first, first + step, ... below nparts.
+  __device__ __forceinline__ void run(const float2* ml, const float* accp, int first, int step, int nparts) {
+    for (int p0 = first; p0 < nparts; p0 += U * step) {
+      float2 mlv[U];
+      float v[U][EPL];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int p = p0 + u * step;
+        if (p < nparts) {
+          mlv[u] = ml[p];
+          if constexpr (EPL == 4) {
+            const float4 t = *reinterpret_cast<const float4*>(accp + static_cast<int64_t>(p) * D);
+            v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+          } else {
+            const float2 t = *reinterpret_cast<const float2*>(accp + static_cast<int64_t>(p) * D);
+            v[u][0] = t.x; v[u][1] = t.y;
+          }
+        } else {
+          mlv[u] = make_float2(kNegInf, 0.f);
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) v[u][e] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) add(mlv[u].x, mlv[u].y, v[u]);
+    }
+  }
+
+  __device__ __forceinline__ void add(float m, float l, const float (&v)[EPL]) {
+    const float Mn = fmaxf(M, m);
+    if (Mn == kNegInf) return;  // nothing but empty partitions so far
+    const float c_old = exp2f(M - Mn), c_new = exp2f(m - Mn);
+    den = den * c_old + l * c_new;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] = o[e] * c_old + v[e] * c_new;
+    M = Mn;
+  }
+};
+
+__device__ __forceinline__ int reduce_parts_of(const DecodeArgs& a, int s) {
   const int len_cap = min(a.max_context_len, a.max_blocks_per_seq * kBlockSize);
   int L = a.context_lens[s];
   L = L < 0 ? 0 : (L > len_cap ? len_cap : L);
-  const int nparts = L > 0 ? (L + a.partition_size - 1) / a.partition_size : 1;
+  return L > 0 ? (L + a.partition_size - 1) / a.partition_size : 1;
+}
+
+constexpr int kReduceWarps = 8;
+
+// Few partitions per row: one warp per (sequence, query head) row, a CTA
+// holding kReduceWarps rows.  Rows of sequences that fit one partition
+// return at once (the partition kernel wrote their output).
+template <int D>
+__global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_rows_kernel(const DecodeArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kReduceWarps + warp;
+  if (row >= static_cast<int64_t>(a.num_seqs) * a.num_q_heads) return;
+  const int nparts = reduce_parts_of(a, static_cast<int>(row / a.num_q_heads));
   if (nparts <= 1) return;
-  const int tid = threadIdx.x;
-  const int lane = tid & 31, wid = tid >> 5;
-  const int64_t row0 = (static_cast<int64_t>(s) * a.num_q_heads + h) * a.max_parts;
-
-  float m = kNegInf;
-  for (int p = tid; p < nparts; p += D) m = fmaxf(m, a.ws_ml[row0 + p].x);
+  RowMerge<D> r;
+  r.run(a.ws_ml + row * a.max_parts, a.ws_acc + row * a.max_parts * D + lane * RowMerge<D>::EPL, 0, 1, nparts);
+  const float inv = r.den > 0.f ? 1.f / r.den : 0.f;
+  const int64_t obase = row * D + lane * RowMerge<D>::EPL;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-  if (lane == 0) red[wid] = m;
-  __syncthreads();
-  m = red[0];
-#pragma unroll
-  for (int w = 1; w < D / 32; ++w) m = fmaxf(m, red[w]);
-  const float mu = (m == kNegInf) ? 0.f : m;
-  __syncthreads();
+  for (int e = 0; e < RowMerge<D>::EPL; ++e) store_out(a.out, obase + e, r.o[e] * inv, a.out_dtype);
+}
 
-  float den = 0.f;
-  for (int p = tid; p < nparts; p += D) {
-    const float2 ml = a.ws_ml[row0 + p];
-    const float w = exp2f(ml.x - mu);
-    w_sm[p] = w;
-    den += w * ml.y;
+// Many partitions per row (long contexts): one CTA per row; warp w merges
+// partitions w, w + kReduceWarps, ... and the warps' states are merged
+// through shared memory.
+template <int D>
+__global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_long_kernel(const DecodeArgs a) {
+  __shared__ float sm_m[kReduceWarps], sm_l[kReduceWarps];
+  __shared__ float sm_o[kReduceWarps][D];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = blockIdx.x;
+  const int nparts = reduce_parts_of(a, static_cast<int>(row / a.num_q_heads));
+  if (nparts <= 1) return;
+  RowMerge<D> r;
+  r.run(a.ws_ml + row * a.max_parts, a.ws_acc + row * a.max_parts * D + lane * RowMerge<D>::EPL, warp,
+        kReduceWarps, nparts);
+  if (lane == 0) {
+    sm_m[warp] = r.M;
+    sm_l[warp] = r.den;
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
-  if (lane == 0) red[wid] = den;
+  for (int e = 0; e < RowMerge<D>::EPL; ++e) sm_o[warp][lane * RowMerge<D>::EPL + e] = r.o[e];
   __syncthreads();
-  den = 0.f;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float M = kNegInf;
 #pragma unroll
-  for (int w = 0; w < D / 32; ++w) den += red[w];
-
-  float o = 0.f;
-  const float* accp = a.ws_acc + row0 * D + tid;
-  for (int p = 0; p < nparts; ++p) o += w_sm[p] * accp[static_cast<int64_t>(p) * D];
-  const float r = den > 0.f ? o / den : 0.f;
-  store_out(a.out, (static_cast<int64_t>(s) * a.num_q_heads + h) * D + tid, r, a.out_dtype);
+    for (int w = 0; w < kReduceWarps; ++w) M = fmaxf(M, sm_m[w]);
+    const float mu = (M == kNegInf) ? 0.f : M;
+    float o = 0.f, den = 0.f;
+#pragma unroll
+    for (int w = 0; w < kReduceWarps; ++w) {
+      const float c = exp2f(sm_m[w] - mu);
+      o += sm_o[w][d] * c;
+      den += sm_l[w] * c;
+    }
+    store_out(a.out, row * D + d, den > 0.f ? o / den : 0.f, a.out_dtype);
+  }
 }
 
 // ------------------------------------------------------------------ launchers
 
-constexpr int kWarpsPerCta = 4;
-constexpr int kStages = 3;
+#ifndef PKV_WARPS_PER_CTA
+#define PKV_WARPS_PER_CTA 2
+#endif
+#ifndef PKV_STAGES
+#define PKV_STAGES 2
+#endif
+constexpr int kWarpsPerCta = PKV_WARPS_PER_CTA;
+constexpr int kStages = PKV_STAGES;
 
 template <int D, bool BF16>
 cudaError_t launch_partitions_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -510,8 +599,7 @@ cudaError_t launch_partitions_t(const DecodeArgs& a, const CUtensorMap& tk, cons
   const int64_t units = static_cast<int64_t>(a.num_kv_heads) * a.num_seqs * a.max_parts;
   const int64_t ctas = (units + NW - 1) / NW;
   if (ctas == 0) return cudaSuccess;
-  kern<<<static_cast<unsigned>(ctas), NW * 32, smem, stream>>>(a, tk, tv);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(NW * 32), smem, stream, a, tk, tv);
 }
 
 }  // namespace
@@ -529,22 +617,18 @@ cudaError_t launch_decode_partitions(const DecodeArgs& a, const CUtensorMap& tma
 
 cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t stream) {
   if (a.max_parts <= 1 || a.num_seqs == 0) return cudaSuccess;
-  const size_t smem = (static_cast<size_t>(a.max_parts) + 32) * sizeof(float);
-  dim3 grid(a.num_q_heads, a.num_seqs);
-  if (head_dim == 128) {
-    cudaError_t e = cudaFuncSetAttribute(decode_reduce_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    decode_reduce_kernel<128><<<grid, 128, smem, stream>>>(a);
-  } else if (head_dim == 64) {
-    cudaError_t e = cudaFuncSetAttribute(decode_reduce_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    decode_reduce_kernel<64><<<grid, 64, smem, stream>>>(a);
-  } else {
+  const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
+  const dim3 block(kReduceWarps * 32);
+  if (a.max_parts > 4 * RowMerge<128>::U) {  // long rows: a CTA per row
+    const dim3 grid(static_cast<unsigned>(rows));
+    if (head_dim == 128) return launch_pdl(decode_reduce_long_kernel<128>, grid, block, 0, stream, a);
+    if (head_dim == 64) return launch_pdl(decode_reduce_long_kernel<64>, grid, block, 0, stream, a);
     return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>((rows + kReduceWarps - 1) / kReduceWarps));
+  if (head_dim == 128) return launch_pdl(decode_reduce_rows_kernel<128>, grid, block, 0, stream, a);
+  if (head_dim == 64) return launch_pdl(decode_reduce_rows_kernel<64>, grid, block, 0, stream, a);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pkv

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace pkv {
 
 constexpr int kBlockSize = 16;  // tokens per KV block
@@ -61,6 +63,25 @@ struct WorkspaceLayout {
   size_t acc_offset, acc_bytes, ml_offset, ml_bytes, total;
 };
 WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_parts);
+
+// Launches `kernel` with programmatic stream serialisation allowed: it may
+// start while the previous grid on the stream finishes, and must execute
+// griddepcontrol.wait before touching memory that grid could write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 cudaError_t launch_write_cache(const WriteCacheArgs& a, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream);

@@ -1,0 +1,51 @@
+"""Parity at the benchmark's full sizes, in the launch configuration bench.py
+times (its partition size, fp32 output, one write token per sequence, the
+recipe's copy-on-write pairs).  Pools are compared bit for bit in full;
+attention is compared on sampled (sequence, head) rows that the oracle
+computes one by one, always including the shortest and longest sequences."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_112_gb300 as pkv
+import pkv_inputs as P
+from tests.gpu_util import ATOL, DeviceStep, to_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkv.load(build_if_missing=True)
+
+
+def _rows(wl, n, rng):
+    S, Hq = wl.num_seqs, wl.num_q_heads
+    picks = {(int(s), int(h)) for s, h in zip(rng.integers(0, S, n), rng.integers(0, Hq, n))}
+    for s in (int(np.argmin(wl.context_lens)), int(np.argmax(wl.context_lens))):
+        picks.update({(s, 0), (s, Hq - 1), (s, Hq // 2)})
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+def test_full_size_step(cfg):
+    wl = P.make_workload(cfg, poison=True)
+    ds = DeviceStep(wl)  # bench.py's partition size and fp32 output
+    out = ds.step().cpu().numpy()
+    assert ds.status_bits() == 0
+    k_ref, v_ref = wl.k_pool.copy(), wl.v_pool.copy()
+    oracle.copy_blocks(k_ref, v_ref, wl.copy_pairs)
+    oracle.write_cache(k_ref, v_ref, wl.k_new, wl.v_new, wl.slot_mapping)
+    assert np.array_equal(to_bits(ds.k_pool), k_ref)
+    assert np.array_equal(to_bits(ds.v_pool), v_ref)
+    rows = _rows(wl, 48, np.random.default_rng(cfg))
+    ref = oracle.decode_attention(wl.q, k_ref, v_ref, wl.block_tables, wl.context_lens, wl.scale, wl.dtype,
+                                  rows=rows)
+    got = np.stack([out[s, h] for s, h in rows])
+    err = float(np.max(np.abs(got.astype(np.float64) - ref)))
+    assert err <= ATOL, err
+    # every row is finite (NaN poison in unowned slots never leaks)
+    assert np.all(np.isfinite(out))
