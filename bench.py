@@ -199,7 +199,7 @@ def run_gpu(args):
         if ev is not None:
             ev[1].record()
         if ws is not None:
-            pkv.decode_reduce(out, cl, num_q_heads=wl.num_q_heads, head_dim=wl.head_dim, partition_size=ps,
+            pkv.decode_reduce(out, cl, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim, partition_size=ps,
                               max_context_len=max_len, workspace=ws, status=status)
 
     nb = step_bytes(wl)
@@ -213,19 +213,27 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize()
 
+    # Timed region A: exactly K steps, nothing else on the stream (value).
     sampler = ClockSampler(local) if rank == 0 else None
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if sampler:
         sampler.start()
     barrier()
     t_start.record()
     for i in range(K):
-        step(W + i, evs[i])
+        step(W + i)
     t_end.record()
     barrier()
     clocks = sampler.stop() if sampler else None
     elapsed_ms = t_start.elapsed_time(t_end)
+    # Timed region B: the same K steps with CUDA events around every launch of
+    # the partition kernel, for its average launch duration (the events stop
+    # consecutive kernels from overlapping, so region A alone gives the step time).
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier()
+    for i in range(K):
+        step(W + i, evs[i])
+    barrier()
     kern_ms = [a.elapsed_time(b) for a, b in evs]
     if world > 1:
         t = torch.tensor([elapsed_ms], device=dev)
@@ -273,6 +281,7 @@ def run_gpu(args):
     ms = elapsed_ms / K
     value = world * nb["step"] / (ms * 1e-3) / 1e9
     kern_avg_ms = statistics.mean(kern_ms)
+    kernel_name = "decode_balanced_kernel" if ps == pkv.PARTITION_BALANCED else "decode_partitions_kernel"
     achieved = nb["attention"] / (kern_avg_ms * 1e-3) / 1e9
     traffic = _recorded_traffic(args.config)
     line = {
@@ -290,7 +299,7 @@ def run_gpu(args):
         "pct_of_hbm_measured": round(100 * value / world / peak, 2),
         "seq_layers_per_s": round(world * wl.num_seqs / (ms * 1e-3), 1),
         "kv_bytes_per_step": nb["kv"], "step_bytes": nb["step"],
-        "roofline": {"bound": "hbm", "kernel": "decode_partitions_kernel", "achieved": round(achieved, 2),
+        "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "bytes_per_launch": nb["attention"],
                      "avg_launch_ms": round(kern_avg_ms, 5)},

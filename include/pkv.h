@@ -94,10 +94,15 @@ pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int
                            int num_kv_heads, int head_dim, int block_size, int num_blocks,
                            pkv_dtype kv_dtype, int32_t* dev_status, void* stream);
 
+/* partition_size value selecting the balanced split (see pkv_decode_attention). */
+#define PKV_PARTITION_BALANCED (-1)
+
 /*
  * Bytes of workspace pkv_decode_attention needs for split-K partial results
- * (0 when every sequence fits one partition).  Host function, no GPU use.
- * partition_size 0 means "no split".  Returns 0 for invalid sizes.
+ * (0 when every sequence fits one partition).  Host function.  For fixed
+ * partitions it makes no GPU call; for PKV_PARTITION_BALANCED the size
+ * depends on the current device's SM count, which it queries (assuming 256
+ * SMs when no device answers).  Returns 0 for invalid sizes.
  */
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_context_len,
                                   int partition_size);
@@ -122,14 +127,21 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, i
  *                  and past ceil(L/16) are never read.
  *   context_lens : int32[num_seqs].
  *   scale        : softmax scale (typically 1/sqrt(head_dim)).
- *   partition_size : tokens per split-K partition, a multiple of 16, or 0 for
- *                  one partition per sequence.
+ *   partition_size : tokens per split-K partition, a multiple of 16; 0 for
+ *                  one partition per sequence; or PKV_PARTITION_BALANCED
+ *                  (-1): the library splits the whole batch into equal
+ *                  contiguous shares of (block, KV head) tiles, one per warp
+ *                  of a persistent grid (one CTA per SM), so every warp
+ *                  streams the same number of bytes whatever the length mix;
+ *                  sequences are cut wherever shares end (needs
+ *                  num_seqs <= 4096).
  *   max_context_len : host-side upper bound on every context_lens[s]; it
  *                  sizes the grid and the workspace (no device read is made
  *                  on the host).  Longer sequences set PKV_DEV_ERR_LENGTH and
  *                  are truncated.
  *   workspace    : device scratch of at least pkv_decode_workspace_bytes()
- *                  bytes, 16-byte aligned (may be NULL when that is 0).
+ *                  bytes, 16-byte aligned (may be NULL when that is 0).  Its
+ *                  contents need no initialisation.
  * Supported: head_dim 64 or 128, block_size 16, 1 <= G <= 8.
  * The two kernels run back to back on `stream`; pkv_decode_partitions and
  * pkv_decode_reduce below expose them separately.
@@ -159,14 +171,15 @@ pkv_status pkv_decode_partitions(void* out, const void* q, const void* k_pool, c
 
 /*
  * pkv_decode_reduce -- the second kernel: merges the partial softmax states of
- * every sequence with more than one partition ("the cheap reduction" of [P1
- * "Inside the paged attention kernel"]):  M = max_p m_p,
+ * every (sequence, query head) row that was split ("the cheap reduction" of
+ * [P1 "Inside the paged attention kernel"]):  M = max_p m_p,
  *     out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p.
  * Arguments as in pkv_decode_attention; it must follow pkv_decode_partitions
- * with the same sizes, workspace and stream.  A no-op when no sequence is split.
+ * with the same sizes, workspace and stream, on the same device.  A no-op
+ * when no row is split (fixed partitions).
  */
 pkv_status pkv_decode_reduce(void* out, const int32_t* context_lens, int num_seqs, int num_q_heads,
-                             int head_dim, int partition_size, int max_context_len,
+                             int num_kv_heads, int head_dim, int partition_size, int max_context_len,
                              const void* workspace, size_t workspace_bytes, pkv_dtype out_dtype,
                              int32_t* dev_status, void* stream);
 

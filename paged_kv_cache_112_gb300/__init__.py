@@ -9,13 +9,13 @@ This package only marshals torch tensors into the C ABI.
 """
 from ._binding import (DEV_ERR_BLOCK, DEV_ERR_LENGTH, DEV_ERR_PAIR, DEV_ERR_SLOT, DEV_ERR_TIMEOUT, PKV_BF16,
                        PKV_ERR_CUDA, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_F16, PKV_F32,
-                       PKV_OK, PkvError, copy_blocks, decode_attention, decode_partitions, decode_reduce,
+                       PKV_OK, PARTITION_BALANCED, PkvError, copy_blocks, decode_attention, decode_partitions, decode_reduce,
                        decode_workspace_bytes, library_path, load, status_string, write_cache)
 
 __all__ = [
     "load", "library_path", "status_string", "write_cache", "copy_blocks", "decode_attention",
     "decode_partitions", "decode_reduce", "decode_workspace_bytes", "PkvError",
     "PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_WORKSPACE", "PKV_ERR_CUDA",
-    "PKV_F32", "PKV_F16", "PKV_BF16",
+    "PKV_F32", "PKV_F16", "PKV_BF16", "PARTITION_BALANCED",
     "DEV_ERR_SLOT", "DEV_ERR_PAIR", "DEV_ERR_BLOCK", "DEV_ERR_LENGTH", "DEV_ERR_TIMEOUT",
 ]

@@ -17,6 +17,7 @@ from . import build as _build
 
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA = range(5)
 PKV_F32, PKV_F16, PKV_BF16 = 0, 1, 2
+PARTITION_BALANCED = -1  # partition_size selecting the library's balanced split
 DEV_ERR_SLOT, DEV_ERR_PAIR, DEV_ERR_BLOCK, DEV_ERR_LENGTH, DEV_ERR_TIMEOUT = 1, 2, 4, 8, 16
 
 _DTYPES = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
@@ -32,7 +33,7 @@ _SIGS = {
                                                                                       _c_void_p, _c_size_t,
                                                                                       _c_int, _c_int, _c_void_p,
                                                                                       _c_void_p],
-    "pkv_decode_reduce": [_c_void_p, _c_void_p] + [_c_int] * 5 + [_c_void_p, _c_size_t, _c_int, _c_void_p,
+    "pkv_decode_reduce": [_c_void_p, _c_void_p] + [_c_int] * 6 + [_c_void_p, _c_size_t, _c_int, _c_void_p,
                                                                   _c_void_p],
     "pkv_status_string": [_c_int],
     "pkv_version": [],
@@ -161,12 +162,12 @@ def decode_partitions(out, q, k_pool, v_pool, block_tables, context_lens, scale,
                                                       stream)), "pkv_decode_partitions")
 
 
-def decode_reduce(out, context_lens, *, num_q_heads, head_dim, partition_size, max_context_len, workspace=None,
-                  status=None, stream=None):
+def decode_reduce(out, context_lens, *, num_q_heads, num_kv_heads, head_dim, partition_size, max_context_len,
+                  workspace=None, status=None, stream=None):
     """pkv_decode_reduce: the second kernel of decode_attention alone."""
     _need_cuda(out, context_lens, workspace, status)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().pkv_decode_reduce(_ptr(out), _ptr(context_lens), int(context_lens.shape[0]), num_q_heads,
-                                    head_dim, int(partition_size), int(max_context_len), _ptr(workspace),
-                                    ws_bytes, _DTYPES[out.dtype], _ptr(status), _stream(stream)),
+                                    num_kv_heads, head_dim, int(partition_size), int(max_context_len),
+                                    _ptr(workspace), ws_bytes, _DTYPES[out.dtype], _ptr(status), _stream(stream)),
            "pkv_decode_reduce")

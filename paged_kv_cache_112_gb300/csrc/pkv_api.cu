@@ -5,21 +5,78 @@
 #include <cmath>
 #include <mutex>
 
-#include "../../include/pkv.h"
+#include "pkv.h"
 #include "pkv_internal.h"
 
 namespace pkv {
 
+namespace {
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+}  // namespace
+
+int current_sm_count(int fallback) {
+  static int cache[256] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) {
+    cudaGetLastError();
+    return fallback;
+  }
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return fallback;
+    }
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
+  struct Entry {
+    const void* kernel;
+    int dev;
+    size_t bytes;
+  };
+  static Entry table[64];
+  static int used = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (table[i].kernel == kernel && table[i].dev == dev && table[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < used; ++i)
+    if (table[i].kernel == kernel && table[i].dev == dev) {
+      table[i].bytes = bytes;
+      return cudaSuccess;
+    }
+  if (used < 64) table[used++] = Entry{kernel, dev, bytes};
+  return cudaSuccess;
+}
+
 WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_parts) {
-  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   WorkspaceLayout w{};
   if (max_parts <= 1) return w;
   const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_parts;
   w.acc_offset = 0;
-  w.acc_bytes = rows * head_dim * sizeof(float);
-  w.ml_offset = up(w.acc_bytes);
-  w.ml_bytes = rows * 2 * sizeof(float);
-  w.total = w.ml_offset + up(w.ml_bytes);
+  w.ml_offset = align256(rows * head_dim * sizeof(float));
+  w.meta_offset = w.ml_offset + align256(rows * 2 * sizeof(float));
+  w.total = w.meta_offset;
+  return w;
+}
+
+WorkspaceLayout balanced_workspace_layout(int num_seqs, int num_q_heads, int head_dim, int64_t warps) {
+  WorkspaceLayout w{};
+  const size_t heads = static_cast<size_t>(num_q_heads < 8 ? num_q_heads : 8);  // group size bound
+  const size_t recs = static_cast<size_t>(warps) * 2 * heads;
+  w.acc_offset = 0;
+  w.ml_offset = align256(recs * head_dim * sizeof(float));
+  w.meta_offset = w.ml_offset + align256(recs * 2 * sizeof(float));
+  w.total = w.meta_offset + align256(static_cast<size_t>(num_seqs) * num_q_heads * 2 * sizeof(int));
   return w;
 }
 
@@ -48,7 +105,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // Describes a pool [num_blocks * 16 rows][num_kv_heads * head_dim / 64 lines][64 elements]
 // so that one box {64, 1, 16} is the 16 token rows of one 128-byte line of
 // one head: half of a (block, head) tile at head_dim 128, all of it at 64.
-bool encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, int head_dim) {
+bool encode_pool_map_uncached(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, int head_dim) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(num_kv_heads) * (head_dim / 64),
@@ -63,15 +120,54 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int num
   return r == CUDA_SUCCESS;
 }
 
+// Descriptors depend only on the pool address and geometry, so recent ones
+// are kept (a small round-robin cache) instead of re-encoded every call.
+bool encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, int head_dim) {
+  struct Entry {
+    const void* pool;
+    int num_blocks, num_kv_heads, head_dim;
+    CUtensorMap map;
+  };
+  static Entry cache[32];
+  static int next = 0;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& e : cache)
+      if (e.pool == pool && e.num_blocks == num_blocks && e.num_kv_heads == num_kv_heads && e.head_dim == head_dim) {
+        *map = e.map;
+        return true;
+      }
+  }
+  if (!encode_pool_map_uncached(map, pool, num_blocks, num_kv_heads, head_dim)) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  cache[next] = Entry{pool, num_blocks, num_kv_heads, head_dim, *map};
+  next = (next + 1) % 32;
+  return true;
+}
+
 int parts_for(int max_context_len, int partition_size, int* ps_out) {
   int ps = partition_size;
-  if (ps == 0) {
+  if (ps <= 0) {  // one partition per sequence
     const int len = max_context_len > 0 ? max_context_len : 1;
     ps = ((len + kBlockSize - 1) / kBlockSize) * kBlockSize;
   }
   *ps_out = ps;
   const int len = max_context_len > 0 ? max_context_len : 1;
   return (len + ps - 1) / ps;
+}
+
+// Workspace of a decode call (fixed partitions or balanced split).
+WorkspaceLayout decode_layout(int num_seqs, int num_q_heads, int head_dim, int max_context_len, int partition_size,
+                              int sm_count, int* max_parts_out) {
+  if (partition_size == PKV_PARTITION_BALANCED) {
+    *max_parts_out = 1;
+    const int64_t warps = static_cast<int64_t>(sm_count) * balanced_warps_per_cta(head_dim);
+    return balanced_workspace_layout(num_seqs, num_q_heads, head_dim, warps);
+  }
+  int ps = 0;
+  *max_parts_out = parts_for(max_context_len, partition_size, &ps);
+  return workspace_layout(num_seqs, num_q_heads, head_dim, *max_parts_out);
 }
 
 struct DecodeCall {
@@ -85,15 +181,17 @@ pkv_status prepare_decode(DecodeCall* c, void* out, const void* q, const void* k
                           int num_blocks, float scale, int partition_size, int max_context_len, void* workspace,
                           size_t workspace_bytes, pkv_dtype kv_dtype, pkv_dtype out_dtype, int32_t* dev_status,
                           bool need_maps) {
+  const bool balanced = partition_size == PKV_PARTITION_BALANCED;
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq < 0 || num_blocks <= 0 ||
-      max_context_len < 0 || partition_size < 0 || !std::isfinite(scale))
+      max_context_len < 0 || (partition_size < 0 && !balanced) || !std::isfinite(scale))
     return PKV_ERR_INVALID_ARG;
   if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
   if (num_q_heads % num_kv_heads != 0) return PKV_ERR_UNSUPPORTED;
   const int group = num_q_heads / num_kv_heads;
   if (group > 8) return PKV_ERR_UNSUPPORTED;
-  if (partition_size % kBlockSize != 0) return PKV_ERR_UNSUPPORTED;
+  if (!balanced && partition_size % kBlockSize != 0) return PKV_ERR_UNSUPPORTED;
+  if (balanced && num_seqs > kBalancedMaxSeqs) return PKV_ERR_UNSUPPORTED;
   if (!kv_dtype_ok(kv_dtype) || (out_dtype != PKV_F32 && out_dtype != PKV_F16 && out_dtype != PKV_BF16))
     return PKV_ERR_INVALID_ARG;
   if (num_seqs > 0 && (!out || !q || !k_pool || !v_pool || !context_lens || (!block_tables && max_blocks_per_seq)))
@@ -101,9 +199,12 @@ pkv_status prepare_decode(DecodeCall* c, void* out, const void* q, const void* k
   if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(q, 4) ||
       !aligned(out, out_dtype == PKV_F32 ? 4 : 2) || !aligned(block_tables, 4) || !aligned(context_lens, 4))
     return PKV_ERR_INVALID_ARG;
-  int ps = 0;
-  const int max_parts = parts_for(max_context_len, partition_size, &ps);
-  const WorkspaceLayout ws = workspace_layout(num_seqs, num_q_heads, head_dim, max_parts);
+  const int sms = balanced ? current_sm_count(0) : 0;
+  if (balanced && sms <= 0) return PKV_ERR_CUDA;
+  int max_parts = 1, ps = 0;
+  const WorkspaceLayout ws =
+      decode_layout(num_seqs, num_q_heads, head_dim, max_context_len, partition_size, sms, &max_parts);
+  parts_for(max_context_len, partition_size, &ps);
   if (ws.total > 0 && (!workspace || workspace_bytes < ws.total || !aligned(workspace, 16)))
     return PKV_ERR_WORKSPACE;
 
@@ -112,8 +213,11 @@ pkv_status prepare_decode(DecodeCall* c, void* out, const void* q, const void* k
   a.q = static_cast<const uint16_t*>(q);
   a.block_tables = block_tables;
   a.context_lens = context_lens;
-  a.ws_acc = ws.total ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws.acc_offset) : nullptr;
-  a.ws_ml = ws.total ? reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + ws.ml_offset) : nullptr;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  a.ws_acc = ws.total ? reinterpret_cast<float*>(wsb + ws.acc_offset) : nullptr;
+  a.ws_ml = ws.total ? reinterpret_cast<float2*>(wsb + ws.ml_offset) : nullptr;
+  a.ws_meta = (ws.total && balanced) ? reinterpret_cast<int2*>(wsb + ws.meta_offset) : nullptr;
+  a.balanced_ctas = balanced ? sms : 0;
   a.dev_status = dev_status;
   a.num_seqs = num_seqs;
   a.num_q_heads = num_q_heads;
@@ -197,12 +301,14 @@ pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int
 
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_context_len,
                                   int partition_size) {
-  if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 || partition_size < 0 ||
-      partition_size % kBlockSize != 0)
+  const bool balanced = partition_size == PKV_PARTITION_BALANCED;
+  if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||
+      (!balanced && (partition_size < 0 || partition_size % kBlockSize != 0)))
     return 0;
-  int ps = 0;
-  const int parts = parts_for(max_context_len, partition_size, &ps);
-  return workspace_layout(num_seqs, num_q_heads, head_dim, parts).total;
+  int parts = 1;
+  return decode_layout(num_seqs, num_q_heads, head_dim, max_context_len, partition_size,
+                       balanced ? current_sm_count(256) : 0, &parts)
+      .total;
 }
 
 pkv_status pkv_decode_partitions(void* out, const void* q, const void* k_pool, const void* v_pool,
@@ -217,42 +323,57 @@ pkv_status pkv_decode_partitions(void* out, const void* q, const void* k_pool, c
                                  partition_size, max_context_len, workspace, workspace_bytes, kv_dtype, out_dtype,
                                  dev_status, true);
   if (st != PKV_OK || num_seqs == 0) return st;
-  return launch_decode_partitions(c.args, c.tmap_k, c.tmap_v, head_dim, kv_dtype == PKV_BF16,
-                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? PKV_OK
-             : PKV_ERR_CUDA;
+  const cudaError_t e = c.args.balanced_ctas
+                            ? launch_decode_balanced(c.args, c.tmap_k, c.tmap_v, head_dim, kv_dtype == PKV_BF16,
+                                                     static_cast<cudaStream_t>(stream))
+                            : launch_decode_partitions(c.args, c.tmap_k, c.tmap_v, head_dim, kv_dtype == PKV_BF16,
+                                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-pkv_status pkv_decode_reduce(void* out, const int32_t* context_lens, int num_seqs, int num_q_heads, int head_dim,
-                             int partition_size, int max_context_len, const void* workspace, size_t workspace_bytes,
-                             pkv_dtype out_dtype, int32_t* dev_status, void* stream) {
-  if (num_seqs < 0 || num_q_heads <= 0 || max_context_len < 0 || partition_size < 0) return PKV_ERR_INVALID_ARG;
+pkv_status pkv_decode_reduce(void* out, const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                             int head_dim, int partition_size, int max_context_len, const void* workspace,
+                             size_t workspace_bytes, pkv_dtype out_dtype, int32_t* dev_status, void* stream) {
+  const bool balanced = partition_size == PKV_PARTITION_BALANCED;
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0 ||
+      (partition_size < 0 && !balanced))
+    return PKV_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  if (partition_size % kBlockSize != 0) return PKV_ERR_UNSUPPORTED;
+  if (num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > 8) return PKV_ERR_UNSUPPORTED;
+  if (!balanced && partition_size % kBlockSize != 0) return PKV_ERR_UNSUPPORTED;
   if (out_dtype != PKV_F32 && out_dtype != PKV_F16 && out_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
-  int ps = 0;
-  const int max_parts = parts_for(max_context_len, partition_size, &ps);
-  const WorkspaceLayout ws = workspace_layout(num_seqs, num_q_heads, head_dim, max_parts);
+  const int sms = balanced ? current_sm_count(0) : 0;
+  if (balanced && sms <= 0) return PKV_ERR_CUDA;
+  int max_parts = 1, ps = 0;
+  const WorkspaceLayout ws =
+      decode_layout(num_seqs, num_q_heads, head_dim, max_context_len, partition_size, sms, &max_parts);
+  parts_for(max_context_len, partition_size, &ps);
   if (ws.total == 0 || num_seqs == 0) return PKV_OK;
   if (!out || !context_lens) return PKV_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < ws.total || !aligned(workspace, 16)) return PKV_ERR_WORKSPACE;
+  uint8_t* wsb = static_cast<uint8_t*>(const_cast<void*>(workspace));
   DecodeArgs a{};
   a.out = out;
   a.context_lens = context_lens;
-  a.ws_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(const_cast<void*>(workspace)) + ws.acc_offset);
-  a.ws_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(const_cast<void*>(workspace)) + ws.ml_offset);
+  a.ws_acc = reinterpret_cast<float*>(wsb + ws.acc_offset);
+  a.ws_ml = reinterpret_cast<float2*>(wsb + ws.ml_offset);
+  a.ws_meta = balanced ? reinterpret_cast<int2*>(wsb + ws.meta_offset) : nullptr;
   a.dev_status = dev_status;
   a.num_seqs = num_seqs;
   a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.group = num_q_heads / num_kv_heads;
   a.partition_size = ps;
   a.max_parts = max_parts;
   a.max_context_len = max_context_len;
-  // The reduce clamps lengths the same way the partition kernel does; the
-  // table width is not needed for that beyond max_context_len.
+  // Lengths are clamped as in the partition kernel; beyond max_context_len the
+  // table width does not matter here.
   a.max_blocks_per_seq = (max_context_len + kBlockSize - 1) / kBlockSize;
   a.out_dtype = static_cast<int>(out_dtype);
-  return launch_decode_reduce(a, head_dim, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK
-                                                                                              : PKV_ERR_CUDA;
+  a.balanced_ctas = balanced ? sms : 0;
+  const cudaError_t e = balanced ? launch_decode_reduce_balanced(a, head_dim, static_cast<cudaStream_t>(stream))
+                                 : launch_decode_reduce(a, head_dim, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 pkv_status pkv_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
@@ -266,8 +387,8 @@ pkv_status pkv_decode_attention(void* out, const void* q, const void* k_pool, co
                                         partition_size, max_context_len, workspace, workspace_bytes, kv_dtype,
                                         out_dtype, dev_status, stream);
   if (st != PKV_OK) return st;
-  return pkv_decode_reduce(out, context_lens, num_seqs, num_q_heads, head_dim, partition_size, max_context_len,
-                           workspace, workspace_bytes, out_dtype, dev_status, stream);
+  return pkv_decode_reduce(out, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, partition_size,
+                           max_context_len, workspace, workspace_bytes, out_dtype, dev_status, stream);
 }
 
 const char* pkv_status_string(pkv_status s) {

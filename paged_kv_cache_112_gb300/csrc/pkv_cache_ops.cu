@@ -33,6 +33,9 @@ __global__ void __launch_bounds__(256) write_cache_kernel(WriteCacheArgs a) {
     const int64_t r = idx / vec_per_row;
     const int which = static_cast<int>(r & 1);  // 0 = K, 1 = V
     const int64_t tok = r >> 1;
+    // The row load does not depend on the slot: issue both loads together.
+    const uint16_t* src = which ? a.v_new + tok * a.v_stride : a.k_new + tok * a.k_stride;
+    const uint4 val = __ldg(reinterpret_cast<const uint4*>(src) + v);
     const int64_t slot = a.slot_mapping[tok];
     if (slot < 0) {
       if (slot != -1 && v == 0 && which == 0) flag(a.dev_status, 1u);  // PKV_DEV_ERR_SLOT
@@ -42,9 +45,7 @@ __global__ void __launch_bounds__(256) write_cache_kernel(WriteCacheArgs a) {
       if (v == 0 && which == 0) flag(a.dev_status, 1u);
       continue;
     }
-    const uint16_t* src = which ? a.v_new + tok * a.v_stride : a.k_new + tok * a.k_stride;
     uint16_t* dst = (which ? a.v_pool : a.k_pool) + slot * a.row_elems;
-    const uint4 val = __ldg(reinterpret_cast<const uint4*>(src) + v);
     reinterpret_cast<uint4*>(dst)[v] = val;
   }
 }
@@ -73,8 +74,7 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(CopyBlocksArgs a) {
 }
 
 int grid_for(int64_t work_items, int threads) {
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = current_sm_count(148);
   const int64_t want = (work_items + threads - 1) / threads;
   const int64_t cap = static_cast<int64_t>(sms) * 16;  // 16 resident 256-thread CTAs per SM at most
   return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);

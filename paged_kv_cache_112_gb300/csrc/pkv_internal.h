@@ -41,8 +41,9 @@ struct DecodeArgs {
   const uint16_t* q;
   const int32_t* block_tables;
   const int32_t* context_lens;
-  float* ws_acc;     // [S][H_q][max_parts][D] unnormalised partial outputs
-  float2* ws_ml;     // [S][H_q][max_parts] (running max in log2 units, running sum)
+  float* ws_acc;     // partial records [..][D]: unnormalised partial outputs
+  float2* ws_ml;     // partial records: (running max in log2 units, running sum)
+  int2* ws_meta;     // balanced split: per (s, g) pair (first warp, 2 * pieces + its slot)
   int32_t* dev_status;
   int num_seqs;
   int num_q_heads;
@@ -55,14 +56,30 @@ struct DecodeArgs {
   int max_context_len;
   float scale_log2;    // scale * log2(e)
   int out_dtype;       // pkv_dtype
+  int balanced_ctas;   // balanced split: persistent CTAs (one per SM); 0 otherwise
   long long timeout_ns;
 };
 
-// Split-K workspace layout (both regions 256-byte aligned).
+// Split-K workspace layout (regions 256-byte aligned).  Fixed partitions:
+// records [S][H_q][max_parts].  Balanced split: per-pair metadata [S][<=H_q]
+// then records [W warps][2 slots][<= 8 heads].
 struct WorkspaceLayout {
-  size_t acc_offset, acc_bytes, ml_offset, ml_bytes, total;
+  size_t acc_offset, ml_offset, meta_offset, total;
 };
 WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_parts);
+WorkspaceLayout balanced_workspace_layout(int num_seqs, int num_q_heads, int head_dim, int64_t warps);
+
+// SM count of the current device, cached per device; `fallback` when no
+// device answers.
+int current_sm_count(int fallback);
+// Raises a kernel's dynamic shared memory limit to `bytes` on the current
+// device (once per kernel, device and size).
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
+
+// Balanced split geometry (pkv_decode_balanced.cu).
+constexpr int kBalancedMaxSeqs = 4096;
+int balanced_warps_per_cta(int head_dim);
+size_t balanced_smem_bytes(int head_dim, int num_seqs);
 
 // Launches `kernel` with programmatic stream serialisation allowed: it may
 // start while the previous grid on the stream finishes, and must execute
@@ -90,5 +107,8 @@ cudaError_t launch_decode_partitions(const DecodeArgs& a, const CUtensorMap& tma
                                      const CUtensorMap& tmap_v, int head_dim, int kv_bf16,
                                      cudaStream_t stream);
 cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t stream);
+cudaError_t launch_decode_balanced(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                   int head_dim, int kv_bf16, cudaStream_t stream);
+cudaError_t launch_decode_reduce_balanced(const DecodeArgs& a, int head_dim, cudaStream_t stream);
 
 }  // namespace pkv

@@ -28,7 +28,7 @@
 // the array as the workspace.
 #include <mutex>
 
-#include "../../include/pkv.h"
+#include "pkv.h"
 #include "pkv_internal.h"
 
 namespace {

@@ -58,6 +58,11 @@ def test_workspace_bytes(lib):
     up = lambda x: (x + 255) // 256 * 256
     assert pkv.decode_workspace_bytes(8, 32, 128, 131072, 512) == up(acc) + up(ml)
     assert pkv.decode_workspace_bytes(8, 32, 128, 100, 24) == 0  # not a multiple of 16 -> invalid
+    # balanced split: per-pair metadata + 2 partial records per warp (group <= 8 heads); without a
+    # device the SM count defaults to 256, else the device's
+    bal = pkv.decode_workspace_bytes(64, 32, 128, 2048, pkv.PARTITION_BALANCED)
+    assert bal >= 64 * 32 * 8 + 256 * 0  # at least the metadata
+    assert pkv.decode_workspace_bytes(64, 32, 128, 2048, -2) == 0
 
 
 FAKE = 0x10000  # never dereferenced: validation fails before any device work

@@ -30,10 +30,12 @@ def _rows(wl, n, rng):
     return sorted(picks)
 
 
-@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
-def test_full_size_step(cfg):
+@pytest.mark.parametrize("cfg,ps", [(2, None), (3, None), (4, None), (5, None),
+                                    (2, pkv.PARTITION_BALANCED), (3, pkv.PARTITION_BALANCED),
+                                    (5, pkv.PARTITION_BALANCED)])
+def test_full_size_step(cfg, ps):
     wl = P.make_workload(cfg, poison=True)
-    ds = DeviceStep(wl)  # bench.py's partition size and fp32 output
+    ds = DeviceStep(wl, partition_size=ps)  # None: the recipe's partition size; fp32 output
     out = ds.step().cpu().numpy()
     assert ds.status_bits() == 0
     k_ref, v_ref = wl.k_pool.copy(), wl.v_pool.copy()

@@ -43,7 +43,7 @@ LENS = [0, 1, 15, 16, 17, 33, 100, 257, 600]
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"{s[0]}q{s[1]}kv{s[2]}d")
-@pytest.mark.parametrize("ps", [0, 16, 48, 512])
+@pytest.mark.parametrize("ps", [0, 16, 48, 512, pkv.PARTITION_BALANCED])
 def test_decode_sweep(dtype, shape, ps):
     Hq, Hkv, D = shape
     lens = [L for L in LENS] + [1]
@@ -96,9 +96,10 @@ def test_write_cache_padding_and_strided_rows():
     assert np.array_equal(to_bits(ds.v_pool), v)
 
 
-def test_split_kernels_equal_fused_call_and_are_deterministic():
+@pytest.mark.parametrize("ps", [64, pkv.PARTITION_BALANCED])
+def test_split_kernels_equal_fused_call_and_are_deterministic(ps):
     wl = P.make_workload(2, num_seqs=6, poison=True)
-    ds = DeviceStep(wl, partition_size=64)
+    ds = DeviceStep(wl, partition_size=ps)
     ds.copy()
     ds.write()
     ds.attend()
@@ -107,9 +108,10 @@ def test_split_kernels_equal_fused_call_and_are_deterministic():
     b = ds.out.clone()
     out2 = torch.empty_like(ds.out)
     pkv.decode_partitions(out2, ds.q, ds.k_pool, ds.v_pool, ds.block_tables, ds.context_lens, wl.scale,
-                          partition_size=64, max_context_len=ds.max_context_len, workspace=ds.workspace)
-    pkv.decode_reduce(out2, ds.context_lens, num_q_heads=wl.num_q_heads, head_dim=wl.head_dim, partition_size=64,
-                      max_context_len=ds.max_context_len, workspace=ds.workspace)
+                          partition_size=ps, max_context_len=ds.max_context_len, workspace=ds.workspace)
+    pkv.decode_reduce(out2, ds.context_lens, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
+                      head_dim=wl.head_dim, partition_size=ps, max_context_len=ds.max_context_len,
+                      workspace=ds.workspace)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
     assert torch.equal(a, out2)
@@ -129,8 +131,22 @@ def test_16bit_output_is_rounded_fp32_output(odt):
 def test_partition_size_does_not_change_much():
     wl = P.make_workload(2, num_seqs=8, poison=True)
     outs = []
-    for ps in (0, 16, 64, 512):
+    for ps in (0, 16, 64, 512, pkv.PARTITION_BALANCED):
         ds = DeviceStep(wl, partition_size=ps)
         outs.append(ds.step().cpu().numpy())
     for o in outs[1:]:
         assert np.max(np.abs(o - outs[0])) <= 1e-4
+
+
+@pytest.mark.parametrize("num_seqs,lens", [(1, ("fixed", [5000])), (300, ("uniform", 1, 40)),
+                                           (40, ("fixed", [16] * 40))])
+def test_balanced_split_shapes(num_seqs, lens):
+    """Balanced split on one long sequence (many warps on one pair), many tiny
+    sequences (a warp crossing many pairs) and block-aligned lengths."""
+    wl = P.make_workload(2, num_seqs=num_seqs, lens=lens, poison=True, partition_size=pkv.PARTITION_BALANCED,
+                         seed=7 + num_seqs)
+    ds = DeviceStep(wl)
+    out = ds.step().cpu().numpy()
+    k_ref, v_ref, ref = oracle.apply_step(wl)
+    assert _max_err(out, ref) <= ATOL
+    assert ds.status_bits() == 0
