@@ -282,8 +282,8 @@ def run_gpu(args):
     value = world * nb["step"] / (ms * 1e-3) / 1e9
     kern_avg_ms = statistics.mean(kern_ms)
     kernel_name = "decode_balanced_kernel" if ps == pkv.PARTITION_BALANCED else "decode_partitions_kernel"
+    traffic = _recorded_traffic(args.config, kernel_name)
     achieved = nb["attention"] / (kern_avg_ms * 1e-3) / 1e9
-    traffic = _recorded_traffic(args.config)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -314,13 +314,15 @@ def run_gpu(args):
     return line
 
 
-def _recorded_traffic(cfg):
+def _recorded_traffic(cfg, kernel):
     """DRAM bytes per launch of the partition kernel from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
+    summary, if it was taken on the current kernel sources; else None."""
     import hashlib
 
+    if kernel != "decode_partitions_kernel":
+        return None
     summ = os.path.join(ROOT, "profiles", f"decode_partitions_config{cfg}_traffic.txt")
-    src = os.path.join(ROOT, "paged_kv_cache_112_gb300", "csrc", "pkv_decode.cu")
+    srcs = [os.path.join(ROOT, "paged_kv_cache_112_gb300", "csrc", f) for f in ("pkv_decode.cu", "pkv_device.cuh")]
     if not os.path.exists(summ):
         return None
     vals = {}
@@ -329,9 +331,11 @@ def _recorded_traffic(cfg):
             if "=" in line and not line.lstrip().startswith("#"):
                 k, v = line.split("=", 1)
                 vals[k.strip()] = v.strip()
-    with open(src, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
-    if vals.get("kernel_source_sha256_16") != sha:
+    h = hashlib.sha256()
+    for p in srcs:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    if vals.get("kernel_source_sha256_16") != h.hexdigest()[:16]:
         return None
     try:
         return int(float(vals["dram_bytes_per_launch"]))
