@@ -57,6 +57,7 @@ typedef enum pkv_dtype { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 } pkv_dtype;
 #define PKV_DEV_ERR_BLOCK 4u    /* decode: block-table entry outside [0, num_blocks) */
 #define PKV_DEV_ERR_LENGTH 8u   /* decode: context length < 0 or > the table / max_context_len */
 #define PKV_DEV_ERR_TIMEOUT 16u /* decode: a wait for a tile copy exceeded its time limit */
+#define PKV_DEV_ERR_SMEM 32u    /* decode: shared memory not 1024-byte aligned; kernel did nothing */
 
 /*
  * pkv_write_cache -- the write path [P1 "The write path: slot mapping and

@@ -18,7 +18,7 @@ from . import build as _build
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA = range(5)
 PKV_F32, PKV_F16, PKV_BF16 = 0, 1, 2
 PARTITION_BALANCED = -1  # partition_size selecting the library's balanced split
-DEV_ERR_SLOT, DEV_ERR_PAIR, DEV_ERR_BLOCK, DEV_ERR_LENGTH, DEV_ERR_TIMEOUT = 1, 2, 4, 8, 16
+DEV_ERR_SLOT, DEV_ERR_PAIR, DEV_ERR_BLOCK, DEV_ERR_LENGTH, DEV_ERR_TIMEOUT, DEV_ERR_SMEM = 1, 2, 4, 8, 16, 32
 
 _DTYPES = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
 _KV_DTYPES = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}

@@ -162,7 +162,7 @@ WorkspaceLayout decode_layout(int num_seqs, int num_q_heads, int head_dim, int m
                               int sm_count, int* max_parts_out) {
   if (partition_size == PKV_PARTITION_BALANCED) {
     *max_parts_out = 1;
-    const int64_t warps = static_cast<int64_t>(sm_count) * balanced_warps_per_cta(head_dim);
+    const int64_t warps = static_cast<int64_t>(sm_count) * balanced_warps_per_cta(head_dim, num_seqs);
     return balanced_workspace_layout(num_seqs, num_q_heads, head_dim, warps);
   }
   int ps = 0;

@@ -18,8 +18,10 @@
 //    all G <= 8 query heads of its KV head: every K/V byte is read once.
 //  * Data movement: TMA (cp.async.bulk.tensor.3d, 128-byte swizzle) copies
 //    one (block, head) tile of K and of V per stage into a per-warp ring of
-//    NST stages completing on mbarriers.  Many small CTAs per SM (14 warps
-//    at D = 128) keep ~220 KB of tiles in flight per SM.
+//    NST stages completing on mbarriers.  Six 2-warp CTAs per SM (12 warps
+//    at D = 128, 2 stages each) keep 24 tiles = 192 KB in flight per SM.
+//    CTA widths that divide H_kv keep a CTA's warps on units of one (s, p):
+//    wider CTAs mixing unit sizes hold shared memory for their slowest warp.
 //  * Math: tensor-core mma.sync (see WarpAttention in pkv_device.cuh).
 //  * Waits are bounded by %globaltimer; on timeout a warp drains its copies,
 //    sets PKV_DEV_ERR_TIMEOUT and returns.  Table entries are range-checked;
@@ -36,10 +38,10 @@ __global__ void __launch_bounds__(NW * 32) decode_partitions_kernel(
     const DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
     const __grid_constant__ CUtensorMap tmap_v) {
   using Geom = TileGeom<D>;
-  extern __shared__ uint8_t smem_dyn[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   griddep_wait();  // every input may come from the previous kernel on the stream
   griddep_launch_dependents();
+  if (smem_misaligned(smem, a.dev_status)) return;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -55,31 +57,37 @@ __global__ void __launch_bounds__(NW * 32) decode_partitions_kernel(
   const int s = static_cast<int>(rest % a.num_seqs);
   const int part = a.max_parts - 1 - static_cast<int>(rest / a.num_seqs);
 
-  const int L = clamped_len(a, s, part == 0 && g == 0 && lane == 0);
   const int PS = a.partition_size;
+  const int G = a.group;
+  const int tok0 = part * PS;
+  // Block-table entries of this partition, 32 per register chunk, and the
+  // query rows do not depend on the sequence length: their loads go out
+  // together with the length's (entries within the table row are always
+  // readable; those past the sequence are never used).
+  const int blk0 = tok0 / kBlockSize;
+  const int32_t* tbl = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + blk0;
+  const int row_left = a.max_blocks_per_seq - blk0;
+  int phys_cur = (lane < row_left) ? __ldg(tbl + lane) : 0;
+  int phys_next = (32 + lane < row_left) ? __ldg(tbl + 32 + lane) : 0;
+  WarpAttention<D, BF16> at;
+  at.load_q(a.q + (static_cast<int64_t>(s) * a.num_q_heads + g * G) * D, G, lane);
+
+  const int L = clamped_len(a, s, part == 0 && g == 0 && lane == 0);
   const int nparts = L > 0 ? (L + PS - 1) / PS : 1;
   if (part >= nparts) return;
-  const int tok0 = part * PS;
   const int ntok = max(0, min(L - tok0, PS));
   const int nblk = (ntok + kBlockSize - 1) / kBlockSize;
-  const int G = a.group;
 
   WarpRing<D, NST> ring{smem_u32(smem + static_cast<size_t>(warp) * NST * Geom::kStageBytes),
                         smem_u32(smem + static_cast<size_t>(NW) * NST * Geom::kStageBytes) + 8 * NST * warp};
   ring.init(lane);
-
-  // Block-table entries of this partition, 32 per register chunk; the next
-  // chunk is fetched one chunk ahead of use.
-  const int32_t* tbl = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + tok0 / kBlockSize;
-  int phys_cur = (lane < nblk) ? __ldg(tbl + lane) : 0;
-  int phys_next = (32 + lane < nblk) ? __ldg(tbl + 32 + lane) : 0;
   uint32_t bad_stage = 0;  // bit st: the tile in stage st came from an invalid entry
 
   auto issue = [&](int j) {  // all lanes call
     if ((j & 31) == 0 && j > 0) {
       phys_cur = phys_next;
       const int nx = j + 32 + lane;
-      phys_next = (nx < nblk) ? __ldg(tbl + nx) : 0;
+      phys_next = (nx < min(nblk, row_left)) ? __ldg(tbl + nx) : 0;
     }
     const int st = j % NST;
     int phys = __shfl_sync(kFull, phys_cur, j & 31);
@@ -93,9 +101,7 @@ __global__ void __launch_bounds__(NW * 32) decode_partitions_kernel(
     ring.issue(j, phys, g, &tmap_k, &tmap_v, lane);
   };
 
-  WarpAttention<D, BF16> at;
   at.reset();
-  at.load_q(a.q + (static_cast<int64_t>(s) * a.num_q_heads + g * G) * D, G, lane);
   for (int j = 0; j < min(nblk, NST); ++j) issue(j);
 
   for (int i = 0; i < nblk; ++i) {
@@ -130,32 +136,39 @@ __device__ __forceinline__ int parts_of(const DecodeArgs& a, int s) {
   return L > 0 ? (L + a.partition_size - 1) / a.partition_size : 1;
 }
 
-constexpr int kReduceWarps = 8;
-constexpr int kLongReduceWarps = 16;
 
-// Few partitions per row: one warp per (sequence, query head) row, a CTA
-// holding kReduceWarps rows.  Rows of sequences that fit one partition
-// return at once (the partition kernel wrote their output).
+// Few partitions per row: one warp per (sequence, query head) row, CTAs of
+// kRowsPerCta warps over consecutive heads of one sequence (grid S x
+// ceil(H_q / kRowsPerCta)).  A sequence that fits one partition costs one
+// length load: the partition kernel already wrote its output.  Small CTAs
+// with a register cap keep ~48 warps resident per SM, so rows of different
+// sequences merge concurrently.
+constexpr int kRowsPerCta = 8;
+
 template <int D>
-__global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_rows_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kRowsPerCta * 32, 6) decode_reduce_rows_kernel(const DecodeArgs a) {
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kReduceWarps + warp;
-  if (row >= static_cast<int64_t>(a.num_seqs) * a.num_q_heads) return;
-  const int nparts = parts_of(a, static_cast<int>(row / a.num_q_heads));
+  const int s = blockIdx.x;
+  const int h = blockIdx.y * kRowsPerCta + warp;
+  if (h >= a.num_q_heads) return;
+  const int nparts = parts_of(a, s);
   if (nparts <= 1) return;
-  RowMerge<D> r;
+  const int64_t row = static_cast<int64_t>(s) * a.num_q_heads + h;
+  RowMerge<D, 4> r;
   const int64_t rec0 = row * a.max_parts;
-  r.run(a.ws_ml, a.ws_acc + lane * RowMerge<D>::EPL, 0, 1, nparts, [&](int k) { return rec0 + k; });
+  r.run(a.ws_ml, a.ws_acc + lane * RowMerge<D, 4>::EPL, 0, 1, nparts, [&](int k) { return rec0 + k; });
   r.store(a.out, row, a.out_dtype, lane);
 }
 
-// Many partitions per row (long contexts): one CTA per row; warp w merges
-// partitions w, w + kLongReduceWarps, ... and the warps' states are merged
-// through shared memory.
+// Many partitions per row (long contexts): one CTA of 16 warps per row (two
+// CTAs per SM); warp w merges partitions w, w + 16, ... in batches of 8 and
+// the warps' states are merged through shared memory.
+constexpr int kLongReduceWarps = 16;
+
 template <int D>
-__global__ void __launch_bounds__(kLongReduceWarps * 32) decode_reduce_long_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kLongReduceWarps * 32, 2) decode_reduce_long_kernel(const DecodeArgs a) {
   __shared__ float sm_m[kLongReduceWarps], sm_l[kLongReduceWarps];
   __shared__ float sm_o[kLongReduceWarps][D];
   griddep_wait();
@@ -206,7 +219,7 @@ cudaError_t launch_partitions_t(const DecodeArgs& a, const CUtensorMap& tk, cons
                                 cudaStream_t stream) {
   using Geom = TileGeom<D>;
   constexpr int NW = kWarpsPerCta, NST = kStages;
-  const size_t smem = 1024 + static_cast<size_t>(NW) * NST * Geom::kStageBytes + NW * NST * 8;
+  const size_t smem = static_cast<size_t>(NW) * NST * Geom::kStageBytes + NW * NST * 8;
   auto kern = decode_partitions_kernel<D, BF16, NW, NST>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
@@ -232,14 +245,14 @@ cudaError_t launch_decode_partitions(const DecodeArgs& a, const CUtensorMap& tma
 cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t stream) {
   if (a.max_parts <= 1 || a.num_seqs == 0) return cudaSuccess;
   const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
-  const dim3 block(kReduceWarps * 32);
-  if (a.max_parts > 4 * RowMerge<128>::U) {  // long rows: a CTA per row
+  if (a.max_parts > 2 * RowMerge<128>::U_batch()) {  // long rows: a CTA per row
     const dim3 grid(static_cast<unsigned>(rows)), block(kLongReduceWarps * 32);
     if (head_dim == 128) return launch_pdl(decode_reduce_long_kernel<128>, grid, block, 0, stream, a);
     if (head_dim == 64) return launch_pdl(decode_reduce_long_kernel<64>, grid, block, 0, stream, a);
     return cudaErrorInvalidValue;
   }
-  const dim3 grid(static_cast<unsigned>((rows + kReduceWarps - 1) / kReduceWarps));
+  const dim3 grid(static_cast<unsigned>(a.num_seqs), static_cast<unsigned>((a.num_q_heads + kRowsPerCta - 1) / kRowsPerCta));
+  const dim3 block(32 * kRowsPerCta);
   if (head_dim == 128) return launch_pdl(decode_reduce_rows_kernel<128>, grid, block, 0, stream, a);
   if (head_dim == 64) return launch_pdl(decode_reduce_rows_kernel<64>, grid, block, 0, stream, a);
   return cudaErrorInvalidValue;

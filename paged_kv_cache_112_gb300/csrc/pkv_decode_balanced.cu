@@ -84,16 +84,16 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     const DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
     const __grid_constant__ CUtensorMap tmap_v) {
   using Geom = TileGeom<D>;
-  extern __shared__ uint8_t smem_dyn[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   const size_t ring_bytes = static_cast<size_t>(NW) * NST * Geom::kStageBytes;
   const uint32_t bars = smem_u32(smem + ring_bytes);
   int* pre = reinterpret_cast<int*>(smem + ring_bytes + NW * NST * 8);  // [S + 1] tile prefix
   int* len = pre + a.num_seqs + 1;                                       // [S] clamped lengths
-  __shared__ int warp_tot[32];
+  int* warp_tot = len + a.num_seqs;                                      // [32] scan scratch
 
   griddep_wait();  // every input may come from the previous kernel on the stream
   griddep_launch_dependents();
+  if (smem_misaligned(smem, a.dev_status)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.num_seqs, Hkv = a.num_kv_heads, G = a.group;
 
@@ -229,61 +229,78 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
   }
 }
 
-// Reduce for the balanced split: one warp per (sequence, query head) row.
-// Rows of pairs a single warp covered return at once; rows of empty
-// sequences are written as zeros here (no warp visits them).
-constexpr int kReduceWarps = 8;
+// Reduce for the balanced split: one warp per (sequence, query head) row,
+// CTAs of kRowsPerCta warps over one sequence's heads (grid S x
+// ceil(H_q / kRowsPerCta)), register-capped so ~48 warps stay resident per
+// SM.  Rows of pairs a single warp covered return at once; rows of empty
+// sequences are written as zeros here (no warp visits them).  The pair
+// metadata and the length are loaded together (the metadata slot is always
+// readable; it is only trusted when the sequence is non-empty).
+constexpr int kRowsPerCta = 8;
 
 template <int D>
-__global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_balanced_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kRowsPerCta * 32, 6) decode_reduce_balanced_kernel(const DecodeArgs a) {
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kReduceWarps + warp;
-  if (row >= static_cast<int64_t>(a.num_seqs) * a.num_q_heads) return;
-  const int s = static_cast<int>(row / a.num_q_heads);
-  const int h = static_cast<int>(row % a.num_q_heads);
+  const int s = blockIdx.x;
+  const int h = blockIdx.y * kRowsPerCta + warp;
+  if (h >= a.num_q_heads) return;
   const int G = a.group, g = h / G, hh = h % G;
+  const int2 meta = a.ws_meta[static_cast<int64_t>(s) * a.num_kv_heads + g];
   const int L = clamped_len(a, s, false);
-  RowMerge<D> r;
+  const int64_t row = static_cast<int64_t>(s) * a.num_q_heads + h;
+  RowMerge<D, 4> r;
   if (L > 0) {
-    const int2 meta = a.ws_meta[static_cast<int64_t>(s) * a.num_kv_heads + g];
     const int pieces = meta.y >> 1, first_slot = meta.y & 1, w0 = meta.x;
     if (pieces == 0) return;
-    r.run(a.ws_ml, a.ws_acc + lane * RowMerge<D>::EPL, 0, 1, pieces, [&](int k) {
+    r.run(a.ws_ml, a.ws_acc + lane * RowMerge<D, 4>::EPL, 0, 1, pieces, [&](int k) {
       return (static_cast<int64_t>(w0 + k) * 2 + (k == 0 ? first_slot : 0)) * G + hh;
     });
   }
   r.store(a.out, row, a.out_dtype, lane);
 }
 
-template <int D>
-constexpr int balanced_warps() { return 12; }
+// Shared memory of one balanced CTA: the warps' rings and barriers, then the
+// per-sequence tile prefix and lengths and the scan scratch (no static
+// shared memory, so the dynamic window starts 1024-byte aligned).
+constexpr size_t kMaxSmemPerCta = 232448;  // sm_100-class opt-in limit (227 KB)
+
 template <int D>
 constexpr int balanced_stages() { return D == 128 ? 2 : 4; }
 
-template <int D, bool BF16>
-cudaError_t launch_balanced_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                              cudaStream_t stream) {
-  constexpr int NW = balanced_warps<D>(), NST = balanced_stages<D>();
-  auto kern = decode_balanced_kernel<D, BF16, NW, NST>;
-  const size_t smem = balanced_smem_bytes(D, a.num_seqs);
+size_t balanced_smem_for(int head_dim, int nw, int num_seqs) {
+  const int nst = head_dim == 128 ? balanced_stages<128>() : balanced_stages<64>();
+  const size_t stage = 2 * static_cast<size_t>(kBlockSize) * head_dim * 2;
+  return nw * nst * stage + nw * nst * 8 + (2 * static_cast<size_t>(num_seqs) + 1 + 32) * sizeof(int);
+}
+
+template <int D, bool BF16, int NW>
+cudaError_t launch_balanced_nw(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                               cudaStream_t stream) {
+  auto kern = decode_balanced_kernel<D, BF16, NW, balanced_stages<D>()>;
+  const size_t smem = balanced_smem_for(D, NW, a.num_seqs);
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(a.balanced_ctas), dim3(NW * 32), smem, stream, a, tk, tv);
 }
 
+template <int D, bool BF16>
+cudaError_t launch_balanced_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                              cudaStream_t stream) {
+  if (balanced_warps_per_cta(D, a.num_seqs) == 14) return launch_balanced_nw<D, BF16, 14>(a, tk, tv, stream);
+  return launch_balanced_nw<D, BF16, 12>(a, tk, tv, stream);
+}
+
 }  // namespace
 
-int balanced_warps_per_cta(int head_dim) {
-  return head_dim == 128 ? balanced_warps<128>() : balanced_warps<64>();
+// 14 warps when their rings and the per-sequence arrays fit one CTA, else 12.
+int balanced_warps_per_cta(int head_dim, int num_seqs) {
+  return balanced_smem_for(head_dim, 14, num_seqs) <= kMaxSmemPerCta ? 14 : 12;
 }
 
 size_t balanced_smem_bytes(int head_dim, int num_seqs) {
-  const int nw = balanced_warps_per_cta(head_dim);
-  const int nst = head_dim == 128 ? balanced_stages<128>() : balanced_stages<64>();
-  const size_t stage = 2 * static_cast<size_t>(kBlockSize) * head_dim * 2;
-  return 1024 + nw * nst * stage + nw * nst * 8 + (2 * static_cast<size_t>(num_seqs) + 1) * sizeof(int);
+  return balanced_smem_for(head_dim, balanced_warps_per_cta(head_dim, num_seqs), num_seqs);
 }
 
 cudaError_t launch_decode_balanced(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
@@ -300,8 +317,9 @@ cudaError_t launch_decode_balanced(const DecodeArgs& a, const CUtensorMap& tmap_
 
 cudaError_t launch_decode_reduce_balanced(const DecodeArgs& a, int head_dim, cudaStream_t stream) {
   if (a.num_seqs == 0) return cudaSuccess;
-  const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
-  const dim3 grid(static_cast<unsigned>((rows + kReduceWarps - 1) / kReduceWarps)), block(kReduceWarps * 32);
+  const dim3 grid(static_cast<unsigned>(a.num_seqs),
+                  static_cast<unsigned>((a.num_q_heads + kRowsPerCta - 1) / kRowsPerCta));
+  const dim3 block(32 * kRowsPerCta);
   if (head_dim == 128) return launch_pdl(decode_reduce_balanced_kernel<128>, grid, block, 0, stream, a);
   if (head_dim == 64) return launch_pdl(decode_reduce_balanced_kernel<64>, grid, block, 0, stream, a);
   return cudaErrorInvalidValue;

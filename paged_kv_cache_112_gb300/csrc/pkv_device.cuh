@@ -158,6 +158,15 @@ __device__ __forceinline__ int clamped_len(const DecodeArgs& a, int s, bool repo
   return L < 0 ? 0 : cap;
 }
 
+// The dynamic shared-memory window starts 1024-byte aligned (the TMA 128-byte
+// swizzle pattern is a function of address bits 4-9).  Kernels check it and,
+// should it ever not hold, flag PKV_DEV_ERR_SMEM and do nothing.
+__device__ __forceinline__ bool smem_misaligned(const void* base, int32_t* status) {
+  if ((smem_u32(base) & 1023u) == 0) return false;
+  if (threadIdx.x == 0) flag(status, 32u);
+  return true;
+}
+
 // ------------------------------------------------------------- tile geometry
 
 // One pipeline stage holds a (block, KV head) tile of K and one of V: 16
@@ -399,10 +408,10 @@ struct WarpAttention {
 // Merges partial states of one output row:
 //     M' = max(M, m_p),  O' = O 2^(M-M') + acc_p 2^(m_p-M'),  l' likewise,
 // lane j owning output elements [EPL*j, EPL*j + EPL).
-template <int D>
+template <int D, int U = 8>  // U: records whose loads are issued together
 struct RowMerge {
   static constexpr int EPL = D / 32;
-  static constexpr int U = 8;  // records whose loads are issued together
+  static constexpr int U_batch() { return U; }
   float M = kNegInf, den = 0.f, o[EPL] = {};
 
   __device__ __forceinline__ void add(float m, float l, const float (&v)[EPL]) {

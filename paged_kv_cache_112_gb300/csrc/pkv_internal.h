@@ -78,7 +78,7 @@ cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
 
 // Balanced split geometry (pkv_decode_balanced.cu).
 constexpr int kBalancedMaxSeqs = 4096;
-int balanced_warps_per_cta(int head_dim);
+int balanced_warps_per_cta(int head_dim, int num_seqs);
 size_t balanced_smem_bytes(int head_dim, int num_seqs);
 
 // Launches `kernel` with programmatic stream serialisation allowed: it may
