@@ -1,8 +1,10 @@
 """Benchmark of one paged decode step on GB300.
 
 A step = the whole hot path over one batch: copy-on-write block copies (when
-the workload has any), write_cache of one new token per sequence, then decode
-attention (partition kernel + reduce kernel).  Default workload: the 8B-class
+the workload has any), the write of one new token per sequence and decode
+attention (partition kernel + reduce kernel).  By default the write is fused
+into the partition kernel (pkv_decode_step); --unfused runs pkv_write_cache
+and pkv_decode_attention as separate calls.  Default workload: the 8B-class
 GQA decode layer (64 sequences, 32 query / 8 KV heads, head_dim 128, bf16,
 context lengths uniform in [128, 2048], blocks scattered over a pool 1.25x
 the need).  Inputs are synthetic, seeded, N(0,1).
@@ -184,23 +186,29 @@ def run_gpu(args):
     replicas = args.replicas or max(1, math.ceil(4 * l2 / pool_bytes))
     pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(replicas - 1)]
     max_len = wl.max_context_len
-    n_launch = 1 + 1 + (1 if pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, max_len, ps)
-                        else 0) + (1 if pairs.shape[0] else 0)
+    n_launch = (1 if args.unfused else 0) + 1 + (1 if ws_bytes else 0) + (1 if pairs.shape[0] else 0)
 
     def step(i, ev=None):
         kp, vp = pools[i % replicas]
         if pairs.shape[0]:
             pkv.copy_blocks(kp, vp, pairs, status=status)
-        pkv.write_cache(k_new, v_new, kp, vp, sm, status=status)
-        if ev is not None:
-            ev[0].record()
-        pkv.decode_partitions(out, q, kp, vp, bt, cl, wl.scale, partition_size=ps, max_context_len=max_len,
-                              workspace=ws, status=status)
+        if not args.unfused:  # the new token's write fused into the partition kernel
+            if ev is not None:
+                ev[0].record()
+            pkv.decode_step_partitions(out, q, k_new, v_new, kp, vp, bt, cl, sm, wl.scale, partition_size=ps,
+                                       max_context_len=max_len, workspace=ws, status=status)
+        else:
+            pkv.write_cache(k_new, v_new, kp, vp, sm, status=status)
+            if ev is not None:
+                ev[0].record()
+            pkv.decode_partitions(out, q, kp, vp, bt, cl, wl.scale, partition_size=ps, max_context_len=max_len,
+                                  workspace=ws, status=status)
         if ev is not None:
             ev[1].record()
         if ws is not None:
-            pkv.decode_reduce(out, cl, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim, partition_size=ps,
-                              max_context_len=max_len, workspace=ws, status=status)
+            pkv.decode_reduce(out, cl, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
+                              head_dim=wl.head_dim, partition_size=ps, max_context_len=max_len, workspace=ws,
+                              status=status)
 
     nb = step_bytes(wl)
     K, W = args.steps, args.warmup
@@ -293,6 +301,7 @@ def run_gpu(args):
                    "partition_size": ps, "max_context_len": max_len, "total_context_tokens":
                    int(wl.context_lens.astype(np.int64).sum()), "num_blocks": wl.num_blocks,
                    "cow_pairs": int(wl.copy_pairs.shape[0]), "out_dtype": "f32",
+                   "entry": "pkv_write_cache + pkv_decode_attention" if args.unfused else "pkv_decode_step",
                    "l2": f"inputs larger than L2: {replicas} pool replicas of {pool_bytes / 1e6:.0f} MB rotated "
                          f"(L2 {l2 / 1e6:.0f} MB)", "parallelism": f"replicas x{world}"},
         "pct_of_hbm_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
@@ -445,6 +454,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="run write_cache and decode attention as separate calls instead of pkv_decode_step")
     args = ap.parse_args(argv)
     if args.steps is None:
         args.steps = 5000 if args.impl == "ours" else 20

@@ -185,6 +185,46 @@ pkv_status pkv_decode_reduce(void* out, const int32_t* context_lens, int num_seq
                              int32_t* dev_status, void* stream);
 
 /*
+ * pkv_decode_step -- one decode step in one call: the write path of the token
+ * generated this step for every sequence, then decode attention over the
+ * history including it ([P1 "The write path"; P3 "End-to-end flow"]).  For
+ * every sequence s with slot_mapping[s] equal to the slot of position
+ * L-1 = context_lens[s]-1 through its block table, the result equals
+ * pkv_write_cache (one token per sequence, rows k_new[s], v_new[s]) followed
+ * by pkv_decode_attention; the write is fused into the attention kernel:
+ * the warp that reads the tile holding position L-1 stores the new rows to
+ * the pools and uses them directly, so no separate write kernel runs.
+ * slot_mapping[s] == -1 means sequence s adds no token this step.  Any other
+ * slot (a token not at the end of its sequence, as in chunked prefill) sets
+ * PKV_DEV_ERR_SLOT and is not written: use pkv_write_cache for those.
+ *   k_new, v_new : [num_seqs][num_kv_heads][head_dim], consecutive sequences
+ *                  new_row_stride elements apart (0 = dense), rows 16-byte
+ *                  aligned.
+ *   k_pool, v_pool : pools (read and written).
+ *   other arguments as in pkv_decode_attention.
+ * pkv_decode_step_partitions is its first kernel alone (follow it with
+ * pkv_decode_reduce, as for pkv_decode_partitions).
+ */
+pkv_status pkv_decode_step(void* out, const void* q, const void* k_new, const void* v_new,
+                           int64_t new_row_stride, void* k_pool, void* v_pool,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, const int32_t* slot_mapping, int num_seqs,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           int num_blocks, float scale, int partition_size, int max_context_len,
+                           void* workspace, size_t workspace_bytes, pkv_dtype kv_dtype,
+                           pkv_dtype out_dtype, int32_t* dev_status, void* stream);
+
+pkv_status pkv_decode_step_partitions(void* out, const void* q, const void* k_new, const void* v_new,
+                                      int64_t new_row_stride, void* k_pool, void* v_pool,
+                                      const int32_t* block_tables, int max_blocks_per_seq,
+                                      const int32_t* context_lens, const int32_t* slot_mapping,
+                                      int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                      int block_size, int num_blocks, float scale, int partition_size,
+                                      int max_context_len, void* workspace, size_t workspace_bytes,
+                                      pkv_dtype kv_dtype, pkv_dtype out_dtype, int32_t* dev_status,
+                                      void* stream);
+
+/*
  * pkv_decode_attention_static_workspace -- pkv_decode_attention for callers
  * that cannot allocate device memory when they run decode (for example
  * plugins whose host framework owns all device memory and forbids

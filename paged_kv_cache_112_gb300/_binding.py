@@ -39,6 +39,10 @@ _SIGS = {
     "pkv_version": [],
 }
 _SIGS["pkv_decode_partitions"] = _SIGS["pkv_decode_attention"]
+_SIGS["pkv_decode_step"] = ([_c_void_p] * 4 + [_c_int64] + [_c_void_p] * 3 + [_c_int] + [_c_void_p] * 2 +
+                            [_c_int] * 6 + [_c_float, _c_int, _c_int, _c_void_p, _c_size_t, _c_int, _c_int,
+                                            _c_void_p, _c_void_p])
+_SIGS["pkv_decode_step_partitions"] = _SIGS["pkv_decode_step"]
 
 _LIB = None
 
@@ -171,3 +175,38 @@ def decode_reduce(out, context_lens, *, num_q_heads, num_kv_heads, head_dim, par
                                     num_kv_heads, head_dim, int(partition_size), int(max_context_len),
                                     _ptr(workspace), ws_bytes, _DTYPES[out.dtype], _ptr(status), _stream(stream)),
            "pkv_decode_reduce")
+
+
+def _step_args(out, q, k_new, v_new, k_pool, v_pool, block_tables, context_lens, slot_mapping, scale,
+               partition_size, max_context_len, workspace, status, stream):
+    base = _decode_args(out, q, k_pool, v_pool, block_tables, context_lens, scale, partition_size,
+                        max_context_len, workspace, status, stream)
+    _need_cuda(slot_mapping)
+    NB, B, Hkv, D = k_pool.shape
+    for t in (k_new, v_new):
+        if not t.is_cuda or t.dim() != 3 or t.shape != (q.shape[0], Hkv, D) or t.stride(2) != 1 or t.stride(1) != D:
+            raise PkvError("k_new/v_new must be CUDA [S, H_kv, D] with dense rows")
+    if k_new.stride(0) != v_new.stride(0) or k_new.dtype != k_pool.dtype or v_new.dtype != k_pool.dtype:
+        raise PkvError("k_new and v_new must share a row stride and the pools' dtype")
+    if slot_mapping.dtype != torch.int32 or slot_mapping.shape != (q.shape[0],):
+        raise PkvError("slot_mapping must be int32 [S]")
+    (o, qp, kp, vp, bt, maxb, cl, S, Hq, Hkv_, D_, B_, NB_, sc, ps, mcl, ws, wsb, kvd, od, st, strm) = base
+    return (o, qp, _ptr(k_new), _ptr(v_new), int(k_new.stride(0)), kp, vp, bt, maxb, cl, _ptr(slot_mapping), S, Hq,
+            Hkv_, D_, B_, NB_, sc, ps, mcl, ws, wsb, kvd, od, st, strm)
+
+
+def decode_step(out, q, k_new, v_new, k_pool, v_pool, block_tables, context_lens, slot_mapping, scale, *,
+                partition_size=0, max_context_len, workspace=None, status=None, stream=None):
+    """pkv_decode_step: write of the new token fused into decode attention, then the reduce."""
+    _check(load().pkv_decode_step(*_step_args(out, q, k_new, v_new, k_pool, v_pool, block_tables, context_lens,
+                                              slot_mapping, scale, partition_size, max_context_len, workspace,
+                                              status, stream)), "pkv_decode_step")
+
+
+def decode_step_partitions(out, q, k_new, v_new, k_pool, v_pool, block_tables, context_lens, slot_mapping, scale, *,
+                           partition_size=0, max_context_len, workspace=None, status=None, stream=None):
+    """pkv_decode_step_partitions: the first kernel of decode_step alone."""
+    _check(load().pkv_decode_step_partitions(*_step_args(out, q, k_new, v_new, k_pool, v_pool, block_tables,
+                                                         context_lens, slot_mapping, scale, partition_size,
+                                                         max_context_len, workspace, status, stream)),
+           "pkv_decode_step_partitions")

@@ -208,6 +208,7 @@ pkv_status prepare_decode(DecodeCall* c, void* out, const void* q, const void* k
   if (ws.total > 0 && (!workspace || workspace_bytes < ws.total || !aligned(workspace, 16)))
     return PKV_ERR_WORKSPACE;
 
+  c->args = DecodeArgs{};  // every field not set below (the fused-step ones) is zero / null
   DecodeArgs& a = c->args;
   a.out = out;
   a.q = static_cast<const uint16_t*>(q);
@@ -263,7 +264,7 @@ pkv_status pkv_write_cache(const void* k_new, const void* v_new, void* k_pool, v
   if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
       !aligned(slot_mapping, 4))
     return PKV_ERR_INVALID_ARG;
-  WriteCacheArgs a;
+  WriteCacheArgs a{};
   a.k_new = static_cast<const uint16_t*>(k_new);
   a.v_new = static_cast<const uint16_t*>(v_new);
   a.k_pool = static_cast<uint16_t*>(k_pool);
@@ -288,7 +289,7 @@ pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int
   if (num_pairs == 0) return PKV_OK;
   if (!k_pool || !v_pool || !pairs) return PKV_ERR_INVALID_ARG;
   if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(pairs, 4)) return PKV_ERR_INVALID_ARG;
-  CopyBlocksArgs a;
+  CopyBlocksArgs a{};
   a.k_pool = static_cast<uint16_t*>(k_pool);
   a.v_pool = static_cast<uint16_t*>(v_pool);
   a.pairs = pairs;
@@ -317,7 +318,7 @@ pkv_status pkv_decode_partitions(void* out, const void* q, const void* k_pool, c
                                  int num_blocks, float scale, int partition_size, int max_context_len,
                                  void* workspace, size_t workspace_bytes, pkv_dtype kv_dtype, pkv_dtype out_dtype,
                                  int32_t* dev_status, void* stream) {
-  DecodeCall c;
+  DecodeCall c{};
   pkv_status st = prepare_decode(&c, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
                                  num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                                  partition_size, max_context_len, workspace, workspace_bytes, kv_dtype, out_dtype,
@@ -374,6 +375,56 @@ pkv_status pkv_decode_reduce(void* out, const int32_t* context_lens, int num_seq
   const cudaError_t e = balanced ? launch_decode_reduce_balanced(a, head_dim, static_cast<cudaStream_t>(stream))
                                  : launch_decode_reduce(a, head_dim, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_decode_step_partitions(void* out, const void* q, const void* k_new, const void* v_new,
+                                      int64_t new_row_stride, void* k_pool, void* v_pool,
+                                      const int32_t* block_tables, int max_blocks_per_seq,
+                                      const int32_t* context_lens, const int32_t* slot_mapping, int num_seqs,
+                                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                      int num_blocks, float scale, int partition_size, int max_context_len,
+                                      void* workspace, size_t workspace_bytes, pkv_dtype kv_dtype,
+                                      pkv_dtype out_dtype, int32_t* dev_status, void* stream) {
+  DecodeCall c{};
+  pkv_status st = prepare_decode(&c, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+                                 num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                                 partition_size, max_context_len, workspace, workspace_bytes, kv_dtype, out_dtype,
+                                 dev_status, true);
+  if (st != PKV_OK || num_seqs == 0) return st;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  const int64_t stride = new_row_stride ? new_row_stride : row;
+  if (!k_new || !v_new || !slot_mapping || new_row_stride < 0 || stride < row || stride % 8 != 0 ||
+      !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 4))
+    return PKV_ERR_INVALID_ARG;
+  DecodeArgs& a = c.args;
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.new_stride = stride;
+  a.slot_mapping = slot_mapping;
+  a.k_pool_w = static_cast<uint16_t*>(k_pool);
+  a.v_pool_w = static_cast<uint16_t*>(v_pool);
+  const cudaError_t e = a.balanced_ctas ? launch_decode_balanced(a, c.tmap_k, c.tmap_v, head_dim,
+                                                                kv_dtype == PKV_BF16, static_cast<cudaStream_t>(stream))
+                                        : launch_decode_partitions(a, c.tmap_k, c.tmap_v, head_dim,
+                                                                   kv_dtype == PKV_BF16,
+                                                                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_decode_step(void* out, const void* q, const void* k_new, const void* v_new, int64_t new_row_stride,
+                           void* k_pool, void* v_pool, const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, const int32_t* slot_mapping, int num_seqs, int num_q_heads,
+                           int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                           int partition_size, int max_context_len, void* workspace, size_t workspace_bytes,
+                           pkv_dtype kv_dtype, pkv_dtype out_dtype, int32_t* dev_status, void* stream) {
+  pkv_status st = pkv_decode_step_partitions(out, q, k_new, v_new, new_row_stride, k_pool, v_pool, block_tables,
+                                             max_blocks_per_seq, context_lens, slot_mapping, num_seqs, num_q_heads,
+                                             num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size,
+                                             max_context_len, workspace, workspace_bytes, kv_dtype, out_dtype,
+                                             dev_status, stream);
+  if (st != PKV_OK) return st;
+  return pkv_decode_reduce(out, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, partition_size,
+                           max_context_len, workspace, workspace_bytes, out_dtype, dev_status, stream);
 }
 
 pkv_status pkv_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,

@@ -33,7 +33,7 @@ namespace {
 
 using namespace dev;
 
-template <int D, bool BF16, int NW, int NST>
+template <int D, bool BF16, int NW, int NST, bool FUSED>
 __global__ void __launch_bounds__(NW * 32) decode_partitions_kernel(
     const DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
     const __grid_constant__ CUtensorMap tmap_v) {
@@ -104,6 +104,14 @@ __global__ void __launch_bounds__(NW * 32) decode_partitions_kernel(
   at.reset();
   for (int j = 0; j < min(nblk, NST); ++j) issue(j);
 
+  // Fused decode step: the last partition of (s, g) holds position L-1.
+  NewToken<D> nt;
+  const bool owns_new = FUSED && part == nparts - 1;
+  if (owns_new) {
+    nt.prefetch(a, s, g, L, lane);
+    if (nblk == 0) nt.commit(a, g, lane);  // empty sequence: only checks the slot
+  }
+
   for (int i = 0; i < nblk; ++i) {
     if (!__all_sync(kFull, ring.wait(i, a.timeout_ns))) {
       ring.drain(i, min(nblk, i + NST), a.timeout_ns);
@@ -113,6 +121,7 @@ __global__ void __launch_bounds__(NW * 32) decode_partitions_kernel(
     const int st = i % NST;
     const int nv = ((bad_stage >> st) & 1) ? 0 : min(kBlockSize, ntok - i * kBlockSize);
     const uint32_t sK = ring.k_tile(i);
+    if (owns_new && i == nblk - 1 && nt.commit(a, g, lane)) nt.patch(sK, sK + Geom::kTileBytes, lane);
     at.tile(sK, sK + Geom::kTileBytes, nv, a.scale_log2, lane);
     __syncwarp();
     if (i + NST < nblk) {
@@ -214,13 +223,13 @@ __global__ void __launch_bounds__(kLongReduceWarps * 32, 2) decode_reduce_long_k
 constexpr int kWarpsPerCta = PKV_WARPS_PER_CTA;
 constexpr int kStages = PKV_STAGES;
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool FUSED>
 cudaError_t launch_partitions_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                 cudaStream_t stream) {
   using Geom = TileGeom<D>;
   constexpr int NW = kWarpsPerCta, NST = kStages;
   const size_t smem = static_cast<size_t>(NW) * NST * Geom::kStageBytes + NW * NST * 8;
-  auto kern = decode_partitions_kernel<D, BF16, NW, NST>;
+  auto kern = decode_partitions_kernel<D, BF16, NW, NST, FUSED>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const int64_t units = static_cast<int64_t>(a.num_kv_heads) * a.num_seqs * a.max_parts;
@@ -229,16 +238,23 @@ cudaError_t launch_partitions_t(const DecodeArgs& a, const CUtensorMap& tk, cons
   return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(NW * 32), smem, stream, a, tk, tv);
 }
 
+template <int D, bool BF16>
+cudaError_t launch_partitions_f(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                                cudaStream_t stream) {
+  return a.k_new ? launch_partitions_t<D, BF16, true>(a, tk, tv, stream)
+                 : launch_partitions_t<D, BF16, false>(a, tk, tv, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_decode_partitions(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                      int head_dim, int kv_bf16, cudaStream_t stream) {
   if (head_dim == 128)
-    return kv_bf16 ? launch_partitions_t<128, true>(a, tmap_k, tmap_v, stream)
-                   : launch_partitions_t<128, false>(a, tmap_k, tmap_v, stream);
+    return kv_bf16 ? launch_partitions_f<128, true>(a, tmap_k, tmap_v, stream)
+                   : launch_partitions_f<128, false>(a, tmap_k, tmap_v, stream);
   if (head_dim == 64)
-    return kv_bf16 ? launch_partitions_t<64, true>(a, tmap_k, tmap_v, stream)
-                   : launch_partitions_t<64, false>(a, tmap_k, tmap_v, stream);
+    return kv_bf16 ? launch_partitions_f<64, true>(a, tmap_k, tmap_v, stream)
+                   : launch_partitions_f<64, false>(a, tmap_k, tmap_v, stream);
   return cudaErrorInvalidValue;
 }
 

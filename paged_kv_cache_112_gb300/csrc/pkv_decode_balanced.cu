@@ -79,7 +79,7 @@ __device__ __forceinline__ void advance(Cursor& c, const int* pre, int S, int Hk
   next_pair(c, pre, S, Hkv);
 }
 
-template <int D, bool BF16, int NW, int NST>
+template <int D, bool BF16, int NW, int NST, bool FUSED>
 __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     const DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
     const __grid_constant__ CUtensorMap tmap_v) {
@@ -186,11 +186,21 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
   int seg_t0 = cc.t, seg_idx = 0;
   at.reset();
   at.load_q(a.q + (static_cast<int64_t>(cc.s) * a.num_q_heads + cc.g * G) * D, G, lane);
+  NewToken<D> nt;
+  // Fused decode step: the warp holding a pair's last tile (position L-1)
+  // owns the new token of that (s, g).
+  auto start_segment = [&](int i) {
+    if constexpr (FUSED) {
+      if (cc.t + (count - i) >= cc.n) nt.prefetch(a, cc.s, cc.g, len[cc.s], lane);
+    }
+  };
+  start_segment(0);
   for (int i = 0; i < count; ++i) {
     if (i > 0 && cc.t == 0) {  // a new (s, g) pair starts here
       seg_t0 = 0;
       at.reset();
       at.load_q(a.q + (static_cast<int64_t>(cc.s) * a.num_q_heads + cc.g * G) * D, G, lane);
+      start_segment(i);
     }
     if (!__all_sync(kFull, ring.wait(i, a.timeout_ns))) {
       ring.drain(i, min(count, i + NST), a.timeout_ns);
@@ -200,6 +210,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     const int st = i % NST;
     const int nv = ((bad_stage >> st) & 1) ? 0 : min(kBlockSize, len[cc.s] - cc.t * kBlockSize);
     const uint32_t sK = ring.k_tile(i);
+    if (FUSED && cc.t == cc.n - 1 && nt.commit(a, cc.g, lane)) nt.patch(sK, sK + Geom::kTileBytes, lane);
     at.tile(sK, sK + Geom::kTileBytes, nv, a.scale_log2, lane);
     __syncwarp();
     if (i + NST < count) {
@@ -278,7 +289,8 @@ size_t balanced_smem_for(int head_dim, int nw, int num_seqs) {
 template <int D, bool BF16, int NW>
 cudaError_t launch_balanced_nw(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream) {
-  auto kern = decode_balanced_kernel<D, BF16, NW, balanced_stages<D>()>;
+  auto kern = a.k_new ? decode_balanced_kernel<D, BF16, NW, balanced_stages<D>(), true>
+                      : decode_balanced_kernel<D, BF16, NW, balanced_stages<D>(), false>;
   const size_t smem = balanced_smem_for(D, NW, a.num_seqs);
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;

@@ -224,6 +224,76 @@ struct WarpRing {
   __device__ __forceinline__ uint32_t k_tile(int i) const { return buf + (i % NST) * Geom::kStageBytes; }
 };
 
+// ---------------------------------------------------- fused new-token write
+
+// The token generated this step, for a warp that reads the tile holding its
+// position L-1 (fused decode step).  Lanes [0, D/8) hold the 16-byte chunks
+// of the K row of KV head g, lanes [16, 16 + D/8) those of the V row.  The
+// warp stores the row to the pools (the write path, "gpu_paged_kv_cache"
+// section "The write path: slot mapping and scatter") and patches it into
+// its shared-memory tile, so the attention sees the new token without
+// waiting for the pool write.  row = offset in its block, or -1 (nothing
+// to do).
+template <int D>
+struct NewToken {
+  uint4 val;
+  int row = -1;
+  int slot = -1;
+  int last_phys = -1;
+
+  // Issues the loads (consumed only by commit(), so their latency hides
+  // behind the tiles the warp streams meanwhile).
+  __device__ __forceinline__ void prefetch(const DecodeArgs& a, int s, int g, int L, int lane) {
+    slot = a.slot_mapping[s];
+    last_phys = L > 0 ? __ldg(a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + (L - 1) / kBlockSize)
+                      : -1;
+    const int c = lane & 15;
+    const uint16_t* src = (lane < 16 ? a.k_new : a.v_new) + static_cast<int64_t>(s) * a.new_stride + g * D + c * 8;
+    val = (c < D / 8) ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
+    row = L > 0 ? (L - 1) % kBlockSize : -1;
+  }
+
+  // Checks that the slot is position L-1 through the table; if so stores the
+  // row to both pools, else flags PKV_DEV_ERR_SLOT (unless the slot is -1)
+  // and drops the token.  Returns whether the tile must be patched.
+  __device__ __forceinline__ bool commit(const DecodeArgs& a, int g, int lane) {
+    if (row < 0 || slot == -1) {
+      if (slot != -1 && lane == 0) flag(a.dev_status, 1u);  // a slot for an empty sequence
+      row = -1;
+      return false;
+    }
+    const bool ok = static_cast<unsigned>(last_phys) < static_cast<unsigned>(a.num_blocks) &&
+                    slot == last_phys * kBlockSize + row;
+    if (!ok) {
+      if (lane == 0) flag(a.dev_status, 1u);  // PKV_DEV_ERR_SLOT
+      row = -1;
+      return false;
+    }
+    const int c = lane & 15;
+    if (c < D / 8) {
+      uint16_t* dst = (lane < 16 ? a.k_pool_w : a.v_pool_w) +
+                      static_cast<int64_t>(slot) * a.num_kv_heads * D + g * D + c * 8;
+      *reinterpret_cast<uint4*>(dst) = val;
+    }
+    return true;
+  }
+
+  // Overwrites token `row` of the K and V tiles in shared memory (TMA
+  // swizzled layout, shared addresses) with the new row.  Call after the
+  // tile's wait.
+  __device__ __forceinline__ void patch(uint32_t k_tile, uint32_t v_tile, int lane) const {
+    const int c = lane & 15;
+    if (c < D / 8) {
+      const int half = c >> 3, cc = c & 7;
+      const uint32_t addr = (lane < 16 ? k_tile : v_tile) + half * 2048 + row * 128 + ((cc ^ (row & 7)) << 4);
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(val.x), "r"(val.y), "r"(val.z),
+                   "r"(val.w)
+                   : "memory");
+    }
+    __syncwarp();
+  }
+};
+
 // ----------------------------------------------------- per-warp attention
 
 // Attention state of one warp serving the G <= 8 query heads of one KV head.

@@ -58,6 +58,14 @@ struct DecodeArgs {
   int out_dtype;       // pkv_dtype
   int balanced_ctas;   // balanced split: persistent CTAs (one per SM); 0 otherwise
   long long timeout_ns;
+  // Fused decode step only: the token generated this step, written to the
+  // pools by the attention kernel itself (null when not fusing).
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  int64_t new_stride;           // elements between consecutive sequences' new rows
+  const int32_t* slot_mapping;  // [S]: slot of position L-1, or -1
+  uint16_t* k_pool_w;
+  uint16_t* v_pool_w;
 };
 
 // Split-K workspace layout (regions 256-byte aligned).  Fixed partitions:
@@ -105,7 +113,7 @@ cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream);
 // kv_bf16: 0 = f16, 1 = bf16.  Tensor maps describe the K and V pools.
 cudaError_t launch_decode_partitions(const DecodeArgs& a, const CUtensorMap& tmap_k,
                                      const CUtensorMap& tmap_v, int head_dim, int kv_bf16,
-                                     cudaStream_t stream);
+                                     cudaStream_t stream);  // fuses the write when a.k_new is set
 cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t stream);
 cudaError_t launch_decode_balanced(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                    int head_dim, int kv_bf16, cudaStream_t stream);

@@ -63,6 +63,16 @@ class DeviceStep:
         torch.cuda.synchronize()
         return self.out
 
+    def fused_step(self, out=None):
+        """copy_blocks, then the write fused into decode attention (pkv_decode_step)."""
+        self.copy()
+        pkv.decode_step(self.out if out is None else out, self.q, self.k_new, self.v_new, self.k_pool, self.v_pool,
+                        self.block_tables, self.context_lens, self.slot_mapping, self.wl.scale,
+                        partition_size=self.partition_size, max_context_len=self.max_context_len,
+                        workspace=self.workspace, status=self.status)
+        torch.cuda.synchronize()
+        return self.out if out is None else out
+
     def status_bits(self) -> int:
         torch.cuda.synchronize()
         return int(self.status.item())
