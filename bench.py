@@ -61,6 +61,26 @@ def _dist():
     return rank, world, local
 
 
+# ------------------------------------------------------- multi-rank timing
+
+def max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's value (the job is as slow as its slowest
+    rank); identity when torch.distributed is not initialised."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank_step: int, world: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job throughput: every rank's bytes over the slowest rank's time (weak scaling)."""
+    return world * bytes_per_rank_step * steps / (elapsed_ms * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------- byte accounting
 
 def step_bytes(wl, out_bytes_per_elem=4):
@@ -243,10 +263,7 @@ def run_gpu(args):
         step(W + i, evs[i])
     barrier()
     kern_ms = [a.elapsed_time(b) for a, b in evs]
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
     st = int(status.item())
     if st != 0:
         raise RuntimeError(f"device status {st} after the timed steps")
@@ -271,12 +288,8 @@ def run_gpu(args):
             host_out.copy_(out, non_blocking=True)
         e1.record()
         barrier()
-        e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": round(world * nb["step"] * Ke / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+        e2e = {"value": round(job_gbs(nb["step"], world, Ke, e_ms), 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": Ke,
                "ms_per_step": round(e_ms / Ke, 5)}
 
@@ -287,7 +300,7 @@ def run_gpu(args):
 
     peak, peak_kind = _peaks()
     ms = elapsed_ms / K
-    value = world * nb["step"] / (ms * 1e-3) / 1e9
+    value = job_gbs(nb["step"], world, K, elapsed_ms)
     kern_avg_ms = statistics.mean(kern_ms)
     kernel_name = "decode_balanced_kernel" if ps == pkv.PARTITION_BALANCED else "decode_partitions_kernel"
     traffic = _recorded_traffic(args.config, kernel_name)
