@@ -8,7 +8,8 @@ The work is done by libpkv (include/pkv.h), hand-written CUDA for sm_103a:
   decode_step       -- the new token's write fused into decode attention
 This package only marshals torch tensors into the C ABI.
 """
-from ._binding import (DEV_ERR_BLOCK, DEV_ERR_LENGTH, DEV_ERR_PAIR, DEV_ERR_SLOT, DEV_ERR_TIMEOUT, PKV_BF16,
+from ._binding import (DEV_ERR_BLOCK, DEV_ERR_LENGTH, DEV_ERR_PAIR, DEV_ERR_SLOT, DEV_ERR_SMEM, DEV_ERR_TIMEOUT,
+                       PKV_BF16,
                        PKV_ERR_CUDA, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_F16, PKV_F32,
                        PKV_OK, PARTITION_BALANCED, PkvError, copy_blocks, decode_attention, decode_partitions, decode_reduce,
                        decode_step, decode_step_partitions, decode_workspace_bytes, library_path, load, status_string,
@@ -20,5 +21,5 @@ __all__ = [
     "PkvError",
     "PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_WORKSPACE", "PKV_ERR_CUDA",
     "PKV_F32", "PKV_F16", "PKV_BF16", "PARTITION_BALANCED",
-    "DEV_ERR_SLOT", "DEV_ERR_PAIR", "DEV_ERR_BLOCK", "DEV_ERR_LENGTH", "DEV_ERR_TIMEOUT",
+    "DEV_ERR_SLOT", "DEV_ERR_PAIR", "DEV_ERR_BLOCK", "DEV_ERR_LENGTH", "DEV_ERR_TIMEOUT", "DEV_ERR_SMEM",
 ]

@@ -13,8 +13,7 @@
 // Mapping onto GB300:
 //  * Work unit = (KV head g, sequence s, partition p), one warp each.  A CTA
 //    is NW warps on consecutive KV heads of the same (s, p), so it reads
-//    neighbouring head rows of every token row of a block.  Partitions are
-//    dispatched from the last index down.  A warp serves
+//    neighbouring head rows of every token row of a block.  A warp serves
 //    all G <= 8 query heads of its KV head: every K/V byte is read once.
 //  * Data movement: TMA (cp.async.bulk.tensor.3d, 128-byte swizzle) copies
 //    one (block, head) tile of K and of V per stage into a per-warp ring of
@@ -33,50 +32,87 @@ namespace {
 
 using namespace dev;
 
-template <int D, bool BF16, int NW, int NST, bool FUSED>
-__global__ void __launch_bounds__(NW * 32) decode_partitions_kernel(
-    const DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
-    const __grid_constant__ CUtensorMap tmap_v) {
-  using Geom = TileGeom<D>;
-  extern __shared__ __align__(1024) uint8_t smem[];
-  griddep_wait();  // every input may come from the previous kernel on the stream
-  griddep_launch_dependents();
-  if (smem_misaligned(smem, a.dev_status)) return;
+// Warps per unit when the host leaves the choice to the device: one when
+// every unit of the batch can have a warp of its own in one wave, else two
+// (a unit then streams twice as fast, which shortens the end of the grid).
+// The units are estimated as H_kv * (sum_s L_s / PS + S / 2) (a sequence's
+// last partition is half full on average), so the test is the total of the
+// lengths against a.one_warp_tokens, the largest total for which that
+// estimate fits the warp slots.  Each warp sums the lengths itself; all
+// warps of the grid read the same lengths and agree.
+__device__ __forceinline__ int device_unit_warps(const DecodeArgs& a, int lane) {
+  constexpr int kPerLane = kDeviceChoiceMaxSeqs / 32;
+  const int S = a.num_seqs;
+  const int cap = min(a.max_context_len, a.max_blocks_per_seq * kBlockSize);
+  float tokens = 0.f;  // same order in every warp, so the same rounding
+#pragma unroll 8
+  for (int k = 0; k < kPerLane; ++k) {
+    if (lane + 32 * k < S) {
+      const int raw = a.context_lens[lane + 32 * k];
+      tokens += static_cast<float>(raw < 0 ? 0 : min(raw, cap));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tokens += __shfl_xor_sync(kFull, tokens, o);
+  return tokens <= a.one_warp_tokens ? 1 : 2;
+}
 
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
+// The warp's first 32 table entries of unit `unit` served by U warps (lane
+// j: the partition's block j * U + sub), read before the length is known:
+// every read index lies in the partition and in the table row; entries
+// past the sequence's blocks are never used.
+template <int U>
+__device__ __forceinline__ int first_entries(const DecodeArgs& a, int64_t unit, int sub, int lane) {
   const int Hkv = a.num_kv_heads;
-  const int64_t unit = static_cast<int64_t>(blockIdx.x) * NW + warp;
-  if (unit >= static_cast<int64_t>(Hkv) * a.num_seqs * a.max_parts) return;
-  // Units run in descending partition index: the later partitions of long
-  // sequences (all full-size) are dispatched first and each sequence's first
-  // partition -- the short tail of most sequences -- last, which shortens
-  // the end of the grid.
+  const int s = static_cast<int>((unit / Hkv) % a.num_seqs);
+  const int part = static_cast<int>(unit / Hkv / a.num_seqs);
+  const int blk = part * (a.partition_size / kBlockSize), e = lane * U + sub;
+  return (e < a.partition_size / kBlockSize && blk + e < a.max_blocks_per_seq)
+             ? __ldg(a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + blk + e)
+             : 0;
+}
+
+// One unit (sequence s, KV head g, partition p) served by U of the CTA's NW
+// warps; `raw_len` is the sequence's context length as read and `first`
+// the warp's first table entries (first_entries<U>).
+template <int D, bool BF16, int NW, int U, int NST, bool FUSED>
+__device__ __forceinline__ void partition_unit(const DecodeArgs& a, const CUtensorMap* tmap_k,
+                                               const CUtensorMap* tmap_v, uint8_t* smem, int64_t unit,
+                                               int raw_len, int first, int warp, int lane) {
+  using Geom = TileGeom<D>;
+  using Att = WarpAttention<D, BF16>;
+  static_assert(NW % U == 0 && NW / U <= 15, "named barriers 1..15, one per unit of the CTA");
+  static_assert(Att::kSaveBytes <= NST * Geom::kStageBytes, "a saved state must fit its warp's ring");
+  const int sub = warp % U;  // the warp's place among its unit's U warps
+  const int Hkv = a.num_kv_heads;
+  // Units run in ascending partition index.  The grid covers every
+  // partition index up to max_parts for every sequence, so most units of a
+  // mixed-length batch are empty; in this order they come last, where they
+  // only fill slots that finishing units free (dispatched first they stall
+  // the start of the grid).
   const int g = static_cast<int>(unit % Hkv);
   const int64_t rest = unit / Hkv;
   const int s = static_cast<int>(rest % a.num_seqs);
-  const int part = a.max_parts - 1 - static_cast<int>(rest / a.num_seqs);
+  const int part = static_cast<int>(rest / a.num_seqs);
 
   const int PS = a.partition_size;
   const int G = a.group;
-  const int tok0 = part * PS;
-  // Block-table entries of this partition, 32 per register chunk, and the
-  // query rows do not depend on the sequence length: their loads go out
-  // together with the length's (entries within the table row are always
-  // readable; those past the sequence are never used).
-  const int blk0 = tok0 / kBlockSize;
-  const int32_t* tbl = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + blk0;
-  const int row_left = a.max_blocks_per_seq - blk0;
-  int phys_cur = (lane < row_left) ? __ldg(tbl + lane) : 0;
-  int phys_next = (32 + lane < row_left) ? __ldg(tbl + 32 + lane) : 0;
-  WarpAttention<D, BF16> at;
-  at.load_q(a.q + (static_cast<int64_t>(s) * a.num_q_heads + g * G) * D, G, lane);
-
-  const int L = clamped_len(a, s, part == 0 && g == 0 && lane == 0);
+  const int L = clamp_len(a, raw_len, part == 0 && g == 0 && sub == 0 && lane == 0);
   const int nparts = L > 0 ? (L + PS - 1) / PS : 1;
-  if (part >= nparts) return;
+  if (part >= nparts) return;  // the unit's warps all leave here
+  Att at;
+  at.load_q(a.q + (static_cast<int64_t>(s) * a.num_q_heads + g * G) * D, G, lane);
+  const int tok0 = part * PS;
   const int ntok = max(0, min(L - tok0, PS));
   const int nblk = (ntok + kBlockSize - 1) / kBlockSize;
+  // The warp's tiles are the partition's blocks sub, sub + U, sub + 2U, ...
+  // Their table entries sit in registers 32 at a time (lane j: the warp's
+  // tile j of the chunk); the next chunk is fetched one chunk ahead of use.
+  const int cnt = nblk > sub ? (nblk - sub + U - 1) / U : 0;
+  const int32_t* tbl = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + tok0 / kBlockSize;
+  auto entry = [&](int i) { return i < cnt ? __ldg(tbl + i * U + sub) : 0; };
+  int phys_cur = first;
+  int phys_next = entry(32 + lane);
 
   WarpRing<D, NST> ring{smem_u32(smem + static_cast<size_t>(warp) * NST * Geom::kStageBytes),
                         smem_u32(smem + static_cast<size_t>(NW) * NST * Geom::kStageBytes) + 8 * NST * warp};
@@ -86,8 +122,7 @@ __global__ void __launch_bounds__(NW * 32) decode_partitions_kernel(
   auto issue = [&](int j) {  // all lanes call
     if ((j & 31) == 0 && j > 0) {
       phys_cur = phys_next;
-      const int nx = j + 32 + lane;
-      phys_next = (nx < min(nblk, row_left)) ? __ldg(tbl + nx) : 0;
+      phys_next = entry(j + 32 + lane);
     }
     const int st = j % NST;
     int phys = __shfl_sync(kFull, phys_cur, j & 31);
@@ -98,44 +133,96 @@ __global__ void __launch_bounds__(NW * 32) decode_partitions_kernel(
     } else {
       bad_stage &= ~(1u << st);
     }
-    ring.issue(j, phys, g, &tmap_k, &tmap_v, lane);
+    ring.issue(j, phys, g, tmap_k, tmap_v, lane);
   };
 
   at.reset();
-  for (int j = 0; j < min(nblk, NST); ++j) issue(j);
+  for (int j = 0; j < min(cnt, NST); ++j) issue(j);
 
-  // Fused decode step: the last partition of (s, g) holds position L-1.
+  // Fused decode step: the last block of the last partition of (s, g) holds
+  // position L-1.
   NewToken<D> nt;
-  const bool owns_new = FUSED && part == nparts - 1;
+  const bool owns_new = FUSED && part == nparts - 1 && sub == (nblk > 0 ? (nblk - 1) % U : 0);
   if (owns_new) {
     nt.prefetch(a, s, g, L, lane);
     if (nblk == 0) nt.commit(a, g, lane);  // empty sequence: only checks the slot
   }
 
-  for (int i = 0; i < nblk; ++i) {
+  for (int i = 0; i < cnt; ++i) {
     if (!__all_sync(kFull, ring.wait(i, a.timeout_ns))) {
-      ring.drain(i, min(nblk, i + NST), a.timeout_ns);
-      if (lane == 0) flag(a.dev_status, 16u);  // PKV_DEV_ERR_TIMEOUT
-      return;
+      ring.drain(i, min(cnt, i + NST), a.timeout_ns);
+      if (lane == 0) flag(a.dev_status, 16u);  // PKV_DEV_ERR_TIMEOUT; the output is undefined
+      break;
     }
+    const int t = i * U + sub;  // block index within the partition
     const int st = i % NST;
-    const int nv = ((bad_stage >> st) & 1) ? 0 : min(kBlockSize, ntok - i * kBlockSize);
+    const int nv = ((bad_stage >> st) & 1) ? 0 : min(kBlockSize, ntok - t * kBlockSize);
     const uint32_t sK = ring.k_tile(i);
-    if (owns_new && i == nblk - 1 && nt.commit(a, g, lane)) nt.patch(sK, sK + Geom::kTileBytes, lane);
+    if (owns_new && t == nblk - 1 && nt.commit(a, g, lane)) nt.patch(sK, sK + Geom::kTileBytes, lane);
     at.tile(sK, sK + Geom::kTileBytes, nv, a.scale_log2, lane);
     __syncwarp();
-    if (i + NST < nblk) {
+    if (i + NST < cnt) {
       fence_proxy_async_smem();
       issue(i + NST);
     }
   }
 
   at.finish_sums();
+  if constexpr (U > 1) {
+    // The unit's warps hand their states to its first warp through their
+    // own (now idle) ring buffers.
+    const uint32_t mine = smem_u32(smem + static_cast<size_t>(warp) * NST * Geom::kStageBytes);
+    if (sub != 0) at.save(mine, lane);
+    named_barrier_sync(1 + warp / U, U * 32);
+    if (sub != 0) return;
+#pragma unroll
+    for (int k = 1; k < U; ++k) at.merge_from(mine + k * NST * Geom::kStageBytes, lane);
+  }
   const int64_t head0 = static_cast<int64_t>(s) * a.num_q_heads + g * G;
   if (nparts == 1)
     at.store_final(a.out, head0, G, a.out_dtype, lane);
   else
     at.store_partial(a.ws_acc, a.ws_ml, head0 * a.max_parts + part, a.max_parts, G, lane);
+}
+
+// Two-warp CTAs.  With one warp per unit (a.unit_warps == 1) CTA b serves
+// units 2b and 2b + 1; with two (== 2) it serves unit b with both warps; 0
+// leaves the choice to device_unit_warps.  The lengths of both candidate
+// units load in the same round trip as the choice's.
+template <int D, bool BF16, int NST, bool FUSED>
+__global__ void __launch_bounds__(64) decode_partitions_kernel(
+    const DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
+    const __grid_constant__ CUtensorMap tmap_v) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  griddep_wait();  // every input may come from the previous kernel on the stream
+  griddep_launch_dependents();
+  if (smem_misaligned(smem, a.dev_status)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t units = static_cast<int64_t>(a.num_kv_heads) * a.num_seqs * a.max_parts;
+  const int64_t unit1 = static_cast<int64_t>(blockIdx.x) * 2 + warp, unit2 = blockIdx.x;
+  auto seq_of = [&](int64_t u) { return static_cast<int>((u / a.num_kv_heads) % a.num_seqs); };
+  int mode = a.unit_warps;
+  // The candidates' lengths and first table entries go out together.
+  const bool c1 = mode != 2 && unit1 < units, c2 = mode != 1 && unit2 < units;
+  const int len1 = c1 ? a.context_lens[seq_of(unit1)] : 0;
+  const int len2 = c2 ? a.context_lens[seq_of(unit2)] : 0;
+  const int first1 = c1 ? first_entries<1>(a, unit1, 0, lane) : 0;
+  const int first2 = c2 ? first_entries<2>(a, unit2, warp, lane) : 0;
+  if (mode == 0) {
+    // Warps whose candidate units are both empty leave in either mode.
+    auto empty = [&](int64_t u, int raw) {
+      const int part = static_cast<int>(u / a.num_kv_heads / a.num_seqs);
+      const int L = raw < 0 ? 0 : raw;
+      return part > 0 && part * a.partition_size >= L;
+    };
+    if ((!c1 || empty(unit1, len1)) && (!c2 || empty(unit2, len2))) return;
+    mode = device_unit_warps(a, lane);
+  }
+  if (mode == 2) {
+    if (c2) partition_unit<D, BF16, 2, 2, NST, FUSED>(a, &tmap_k, &tmap_v, smem, unit2, len2, first2, warp, lane);
+  } else if (c1) {
+    partition_unit<D, BF16, 2, 1, NST, FUSED>(a, &tmap_k, &tmap_v, smem, unit1, len1, first1, warp, lane);
+  }
 }
 
 // --------------------------------------------------------------- reduce kernels
@@ -214,28 +301,63 @@ __global__ void __launch_bounds__(kLongReduceWarps * 32, 2) decode_reduce_long_k
 
 // ------------------------------------------------------------------ launchers
 
-#ifndef PKV_WARPS_PER_CTA
-#define PKV_WARPS_PER_CTA 2
-#endif
-#ifndef PKV_STAGES
-#define PKV_STAGES 2
-#endif
-constexpr int kWarpsPerCta = PKV_WARPS_PER_CTA;
-constexpr int kStages = PKV_STAGES;
+constexpr int kStages = 2;
+
+// Warp slots of the partition kernel on the current device (SMs x resident
+// CTAs x 2 warps), cached per kernel.
+int partition_warp_slots(const void* kern, size_t smem) {
+  static const void* cached_kern[16] = {};
+  static int cached_slots[16] = {};
+  static int cached_dev[16] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  for (int i = 0; i < 16; ++i)
+    if (cached_kern[i] == kern && cached_dev[i] == dev) return cached_slots[i];
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 64, smem) != cudaSuccess || per_sm <= 0) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  const int slots = current_sm_count(1) * per_sm * 2;
+  for (int i = 0; i < 16; ++i)
+    if (!cached_kern[i]) {
+      cached_kern[i] = kern;
+      cached_dev[i] = dev;
+      cached_slots[i] = slots;
+      break;
+    }
+  return slots;
+}
 
 template <int D, bool BF16, bool FUSED>
-cudaError_t launch_partitions_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_partitions_t(const DecodeArgs& a_in, const CUtensorMap& tk, const CUtensorMap& tv,
                                 cudaStream_t stream) {
   using Geom = TileGeom<D>;
-  constexpr int NW = kWarpsPerCta, NST = kStages;
-  const size_t smem = static_cast<size_t>(NW) * NST * Geom::kStageBytes + NW * NST * 8;
-  auto kern = decode_partitions_kernel<D, BF16, NW, NST, FUSED>;
+  constexpr int NST = kStages;
+  const size_t smem = 2 * NST * Geom::kStageBytes + 2 * NST * 8;
+  auto kern = decode_partitions_kernel<D, BF16, NST, FUSED>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
+  DecodeArgs a = a_in;
   const int64_t units = static_cast<int64_t>(a.num_kv_heads) * a.num_seqs * a.max_parts;
-  const int64_t ctas = (units + NW - 1) / NW;
-  if (ctas == 0) return cudaSuccess;
-  return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(NW * 32), smem, stream, a, tk, tv);
+  if (units == 0) return cudaSuccess;
+  // One warp per unit when every unit surely has a warp slot of its own,
+  // two when the sequences alone (a unit each at least) overfill the slots;
+  // otherwise the kernel counts the units.
+  a.warp_slots = partition_warp_slots(reinterpret_cast<const void*>(kern), smem);
+  const int64_t min_units = static_cast<int64_t>(a.num_kv_heads) * a.num_seqs;
+  if (units <= a.warp_slots) {
+    a.unit_warps = 1;
+  } else if (min_units > a.warp_slots || a.num_seqs > kDeviceChoiceMaxSeqs) {
+    a.unit_warps = 2;
+  } else {
+    // H_kv * (T / PS + S / 2) <= slots  <=>  T <= (slots / H_kv - S / 2) * PS
+    a.unit_warps = 0;
+    a.one_warp_tokens = static_cast<float>(
+        (static_cast<double>(a.warp_slots) / a.num_kv_heads - 0.5 * a.num_seqs) * a.partition_size);
+  }
+  const int64_t ctas = a.unit_warps == 1 ? (units + 1) / 2 : units;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(64), smem, stream, a, tk, tv);
 }
 
 template <int D, bool BF16>

@@ -81,6 +81,11 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Barrier `id` (1..15) over `nthreads` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -153,6 +158,14 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, float v, int d
 __device__ __forceinline__ int clamped_len(const DecodeArgs& a, int s, bool report) {
   const int cap = min(a.max_context_len, a.max_blocks_per_seq * kBlockSize);
   const int L = a.context_lens[s];
+  if (L >= 0 && L <= cap) return L;
+  if (report) flag(a.dev_status, 8u);
+  return L < 0 ? 0 : cap;
+}
+
+// The same for a length already read.
+__device__ __forceinline__ int clamp_len(const DecodeArgs& a, int L, bool report) {
+  const int cap = min(a.max_context_len, a.max_blocks_per_seq * kBlockSize);
   if (L >= 0 && L <= cap) return L;
   if (report) flag(a.dev_status, 8u);
   return L < 0 ? 0 : cap;
@@ -322,14 +335,22 @@ struct WarpAttention {
 
   // B operand of QK^T: lane holds q[head lane/4][16kk + 2(lane%4) + {0,1}]
   // and +8.  `qhead0` points at the group's first head row; heads >= G are 0.
-  __device__ __forceinline__ void load_q(const uint16_t* qhead0, int G, int lane) {
+  __device__ __forceinline__ static void fetch_q(uint32_t (&dst)[KT][2], const uint16_t* qhead0, int G, int lane) {
     const int gr = lane >> 2, tq = lane & 3;
     const bool live = gr < G;
     const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qhead0 + (live ? gr : 0) * D);
 #pragma unroll
     for (int kk = 0; kk < KT; ++kk) {
-      qf[kk][0] = live ? __ldg(qrow + kk * 8 + tq) : 0u;
-      qf[kk][1] = live ? __ldg(qrow + kk * 8 + 4 + tq) : 0u;
+      dst[kk][0] = live ? __ldg(qrow + kk * 8 + tq) : 0u;
+      dst[kk][1] = live ? __ldg(qrow + kk * 8 + 4 + tq) : 0u;
+    }
+  }
+  __device__ __forceinline__ void load_q(const uint16_t* qhead0, int G, int lane) { fetch_q(qf, qhead0, G, lane); }
+  __device__ __forceinline__ void set_q(const uint32_t (&src)[KT][2]) {
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk) {
+      qf[kk][0] = src[kk][0];
+      qf[kk][1] = src[kk][1];
     }
   }
 
@@ -444,6 +465,54 @@ struct WarpAttention {
         store_out(out, (out_head0 + hb) * D + d, acc[mt][1] * ib, dtype);
         store_out(out, (out_head0 + hb) * D + d + 8, acc[mt][3] * ib, dtype);
       }
+    }
+  }
+
+  // Cross-warp merge of two states over disjoint token sets (the same
+  // rescaling as the online softmax).  save() writes this lane's fragments
+  // to shared memory at `buf` as [element][lane] floats (kSaveBytes in all);
+  // merge_from() folds such a saved state into this one.  Both run after
+  // finish_sums(), so every lane holds its heads' full running sums.
+  static constexpr int kSaveFloats = KT * 4 + 4;
+  static constexpr int kSaveBytes = kSaveFloats * 32 * 4;
+
+  __device__ __forceinline__ void save(uint32_t buf, int lane) const {
+    auto put = [&](int e, float v) {
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(buf + (e * 32 + lane) * 4), "f"(v) : "memory");
+    };
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) put(mt * 4 + j, acc[mt][j]);
+    put(KT * 4 + 0, m_a);
+    put(KT * 4 + 1, m_b);
+    put(KT * 4 + 2, l_a);
+    put(KT * 4 + 3, l_b);
+  }
+
+  __device__ __forceinline__ void merge_from(uint32_t buf, int lane) {
+    auto get = [&](int e) {
+      float v;
+      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(buf + (e * 32 + lane) * 4) : "memory");
+      return v;
+    };
+    const float mo_a = get(KT * 4 + 0), mo_b = get(KT * 4 + 1);
+    const float lo_a = get(KT * 4 + 2), lo_b = get(KT * 4 + 3);
+    const float M_a = fmaxf(m_a, mo_a), M_b = fmaxf(m_b, mo_b);
+    // Two empty states stay empty (and no -inf - -inf is formed).
+    const float u_a = (M_a == kNegInf) ? 0.f : M_a, u_b = (M_b == kNegInf) ? 0.f : M_b;
+    const float ca = exp2f(m_a - u_a), coa = exp2f(mo_a - u_a);
+    const float cb = exp2f(m_b - u_b), cob = exp2f(mo_b - u_b);
+    l_a = l_a * ca + lo_a * coa;
+    l_b = l_b * cb + lo_b * cob;
+    m_a = M_a;
+    m_b = M_b;
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt) {
+      acc[mt][0] = acc[mt][0] * ca + get(mt * 4 + 0) * coa;
+      acc[mt][1] = acc[mt][1] * cb + get(mt * 4 + 1) * cob;
+      acc[mt][2] = acc[mt][2] * ca + get(mt * 4 + 2) * coa;
+      acc[mt][3] = acc[mt][3] * cb + get(mt * 4 + 3) * cob;
     }
   }
 
