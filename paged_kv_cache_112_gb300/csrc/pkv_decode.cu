@@ -32,31 +32,6 @@ namespace {
 
 using namespace dev;
 
-// Warps per unit when the host leaves the choice to the device: one when
-// every unit of the batch can have a warp of its own in one wave, else two
-// (a unit then streams twice as fast, which shortens the end of the grid).
-// The units are estimated as H_kv * (sum_s L_s / PS + S / 2) (a sequence's
-// last partition is half full on average), so the test is the total of the
-// lengths against a.one_warp_tokens, the largest total for which that
-// estimate fits the warp slots.  Each warp sums the lengths itself; all
-// warps of the grid read the same lengths and agree.
-__device__ __forceinline__ int device_unit_warps(const DecodeArgs& a, int lane) {
-  constexpr int kPerLane = kDeviceChoiceMaxSeqs / 32;
-  const int S = a.num_seqs;
-  const int cap = min(a.max_context_len, a.max_blocks_per_seq * kBlockSize);
-  float tokens = 0.f;  // same order in every warp, so the same rounding
-#pragma unroll 8
-  for (int k = 0; k < kPerLane; ++k) {
-    if (lane + 32 * k < S) {
-      const int raw = a.context_lens[lane + 32 * k];
-      tokens += static_cast<float>(raw < 0 ? 0 : min(raw, cap));
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tokens += __shfl_xor_sync(kFull, tokens, o);
-  return tokens <= a.one_warp_tokens ? 1 : 2;
-}
-
 // The warp's first 32 table entries of unit `unit` served by U warps (lane
 // j: the partition's block j * U + sub), read before the length is known:
 // every read index lies in the partition and in the table row; entries
@@ -186,9 +161,8 @@ __device__ __forceinline__ void partition_unit(const DecodeArgs& a, const CUtens
 }
 
 // Two-warp CTAs.  With one warp per unit (a.unit_warps == 1) CTA b serves
-// units 2b and 2b + 1; with two (== 2) it serves unit b with both warps; 0
-// leaves the choice to device_unit_warps.  The lengths of both candidate
-// units load in the same round trip as the choice's.
+// units 2b and 2b + 1; with two (== 2) it serves unit b with both warps.
+// A unit's length and first table entries go out together.
 template <int D, bool BF16, int NST, bool FUSED>
 __global__ void __launch_bounds__(64) decode_partitions_kernel(
     const DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
@@ -201,27 +175,13 @@ __global__ void __launch_bounds__(64) decode_partitions_kernel(
   const int64_t units = static_cast<int64_t>(a.num_kv_heads) * a.num_seqs * a.max_parts;
   const int64_t unit1 = static_cast<int64_t>(blockIdx.x) * 2 + warp, unit2 = blockIdx.x;
   auto seq_of = [&](int64_t u) { return static_cast<int>((u / a.num_kv_heads) % a.num_seqs); };
-  int mode = a.unit_warps;
-  // The candidates' lengths and first table entries go out together.
-  const bool c1 = mode != 2 && unit1 < units, c2 = mode != 1 && unit2 < units;
-  const int len1 = c1 ? a.context_lens[seq_of(unit1)] : 0;
-  const int len2 = c2 ? a.context_lens[seq_of(unit2)] : 0;
-  const int first1 = c1 ? first_entries<1>(a, unit1, 0, lane) : 0;
-  const int first2 = c2 ? first_entries<2>(a, unit2, warp, lane) : 0;
-  if (mode == 0) {
-    // Warps whose candidate units are both empty leave in either mode.
-    auto empty = [&](int64_t u, int raw) {
-      const int part = static_cast<int>(u / a.num_kv_heads / a.num_seqs);
-      const int L = raw < 0 ? 0 : raw;
-      return part > 0 && part * a.partition_size >= L;
-    };
-    if ((!c1 || empty(unit1, len1)) && (!c2 || empty(unit2, len2))) return;
-    mode = device_unit_warps(a, lane);
-  }
-  if (mode == 2) {
-    if (c2) partition_unit<D, BF16, 2, 2, NST, FUSED>(a, &tmap_k, &tmap_v, smem, unit2, len2, first2, warp, lane);
-  } else if (c1) {
-    partition_unit<D, BF16, 2, 1, NST, FUSED>(a, &tmap_k, &tmap_v, smem, unit1, len1, first1, warp, lane);
+  if (a.unit_warps == 2) {
+    if (unit2 < units)
+      partition_unit<D, BF16, 2, 2, NST, FUSED>(a, &tmap_k, &tmap_v, smem, unit2, a.context_lens[seq_of(unit2)],
+                                                first_entries<2>(a, unit2, warp, lane), warp, lane);
+  } else if (unit1 < units) {
+    partition_unit<D, BF16, 2, 1, NST, FUSED>(a, &tmap_k, &tmap_v, smem, unit1, a.context_lens[seq_of(unit1)],
+                                              first_entries<1>(a, unit1, 0, lane), warp, lane);
   }
 }
 
@@ -341,21 +301,14 @@ cudaError_t launch_partitions_t(const DecodeArgs& a_in, const CUtensorMap& tk, c
   DecodeArgs a = a_in;
   const int64_t units = static_cast<int64_t>(a.num_kv_heads) * a.num_seqs * a.max_parts;
   if (units == 0) return cudaSuccess;
-  // One warp per unit when every unit surely has a warp slot of its own,
-  // two when the sequences alone (a unit each at least) overfill the slots;
-  // otherwise the kernel counts the units.
-  a.warp_slots = partition_warp_slots(reinterpret_cast<const void*>(kern), smem);
-  const int64_t min_units = static_cast<int64_t>(a.num_kv_heads) * a.num_seqs;
-  if (units <= a.warp_slots) {
-    a.unit_warps = 1;
-  } else if (min_units > a.warp_slots || a.num_seqs > kDeviceChoiceMaxSeqs) {
-    a.unit_warps = 2;
-  } else {
-    // H_kv * (T / PS + S / 2) <= slots  <=>  T <= (slots / H_kv - S / 2) * PS
-    a.unit_warps = 0;
-    a.one_warp_tokens = static_cast<float>(
-        (static_cast<double>(a.warp_slots) / a.num_kv_heads - 0.5 * a.num_seqs) * a.partition_size);
-  }
+  // Two warps per unit when the sequences alone (a unit each at least)
+  // overfill the warp slots: there are surely more units than one wave.
+  // Otherwise one, which keeps every unit of a single-wave batch running
+  // from the start.  (The host does not see the lengths; estimating the
+  // unit count on the device cost more than it gained on the benchmarked
+  // batches.)
+  const int slots = partition_warp_slots(reinterpret_cast<const void*>(kern), smem);
+  a.unit_warps = static_cast<int64_t>(a.num_kv_heads) * a.num_seqs > slots ? 2 : 1;
   const int64_t ctas = a.unit_warps == 1 ? (units + 1) / 2 : units;
   return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(64), smem, stream, a, tk, tv);
 }

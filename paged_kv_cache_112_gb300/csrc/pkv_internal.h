@@ -57,9 +57,7 @@ struct DecodeArgs {
   float scale_log2;    // scale * log2(e)
   int out_dtype;       // pkv_dtype
   int balanced_ctas;   // balanced split: persistent CTAs (one per SM); 0 otherwise
-  int unit_warps;      // fixed partitions: warps per unit (1 or 2), 0 = counted on the device
-  int warp_slots;      // fixed partitions: warps of the partition kernel resident at once
-  float one_warp_tokens;  // unit_warps 0: one warp per unit while the lengths total at most this
+  int unit_warps;      // fixed partitions: warps per unit (1 or 2)
   long long timeout_ns;
   // Fused decode step only: the token generated this step, written to the
   // pools by the attention kernel itself (null when not fusing).
@@ -86,10 +84,6 @@ int current_sm_count(int fallback);
 // Raises a kernel's dynamic shared memory limit to `bytes` on the current
 // device (once per kernel, device and size).
 cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
-
-// Largest batch for which the partition kernel counts its units on the
-// device to choose the warps per unit.
-constexpr int kDeviceChoiceMaxSeqs = 1024;
 
 // Balanced split geometry (pkv_decode_balanced.cu).
 constexpr int kBalancedMaxSeqs = 4096;

@@ -1,12 +1,12 @@
 """The partition kernel serves a unit (sequence, KV head, partition) with one
 warp, or with two warps that split its blocks and merge their softmax states
-through shared memory.  The host picks one warp when every unit surely fits
-one wave of warp slots, two when the sequences alone overfill it, and
-otherwise leaves the choice to each CTA, which estimates the unit count
-from the context lengths.  These cases force each branch on a GB300 (152
-SMs x 6 CTAs x 2 warps = 1824 warp slots) with short sequences the oracle
-finishes quickly, and check the results against the oracle; on another GPU
-the branches may differ but every result must still match."""
+through shared memory.  The host picks two when the sequences alone
+(H_kv x S, a unit each at least) overfill one wave of warp slots, else one.
+These cases take each path on a GB300 (152 SMs x 6 CTAs x 2 warps = 1824
+warp slots) with short sequences the oracle finishes quickly, including a
+one-warp batch whose partition-indexed grid is mostly empty and one whose
+units exceed a wave; on another GPU the paths may differ but every result
+must still match."""
 import numpy as np
 import pytest
 import torch
@@ -27,13 +27,13 @@ def _lib():
 
 
 CASES = {
-    # 256 x 8 = 2048 sequence-heads > 1824 slots: the host picks two warps per unit.
-    "host_two": dict(cfg=3, num_seqs=256, lens=("uniform", 1, 90), ps=32, max_len=None),
-    # 64 x 8 = 512 sequence-heads, bound 64 x 8 x 16 units > slots: the device
-    # estimates 8 x (64 x 15 / 16 + 32) = 736 units <= 1824 -> one warp.
-    "device_one": dict(cfg=2, num_seqs=64, lens=("uniform", 1, 30), ps=16, max_len=256),
-    # same shape, lengths near the bound: 8 x (64 x ~240 / 16 + 32) > 1824 -> two warps.
-    "device_two": dict(cfg=2, num_seqs=64, lens=("uniform", 224, 255), ps=16, max_len=256),
+    # 256 x 8 = 2048 sequence-heads > 1824 slots: two warps per unit.
+    "two_warps": dict(cfg=3, num_seqs=256, lens=("uniform", 1, 90), ps=32, max_len=None),
+    # 64 x 8 = 512 sequence-heads: one warp; a bound of 16 partitions per sequence
+    # while the lengths need at most 2 leaves most of the grid empty.
+    "one_warp_sparse": dict(cfg=2, num_seqs=64, lens=("uniform", 1, 30), ps=16, max_len=256),
+    # same shape, lengths near the bound: 64 x 8 x ~15 units, several waves of one-warp units.
+    "one_warp_waves": dict(cfg=2, num_seqs=64, lens=("uniform", 224, 255), ps=16, max_len=256),
 }
 
 
