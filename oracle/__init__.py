@@ -12,6 +12,10 @@ Contents
                       tables (C++ in csrc/pkv_oracle.cpp, threaded over rows).
   brute            -- a pure-Python restatement used to pin the C++ one.
   sizing           -- the pages' closed forms for KV bytes, blocks and waste.
+  e4m3_decode, e4m3_encode, write_cache_fp8, copy_blocks_fp8,
+  decode_attention_fp8, apply_step_fp8
+                   -- the same path over FP8 (e4m3) pools with one scale per
+                      (physical block, KV head) for K and for V.
 
 Sources (four web pages on paged KV caches):
   * "gpu_paged_kv_cache" (aicassindra), section "The write path: slot mapping
@@ -23,6 +27,15 @@ Sources (four web pages on paged KV caches):
   * "PagedAttention internals" section 02 and "tm_paged_attention" (aicassindra)
     "The architecture" / "End-to-end flow": the table translation and the
     decode step attending over the full history.
+  * "PagedAttention internals" section 06, "Blocks as quantization groups":
+    the 16-token block as the quantization group, its scales riding with the
+    block, including across copy-on-write; and "KV Cache & PagedAttention"
+    (lattice-ai-eng) sections 5 ("Quality") and 7: K, V stored in FP8 on
+    Hopper/Blackwell.  Readings: one float scale per
+    (block, KV head) for K and for V; a value is decode(code) * scale; the
+    write path quantizes a new row with its block's scale as
+    e4m3(float32(x) / float32(scale)), rounding to nearest-even and
+    saturating to +-448 (the format has no infinities).
 """
 from __future__ import annotations
 
@@ -33,7 +46,8 @@ import numpy as np
 
 from . import build as _build
 
-__all__ = ["write_cache", "copy_blocks", "decode_attention", "hardware_threads"]
+__all__ = ["write_cache", "copy_blocks", "decode_attention", "hardware_threads", "e4m3_decode", "e4m3_encode",
+           "write_cache_fp8", "copy_blocks_fp8", "decode_attention_fp8", "apply_step_fp8"]
 
 _LIB = None
 
@@ -46,6 +60,10 @@ def _lib():
         f = lib.pkv_oracle_decode_attention
         f.restype = ctypes.c_int
         f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_void_p] + [ctypes.c_int] * 6 + [
+            ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
+        f8 = lib.pkv_oracle_decode_attention_fp8
+        f8.restype = ctypes.c_int
+        f8.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int, ctypes.c_void_p] + [ctypes.c_int] * 6 + [
             ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
         lib.pkv_oracle_hardware_threads.restype = ctypes.c_int
         _LIB = lib
@@ -126,6 +144,124 @@ def apply_step(wl, *, attention: bool = True, rows=None):
     if attention:
         out = decode_attention(wl.q, k, v, wl.block_tables, wl.context_lens, wl.scale, wl.dtype, rows=rows)
     return k, v, out
+
+
+# ------------------------------------------------------------------ FP8 pools
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """e4m3 codes (uint8) -> float64, from the format's definition: sign bit,
+    4 exponent bits (bias 7), 3 mantissa bits; exponent 0 is subnormal
+    (m/8 * 2^-6); exponent 15 with mantissa 7 is NaN; no infinities."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where((c >> 7) & 1, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    v = np.where(e == 0, np.ldexp(m.astype(np.float64), -9), np.ldexp((8 + m).astype(np.float64), e - 10))
+    v = np.where((e == 15) & (m == 7), np.nan, v)
+    return sign * v
+
+
+_E4M3_POS = e4m3_decode(np.arange(0x7F, dtype=np.uint8))  # codes 0x00..0x7E: 0 .. 448, ascending
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """float32 values -> e4m3 codes: round to the nearest representable value,
+    ties to the even code (even mantissa), magnitudes above 448 saturate to
+    448, NaN -> 0x7F (with the sign bit).  Nearest-value search over the
+    format's finite values."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    sign = np.signbit(x).astype(np.int64) << 7
+    a = np.minimum(np.abs(np.nan_to_num(x, nan=0.0)), 448.0)
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, 0x7E)
+    lo = np.clip(hi - 1, 0, 0x7E)
+    d_lo, d_hi = a - _E4M3_POS[lo], _E4M3_POS[hi] - a
+    pick = np.where(d_hi < d_lo, hi, np.where(d_lo < d_hi, lo, np.where(lo % 2 == 0, lo, hi)))
+    code = np.where(np.isnan(x), 0x7F, pick) | sign
+    return code.astype(np.uint8)
+
+
+def _widen16(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """16-bit patterns -> float32 (exact)."""
+    b = np.asarray(bits, dtype=np.uint16)
+    if dtype == "f16":
+        return b.view(np.float16).astype(np.float32)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def write_cache_fp8(k8: np.ndarray, v8: np.ndarray, k_scale: np.ndarray, v_scale: np.ndarray, k_new: np.ndarray,
+                    v_new: np.ndarray, slot_mapping: np.ndarray, dtype: str) -> None:
+    """In place: for each token i with slot >= 0 (block b = slot // B, offset
+    o = slot % B) and KV head g, pool[b][o][g] = e4m3(float32(new[i][g]) /
+    scale[b][g]) for K and V.  new rows hold `dtype` (f16/bf16) patterns."""
+    B = k8.shape[1]
+    for i, slot in enumerate(np.asarray(slot_mapping).tolist()):
+        if slot < 0:
+            continue
+        b, o = divmod(slot, B)
+        for pool, scales, new in ((k8, k_scale, k_new), (v8, v_scale, v_new)):
+            x = _widen16(new[i], dtype)  # [H_kv, D]
+            pool[b, o] = e4m3_encode(x / scales[b].astype(np.float32)[:, None])
+
+
+def copy_blocks_fp8(k8: np.ndarray, v8: np.ndarray, k_scale: np.ndarray, v_scale: np.ndarray,
+                    pairs: np.ndarray) -> None:
+    """In place: for each (src, dst) pair, block dst := block src, codes and scales (K and V)."""
+    for src, dst in np.asarray(pairs).reshape(-1, 2).tolist():
+        k8[dst] = k8[src]
+        v8[dst] = v8[src]
+        k_scale[dst] = k_scale[src]
+        v_scale[dst] = v_scale[src]
+
+
+def decode_attention_fp8(q: np.ndarray, k8: np.ndarray, v8: np.ndarray, k_scale: np.ndarray, v_scale: np.ndarray,
+                         block_tables: np.ndarray, context_lens: np.ndarray, scale: float, dtype: str, rows=None,
+                         num_threads: int = 0) -> np.ndarray:
+    """fp64 paged decode attention over FP8 pools: K = e4m3_decode(k8) *
+    k_scale[block][g] (V likewise); q holds `dtype` patterns.  Returns as
+    decode_attention does."""
+    lib = _lib()
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k8 = np.ascontiguousarray(k8, dtype=np.uint8)
+    v8 = np.ascontiguousarray(v8, dtype=np.uint8)
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    S, Hq, D = q.shape
+    NB, B, Hkv, D2 = k8.shape
+    assert D2 == D and v8.shape == k8.shape and ks.shape == (NB, Hkv) and vs.shape == (NB, Hkv)
+    if rows is None:
+        out = np.zeros((S, Hq, D), dtype=np.float64)
+        rows_arr, n = None, S * Hq
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+        n = rows_arr.shape[0]
+        out = np.zeros((n, D), dtype=np.float64)
+    if n == 0:
+        return out
+    rc = lib.pkv_oracle_decode_attention_fp8(
+        out.ctypes.data, q.ctypes.data, k8.ctypes.data, v8.ctypes.data, ks.ctypes.data, vs.ctypes.data,
+        bt.ctypes.data, bt.shape[1], cl.ctypes.data, S, Hq, Hkv, D, B, NB, float(scale), 1 if dtype == "bf16" else 0,
+        None if rows_arr is None else rows_arr.ctypes.data, n, int(num_threads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the input (code {rc}): table entry or length out of range")
+    return out
+
+
+def apply_step_fp8(wl, pools, *, attention: bool = True, rows=None):
+    """One decode step of a workload over its FP8 pools (pkv_inputs.Fp8Pools),
+    on copies: copy_blocks_fp8, write_cache_fp8, then (optionally) attention.
+    Returns (k8, v8, k_scale, v_scale, out_or_None)."""
+    k8, v8 = pools.k8.copy(), pools.v8.copy()
+    ks, vs = pools.k_scale.copy(), pools.v_scale.copy()
+    copy_blocks_fp8(k8, v8, ks, vs, wl.copy_pairs)
+    write_cache_fp8(k8, v8, ks, vs, wl.k_new, wl.v_new, wl.slot_mapping, wl.dtype)
+    out = None
+    if attention:
+        out = decode_attention_fp8(wl.q, k8, v8, ks, vs, wl.block_tables, wl.context_lens, wl.scale, wl.dtype,
+                                   rows=rows)
+    return k8, v8, ks, vs, out
 
 
 if os.environ.get("PKV_ORACLE_EAGER_BUILD"):

@@ -31,6 +31,12 @@
 //
 // Pool layout: [num_blocks][block_size][num_kv_heads][head_dim], 16-bit
 // elements (IEEE binary16 or bfloat16 bit patterns).
+//
+// FP8 pools ("PagedAttention internals" section 06, "Blocks as quantization
+// groups": a 16-token block is the quantization group, its scales ride with
+// the block; "KV Cache & PagedAttention" section 5: K, V in FP8): 8-bit e4m3 codes with one scale per (physical block, KV head)
+// for K and one for V; an element's value is decode(code) * scale.  The
+// query stays 16-bit.
 
 #include <atomic>
 #include <cmath>
@@ -65,11 +71,33 @@ double bf16_bits_to_double(uint16_t b) {
   return static_cast<double>(f);
 }
 
+// e4m3 (OCP FP8, "fn" variant): sign bit, 4 exponent bits with bias 7, 3
+// mantissa bits; no infinities; exponent 15 with mantissa 7 is NaN; the
+// largest finite magnitude is 1.75 * 2^8 = 448.  From the format's definition.
+double e4m3_to_double(uint8_t c) {
+  const int sign = (c >> 7) & 1;
+  const int e = (c >> 3) & 0xF;
+  const int m = c & 0x7;
+  double v;
+  if (e == 15 && m == 7) {
+    v = NAN;
+  } else if (e == 0) {
+    v = std::ldexp(static_cast<double>(m), -9);  // subnormal: (m / 8) * 2^-6
+  } else {
+    v = std::ldexp(static_cast<double>(8 + m), e - 10);  // (1 + m/8) * 2^(e-7)
+  }
+  return sign ? -v : v;
+}
+
 struct Problem {
   double* out;
   const uint16_t* q;
   const uint16_t* k_pool;
   const uint16_t* v_pool;
+  const uint8_t* k8;       // FP8 pools (then k_pool / v_pool are unused)
+  const uint8_t* v8;
+  const float* k_scale;    // [num_blocks][num_kv_heads]
+  const float* v_scale;
   const int32_t* block_tables;
   int max_blocks_per_seq;
   const int32_t* context_lens;
@@ -102,9 +130,17 @@ int one_row(const Problem& P, int s, int h, double* out_row) {
     if (phys < 0 || phys >= P.num_blocks) return 1;
     const int off = t % B;
     const int64_t base = ((phys * B + off) * P.num_kv_heads + g) * static_cast<int64_t>(D);
-    for (int d = 0; d < D; ++d) {
-      K[static_cast<size_t>(t) * D + d] = widen(P, P.k_pool[base + d]);
-      V[static_cast<size_t>(t) * D + d] = widen(P, P.v_pool[base + d]);
+    if (P.k8) {
+      const double ks = P.k_scale[phys * P.num_kv_heads + g], vs = P.v_scale[phys * P.num_kv_heads + g];
+      for (int d = 0; d < D; ++d) {
+        K[static_cast<size_t>(t) * D + d] = e4m3_to_double(P.k8[base + d]) * ks;
+        V[static_cast<size_t>(t) * D + d] = e4m3_to_double(P.v8[base + d]) * vs;
+      }
+    } else {
+      for (int d = 0; d < D; ++d) {
+        K[static_cast<size_t>(t) * D + d] = widen(P, P.k_pool[base + d]);
+        V[static_cast<size_t>(t) * D + d] = widen(P, P.v_pool[base + d]);
+      }
     }
   }
   std::vector<double> qv(D);
@@ -133,6 +169,9 @@ int one_row(const Problem& P, int s, int h, double* out_row) {
   return 0;
 }
 
+// Runs one_row over the requested rows on num_threads threads (0: all).
+int run_rows(const Problem& P, int num_threads);
+
 }  // namespace
 
 extern "C" {
@@ -149,10 +188,41 @@ int pkv_oracle_decode_attention(double* out, const uint16_t* q, const uint16_t* 
   if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens) return 2;
   if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0)
     return 2;
-  Problem P{out,          q,           k_pool,      v_pool,       block_tables,
-            max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
-            head_dim,     block_size,  num_blocks,  scale,        is_bf16,
-            rows,         rows ? n_rows : num_seqs * num_q_heads};
+  Problem P{out,          q,           k_pool,      v_pool,       nullptr,     nullptr,
+            nullptr,      nullptr,     block_tables, max_blocks_per_seq, context_lens, num_seqs,
+            num_q_heads,  num_kv_heads, head_dim,   block_size,  num_blocks,  scale,
+            is_bf16,      rows,        rows ? n_rows : num_seqs * num_q_heads};
+  return run_rows(P, num_threads);
+}
+
+// The same over FP8 pools: k8, v8 are e4m3 codes [num_blocks][block_size]
+// [num_kv_heads][head_dim]; k_scale, v_scale are float [num_blocks]
+// [num_kv_heads]; q is 16-bit (is_bf16 selects its format).
+int pkv_oracle_decode_attention_fp8(double* out, const uint16_t* q, const uint8_t* k8, const uint8_t* v8,
+                                    const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                                    int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                    int num_blocks, double scale, int is_bf16, const int32_t* rows,
+                                    int n_rows, int num_threads) {
+  if (!out || !q || !k8 || !v8 || !k_scale || !v_scale || !block_tables || !context_lens) return 2;
+  if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0)
+    return 2;
+  Problem P{out,          q,           nullptr,     nullptr,      k8,          v8,
+            k_scale,      v_scale,     block_tables, max_blocks_per_seq, context_lens, num_seqs,
+            num_q_heads,  num_kv_heads, head_dim,   block_size,  num_blocks,  scale,
+            is_bf16,      rows,        rows ? n_rows : num_seqs * num_q_heads};
+  return run_rows(P, num_threads);
+}
+
+int pkv_oracle_hardware_threads(void) {
+  return static_cast<int>(std::thread::hardware_concurrency());
+}
+
+}  // extern "C"
+
+namespace {
+
+int run_rows(const Problem& P, int num_threads) {
   std::atomic<int> next{0}, status{0};
   auto worker = [&]() {
     for (;;) {
@@ -177,8 +247,4 @@ int pkv_oracle_decode_attention(double* out, const uint16_t* q, const uint16_t* 
   return status.load();
 }
 
-int pkv_oracle_hardware_threads(void) {
-  return static_cast<int>(std::thread::hardware_concurrency());
-}
-
-}  // extern "C"
+}  // namespace

@@ -170,6 +170,7 @@ class Workload:
     refcount: dict
     protected_blocks: np.ndarray  # blocks that must stay bit-unchanged by the step
     poisoned: bool
+    live: np.ndarray  # bool [num_blocks, block_size]: slots holding a token cached before the step
 
     @property
     def max_context_len(self) -> int:
@@ -329,5 +330,78 @@ def make_workload(cfg: int, *, poison: bool = False, seed: int | None = None, **
         copy_pairs=np.asarray(pairs, dtype=np.int32).reshape(-1, 2),
         q=q, k_new=k_new, v_new=v_new, k_pool=k_pool, v_pool=v_pool,
         refcount=dict(bm.refcount), protected_blocks=np.asarray(sorted(protected), dtype=np.int32),
-        poisoned=poison,
+        poisoned=poison, live=live,
     )
+
+
+# ------------------------------------------------------------------ FP8 pools
+#
+# FP8 (e4m3) pools for the quantised-cache variant: one byte per element in the
+# same [num_blocks, block_size, H_kv, D] layout, plus one float32 scale per
+# (block, KV head) for K and for V.  Codes are drawn directly (this module
+# encodes nothing): sign uniform, magnitude code uniform over
+# [FP8_MIN_MAG_CODE, 0x7E] (0.25 .. 448, log-uniform in value), so no draw is
+# 0x7F/0xFF, the format's NaN.  Scales are 2^u with u ~ U[-7.5, -6.5] (so a
+# block's largest magnitude 448 * scale lies in 2.5 .. 5, like a per-block
+# absmax scale over N(0,1) data), or, with exact=True, integer powers of two
+# (-8..-6) so that every dequantised value is exact in 16 bits.
+
+FP8_NAN = 0x7F
+FP8_MIN_MAG_CODE = 0x28
+
+
+@dataclass
+class Fp8Pools:
+    k8: np.ndarray       # uint8 [NB, B, H_kv, D]
+    v8: np.ndarray
+    k_scale: np.ndarray  # float32 [NB, H_kv]
+    v_scale: np.ndarray
+
+    def kv_bytes_read(self, wl: "Workload") -> int:
+        """Bytes a decode pass over `wl` reads from these pools: one byte per
+        element plus the K and V scale of each (table entry, KV head)."""
+        toks = int(wl.context_lens.astype(np.int64).sum())
+        blocks = int(((wl.context_lens.astype(np.int64) + wl.block_size - 1) // wl.block_size).sum())
+        return toks * wl.num_kv_heads * wl.head_dim * 2 + blocks * wl.num_kv_heads * 4 * 2
+
+
+def draw_fp8_codes(shape, rng):
+    """e4m3 codes: random sign, magnitude code uniform over [FP8_MIN_MAG_CODE, 0x7E]."""
+    mag = rng.integers(FP8_MIN_MAG_CODE, 0x7E, size=shape, endpoint=True, dtype=np.int64)
+    sign = rng.integers(0, 2, size=shape, dtype=np.int64) << 7
+    return (mag | sign).astype(np.uint8)
+
+
+def make_fp8_pools(wl: Workload, *, seed: int | None = None, exact: bool = False,
+                   poison: bool | None = None) -> Fp8Pools:
+    """Seeded FP8 pools for workload `wl` (its tables, lengths, slot mapping
+    and copy pairs; its 16-bit pools are not used).  With poison (default:
+    wl.poisoned) every slot holding no live token reads as NaN codes, and the
+    scales of blocks that neither a table (after the step) nor a copy source
+    references, and of copy-on-write destinations (overwritten by the step's
+    copy before any read), are NaN."""
+    rng = np.random.default_rng((wl.cfg * 7919 + 17) if seed is None else seed)
+    shape = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+    k8 = draw_fp8_codes(shape, rng)
+    v8 = draw_fp8_codes(shape, rng)
+    sshape = (wl.num_blocks, wl.num_kv_heads)
+    if exact:
+        ks = np.ldexp(1.0, rng.integers(-8, -6, size=sshape, endpoint=True)).astype(np.float32)
+        vs = np.ldexp(1.0, rng.integers(-8, -6, size=sshape, endpoint=True)).astype(np.float32)
+    else:
+        ks = np.exp2(rng.uniform(-7.5, -6.5, size=sshape)).astype(np.float32)
+        vs = np.exp2(rng.uniform(-7.5, -6.5, size=sshape)).astype(np.float32)
+    if wl.poisoned if poison is None else poison:
+        k8[~wl.live] = FP8_NAN
+        v8[~wl.live] = FP8_NAN
+        used = np.zeros(wl.num_blocks, dtype=bool)
+        t = wl.block_tables
+        used[t[t >= 0]] = True
+        if wl.copy_pairs.size:
+            used[wl.copy_pairs[:, 0]] = True
+        dead = ~used
+        if wl.copy_pairs.size:
+            dead[wl.copy_pairs[:, 1]] = True
+        ks[dead] = np.nan
+        vs[dead] = np.nan
+    return Fp8Pools(k8=k8, v8=v8, k_scale=ks, v_scale=vs)
