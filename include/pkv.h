@@ -251,6 +251,69 @@ pkv_status pkv_decode_attention_static_workspace(
     int head_dim, int block_size, int num_blocks, float scale, int partition_size, int max_context_len,
     pkv_dtype kv_dtype, pkv_dtype out_dtype, int32_t* dev_status, void* stream);
 
+/*
+ * ---------------------------------------------------------------- FP8 pools
+ *
+ * Pools of 8-bit e4m3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits; largest finite magnitude 448; codes 0x7F/0xFF are NaN; no infinity)
+ * in the same [num_blocks][block_size][num_kv_heads][head_dim] layout, one
+ * byte per element, halving the bytes decode reads ([P4 section 5]: K, V
+ * stored in FP8).  The 16-token block is the quantisation group and its
+ * scales ride with it, through copy-on-write included [P2 section 06,
+ * "Blocks as quantization groups"]:
+ *   k_scale, v_scale : float32 [num_blocks][num_kv_heads], device, 4-byte
+ *                      aligned; element value = decode(code) * scale of its
+ *                      (block, KV head).
+ * The library never chooses a scale: the caller sets a block's scales when
+ * it allocates the block (e.g. from a calibrated per-layer amax) and the
+ * write path quantises new rows with them.  Pool pointers 16-byte aligned.
+ */
+
+/*
+ * pkv_write_cache_fp8 -- the write path into FP8 pools: for every token i
+ * with slot_mapping[i] >= 0 (b = slot / 16, o = slot % 16) and KV head g,
+ *     k_pool[b][o][g][:] = e4m3(float32(k_new[i][g][:]) / k_scale[b][g])
+ * (and V likewise), the division in IEEE float32, rounded to the nearest
+ * code with ties to the even mantissa, magnitudes beyond 448 saturating to
+ * +-448.  k_new, v_new hold new_dtype (PKV_F16 / PKV_BF16) values, rows
+ * 16-byte aligned, new_row_stride as in pkv_write_cache.  head_dim must be a
+ * multiple of 16.  Padding (-1) and error handling as pkv_write_cache.
+ */
+pkv_status pkv_write_cache_fp8(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                               const float* k_scale, const float* v_scale, const int32_t* slot_mapping,
+                               int num_tokens, int64_t new_row_stride, int num_kv_heads, int head_dim,
+                               int block_size, int num_blocks, pkv_dtype new_dtype, int32_t* dev_status,
+                               void* stream);
+
+/*
+ * pkv_copy_blocks_fp8 -- copy-on-write over FP8 pools: for each pair, block
+ * dst := block src in both pools (bytes), and k_scale[dst][:] :=
+ * k_scale[src][:], v_scale likewise.  Pair rules and errors as
+ * pkv_copy_blocks.
+ */
+pkv_status pkv_copy_blocks_fp8(void* k_pool, void* v_pool, float* k_scale, float* v_scale,
+                               const int32_t* pairs, int num_pairs, int num_kv_heads, int head_dim,
+                               int block_size, int num_blocks, int32_t* dev_status, void* stream);
+
+/*
+ * pkv_decode_attention_fp8 -- pkv_decode_attention over FP8 pools:
+ *     k_t = decode(k_pool[block_tables[s][t/16]][t%16][g]) * k_scale[that block][g],
+ * v_t likewise, the rest as pkv_decode_attention (same workspace size from
+ * pkv_decode_workspace_bytes, same split-K partials and reduce kernel).
+ * q has q_dtype (PKV_F16 or PKV_BF16) and must be 16-byte aligned.
+ * Supported: head_dim 128, fixed partitions (partition_size >= 0; the
+ * balanced split returns PKV_ERR_UNSUPPORTED).  Rows of tokens >= L in a
+ * sequence's last block, NaN codes included, are never used.
+ */
+pkv_status pkv_decode_attention_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                    const float* k_scale, const float* v_scale,
+                                    const int32_t* block_tables, int max_blocks_per_seq,
+                                    const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                    int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                    float scale, int partition_size, int max_context_len,
+                                    void* workspace, size_t workspace_bytes, pkv_dtype q_dtype,
+                                    pkv_dtype out_dtype, int32_t* dev_status, void* stream);
+
 /* Static string naming a status code.  Host function. */
 const char* pkv_status_string(pkv_status status);
 

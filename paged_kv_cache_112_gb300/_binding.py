@@ -43,6 +43,11 @@ _SIGS["pkv_decode_step"] = ([_c_void_p] * 4 + [_c_int64] + [_c_void_p] * 3 + [_c
                             [_c_int] * 6 + [_c_float, _c_int, _c_int, _c_void_p, _c_size_t, _c_int, _c_int,
                                             _c_void_p, _c_void_p])
 _SIGS["pkv_decode_step_partitions"] = _SIGS["pkv_decode_step"]
+_SIGS["pkv_write_cache_fp8"] = [_c_void_p] * 7 + [_c_int, _c_int64] + [_c_int] * 5 + [_c_void_p, _c_void_p]
+_SIGS["pkv_copy_blocks_fp8"] = [_c_void_p] * 5 + [_c_int] * 5 + [_c_void_p, _c_void_p]
+_SIGS["pkv_decode_attention_fp8"] = ([_c_void_p] * 7 + [_c_int, _c_void_p] + [_c_int] * 6 +
+                                     [_c_float, _c_int, _c_int, _c_void_p, _c_size_t, _c_int, _c_int, _c_void_p,
+                                      _c_void_p])
 
 _LIB = None
 
@@ -210,3 +215,62 @@ def decode_step_partitions(out, q, k_new, v_new, k_pool, v_pool, block_tables, c
                                                          context_lens, slot_mapping, scale, partition_size,
                                                          max_context_len, workspace, status, stream)),
            "pkv_decode_step_partitions")
+
+
+# ------------------------------------------------------------------ FP8 pools
+# Pools are uint8 [NB, 16, H_kv, D] tensors of e4m3 codes; scales float32
+# [NB, H_kv] (one per block and KV head, for K and for V).
+
+
+def _fp8_pools(k_pool, v_pool, k_scale, v_scale):
+    _need_cuda(k_pool, v_pool, k_scale, v_scale)
+    if k_pool.dtype != torch.uint8 or v_pool.dtype != torch.uint8 or v_pool.shape != k_pool.shape:
+        raise PkvError("FP8 pools must be uint8 tensors of one shape [NB, 16, H_kv, D]")
+    NB, B, Hkv, D = k_pool.shape
+    for sc in (k_scale, v_scale):
+        if sc.dtype != torch.float32 or tuple(sc.shape) != (NB, Hkv):
+            raise PkvError("scales must be float32 [NB, H_kv]")
+    return NB, B, Hkv, D
+
+
+def write_cache_fp8(k_new, v_new, k_pool, v_pool, k_scale, v_scale, slot_mapping, *, status=None, stream=None):
+    """pkv_write_cache_fp8: k_new/v_new f16/bf16 [T, H_kv, D] quantised into the FP8 pools."""
+    NB, B, Hkv, D = _fp8_pools(k_pool, v_pool, k_scale, v_scale)
+    _need_cuda(slot_mapping, status)
+    T = k_new.shape[0]
+    for t in (k_new, v_new):
+        if not t.is_cuda or t.dim() != 3 or t.shape[1:] != (Hkv, D) or t.stride(2) != 1 or t.stride(1) != D:
+            raise PkvError("k_new/v_new must be CUDA [T, H_kv, D] with dense rows")
+    if k_new.stride(0) != v_new.stride(0) or k_new.dtype != v_new.dtype:
+        raise PkvError("k_new and v_new must share a row stride and a dtype")
+    _check(load().pkv_write_cache_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
+                                      _ptr(v_scale), _ptr(slot_mapping), T, int(k_new.stride(0)), Hkv, D, B, NB,
+                                      _kv_dtype(k_new), _ptr(status), _stream(stream)), "pkv_write_cache_fp8")
+
+
+def copy_blocks_fp8(k_pool, v_pool, k_scale, v_scale, pairs, *, status=None, stream=None):
+    """pkv_copy_blocks_fp8: pairs int32 [P, 2] (src, dst); codes and scales move together."""
+    NB, B, Hkv, D = _fp8_pools(k_pool, v_pool, k_scale, v_scale)
+    _need_cuda(pairs, status)
+    _check(load().pkv_copy_blocks_fp8(_ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(pairs),
+                                      int(pairs.shape[0]), Hkv, D, B, NB, _ptr(status), _stream(stream)),
+           "pkv_copy_blocks_fp8")
+
+
+def decode_attention_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, context_lens, scale, *,
+                         partition_size=0, max_context_len, workspace=None, status=None, stream=None):
+    """pkv_decode_attention_fp8 (partition kernel + reduce kernel); q f16/bf16 [S, H_q, D]."""
+    NB, B, Hkv, D = _fp8_pools(k_pool, v_pool, k_scale, v_scale)
+    _need_cuda(out, q, block_tables, context_lens, workspace, status)
+    S, Hq, Dq = q.shape
+    if Dq != D or out.shape != q.shape or out.dtype not in _DTYPES:
+        raise PkvError("q and out must be [S, H_q, D] with the pools' D")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise PkvError("block_tables and context_lens must be int32")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().pkv_decode_attention_fp8(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
+                                           _ptr(v_scale), _ptr(block_tables), int(block_tables.shape[1]),
+                                           _ptr(context_lens), S, Hq, Hkv, D, B, NB, float(scale),
+                                           int(partition_size), int(max_context_len), _ptr(workspace), ws_bytes,
+                                           _kv_dtype(q), _DTYPES[out.dtype], _ptr(status), _stream(stream)),
+           "pkv_decode_attention_fp8")

@@ -102,30 +102,36 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Describes a pool [num_blocks * 16 rows][num_kv_heads * head_dim / 64 lines][64 elements]
-// so that one box {64, 1, 16} is the 16 token rows of one 128-byte line of
-// one head: half of a (block, head) tile at head_dim 128, all of it at 64.
-bool encode_pool_map_uncached(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, int head_dim) {
+// Describes a pool of `eb`-byte elements as [num_blocks * 16 rows]
+// [num_kv_heads * head_dim * eb / 128 lines][128 bytes] so that one box is
+// the 16 token rows of one 128-byte line of one head: a (block, head) tile
+// is head_dim * eb / 128 boxes (16-bit: 2 at head_dim 128, 1 at 64; FP8: 1
+// at head_dim 128).
+bool encode_pool_map_uncached(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, int head_dim,
+                              int eb) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(num_kv_heads) * (head_dim / 64),
+  const cuuint32_t line = 128 / eb;  // elements per 128-byte line
+  const cuuint64_t dims[3] = {line, static_cast<cuuint64_t>(num_kv_heads) * (head_dim / line),
                               static_cast<cuuint64_t>(num_blocks) * kBlockSize};
-  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
-  const cuuint32_t box[3] = {64, 1, kBlockSize};
+  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(num_kv_heads) * head_dim * eb};
+  const cuuint32_t box[3] = {line, 1, kBlockSize};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        head_dim >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+  const CUresult r = fn(map, eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
+                        const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B,
+                        head_dim * eb >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
 // Descriptors depend only on the pool address and geometry, so recent ones
 // are kept (a small round-robin cache) instead of re-encoded every call.
-bool encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, int head_dim) {
+bool encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, int head_dim,
+                     int eb = 2) {
   struct Entry {
     const void* pool;
-    int num_blocks, num_kv_heads, head_dim;
+    int num_blocks, num_kv_heads, head_dim, eb;
     CUtensorMap map;
   };
   static Entry cache[32];
@@ -134,14 +140,15 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int num
   {
     std::lock_guard<std::mutex> lock(mu);
     for (const Entry& e : cache)
-      if (e.pool == pool && e.num_blocks == num_blocks && e.num_kv_heads == num_kv_heads && e.head_dim == head_dim) {
+      if (e.pool == pool && e.num_blocks == num_blocks && e.num_kv_heads == num_kv_heads &&
+          e.head_dim == head_dim && e.eb == eb) {
         *map = e.map;
         return true;
       }
   }
-  if (!encode_pool_map_uncached(map, pool, num_blocks, num_kv_heads, head_dim)) return false;
+  if (!encode_pool_map_uncached(map, pool, num_blocks, num_kv_heads, head_dim, eb)) return false;
   std::lock_guard<std::mutex> lock(mu);
-  cache[next] = Entry{pool, num_blocks, num_kv_heads, head_dim, *map};
+  cache[next] = Entry{pool, num_blocks, num_kv_heads, head_dim, eb, *map};
   next = (next + 1) % 32;
   return true;
 }
@@ -440,6 +447,97 @@ pkv_status pkv_decode_attention(void* out, const void* q, const void* k_pool, co
   if (st != PKV_OK) return st;
   return pkv_decode_reduce(out, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, partition_size,
                            max_context_len, workspace, workspace_bytes, out_dtype, dev_status, stream);
+}
+
+// ------------------------------------------------------------ FP8 pools
+
+pkv_status pkv_write_cache_fp8(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                               const float* k_scale, const float* v_scale, const int32_t* slot_mapping,
+                               int num_tokens, int64_t new_row_stride, int num_kv_heads, int head_dim,
+                               int block_size, int num_blocks, pkv_dtype new_dtype, int32_t* dev_status,
+                               void* stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || new_row_stride < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (!kv_dtype_ok(new_dtype)) return PKV_ERR_INVALID_ARG;
+  if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  if (head_dim % 16 != 0) return PKV_ERR_UNSUPPORTED;  // 16 codes per vector, within one head
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !k_pool || !v_pool || !k_scale || !v_scale || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  const int row = num_kv_heads * head_dim;
+  const int64_t stride = new_row_stride ? new_row_stride : row;
+  if (stride < row || stride % 8 != 0) return PKV_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+      !aligned(k_scale, 4) || !aligned(v_scale, 4) || !aligned(slot_mapping, 4))
+    return PKV_ERR_INVALID_ARG;
+  WriteCacheFp8Args a{};
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.k_pool = static_cast<uint8_t*>(k_pool);
+  a.v_pool = static_cast<uint8_t*>(v_pool);
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.slot_mapping = slot_mapping;
+  a.dev_status = dev_status;
+  a.stride = stride;
+  a.num_slots = static_cast<int64_t>(num_blocks) * kBlockSize;
+  a.num_tokens = num_tokens;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.new_bf16 = new_dtype == PKV_BF16;
+  return launch_write_cache_fp8(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_copy_blocks_fp8(void* k_pool, void* v_pool, float* k_scale, float* v_scale, const int32_t* pairs,
+                               int num_pairs, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                               int32_t* dev_status, void* stream) {
+  if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+  if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PKV_OK;
+  if (!k_pool || !v_pool || !k_scale || !v_scale || !pairs) return PKV_ERR_INVALID_ARG;
+  if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(k_scale, 4) || !aligned(v_scale, 4) ||
+      !aligned(pairs, 4))
+    return PKV_ERR_INVALID_ARG;
+  CopyBlocksArgs a{};
+  a.k_pool = static_cast<uint16_t*>(k_pool);
+  a.v_pool = static_cast<uint16_t*>(v_pool);
+  a.pairs = pairs;
+  a.dev_status = dev_status;
+  a.block_elems = static_cast<int64_t>(kBlockSize) * num_kv_heads * head_dim / 2;  // 16 * H_kv * D bytes
+  a.num_pairs = num_pairs;
+  a.num_blocks = num_blocks;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.scales_per_block = num_kv_heads;
+  return launch_copy_blocks(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_decode_attention_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                    const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                                    int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                                    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                    float scale, int partition_size, int max_context_len, void* workspace,
+                                    size_t workspace_bytes, pkv_dtype q_dtype, pkv_dtype out_dtype,
+                                    int32_t* dev_status, void* stream) {
+  if (partition_size == PKV_PARTITION_BALANCED) return PKV_ERR_UNSUPPORTED;
+  DecodeCall c{};
+  pkv_status st = prepare_decode(&c, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+                                 num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                                 partition_size, max_context_len, workspace, workspace_bytes, q_dtype, out_dtype,
+                                 dev_status, false);
+  if (st != PKV_OK) return st;
+  if (head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (!k_scale || !v_scale || !aligned(k_scale, 4) || !aligned(v_scale, 4) || !aligned(q, 16))
+    return PKV_ERR_INVALID_ARG;
+  c.args.k_scale = k_scale;
+  c.args.v_scale = v_scale;
+  if (!encode_pool_map(&c.tmap_k, k_pool, num_blocks, num_kv_heads, head_dim, 1) ||
+      !encode_pool_map(&c.tmap_v, v_pool, num_blocks, num_kv_heads, head_dim, 1))
+    return PKV_ERR_CUDA;
+  const cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  if (launch_decode_partitions_fp8(c.args, c.tmap_k, c.tmap_v, head_dim, q_dtype == PKV_BF16, strm) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return launch_decode_reduce(c.args, head_dim, strm) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 const char* pkv_status_string(pkv_status s) {

@@ -13,6 +13,8 @@
 // threads move adjacent vectors of the same row (coalesced 128-byte lines on
 // both sides).  Grids are capped at a multiple of the SM count and
 // grid-stride over the work.
+#include <cuda_fp16.h>
+
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -71,6 +73,74 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(CopyBlocksArgs a) {
     const uint4 val = reinterpret_cast<const uint4*>(pool + src * a.block_elems)[v];
     reinterpret_cast<uint4*>(pool + dst * a.block_elems)[v] = val;
   }
+  // FP8 pools: the block's scales travel with it ("PagedAttention
+  // internals", section 06).
+  if (a.k_scale) {
+    const int64_t n = static_cast<int64_t>(a.num_pairs) * 2 * a.scales_per_block;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      const int h = static_cast<int>(idx % a.scales_per_block);
+      const int64_t r = idx / a.scales_per_block;
+      const int64_t pair = r >> 1;
+      const int src = a.pairs[2 * pair];
+      const int dst = a.pairs[2 * pair + 1];
+      if (src < 0 || src >= a.num_blocks || dst < 0 || dst >= a.num_blocks) continue;  // flagged above
+      float* sc = (r & 1) ? a.v_scale : a.k_scale;
+      sc[static_cast<int64_t>(dst) * a.scales_per_block + h] = sc[static_cast<int64_t>(src) * a.scales_per_block + h];
+    }
+  }
+}
+
+// FP8 write path: each thread quantises 16 consecutive elements of one new
+// row (one head's slice) with the scale of the destination block and KV
+// head, e4m3(float32(x) / scale) rounded to nearest even and saturated to
+// the largest finite code, and stores the 16 codes as one vector.
+__device__ __forceinline__ float widen16(uint32_t bits, bool bf16) {
+  return bf16 ? __uint_as_float(bits << 16) : __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+}
+
+// Two floats -> two e4m3 codes, `lo` in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2_satfinite(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__global__ void __launch_bounds__(256) write_cache_fp8_kernel(WriteCacheFp8Args a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int row = a.num_kv_heads * a.head_dim;
+  const int vec_per_row = row / 16;
+  const int64_t total = static_cast<int64_t>(a.num_tokens) * 2 * vec_per_row;
+  const bool bf16 = a.new_bf16 != 0;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int v = static_cast<int>(idx % vec_per_row);
+    const int64_t r = idx / vec_per_row;
+    const int which = static_cast<int>(r & 1);
+    const int64_t tok = r >> 1;
+    const uint4* src = reinterpret_cast<const uint4*>((which ? a.v_new : a.k_new) + tok * a.stride) + 2 * v;
+    const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
+    const int64_t slot = a.slot_mapping[tok];
+    if (slot < 0 || slot >= a.num_slots) {
+      if (slot != -1 && v == 0 && which == 0) flag(a.dev_status, 1u);  // PKV_DEV_ERR_SLOT
+      continue;
+    }
+    const int g = (v * 16) / a.head_dim;
+    const float sc = (which ? a.v_scale : a.k_scale)[(slot / kBlockSize) * a.num_kv_heads + g];
+    const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t e01 = e4m3x2_satfinite(__fdiv_rn(widen16(w[2 * i] & 0xffffu, bf16), sc),
+                                            __fdiv_rn(widen16(w[2 * i] >> 16, bf16), sc));
+      const uint32_t e23 = e4m3x2_satfinite(__fdiv_rn(widen16(w[2 * i + 1] & 0xffffu, bf16), sc),
+                                            __fdiv_rn(widen16(w[2 * i + 1] >> 16, bf16), sc));
+      c[i] = e01 | (e23 << 16);
+    }
+    uint8_t* dst = (which ? a.v_pool : a.k_pool) + slot * row;
+    reinterpret_cast<uint4*>(dst)[v] = make_uint4(c[0], c[1], c[2], c[3]);
+  }
 }
 
 int grid_for(int64_t work_items, int threads) {
@@ -92,6 +162,12 @@ cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream) {
   const int64_t work = static_cast<int64_t>(a.num_pairs) * 2 * (a.block_elems / 8);
   if (work == 0) return cudaSuccess;
   return launch_pdl(copy_blocks_kernel, dim3(grid_for(work, 256)), dim3(256), 0, stream, a);
+}
+
+cudaError_t launch_write_cache_fp8(const WriteCacheFp8Args& a, cudaStream_t stream) {
+  const int64_t work = static_cast<int64_t>(a.num_tokens) * 2 * (a.num_kv_heads * a.head_dim / 16);
+  if (work == 0) return cudaSuccess;
+  return launch_pdl(write_cache_fp8_kernel, dim3(grid_for(work, 256)), dim3(256), 0, stream, a);
 }
 
 }  // namespace pkv

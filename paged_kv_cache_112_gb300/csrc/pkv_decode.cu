@@ -32,21 +32,6 @@ namespace {
 
 using namespace dev;
 
-// The warp's first 32 table entries of unit `unit` served by U warps (lane
-// j: the partition's block j * U + sub), read before the length is known:
-// every read index lies in the partition and in the table row; entries
-// past the sequence's blocks are never used.
-template <int U>
-__device__ __forceinline__ int first_entries(const DecodeArgs& a, int64_t unit, int sub, int lane) {
-  const int Hkv = a.num_kv_heads;
-  const int s = static_cast<int>((unit / Hkv) % a.num_seqs);
-  const int part = static_cast<int>(unit / Hkv / a.num_seqs);
-  const int blk = part * (a.partition_size / kBlockSize), e = lane * U + sub;
-  return (e < a.partition_size / kBlockSize && blk + e < a.max_blocks_per_seq)
-             ? __ldg(a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + blk + e)
-             : 0;
-}
-
 // One unit (sequence s, KV head g, partition p) served by U of the CTA's NW
 // warps; `raw_len` is the sequence's context length as read and `first`
 // the warp's first table entries (first_entries<U>).

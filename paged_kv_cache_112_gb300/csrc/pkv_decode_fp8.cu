@@ -1,0 +1,435 @@
+// Paged decode attention over FP8 (e4m3) pools for sm_103a: partition
+// kernel (the reduce kernel is the 16-bit path's, its workspace records are
+// the same).
+//
+// What is computed: the attention of pkv_decode_attention with
+// k_t = decode(k8_t) * k_scale[block][g] and v_t likewise, one float scale per
+// (physical block, KV head) -- the 16-token block as the quantisation group
+// whose scales travel with it ("PagedAttention internals", section 06
+// "Blocks as quantization groups"; "KV Cache & PagedAttention", section 5:
+// K, V stored in FP8 halve the bytes decode reads).
+//
+// Mapping onto GB300 (head_dim 128):
+//  * Same units, grid, warps-per-unit rule and per-warp TMA ring as the
+//    16-bit kernel; a (block, head) tile is 16 rows x 128 bytes of codes,
+//    one TMA box in the 128-byte swizzle, so a stage (K + V) is 4 KB and the
+//    ring holds 4 stages.
+//  * Both contractions run on the tensor cores as f16 mma.sync m16n8k16:
+//    e4m3 -> f16 is exact (cvt.rn.f16x2.e4m3x2).  bf16 queries are
+//    converted to f16 after a power-of-two prescale that keeps the group's
+//    largest |q| inside the f16 range.
+//  * No ldmatrix: the dot product is invariant under any permutation of the
+//    head dimension applied to both q and k, and the output rows of
+//    O^T = V^T P^T may be stored in any order.  Both are chosen so that lane
+//    (gr = lane/4, tq = lane%4) needs exactly bytes [32tq, 32tq+32) of token
+//    rows gr and gr+8: two 16-byte shared loads per row, conflict-free under
+//    the swizzle.  For QK^T, k-step kk takes codes 32tq+4kk+{0,1} (A cols
+//    2tq, 2tq+1) and 32tq+4kk+{2,3} (cols 2tq+8, 2tq+9).  For PV, code pair
+//    j of a row (dims 32tq+2j, +1) is column pair tq of an 8x8 block, which
+//    movmatrix transposes into the V^T A fragment; M-tile mt covers pairs 2mt
+//    and 2mt+1, so accumulator row gr (+8) of mt is output dim
+//    32(gr/2) + 4mt + gr%2 (+2).
+//  * Scales: the K scale multiplies the tile's scores with the softmax scale
+//    (one multiplier per tile); the V scale multiplies the tile's P.V product
+//    as it is added to the accumulator.  Both are read with the table
+//    entries, one chunk of 32 tiles at a time.
+#include "pkv_device.cuh"
+
+namespace pkv {
+namespace {
+
+using namespace dev;
+
+constexpr int kFp8Stages = 4;
+
+// Four e4m3 codes (bytes 0..3 of w) -> two f16x2 (codes 0,1 in lo; 2,3 in hi;
+// the lower-addressed code in the lower half).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\t"
+      "mov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// 16 bytes of shared memory into r[0..3].
+__device__ __forceinline__ void lds128(uint32_t* r, uint32_t addr) {
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// Attention state of one warp serving the G <= 8 query heads of one KV head
+// over FP8 tiles (layout and permutations as described at the top).
+template <int D>
+struct WarpAttentionFp8 : SoftmaxState<D / 16> {
+  static_assert(D == 128, "FP8 tiles are one 128-byte line per head row");
+  static constexpr int KT = D / 16;
+  using Base = SoftmaxState<KT>;
+  using Base::acc;
+  uint32_t qf[KT][2];  // f16x2: q[head gr][32tq + 4kk + {0,1}] and {2,3}
+
+  // Loads the group's query rows (heads >= G read as 0) in the permuted
+  // order and returns the power of two by which they were scaled down (1
+  // for f16; for bf16, 2^e with the group's max |q| / 2^e below 2^15).
+  template <bool QBF16>
+  __device__ __forceinline__ float load_q(const uint16_t* qhead0, int G, int lane) {
+    const int gr = lane >> 2, tq = lane & 3;
+    const bool live = gr < G;
+    const uint4* src = reinterpret_cast<const uint4*>(qhead0 + (live ? gr : 0) * D + 32 * tq);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = live ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+      w[4 * i] = v.x;
+      w[4 * i + 1] = v.y;
+      w[4 * i + 2] = v.z;
+      w[4 * i + 3] = v.w;
+    }
+    float down = 1.f;
+    if constexpr (QBF16) {
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float2 f = unpack_bf16(w[i]);
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+      // 2^e >= amax / 2^14.99: exponent of amax minus 14, at least 0.
+      const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xff) - 127;
+      const int e = min(max(ex - 14, 0), 120);
+      const float mul = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, exact
+      down = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float2 f = unpack_bf16(w[i]);
+        w[i] = pack_f16(f.x * mul, f.y * mul);
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk) {
+      qf[kk][0] = w[2 * kk];
+      qf[kk][1] = w[2 * kk + 1];
+    }
+    return down;
+  }
+
+  // One tile: nv valid tokens (rows >= nv are masked, whatever they hold).
+  // sl2k = log2(e) * softmax scale * q prescale * K scale; vscale = V scale.
+  __device__ __forceinline__ void tile(uint32_t sK, uint32_t sV, int nv, float sl2k, float vscale, int lane) {
+    const int gr = lane >> 2, tq = lane & 3;
+    // Rows gr and gr+8 share the swizzle phase (row & 7 == gr).
+    const uint32_t off0 = gr * 128 + (((2 * tq) ^ gr) << 4);
+    const uint32_t off1 = gr * 128 + (((2 * tq + 1) ^ gr) << 4);
+    uint32_t k0[8], k1[8], v0[8], v1[8];  // rows gr, gr+8: words i = codes [32tq + 4i, +4)
+    lds128(k0, sK + off0);
+    lds128(k0 + 4, sK + off1);
+    lds128(k1, sK + 1024 + off0);
+    lds128(k1 + 4, sK + 1024 + off1);
+    lds128(v0, sV + off0);
+    lds128(v0 + 4, sV + off1);
+    lds128(v1, sV + 1024 + off0);
+    lds128(v1 + 4, sV + 1024 + off1);
+
+    // Scores S^T[token][head]; even and odd k-steps in separate chains.
+    float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk) {
+      uint32_t a[4];
+      e4m3x4_to_f16x4(k0[kk], a[0], a[2]);
+      e4m3x4_to_f16x4(k1[kk], a[1], a[3]);
+      if (kk & 1)
+        mma_16816<false>(c2, a, qf[kk][0], qf[kk][1]);
+      else
+        mma_16816<false>(c, a, qf[kk][0], qf[kk][1]);
+    }
+    float s0 = (c[0] + c2[0]) * sl2k, s1 = (c[1] + c2[1]) * sl2k;
+    float s2 = (c[2] + c2[2]) * sl2k, s3 = (c[3] + c2[3]) * sl2k;
+    if (gr >= nv) s0 = s1 = kNegInf;
+    if (gr + 8 >= nv) s2 = s3 = kNegInf;
+    float p0, p1, p2, p3;
+    this->online_update(s0, s1, s2, s3, p0, p1, p2, p3);
+
+    // P^T as f16 hi + lo parts (two MMAs), so the weights keep ~2^-22
+    // relative precision.
+    const uint32_t h0 = pack_f16(p0, p1), h1 = pack_f16(p2, p3);
+    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
+    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
+    const uint32_t pb0 = movmatrix_trans(h0), pb1 = movmatrix_trans(h1);
+    const uint32_t pl0 = movmatrix_trans(pack_f16(p0 - f0.x, p1 - f0.y));
+    const uint32_t pl1 = movmatrix_trans(pack_f16(p2 - f1.x, p3 - f1.y));
+
+    // V codes of tokens >= nv may be anything (NaN codes included): zero them.
+    if (nv < kBlockSize) {
+      if (gr >= nv) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v0[i] = 0u;
+      }
+      if (gr + 8 >= nv) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v1[i] = 0u;
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt) {
+      uint32_t x00, x01, x10, x11;  // 8x8 blocks (tokens 0-7 | 8-15) x (pair 2mt | 2mt+1)
+      e4m3x4_to_f16x4(v0[mt], x00, x01);
+      e4m3x4_to_f16x4(v1[mt], x10, x11);
+      uint32_t va[4];
+      va[0] = movmatrix_trans(x00);  // rows: pair 2mt, k: tokens 0-7
+      va[1] = movmatrix_trans(x01);  // rows: pair 2mt+1, k: tokens 0-7
+      va[2] = movmatrix_trans(x10);  // rows: pair 2mt, k: tokens 8-15
+      va[3] = movmatrix_trans(x11);
+      float t[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_16816<false>(t, va, pb0, pb1);
+      mma_16816<false>(t, va, pl0, pl1);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[mt][j] = fmaf(vscale, t[j], acc[mt][j]);
+    }
+  }
+
+  // Output dim of accumulator row gr of M-tile mt (row gr+8: +2).
+  __device__ __forceinline__ static int out_dim(int mt, int gr) { return 32 * (gr >> 1) + 4 * mt + (gr & 1); }
+
+  __device__ __forceinline__ void store_final(void* out, int64_t out_head0, int G, int dtype, int lane) const {
+    const int gr = lane >> 2, tq = lane & 3;
+    const int ha = 2 * tq, hb = ha + 1;
+    const float ia = this->l_a > 0.f ? 1.f / this->l_a : 0.f;
+    const float ib = this->l_b > 0.f ? 1.f / this->l_b : 0.f;
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt) {
+      const int d = out_dim(mt, gr);
+      if (ha < G) {
+        store_out(out, (out_head0 + ha) * D + d, acc[mt][0] * ia, dtype);
+        store_out(out, (out_head0 + ha) * D + d + 2, acc[mt][2] * ia, dtype);
+      }
+      if (hb < G) {
+        store_out(out, (out_head0 + hb) * D + d, acc[mt][1] * ib, dtype);
+        store_out(out, (out_head0 + hb) * D + d + 2, acc[mt][3] * ib, dtype);
+      }
+    }
+  }
+
+  __device__ __forceinline__ void store_partial(float* ws_acc, float2* ws_ml, int64_t rec0, int64_t rec_stride,
+                                                int G, int lane) const {
+    const int gr = lane >> 2, tq = lane & 3;
+    const int ha = 2 * tq, hb = ha + 1;
+    const int64_t ra = rec0 + ha * rec_stride, rb = rec0 + hb * rec_stride;
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt) {
+      const int d = out_dim(mt, gr);
+      if (ha < G) {
+        ws_acc[ra * D + d] = acc[mt][0];
+        ws_acc[ra * D + d + 2] = acc[mt][2];
+      }
+      if (hb < G) {
+        ws_acc[rb * D + d] = acc[mt][1];
+        ws_acc[rb * D + d + 2] = acc[mt][3];
+      }
+    }
+    if (gr == 0) {
+      if (ha < G) ws_ml[ra] = make_float2(this->m_a, this->l_a);
+      if (hb < G) ws_ml[rb] = make_float2(this->m_b, this->l_b);
+    }
+  }
+};
+
+// One unit (sequence s, KV head g, partition p) served by U of the CTA's NW
+// warps; `raw_len` is the sequence's context length as read and `first` the
+// warp's first table entries (first_entries<U>).  The control flow is the
+// 16-bit kernel's; the per-tile scales come with the table entries.
+template <int D, bool QBF16, int NW, int U, int NST>
+__device__ __forceinline__ void partition_unit_fp8(const DecodeArgs& a, const CUtensorMap* tmap_k,
+                                                   const CUtensorMap* tmap_v, uint8_t* smem, int64_t unit,
+                                                   int raw_len, int first, int warp, int lane) {
+  using Geom = TileGeom<D, 1>;
+  using Att = WarpAttentionFp8<D>;
+  static_assert(NW % U == 0 && NW / U <= 15, "named barriers 1..15, one per unit of the CTA");
+  static_assert(Att::kSaveBytes <= NST * Geom::kStageBytes, "a saved state must fit its warp's ring");
+  const int sub = warp % U;
+  const int Hkv = a.num_kv_heads;
+  const int g = static_cast<int>(unit % Hkv);
+  const int64_t rest = unit / Hkv;
+  const int s = static_cast<int>(rest % a.num_seqs);
+  const int part = static_cast<int>(rest / a.num_seqs);
+
+  const int PS = a.partition_size;
+  const int G = a.group;
+  const int L = clamp_len(a, raw_len, part == 0 && g == 0 && sub == 0 && lane == 0);
+  const int nparts = L > 0 ? (L + PS - 1) / PS : 1;
+  if (part >= nparts) return;
+  Att at;
+  const float q_up = at.template load_q<QBF16>(a.q + (static_cast<int64_t>(s) * a.num_q_heads + g * G) * D, G, lane);
+  const float sl2q = a.scale_log2 * q_up;
+  const int tok0 = part * PS;
+  const int ntok = max(0, min(L - tok0, PS));
+  const int nblk = (ntok + kBlockSize - 1) / kBlockSize;
+  const int cnt = nblk > sub ? (nblk - sub + U - 1) / U : 0;
+  const int32_t* tbl = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + tok0 / kBlockSize;
+  auto entry = [&](int i) { return i < cnt ? __ldg(tbl + i * U + sub) : 0; };
+  // Scales of (entry, g); 1 for an entry outside the pool (its tile is masked).
+  auto ks_of = [&](int phys) {
+    return static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks)
+               ? __ldg(a.k_scale + static_cast<int64_t>(phys) * Hkv + g)
+               : 1.f;
+  };
+  auto vs_of = [&](int phys) {
+    return static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks)
+               ? __ldg(a.v_scale + static_cast<int64_t>(phys) * Hkv + g)
+               : 1.f;
+  };
+  // Lane j holds the entry and scales of the warp's tile j of the current
+  // chunk of 32 (the previous chunk's scales stay until its last tile, which
+  // is consumed up to NST - 1 tiles after the next chunk's first issue).
+  int phys_cur = first;
+  int phys_next = entry(32 + lane);
+  float ks_cur = ks_of(first), vs_cur = vs_of(first), ks_prev = 1.f, vs_prev = 1.f;
+  int chunk_cur = 0;
+
+  WarpRing<D, NST, 1> ring{smem_u32(smem + static_cast<size_t>(warp) * NST * Geom::kStageBytes),
+                           smem_u32(smem + static_cast<size_t>(NW) * NST * Geom::kStageBytes) + 8 * NST * warp};
+  ring.init(lane);
+  uint32_t bad_stage = 0;
+
+  auto issue = [&](int j) {  // all lanes call
+    if ((j & 31) == 0 && j > 0) {
+      phys_cur = phys_next;
+      phys_next = entry(j + 32 + lane);
+      ks_prev = ks_cur;
+      vs_prev = vs_cur;
+      ks_cur = ks_of(phys_cur);
+      vs_cur = vs_of(phys_cur);
+      chunk_cur = j >> 5;
+    }
+    const int st = j % NST;
+    int phys = __shfl_sync(kFull, phys_cur, j & 31);
+    if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
+      if (lane == 0) flag(a.dev_status, 4u);  // PKV_DEV_ERR_BLOCK
+      phys = 0;
+      bad_stage |= 1u << st;
+    } else {
+      bad_stage &= ~(1u << st);
+    }
+    ring.issue(j, phys, g, tmap_k, tmap_v, lane);
+  };
+
+  at.reset();
+  for (int j = 0; j < min(cnt, NST); ++j) issue(j);
+
+  for (int i = 0; i < cnt; ++i) {
+    if (!__all_sync(kFull, ring.wait(i, a.timeout_ns))) {
+      ring.drain(i, min(cnt, i + NST), a.timeout_ns);
+      if (lane == 0) flag(a.dev_status, 16u);  // PKV_DEV_ERR_TIMEOUT; the output is undefined
+      break;
+    }
+    const int t = i * U + sub;
+    const int st = i % NST;
+    const int nv = ((bad_stage >> st) & 1) ? 0 : min(kBlockSize, ntok - t * kBlockSize);
+    const bool cur = (i >> 5) == chunk_cur;
+    const float ksc = __shfl_sync(kFull, cur ? ks_cur : ks_prev, i & 31);
+    const float vsc = __shfl_sync(kFull, cur ? vs_cur : vs_prev, i & 31);
+    const uint32_t sK = ring.k_tile(i);
+    at.tile(sK, sK + Geom::kTileBytes, nv, sl2q * ksc, vsc, lane);
+    __syncwarp();
+    if (i + NST < cnt) {
+      fence_proxy_async_smem();
+      issue(i + NST);
+    }
+  }
+
+  at.finish_sums();
+  if constexpr (U > 1) {
+    const uint32_t mine = smem_u32(smem + static_cast<size_t>(warp) * NST * Geom::kStageBytes);
+    if (sub != 0) at.save(mine, lane);
+    named_barrier_sync(1 + warp / U, U * 32);
+    if (sub != 0) return;
+#pragma unroll
+    for (int k = 1; k < U; ++k) at.merge_from(mine + k * NST * Geom::kStageBytes, lane);
+  }
+  const int64_t head0 = static_cast<int64_t>(s) * a.num_q_heads + g * G;
+  if (nparts == 1)
+    at.store_final(a.out, head0, G, a.out_dtype, lane);
+  else
+    at.store_partial(a.ws_acc, a.ws_ml, head0 * a.max_parts + part, a.max_parts, G, lane);
+}
+
+// Two-warp CTAs, units assigned as in the 16-bit kernel.  Six per SM (12
+// warps x 4 stages x 4 KB = 192 KB of tiles in flight); the bound lets the
+// tile's loads and conversions keep all their registers (154, no spills).
+template <int D, bool QBF16, int NST>
+__global__ void __launch_bounds__(64, 6) decode_partitions_fp8_kernel(
+    const DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
+    const __grid_constant__ CUtensorMap tmap_v) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  griddep_wait();
+  griddep_launch_dependents();
+  if (smem_misaligned(smem, a.dev_status)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t units = static_cast<int64_t>(a.num_kv_heads) * a.num_seqs * a.max_parts;
+  const int64_t unit1 = static_cast<int64_t>(blockIdx.x) * 2 + warp, unit2 = blockIdx.x;
+  auto seq_of = [&](int64_t u) { return static_cast<int>((u / a.num_kv_heads) % a.num_seqs); };
+  if (a.unit_warps == 2) {
+    if (unit2 < units)
+      partition_unit_fp8<D, QBF16, 2, 2, NST>(a, &tmap_k, &tmap_v, smem, unit2, a.context_lens[seq_of(unit2)],
+                                              first_entries<2>(a, unit2, warp, lane), warp, lane);
+  } else if (unit1 < units) {
+    partition_unit_fp8<D, QBF16, 2, 1, NST>(a, &tmap_k, &tmap_v, smem, unit1, a.context_lens[seq_of(unit1)],
+                                            first_entries<1>(a, unit1, 0, lane), warp, lane);
+  }
+}
+
+// Warp slots of the kernel on the current device (SMs x resident CTAs x 2).
+int fp8_warp_slots(const void* kern, size_t smem) {
+  static const void* cached_kern[4] = {};
+  static int cached_slots[4] = {};
+  static int cached_dev[4] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  for (int i = 0; i < 4; ++i)
+    if (cached_kern[i] == kern && cached_dev[i] == dev) return cached_slots[i];
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 64, smem) != cudaSuccess || per_sm <= 0) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  const int slots = current_sm_count(1) * per_sm * 2;
+  for (int i = 0; i < 4; ++i)
+    if (!cached_kern[i]) {
+      cached_kern[i] = kern;
+      cached_dev[i] = dev;
+      cached_slots[i] = slots;
+      break;
+    }
+  return slots;
+}
+
+template <int D, bool QBF16>
+cudaError_t launch_fp8_t(const DecodeArgs& a_in, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+  using Geom = TileGeom<D, 1>;
+  constexpr int NST = kFp8Stages;
+  const size_t smem = 2 * NST * Geom::kStageBytes + 2 * NST * 8;
+  auto kern = decode_partitions_fp8_kernel<D, QBF16, NST>;
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  DecodeArgs a = a_in;
+  const int64_t units = static_cast<int64_t>(a.num_kv_heads) * a.num_seqs * a.max_parts;
+  if (units == 0) return cudaSuccess;
+  // Warps per unit: the 16-bit kernel's rule.
+  const int slots = fp8_warp_slots(reinterpret_cast<const void*>(kern), smem);
+  a.unit_warps = static_cast<int64_t>(a.num_kv_heads) * a.num_seqs > slots ? 2 : 1;
+  const int64_t ctas = a.unit_warps == 1 ? (units + 1) / 2 : units;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(64), smem, stream, a, tk, tv);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_partitions_fp8(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                         int head_dim, int q_bf16, cudaStream_t stream) {
+  if (head_dim != 128) return cudaErrorInvalidValue;
+  return q_bf16 ? launch_fp8_t<128, true>(a, tmap_k, tmap_v, stream)
+                : launch_fp8_t<128, false>(a, tmap_k, tmap_v, stream);
+}
+
+}  // namespace pkv

@@ -183,20 +183,21 @@ __device__ __forceinline__ bool smem_misaligned(const void* base, int32_t* statu
 // ------------------------------------------------------------- tile geometry
 
 // One pipeline stage holds a (block, KV head) tile of K and one of V: 16
-// tokens x D elements each, stored as D/64 sub-tiles of [16 rows][128 bytes]
-// in the TMA 128-byte swizzle (16-byte chunk c of row r sits at c ^ (r & 7)).
-// Every sub-tile starts on a 1024-byte boundary.
-template <int D>
+// tokens x D elements of EB bytes each, stored as D*EB/128 sub-tiles of
+// [16 rows][128 bytes] in the TMA 128-byte swizzle (16-byte chunk c of row r
+// sits at c ^ (r & 7)).  Every sub-tile starts on a 1024-byte boundary.
+template <int D, int EB = 2>
 struct TileGeom {
-  static constexpr int kHalves = D / 64;
-  static constexpr int kTileBytes = kBlockSize * D * 2;
+  static_assert((D * EB) % 128 == 0, "a head row is whole 128-byte lines");
+  static constexpr int kHalves = D * EB / 128;  // 128-byte lines per head row
+  static constexpr int kTileBytes = kBlockSize * D * EB;
   static constexpr int kStageBytes = 2 * kTileBytes;
 };
 
 // A warp's private ring of NST stages, each completing on its own mbarrier.
-template <int D, int NST>
+template <int D, int NST, int EB = 2>
 struct WarpRing {
-  using Geom = TileGeom<D>;
+  using Geom = TileGeom<D, EB>;
   uint32_t buf;  // shared address of stage 0
   uint32_t bar;  // shared address of the stage-0 mbarrier
 
@@ -236,6 +237,22 @@ struct WarpRing {
 
   __device__ __forceinline__ uint32_t k_tile(int i) const { return buf + (i % NST) * Geom::kStageBytes; }
 };
+
+// The warp's first 32 table entries of unit `unit` (KV head, sequence,
+// partition; partition-major) served by U warps (lane j: the partition's
+// block j * U + sub), read before the length is known: every read index lies
+// in the partition and in the table row; entries past the sequence's blocks
+// are never used.
+template <int U>
+__device__ __forceinline__ int first_entries(const DecodeArgs& a, int64_t unit, int sub, int lane) {
+  const int Hkv = a.num_kv_heads;
+  const int s = static_cast<int>((unit / Hkv) % a.num_seqs);
+  const int part = static_cast<int>(unit / Hkv / a.num_seqs);
+  const int blk = part * (a.partition_size / kBlockSize), e = lane * U + sub;
+  return (e < a.partition_size / kBlockSize && blk + e < a.max_blocks_per_seq)
+             ? __ldg(a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + blk + e)
+             : 0;
+}
 
 // ---------------------------------------------------- fused new-token write
 
@@ -307,22 +324,15 @@ struct NewToken {
   }
 };
 
-// ----------------------------------------------------- per-warp attention
+// ------------------------------------------------ per-warp softmax state
 
-// Attention state of one warp serving the G <= 8 query heads of one KV head.
-// Both contractions run on the tensor cores (mma.sync m16n8k16, fp32
-// accumulation):
-//   S^T[16 tok x 8 heads] = K[16 x D] Q^T[D x 8]     (tokens on M)
-//   O^T[D x 8 heads]     += V^T[D x 16] P^T[16 x 8]  (head_dim on M)
-// V^T comes from ldmatrix.trans; P^T is S^T's C fragment transposed in
-// registers with movmatrix.  P is rounded to the KV type for the MMA; for
-// bf16 it is split into hi + lo parts (two MMAs), keeping the rounding error
-// near 2^-17 relative (fp16 alone is 2^-11).  Lane (gr = lane/4, tq = lane%4)
-// owns heads 2tq and 2tq+1 (a, b) and the output rows d = 16mt + gr (+8).
-template <int D, bool BF16>
-struct WarpAttention {
-  static constexpr int KT = D / 16;
-  uint32_t qf[KT][2];
+// Running softmax state of one warp serving up to 8 query heads, with the
+// output accumulator in the C-fragment layout of an m16n8 MMA whose N index
+// is the head: lane (gr = lane/4, tq = lane%4) owns heads 2tq and 2tq+1 (a,
+// b); acc[mt][0..3] = rows (gr, head a), (gr, head b), (gr+8, head a),
+// (gr+8, head b) of M-tile mt.  Scores are in log2 units.
+template <int KT>
+struct SoftmaxState {
   float acc[KT][4];
   float m_a, m_b, l_a, l_b;
 
@@ -333,53 +343,12 @@ struct WarpAttention {
     l_a = l_b = 0.f;
   }
 
-  // B operand of QK^T: lane holds q[head lane/4][16kk + 2(lane%4) + {0,1}]
-  // and +8.  `qhead0` points at the group's first head row; heads >= G are 0.
-  __device__ __forceinline__ static void fetch_q(uint32_t (&dst)[KT][2], const uint16_t* qhead0, int G, int lane) {
-    const int gr = lane >> 2, tq = lane & 3;
-    const bool live = gr < G;
-    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qhead0 + (live ? gr : 0) * D);
-#pragma unroll
-    for (int kk = 0; kk < KT; ++kk) {
-      dst[kk][0] = live ? __ldg(qrow + kk * 8 + tq) : 0u;
-      dst[kk][1] = live ? __ldg(qrow + kk * 8 + 4 + tq) : 0u;
-    }
-  }
-  __device__ __forceinline__ void load_q(const uint16_t* qhead0, int G, int lane) { fetch_q(qf, qhead0, G, lane); }
-  __device__ __forceinline__ void set_q(const uint32_t (&src)[KT][2]) {
-#pragma unroll
-    for (int kk = 0; kk < KT; ++kk) {
-      qf[kk][0] = src[kk][0];
-      qf[kk][1] = src[kk][1];
-    }
-  }
-
-  // One tile: nv valid tokens (rows >= nv are masked, whatever they hold).
-  __device__ __forceinline__ void tile(uint32_t sK, uint32_t sV, int nv, float sl2, int lane) {
-    const int gr = lane >> 2, tq = lane & 3;
-    const int rowK = (lane & 7) + ((lane >> 3) & 1) * 8;
-    const int colK = lane >> 4;
-    const int rowV = (lane & 7) + (lane >> 4) * 8;
-    const int colV = (lane >> 3) & 1;
-
-    // Scores; even and odd k-steps accumulate in separate chains.
-    float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int kk = 0; kk < KT; ++kk) {
-      const int chunk = ((kk & 3) << 1) + colK;
-      uint32_t ka[4];
-      ldsm_x4(ka, sK + (kk >> 2) * 2048 + rowK * 128 + ((chunk ^ (rowK & 7)) << 4));
-      if (kk & 1)
-        mma_16816<BF16>(c2, ka, qf[kk][0], qf[kk][1]);
-      else
-        mma_16816<BF16>(c, ka, qf[kk][0], qf[kk][1]);
-    }
-    float s0 = (c[0] + c2[0]) * sl2, s1 = (c[1] + c2[1]) * sl2;
-    float s2 = (c[2] + c2[2]) * sl2, s3 = (c[3] + c2[3]) * sl2;
-    if (gr >= nv) s0 = s1 = kNegInf;
-    if (gr + 8 >= nv) s2 = s3 = kNegInf;
-
-    // Online softmax (log2 units): block max per head over the 16 tokens.
+  // One tile of 16 tokens: this lane's scores s0 = (token gr, head a), s1 =
+  // (gr, b), s2 = (gr+8, a), s3 = (gr+8, b), masked ones -inf.  Updates the
+  // running max and sum, rescales the accumulator and returns the weights.
+  __device__ __forceinline__ void online_update(float s0, float s1, float s2, float s3, float& p0, float& p1,
+                                                float& p2, float& p3) {
+    // Block max per head over the 16 tokens (lanes with equal lane%4).
     float mx_a = fmaxf(s0, s2), mx_b = fmaxf(s1, s3);
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
@@ -392,8 +361,10 @@ struct WarpAttention {
     const float al_a = exp2f(m_a - u_a), al_b = exp2f(m_b - u_b);
     m_a = mn_a;
     m_b = mn_b;
-    const float p0 = exp2f(s0 - u_a), p2 = exp2f(s2 - u_a);
-    const float p1 = exp2f(s1 - u_b), p3 = exp2f(s3 - u_b);
+    p0 = exp2f(s0 - u_a);
+    p2 = exp2f(s2 - u_a);
+    p1 = exp2f(s1 - u_b);
+    p3 = exp2f(s3 - u_b);
     l_a = l_a * al_a + (p0 + p2);
     l_b = l_b * al_b + (p1 + p3);
 #pragma unroll
@@ -403,39 +374,6 @@ struct WarpAttention {
       acc[mt][2] *= al_a;
       acc[mt][3] *= al_b;
     }
-
-    uint32_t pb0, pb1, pl0 = 0, pl1 = 0;
-    if constexpr (BF16) {
-      const uint32_t h0 = pack_bf16(p0, p1), h1 = pack_bf16(p2, p3);
-      const float2 f0 = unpack_bf16(h0), f1 = unpack_bf16(h1);
-      pb0 = movmatrix_trans(h0);
-      pb1 = movmatrix_trans(h1);
-      pl0 = movmatrix_trans(pack_bf16(p0 - f0.x, p1 - f0.y));
-      pl1 = movmatrix_trans(pack_bf16(p2 - f1.x, p3 - f1.y));
-    } else {
-      pb0 = movmatrix_trans(pack_f16(p0, p1));
-      pb1 = movmatrix_trans(pack_f16(p2, p3));
-    }
-
-    // V rows past the valid tokens may hold anything (even NaN): zero them in
-    // the A fragment (lane holds tokens 2tq, 2tq+1 and 8+2tq, 9+2tq).
-    uint32_t m01 = kFull, m23 = kFull;
-    if (nv < kBlockSize) {
-      m01 = (2 * tq < nv ? 0x0000ffffu : 0u) | (2 * tq + 1 < nv ? 0xffff0000u : 0u);
-      m23 = (2 * tq + 8 < nv ? 0x0000ffffu : 0u) | (2 * tq + 9 < nv ? 0xffff0000u : 0u);
-    }
-#pragma unroll
-    for (int mt = 0; mt < KT; ++mt) {
-      const int chunk = ((mt & 3) << 1) + colV;
-      uint32_t va[4];
-      ldsm_x4_trans(va, sV + (mt >> 2) * 2048 + rowV * 128 + ((chunk ^ (rowV & 7)) << 4));
-      va[0] &= m01;
-      va[1] &= m01;
-      va[2] &= m23;
-      va[3] &= m23;
-      mma_16816<BF16>(acc[mt], va, pb0, pb1);
-      if constexpr (BF16) mma_16816<BF16>(acc[mt], va, pl0, pl1);
-    }
   }
 
   // Per-head sums over all lanes (lanes with the same lane%4 share heads).
@@ -444,27 +382,6 @@ struct WarpAttention {
     for (int o = 4; o < 32; o <<= 1) {
       l_a += __shfl_xor_sync(kFull, l_a, o);
       l_b += __shfl_xor_sync(kFull, l_b, o);
-    }
-  }
-
-  // Normalised output rows of heads [0, G) of the group; out_head0 = index of
-  // the group's first row in [S * H_q].
-  __device__ __forceinline__ void store_final(void* out, int64_t out_head0, int G, int dtype, int lane) const {
-    const int gr = lane >> 2, tq = lane & 3;
-    const int ha = 2 * tq, hb = ha + 1;
-    const float ia = l_a > 0.f ? 1.f / l_a : 0.f;
-    const float ib = l_b > 0.f ? 1.f / l_b : 0.f;
-#pragma unroll
-    for (int mt = 0; mt < KT; ++mt) {
-      const int d = mt * 16 + gr;
-      if (ha < G) {
-        store_out(out, (out_head0 + ha) * D + d, acc[mt][0] * ia, dtype);
-        store_out(out, (out_head0 + ha) * D + d + 8, acc[mt][2] * ia, dtype);
-      }
-      if (hb < G) {
-        store_out(out, (out_head0 + hb) * D + d, acc[mt][1] * ib, dtype);
-        store_out(out, (out_head0 + hb) * D + d + 8, acc[mt][3] * ib, dtype);
-      }
     }
   }
 
@@ -513,6 +430,133 @@ struct WarpAttention {
       acc[mt][1] = acc[mt][1] * cb + get(mt * 4 + 1) * cob;
       acc[mt][2] = acc[mt][2] * ca + get(mt * 4 + 2) * coa;
       acc[mt][3] = acc[mt][3] * cb + get(mt * 4 + 3) * cob;
+    }
+  }
+};
+
+// ----------------------------------------------------- per-warp attention
+
+// Attention state of one warp serving the G <= 8 query heads of one KV head.
+// Both contractions run on the tensor cores (mma.sync m16n8k16, fp32
+// accumulation):
+//   S^T[16 tok x 8 heads] = K[16 x D] Q^T[D x 8]     (tokens on M)
+//   O^T[D x 8 heads]     += V^T[D x 16] P^T[16 x 8]  (head_dim on M)
+// V^T comes from ldmatrix.trans; P^T is S^T's C fragment transposed in
+// registers with movmatrix.  P is rounded to the KV type for the MMA; for
+// bf16 it is split into hi + lo parts (two MMAs), keeping the rounding error
+// near 2^-17 relative (fp16 alone is 2^-11).  Lane (gr = lane/4, tq = lane%4)
+// owns heads 2tq and 2tq+1 (a, b) and the output rows d = 16mt + gr (+8).
+template <int D, bool BF16>
+struct WarpAttention : SoftmaxState<D / 16> {
+  static constexpr int KT = D / 16;
+  using Base = SoftmaxState<KT>;
+  using Base::acc;
+  using Base::l_a;
+  using Base::l_b;
+  using Base::m_a;
+  using Base::m_b;
+  uint32_t qf[KT][2];
+
+  // B operand of QK^T: lane holds q[head lane/4][16kk + 2(lane%4) + {0,1}]
+  // and +8.  `qhead0` points at the group's first head row; heads >= G are 0.
+  __device__ __forceinline__ static void fetch_q(uint32_t (&dst)[KT][2], const uint16_t* qhead0, int G, int lane) {
+    const int gr = lane >> 2, tq = lane & 3;
+    const bool live = gr < G;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qhead0 + (live ? gr : 0) * D);
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk) {
+      dst[kk][0] = live ? __ldg(qrow + kk * 8 + tq) : 0u;
+      dst[kk][1] = live ? __ldg(qrow + kk * 8 + 4 + tq) : 0u;
+    }
+  }
+  __device__ __forceinline__ void load_q(const uint16_t* qhead0, int G, int lane) { fetch_q(qf, qhead0, G, lane); }
+  __device__ __forceinline__ void set_q(const uint32_t (&src)[KT][2]) {
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk) {
+      qf[kk][0] = src[kk][0];
+      qf[kk][1] = src[kk][1];
+    }
+  }
+
+  // One tile: nv valid tokens (rows >= nv are masked, whatever they hold).
+  __device__ __forceinline__ void tile(uint32_t sK, uint32_t sV, int nv, float sl2, int lane) {
+    const int gr = lane >> 2, tq = lane & 3;
+    const int rowK = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int colK = lane >> 4;
+    const int rowV = (lane & 7) + (lane >> 4) * 8;
+    const int colV = (lane >> 3) & 1;
+
+    // Scores; even and odd k-steps accumulate in separate chains.
+    float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk) {
+      const int chunk = ((kk & 3) << 1) + colK;
+      uint32_t ka[4];
+      ldsm_x4(ka, sK + (kk >> 2) * 2048 + rowK * 128 + ((chunk ^ (rowK & 7)) << 4));
+      if (kk & 1)
+        mma_16816<BF16>(c2, ka, qf[kk][0], qf[kk][1]);
+      else
+        mma_16816<BF16>(c, ka, qf[kk][0], qf[kk][1]);
+    }
+    float s0 = (c[0] + c2[0]) * sl2, s1 = (c[1] + c2[1]) * sl2;
+    float s2 = (c[2] + c2[2]) * sl2, s3 = (c[3] + c2[3]) * sl2;
+    if (gr >= nv) s0 = s1 = kNegInf;
+    if (gr + 8 >= nv) s2 = s3 = kNegInf;
+    float p0, p1, p2, p3;
+    this->online_update(s0, s1, s2, s3, p0, p1, p2, p3);
+
+    uint32_t pb0, pb1, pl0 = 0, pl1 = 0;
+    if constexpr (BF16) {
+      const uint32_t h0 = pack_bf16(p0, p1), h1 = pack_bf16(p2, p3);
+      const float2 f0 = unpack_bf16(h0), f1 = unpack_bf16(h1);
+      pb0 = movmatrix_trans(h0);
+      pb1 = movmatrix_trans(h1);
+      pl0 = movmatrix_trans(pack_bf16(p0 - f0.x, p1 - f0.y));
+      pl1 = movmatrix_trans(pack_bf16(p2 - f1.x, p3 - f1.y));
+    } else {
+      pb0 = movmatrix_trans(pack_f16(p0, p1));
+      pb1 = movmatrix_trans(pack_f16(p2, p3));
+    }
+
+    // V rows past the valid tokens may hold anything (even NaN): zero them in
+    // the A fragment (lane holds tokens 2tq, 2tq+1 and 8+2tq, 9+2tq).
+    uint32_t m01 = kFull, m23 = kFull;
+    if (nv < kBlockSize) {
+      m01 = (2 * tq < nv ? 0x0000ffffu : 0u) | (2 * tq + 1 < nv ? 0xffff0000u : 0u);
+      m23 = (2 * tq + 8 < nv ? 0x0000ffffu : 0u) | (2 * tq + 9 < nv ? 0xffff0000u : 0u);
+    }
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt) {
+      const int chunk = ((mt & 3) << 1) + colV;
+      uint32_t va[4];
+      ldsm_x4_trans(va, sV + (mt >> 2) * 2048 + rowV * 128 + ((chunk ^ (rowV & 7)) << 4));
+      va[0] &= m01;
+      va[1] &= m01;
+      va[2] &= m23;
+      va[3] &= m23;
+      mma_16816<BF16>(acc[mt], va, pb0, pb1);
+      if constexpr (BF16) mma_16816<BF16>(acc[mt], va, pl0, pl1);
+    }
+  }
+
+  // Normalised output rows of heads [0, G) of the group; out_head0 = index of
+  // the group's first row in [S * H_q].
+  __device__ __forceinline__ void store_final(void* out, int64_t out_head0, int G, int dtype, int lane) const {
+    const int gr = lane >> 2, tq = lane & 3;
+    const int ha = 2 * tq, hb = ha + 1;
+    const float ia = l_a > 0.f ? 1.f / l_a : 0.f;
+    const float ib = l_b > 0.f ? 1.f / l_b : 0.f;
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt) {
+      const int d = mt * 16 + gr;
+      if (ha < G) {
+        store_out(out, (out_head0 + ha) * D + d, acc[mt][0] * ia, dtype);
+        store_out(out, (out_head0 + ha) * D + d + 8, acc[mt][2] * ia, dtype);
+      }
+      if (hb < G) {
+        store_out(out, (out_head0 + hb) * D + d, acc[mt][1] * ib, dtype);
+        store_out(out, (out_head0 + hb) * D + d + 8, acc[mt][3] * ib, dtype);
+      }
     }
   }
 

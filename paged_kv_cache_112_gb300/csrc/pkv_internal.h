@@ -26,14 +26,38 @@ struct WriteCacheArgs {
   int row_elems;      // num_kv_heads * head_dim
 };
 
+// FP8 pools: e4m3 codes plus one float scale per (block, KV head) for K and
+// for V.  New rows arrive as 16-bit values and are quantised with their
+// block's scale.
+struct WriteCacheFp8Args {
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  uint8_t* k_pool;
+  uint8_t* v_pool;
+  const float* k_scale;  // [num_blocks][num_kv_heads]
+  const float* v_scale;
+  const int32_t* slot_mapping;
+  int32_t* dev_status;
+  int64_t stride;        // elements between consecutive new tokens
+  int64_t num_slots;
+  int num_tokens;
+  int num_kv_heads;
+  int head_dim;
+  int new_bf16;          // new rows: 0 = f16, 1 = bf16
+};
+
 struct CopyBlocksArgs {
   uint16_t* k_pool;
   uint16_t* v_pool;
   const int32_t* pairs;
   int32_t* dev_status;
-  int64_t block_elems;  // block_size * num_kv_heads * head_dim
+  int64_t block_elems;  // block bytes / 2 (block_size * num_kv_heads * head_dim for 16-bit pools)
   int num_pairs;
   int num_blocks;
+  // FP8 pools only (null otherwise): per-block scales copied with the block.
+  float* k_scale;
+  float* v_scale;
+  int scales_per_block;  // num_kv_heads
 };
 
 struct DecodeArgs {
@@ -67,6 +91,9 @@ struct DecodeArgs {
   const int32_t* slot_mapping;  // [S]: slot of position L-1, or -1
   uint16_t* k_pool_w;
   uint16_t* v_pool_w;
+  // FP8 pools only: per-(block, KV head) scales, [num_blocks][num_kv_heads].
+  const float* k_scale;
+  const float* v_scale;
 };
 
 // Split-K workspace layout (regions 256-byte aligned).  Fixed partitions:
@@ -116,6 +143,12 @@ cudaError_t launch_decode_partitions(const DecodeArgs& a, const CUtensorMap& tma
                                      const CUtensorMap& tmap_v, int head_dim, int kv_bf16,
                                      cudaStream_t stream);  // fuses the write when a.k_new is set
 cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t stream);
+// FP8 pools (pkv_decode_fp8.cu): tensor maps describe the uint8 pools;
+// q_bf16: 0 = f16 queries, 1 = bf16.
+cudaError_t launch_decode_partitions_fp8(const DecodeArgs& a, const CUtensorMap& tmap_k,
+                                         const CUtensorMap& tmap_v, int head_dim, int q_bf16,
+                                         cudaStream_t stream);
+cudaError_t launch_write_cache_fp8(const WriteCacheFp8Args& a, cudaStream_t stream);
 cudaError_t launch_decode_balanced(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                    int head_dim, int kv_bf16, cudaStream_t stream);
 cudaError_t launch_decode_reduce_balanced(const DecodeArgs& a, int head_dim, cudaStream_t stream);

@@ -367,9 +367,9 @@ class Fp8Pools:
 
 def draw_fp8_codes(shape, rng):
     """e4m3 codes: random sign, magnitude code uniform over [FP8_MIN_MAG_CODE, 0x7E]."""
-    mag = rng.integers(FP8_MIN_MAG_CODE, 0x7E, size=shape, endpoint=True, dtype=np.int64)
-    sign = rng.integers(0, 2, size=shape, dtype=np.int64) << 7
-    return (mag | sign).astype(np.uint8)
+    mag = rng.integers(FP8_MIN_MAG_CODE, 0x7E, size=shape, endpoint=True, dtype=np.uint8)
+    mag |= rng.integers(0, 2, size=shape, dtype=np.uint8) << np.uint8(7)
+    return mag
 
 
 def make_fp8_pools(wl: Workload, *, seed: int | None = None, exact: bool = False,

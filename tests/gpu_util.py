@@ -76,3 +76,59 @@ class DeviceStep:
     def status_bits(self) -> int:
         torch.cuda.synchronize()
         return int(self.status.item())
+
+
+class DeviceStepFp8:
+    """Device copies of one workload over FP8 pools (pkv_inputs.Fp8Pools)."""
+
+    def __init__(self, wl, pools, partition_size=None, out_dtype=torch.float32, device="cuda"):
+        self.wl = wl
+        dt = wl.dtype
+        self.q = to_dev(wl.q, dt, device)
+        self.k_new = to_dev(wl.k_new, dt, device)
+        self.v_new = to_dev(wl.v_new, dt, device)
+        self.k8 = torch.from_numpy(pools.k8).to(device)
+        self.v8 = torch.from_numpy(pools.v8).to(device)
+        self.k_scale = torch.from_numpy(pools.k_scale).to(device)
+        self.v_scale = torch.from_numpy(pools.v_scale).to(device)
+        self.block_tables = torch.from_numpy(wl.block_tables).to(device)
+        self.context_lens = torch.from_numpy(wl.context_lens).to(device)
+        self.slot_mapping = torch.from_numpy(wl.slot_mapping).to(device)
+        self.pairs = torch.from_numpy(np.ascontiguousarray(wl.copy_pairs, dtype=np.int32)).to(device)
+        self.partition_size = wl.partition_size if partition_size is None else partition_size
+        self.max_context_len = wl.max_context_len
+        self.out = torch.empty(wl.q.shape, dtype=out_dtype, device=device)
+        self.set_workspace(self.max_context_len)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def set_workspace(self, max_context_len):
+        self.max_context_len = max_context_len
+        wl = self.wl
+        nbytes = pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, max_context_len,
+                                            self.partition_size)
+        self.workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=self.q.device) if nbytes else None
+
+    def copy(self):
+        if self.pairs.shape[0]:
+            pkv.copy_blocks_fp8(self.k8, self.v8, self.k_scale, self.v_scale, self.pairs, status=self.status)
+
+    def write(self):
+        pkv.write_cache_fp8(self.k_new, self.v_new, self.k8, self.v8, self.k_scale, self.v_scale,
+                            self.slot_mapping, status=self.status)
+
+    def attend(self, out=None):
+        pkv.decode_attention_fp8(self.out if out is None else out, self.q, self.k8, self.v8, self.k_scale,
+                                 self.v_scale, self.block_tables, self.context_lens, self.wl.scale,
+                                 partition_size=self.partition_size, max_context_len=self.max_context_len,
+                                 workspace=self.workspace, status=self.status)
+
+    def step(self):
+        self.copy()
+        self.write()
+        self.attend()
+        torch.cuda.synchronize()
+        return self.out
+
+    def status_bits(self) -> int:
+        torch.cuda.synchronize()
+        return int(self.status.item())

@@ -1,0 +1,177 @@
+"""FP8 (e4m3) pools with per-(block, KV head) scales on the GPU, checked
+against the FP8 oracle: the write path and the copy-on-write copy bit for
+bit (codes and scales), decode attention within ATOL, at sizes the oracle
+finishes in seconds (several partitions, ragged tails, one and two warps per
+unit, both reduce kernels) and at the benchmark's full sizes on sampled
+rows.  Pools are poisoned: NaN codes in every slot no sequence owns and NaN
+scales on blocks nothing references."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_112_gb300 as pkv
+import pkv_inputs as P
+from tests.gpu_util import ATOL, DeviceStepFp8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkv.load(build_if_missing=True)
+
+
+def _ref_pools(wl, pools):
+    k8, v8 = pools.k8.copy(), pools.v8.copy()
+    ks, vs = pools.k_scale.copy(), pools.v_scale.copy()
+    oracle.copy_blocks_fp8(k8, v8, ks, vs, wl.copy_pairs)
+    oracle.write_cache_fp8(k8, v8, ks, vs, wl.k_new, wl.v_new, wl.slot_mapping, wl.dtype)
+    return k8, v8, ks, vs
+
+
+def _check_pools(ds, ref):
+    k8, v8, ks, vs = ref
+    assert np.array_equal(ds.k8.cpu().numpy(), k8)
+    assert np.array_equal(ds.v8.cpu().numpy(), v8)
+    assert np.array_equal(ds.k_scale.cpu().numpy(), ks, equal_nan=True)
+    assert np.array_equal(ds.v_scale.cpu().numpy(), vs, equal_nan=True)
+
+
+SMALL = {
+    # several partitions and ragged tails, one warp per unit
+    "c2_ps16": dict(cfg=2, num_seqs=12, lens=("uniform", 1, 300), ps=16),
+    "c2_ps64": dict(cfg=2, num_seqs=12, lens=("uniform", 1, 300), ps=64),
+    "c2_single": dict(cfg=2, num_seqs=12, lens=("uniform", 1, 300), ps=0),
+    # 256 x 8 sequence-heads overfill the warp slots: two warps per unit
+    "c3_two_warps": dict(cfg=3, num_seqs=256, lens=("uniform", 1, 90), ps=32),
+    # shared prefix, copy-on-write of partial tail blocks
+    "c5_prefix": dict(cfg=5, num_seqs=8, lens=("prefix", 64, 0, 40), ps=32),
+    # more than 16 partitions per row: the long-row reduce kernel
+    "c4_long": dict(cfg=4, num_seqs=2, lens=("uniform", 3000, 5000), ps=128),
+}
+
+
+def _small(case, dtype=None):
+    c = dict(SMALL[case])
+    kw = dict(num_seqs=c["num_seqs"], lens=c["lens"], partition_size=c["ps"])
+    if dtype:
+        kw["dtype"] = dtype
+    wl = P.make_workload(c["cfg"], poison=True, **kw)
+    return wl, P.make_fp8_pools(wl)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("case", sorted(SMALL))
+def test_fp8_step_matches_oracle(case, dtype):
+    wl, pools = _small(case, dtype)
+    ds = DeviceStepFp8(wl, pools)
+    out = ds.step().cpu().numpy()
+    assert ds.status_bits() == 0
+    ref_pools = _ref_pools(wl, pools)
+    _check_pools(ds, ref_pools)
+    k8, v8, ks, vs = ref_pools
+    ref = oracle.decode_attention_fp8(wl.q, k8, v8, ks, vs, wl.block_tables, wl.context_lens, wl.scale, wl.dtype)
+    assert np.all(np.isfinite(out))
+    err = float(np.max(np.abs(out.astype(np.float64) - ref)))
+    assert err <= ATOL, err
+
+
+def test_fp8_write_saturates_and_rounds_like_the_oracle():
+    """New rows scaled up so that many quotients pass 448: saturated codes
+    and round-to-nearest-even agree with the oracle bit for bit."""
+    wl, pools = _small("c2_ps16", "bf16")
+    big = P.bits_to_f32(wl.k_new, "bf16") * 40.0
+    wl.k_new = P.f32_to_bits(big, "bf16")
+    ds = DeviceStepFp8(wl, pools)
+    ds.copy()
+    ds.write()
+    assert ds.status_bits() == 0
+    _check_pools(ds, _ref_pools(wl, pools))
+    k8 = ds.k8.cpu().numpy()
+    written = np.stack([k8[s // 16, s % 16] for s in wl.slot_mapping.tolist()])
+    assert np.mean((written & 0x7F) == 0x7E) > 0.05
+
+
+def test_fp8_bf16_queries_beyond_f16_range():
+    """bf16 queries of magnitude ~1e6 (beyond f16) with the softmax scale
+    reduced to match: the kernel's power-of-two prescale keeps them exact."""
+    wl, pools = _small("c2_ps64", "bf16")
+    wl.q = P.f32_to_bits(P.bits_to_f32(wl.q, "bf16") * np.float32(2.0 ** 20), "bf16")
+    assert np.max(np.abs(P.bits_to_f32(wl.q, "bf16"))) > 65504
+    wl.scale = wl.scale * 2.0 ** -20
+    ds = DeviceStepFp8(wl, pools)
+    out = ds.step().cpu().numpy()
+    assert ds.status_bits() == 0
+    k8, v8, ks, vs = _ref_pools(wl, pools)
+    ref = oracle.decode_attention_fp8(wl.q, k8, v8, ks, vs, wl.block_tables, wl.context_lens, wl.scale, wl.dtype)
+    assert float(np.max(np.abs(out - ref))) <= ATOL
+
+
+def test_fp8_empty_and_one_token_sequences():
+    """L = 0 gives a zero row; L = 1 gives the dequantised v_0."""
+    wl, pools = _small("c2_ps16", "f16")
+    ds = DeviceStepFp8(wl, pools)
+    ds.copy()
+    ds.write()
+    cl = wl.context_lens.copy()
+    cl[0], cl[1] = 0, 1
+    ds.context_lens.copy_(torch.from_numpy(cl))
+    ds.attend()
+    out = ds.out.cpu().numpy()
+    assert ds.status_bits() == 0
+    k8, v8, ks, vs = _ref_pools(wl, pools)
+    ref = oracle.decode_attention_fp8(wl.q, k8, v8, ks, vs, wl.block_tables, cl, wl.scale, wl.dtype)
+    assert np.array_equal(out[0], np.zeros_like(out[0]))
+    assert float(np.max(np.abs(out - ref))) <= ATOL
+
+
+def test_fp8_bad_table_entry_is_flagged():
+    wl, pools = _small("c2_ps64", "f16")
+    ds = DeviceStepFp8(wl, pools)
+    ds.copy()
+    ds.write()
+    bt = wl.block_tables.copy()
+    s_bad = int(np.argmax(wl.context_lens))
+    bt[s_bad, 0] = wl.num_blocks + 3
+    ds.block_tables.copy_(torch.from_numpy(bt))
+    ds.attend()
+    assert ds.status_bits() & pkv.DEV_ERR_BLOCK
+    out = ds.out.cpu().numpy()
+    k8, v8, ks, vs = _ref_pools(wl, pools)
+    keep = [s for s in range(wl.num_seqs) if s != s_bad]
+    rows = [(s, h) for s in keep for h in range(wl.num_q_heads)]
+    ref = oracle.decode_attention_fp8(wl.q, k8, v8, ks, vs, wl.block_tables, wl.context_lens, wl.scale, wl.dtype,
+                                      rows=rows)
+    got = np.stack([out[s, h] for s, h in rows])
+    assert float(np.max(np.abs(got - ref))) <= ATOL
+
+
+def _rows(wl, n, rng):
+    S, Hq = wl.num_seqs, wl.num_q_heads
+    picks = {(int(s), int(h)) for s, h in zip(rng.integers(0, S, n), rng.integers(0, Hq, n))}
+    for s in (int(np.argmin(wl.context_lens)), int(np.argmax(wl.context_lens))):
+        picks.update({(s, 0), (s, Hq - 1), (s, Hq // 2)})
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+def test_fp8_full_size_step(cfg):
+    """The benchmark's workloads (recipe partition sizes, fp32 output)."""
+    wl = P.make_workload(cfg, poison=True)
+    pools = P.make_fp8_pools(wl)
+    ds = DeviceStepFp8(wl, pools)
+    out = ds.step().cpu().numpy()
+    assert ds.status_bits() == 0
+    ref_pools = _ref_pools(wl, pools)
+    _check_pools(ds, ref_pools)
+    k8, v8, ks, vs = ref_pools
+    rows = _rows(wl, 48, np.random.default_rng(cfg))
+    ref = oracle.decode_attention_fp8(wl.q, k8, v8, ks, vs, wl.block_tables, wl.context_lens, wl.scale, wl.dtype,
+                                      rows=rows)
+    got = np.stack([out[s, h] for s, h in rows])
+    err = float(np.max(np.abs(got.astype(np.float64) - ref)))
+    assert err <= ATOL, err
+    assert np.all(np.isfinite(out))
