@@ -16,6 +16,11 @@ context lengths, new-token rows read and written, copy-on-write block bytes)
 divided by the device time of exactly K steps.  Between timed steps the K/V
 pools rotate over R device replicas whose total exceeds L2 several times.
 
+`--kv fp8` runs the same step over FP8 (e4m3) pools with one float scale per
+(block, KV head): copy-on-write, the quantising write and decode attention
+through the *_fp8 entry points; bytes count one byte per K/V element plus
+the scales.
+
 `--impl reference` times the fp64 CPU oracle instead (a deliberately slow
 statement of the same computation) on a bounded sample of the workload.
 
@@ -96,6 +101,21 @@ def step_bytes(wl, out_bytes_per_elem=4):
     T = wl.slot_mapping.shape[0]
     write = 2 * T * Hkv * D * 2 * 2 + T * 4  # read new rows + write pool rows, K and V; slots
     cow = wl.copy_pairs.shape[0] * (2 * 16 * Hkv * D * 2 * 2 + 8)
+    return {"attention": attn, "kv": kv, "write": write, "copy": cow, "step": attn + write + cow}
+
+
+def step_bytes_fp8(wl, out_bytes_per_elem=4):
+    """step_bytes over FP8 pools: one byte per K/V element plus the K and V
+    scale (4 bytes each) of every (table entry, KV head) read; the write reads
+    16-bit rows and a scale pair and writes codes; a copy moves codes and scales."""
+    S, Hq, Hkv, D = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    L = wl.context_lens.astype(np.int64)
+    blocks = int(np.sum((L + 15) // 16))
+    kv = int(L.sum()) * Hkv * D * 2 + blocks * Hkv * 2 * 4
+    attn = kv + blocks * 4 + S * Hq * D * 2 + S * Hq * D * out_bytes_per_elem + S * 4
+    T = wl.slot_mapping.shape[0]
+    write = 2 * T * Hkv * D * (2 + 1) + T * Hkv * 2 * 4 + T * 4
+    cow = wl.copy_pairs.shape[0] * (2 * (16 * Hkv * D + Hkv * 4) * 2 + 8)
     return {"attention": attn, "kv": kv, "write": write, "copy": cow, "step": attn + write + cow}
 
 
@@ -194,8 +214,15 @@ def run_gpu(args):
 
     q, k_new, v_new = view("q"), view("k_new"), view("v_new")
     bt, cl, sm, pairs = view("bt"), view("cl"), view("sm"), view("pairs")
-    k0 = torch.from_numpy(wl.k_pool.view(np.int16)).to(dev).view(dt)
-    v0 = torch.from_numpy(wl.v_pool.view(np.int16)).to(dev).view(dt)
+    fp8 = args.kv == "fp8"
+    if fp8:  # e4m3 codes + per-(block, KV head) scales; the write path quantises the new rows
+        f8 = P.make_fp8_pools(wl, poison=False)
+        k0, v0 = torch.from_numpy(f8.k8).to(dev), torch.from_numpy(f8.v8).to(dev)
+        ks0, vs0 = torch.from_numpy(f8.k_scale).to(dev), torch.from_numpy(f8.v_scale).to(dev)
+    else:
+        k0 = torch.from_numpy(wl.k_pool.view(np.int16)).to(dev).view(dt)
+        v0 = torch.from_numpy(wl.v_pool.view(np.int16)).to(dev).view(dt)
+        ks0 = vs0 = None
     out = torch.empty(q.shape, dtype=torch.float32, device=dev)
     ws_bytes = pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, wl.max_context_len, ps)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
@@ -204,12 +231,32 @@ def run_gpu(args):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     pool_bytes = 2 * k0.numel() * k0.element_size()
     replicas = args.replicas or max(1, math.ceil(4 * l2 / pool_bytes))
-    pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(replicas - 1)]
+    clone = lambda t: None if t is None else t.clone()
+    pools = [(k0, v0, ks0, vs0)] + [(k0.clone(), v0.clone(), clone(ks0), clone(vs0)) for _ in range(replicas - 1)]
     max_len = wl.max_context_len
-    n_launch = (1 if args.unfused else 0) + 1 + (1 if ws_bytes else 0) + (1 if pairs.shape[0] else 0)
+    unfused = args.unfused or fp8
+    n_launch = (1 if unfused else 0) + 1 + (1 if ws_bytes else 0) + (1 if pairs.shape[0] else 0)
+
+    def step_fp8(i, ev=None):
+        kp, vp, ksp, vsp = pools[i % replicas]
+        if pairs.shape[0]:
+            pkv.copy_blocks_fp8(kp, vp, ksp, vsp, pairs, status=status)
+        pkv.write_cache_fp8(k_new, v_new, kp, vp, ksp, vsp, sm, status=status)
+        if ev is not None:
+            ev[0].record()
+        pkv.decode_partitions_fp8(out, q, kp, vp, ksp, vsp, bt, cl, wl.scale, partition_size=ps,
+                                  max_context_len=max_len, workspace=ws, status=status)
+        if ev is not None:
+            ev[1].record()
+        if ws is not None:
+            pkv.decode_reduce(out, cl, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
+                              head_dim=wl.head_dim, partition_size=ps, max_context_len=max_len, workspace=ws,
+                              status=status)
 
     def step(i, ev=None):
-        kp, vp = pools[i % replicas]
+        if fp8:
+            return step_fp8(i, ev)
+        kp, vp = pools[i % replicas][:2]
         if pairs.shape[0]:
             pkv.copy_blocks(kp, vp, pairs, status=status)
         if not args.unfused:  # the new token's write fused into the partition kernel
@@ -230,7 +277,7 @@ def run_gpu(args):
                               head_dim=wl.head_dim, partition_size=ps, max_context_len=max_len, workspace=ws,
                               status=status)
 
-    nb = step_bytes(wl)
+    nb = step_bytes_fp8(wl) if fp8 else step_bytes(wl)
     K, W = args.steps, args.warmup
     for i in range(W):
         step(i)
@@ -302,19 +349,24 @@ def run_gpu(args):
     ms = elapsed_ms / K
     value = job_gbs(nb["step"], world, K, elapsed_ms)
     kern_avg_ms = statistics.mean(kern_ms)
-    kernel_name = "decode_balanced_kernel" if ps == pkv.PARTITION_BALANCED else "decode_partitions_kernel"
+    if fp8:
+        kernel_name = "decode_partitions_fp8_kernel"
+    else:
+        kernel_name = "decode_balanced_kernel" if ps == pkv.PARTITION_BALANCED else "decode_partitions_kernel"
     traffic = _recorded_traffic(args.config, kernel_name)
     achieved = nb["attention"] / (kern_avg_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": wl.dtype, "data": "synthetic",
+        "dtype": f"e4m3 KV, {wl.dtype} q" if fp8 else wl.dtype, "data": "synthetic",
         "config": {"workload": wl.name, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
                    "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": 16,
                    "partition_size": ps, "max_context_len": max_len, "total_context_tokens":
                    int(wl.context_lens.astype(np.int64).sum()), "num_blocks": wl.num_blocks,
                    "cow_pairs": int(wl.copy_pairs.shape[0]), "out_dtype": "f32",
-                   "entry": "pkv_write_cache + pkv_decode_attention" if args.unfused else "pkv_decode_step",
+                   "kv_cache": "e4m3 + per-(block, KV head) f32 scales" if fp8 else wl.dtype,
+                   "entry": ("pkv_copy_blocks_fp8 + pkv_write_cache_fp8 + pkv_decode_attention_fp8" if fp8 else
+                             "pkv_write_cache + pkv_decode_attention" if args.unfused else "pkv_decode_step"),
                    "l2": f"inputs larger than L2: {replicas} pool replicas of {pool_bytes / 1e6:.0f} MB rotated "
                          f"(L2 {l2 / 1e6:.0f} MB)", "parallelism": f"replicas x{world}"},
         "pct_of_hbm_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
@@ -330,7 +382,7 @@ def run_gpu(args):
         "e2e": e2e,
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds, f8 if fp8 else None)
     if world > 1:
         dist.destroy_process_group()
     return line
@@ -341,10 +393,13 @@ def _recorded_traffic(cfg, kernel):
     summary, if it was taken on the current kernel sources; else None."""
     import hashlib
 
-    if kernel != "decode_partitions_kernel":
+    sources = {"decode_partitions_kernel": ("decode_partitions", "pkv_decode.cu"),
+               "decode_partitions_fp8_kernel": ("decode_partitions_fp8", "pkv_decode_fp8.cu")}
+    if kernel not in sources:
         return None
-    summ = os.path.join(ROOT, "profiles", f"decode_partitions_config{cfg}_traffic.txt")
-    srcs = [os.path.join(ROOT, "paged_kv_cache_112_gb300", "csrc", f) for f in ("pkv_decode.cu", "pkv_device.cuh")]
+    stem, src = sources[kernel]
+    summ = os.path.join(ROOT, "profiles", f"{stem}_config{cfg}_traffic.txt")
+    srcs = [os.path.join(ROOT, "paged_kv_cache_112_gb300", "csrc", f) for f in (src, "pkv_device.cuh")]
     if not os.path.exists(summ):
         return None
     vals = {}
@@ -367,42 +422,53 @@ def _recorded_traffic(cfg, kernel):
 
 # ------------------------------------------------------------ CPU oracle arm
 
-def _oracle_pass(wl, seqs, k_pool, v_pool, threads):
+def _oracle_pass(wl, seqs, pools, threads):
     import oracle
 
     rows = [(s, h) for s in seqs for h in range(wl.num_q_heads)]
-    oracle.decode_attention(wl.q, k_pool, v_pool, wl.block_tables, wl.context_lens, wl.scale, wl.dtype,
-                            rows=rows, num_threads=threads)
+    if len(pools) == 4:  # FP8 codes and scales
+        oracle.decode_attention_fp8(wl.q, *pools, wl.block_tables, wl.context_lens, wl.scale, wl.dtype, rows=rows,
+                                    num_threads=threads)
+    else:
+        oracle.decode_attention(wl.q, *pools, wl.block_tables, wl.context_lens, wl.scale, wl.dtype, rows=rows,
+                                num_threads=threads)
 
 
-def _sample_bytes(wl, seqs):
+def _sample_bytes(wl, seqs, elem_bytes=2):
     L = wl.context_lens.astype(np.int64)[list(seqs)]
-    return int(L.sum()) * wl.num_kv_heads * wl.head_dim * 2 * 2
+    return int(L.sum()) * wl.num_kv_heads * wl.head_dim * 2 * elem_bytes
 
 
-def cpu_baseline(wl, seconds):
+def cpu_baseline(wl, seconds, fp8_pools=None):
     """The oracle, as it stands, on whole sequences of the workload, repeated
-    for about `seconds` of wall time on all host cores."""
+    for about `seconds` of wall time on all host cores (over FP8 pools when
+    given)."""
     import oracle
 
     threads = oracle.hardware_threads()
-    k, v, _ = oracle.apply_step(wl, attention=False)
+    if fp8_pools is not None:
+        pools = oracle.apply_step_fp8(wl, fp8_pools, attention=False)[:4]
+        eb = 1
+    else:
+        pools = oracle.apply_step(wl, attention=False)[:2]
+        eb = 2
     order = list(range(wl.num_seqs))
     t0 = time.perf_counter()
-    _oracle_pass(wl, order[:1], k, v, threads)
+    _oracle_pass(wl, order[:1], pools, threads)
     per_seq = max(time.perf_counter() - t0, 1e-4)
     n = max(1, min(wl.num_seqs, int(seconds / 3 / per_seq)))
     seqs = order[:n]
     done_bytes, t0, reps = 0, time.perf_counter(), 0
     while True:
-        _oracle_pass(wl, seqs, k, v, threads)
-        done_bytes += _sample_bytes(wl, seqs)
+        _oracle_pass(wl, seqs, pools, threads)
+        done_bytes += _sample_bytes(wl, seqs, eb)
         reps += 1
         if time.perf_counter() - t0 >= seconds or reps >= 1000:
             break
     dt = time.perf_counter() - t0
     return {"value": round(done_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"fp64 oracle over the first {n} of {wl.num_seqs} sequences (all query heads), "
+            "sample": f"fp64 oracle{' (FP8 pools)' if eb == 1 else ''} over the first {n} of {wl.num_seqs} "
+                      f"sequences (all query heads), "
                       f"{reps} passes, {dt:.1f} s wall"}
 
 
@@ -415,13 +481,19 @@ def run_reference(args):
 
     wl = P.make_workload(args.config, poison=False)
     threads = oracle.hardware_threads()
-    k, v, _ = oracle.apply_step(wl, attention=False)
+    fp8 = args.kv == "fp8"
+    if fp8:
+        pools = oracle.apply_step_fp8(wl, P.make_fp8_pools(wl, poison=False), attention=False)[:4]
+        attend = oracle.decode_attention_fp8
+    else:
+        pools = oracle.apply_step(wl, attention=False)[:2]
+        attend = oracle.decode_attention
     K, W = args.steps, args.warmup
     # size one step's sample so that W + K steps take about args.ref_seconds
     rows_all = [(s, h) for s in range(wl.num_seqs) for h in range(wl.num_q_heads)]
     t0 = time.perf_counter()
-    oracle.decode_attention(wl.q, k, v, wl.block_tables, wl.context_lens, wl.scale, wl.dtype,
-                            rows=rows_all[: wl.num_q_heads], num_threads=threads)
+    attend(wl.q, *pools, wl.block_tables, wl.context_lens, wl.scale, wl.dtype, rows=rows_all[: wl.num_q_heads],
+           num_threads=threads)
     per_row = max((time.perf_counter() - t0) / wl.num_q_heads, 1e-6)
     budget = args.ref_seconds / max(1, K + W)
     n_rows = int(max(1, min(len(rows_all), budget / per_row)))
@@ -429,11 +501,11 @@ def run_reference(args):
     G = wl.num_q_heads // wl.num_kv_heads
     L = wl.context_lens.astype(np.int64)
     # KV bytes the sampled rows account for (a row reads 1/G of its KV head's bytes)
-    sample_bytes = sum(int(L[s]) * wl.head_dim * 2 * 2 for s, _ in rows) / G
+    eb = 1 if fp8 else 2
+    sample_bytes = sum(int(L[s]) * wl.head_dim * 2 * eb for s, _ in rows) / G
 
     def one():
-        oracle.decode_attention(wl.q, k, v, wl.block_tables, wl.context_lens, wl.scale, wl.dtype, rows=rows,
-                                num_threads=threads)
+        attend(wl.q, *pools, wl.block_tables, wl.context_lens, wl.scale, wl.dtype, rows=rows, num_threads=threads)
 
     for _ in range(W):
         one()
@@ -443,8 +515,8 @@ def run_reference(args):
     dt = time.perf_counter() - t0
     ms = dt / K * 1e3
     value = sample_bytes / (ms * 1e-3) / 1e9
-    sample = (f"fp64 oracle, {n_rows} (sequence, query head) rows of {len(rows_all)} per step, "
-              f"{threads} threads")
+    sample = (f"fp64 oracle{' (FP8 pools)' if fp8 else ''}, {n_rows} (sequence, query head) rows of "
+              f"{len(rows_all)} per step, {threads} threads")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -469,6 +541,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused", action="store_true",
                     help="run write_cache and decode attention as separate calls instead of pkv_decode_step")
+    ap.add_argument("--kv", default="16bit", choices=["16bit", "fp8"],
+                    help="KV pool format: the workload's 16-bit type, or e4m3 codes with per-(block, KV head) "
+                         "scales (copy, write and attention through the *_fp8 entry points)")
     args = ap.parse_args(argv)
     if args.steps is None:
         args.steps = 5000 if args.impl == "ours" else 20

@@ -314,6 +314,20 @@ pkv_status pkv_decode_attention_fp8(void* out, const void* q, const void* k_pool
                                     void* workspace, size_t workspace_bytes, pkv_dtype q_dtype,
                                     pkv_dtype out_dtype, int32_t* dev_status, void* stream);
 
+/*
+ * pkv_decode_partitions_fp8 -- the first of the two kernels of
+ * pkv_decode_attention_fp8 (same arguments); follow it with
+ * pkv_decode_reduce exactly as pkv_decode_partitions.
+ */
+pkv_status pkv_decode_partitions_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                     const float* k_scale, const float* v_scale,
+                                     const int32_t* block_tables, int max_blocks_per_seq,
+                                     const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                     int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                     float scale, int partition_size, int max_context_len,
+                                     void* workspace, size_t workspace_bytes, pkv_dtype q_dtype,
+                                     pkv_dtype out_dtype, int32_t* dev_status, void* stream);
+
 /* Static string naming a status code.  Host function. */
 const char* pkv_status_string(pkv_status status);
 

@@ -48,6 +48,7 @@ _SIGS["pkv_copy_blocks_fp8"] = [_c_void_p] * 5 + [_c_int] * 5 + [_c_void_p, _c_v
 _SIGS["pkv_decode_attention_fp8"] = ([_c_void_p] * 7 + [_c_int, _c_void_p] + [_c_int] * 6 +
                                      [_c_float, _c_int, _c_int, _c_void_p, _c_size_t, _c_int, _c_int, _c_void_p,
                                       _c_void_p])
+_SIGS["pkv_decode_partitions_fp8"] = _SIGS["pkv_decode_attention_fp8"]
 
 _LIB = None
 
@@ -257,9 +258,8 @@ def copy_blocks_fp8(k_pool, v_pool, k_scale, v_scale, pairs, *, status=None, str
            "pkv_copy_blocks_fp8")
 
 
-def decode_attention_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, context_lens, scale, *,
-                         partition_size=0, max_context_len, workspace=None, status=None, stream=None):
-    """pkv_decode_attention_fp8 (partition kernel + reduce kernel); q f16/bf16 [S, H_q, D]."""
+def _decode_fp8_args(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, context_lens, scale, partition_size,
+                     max_context_len, workspace, status, stream):
     NB, B, Hkv, D = _fp8_pools(k_pool, v_pool, k_scale, v_scale)
     _need_cuda(out, q, block_tables, context_lens, workspace, status)
     S, Hq, Dq = q.shape
@@ -268,9 +268,25 @@ def decode_attention_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables,
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise PkvError("block_tables and context_lens must be int32")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load().pkv_decode_attention_fp8(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
-                                           _ptr(v_scale), _ptr(block_tables), int(block_tables.shape[1]),
-                                           _ptr(context_lens), S, Hq, Hkv, D, B, NB, float(scale),
-                                           int(partition_size), int(max_context_len), _ptr(workspace), ws_bytes,
-                                           _kv_dtype(q), _DTYPES[out.dtype], _ptr(status), _stream(stream)),
+    return (_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
+            int(block_tables.shape[1]), _ptr(context_lens), S, Hq, Hkv, D, B, NB, float(scale), int(partition_size),
+            int(max_context_len), _ptr(workspace), ws_bytes, _kv_dtype(q), _DTYPES[out.dtype], _ptr(status),
+            _stream(stream))
+
+
+def decode_attention_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, context_lens, scale, *,
+                         partition_size=0, max_context_len, workspace=None, status=None, stream=None):
+    """pkv_decode_attention_fp8 (partition kernel + reduce kernel); q f16/bf16 [S, H_q, D]."""
+    _check(load().pkv_decode_attention_fp8(*_decode_fp8_args(out, q, k_pool, v_pool, k_scale, v_scale, block_tables,
+                                                             context_lens, scale, partition_size, max_context_len,
+                                                             workspace, status, stream)),
            "pkv_decode_attention_fp8")
+
+
+def decode_partitions_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, context_lens, scale, *,
+                          partition_size=0, max_context_len, workspace=None, status=None, stream=None):
+    """pkv_decode_partitions_fp8: the first kernel of decode_attention_fp8 alone (follow with decode_reduce)."""
+    _check(load().pkv_decode_partitions_fp8(*_decode_fp8_args(out, q, k_pool, v_pool, k_scale, v_scale,
+                                                              block_tables, context_lens, scale, partition_size,
+                                                              max_context_len, workspace, status, stream)),
+           "pkv_decode_partitions_fp8")

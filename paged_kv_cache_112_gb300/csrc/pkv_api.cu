@@ -511,13 +511,13 @@ pkv_status pkv_copy_blocks_fp8(void* k_pool, void* v_pool, float* k_scale, float
   return launch_copy_blocks(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-pkv_status pkv_decode_attention_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
-                                    const float* k_scale, const float* v_scale, const int32_t* block_tables,
-                                    int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
-                                    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                                    float scale, int partition_size, int max_context_len, void* workspace,
-                                    size_t workspace_bytes, pkv_dtype q_dtype, pkv_dtype out_dtype,
-                                    int32_t* dev_status, void* stream) {
+pkv_status pkv_decode_partitions_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                     const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                                     int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                                     int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                     float scale, int partition_size, int max_context_len, void* workspace,
+                                     size_t workspace_bytes, pkv_dtype q_dtype, pkv_dtype out_dtype,
+                                     int32_t* dev_status, void* stream) {
   if (partition_size == PKV_PARTITION_BALANCED) return PKV_ERR_UNSUPPORTED;
   DecodeCall c{};
   pkv_status st = prepare_decode(&c, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
@@ -534,10 +534,26 @@ pkv_status pkv_decode_attention_fp8(void* out, const void* q, const void* k_pool
   if (!encode_pool_map(&c.tmap_k, k_pool, num_blocks, num_kv_heads, head_dim, 1) ||
       !encode_pool_map(&c.tmap_v, v_pool, num_blocks, num_kv_heads, head_dim, 1))
     return PKV_ERR_CUDA;
-  const cudaStream_t strm = static_cast<cudaStream_t>(stream);
-  if (launch_decode_partitions_fp8(c.args, c.tmap_k, c.tmap_v, head_dim, q_dtype == PKV_BF16, strm) != cudaSuccess)
-    return PKV_ERR_CUDA;
-  return launch_decode_reduce(c.args, head_dim, strm) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return launch_decode_partitions_fp8(c.args, c.tmap_k, c.tmap_v, head_dim, q_dtype == PKV_BF16,
+                                      static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_decode_attention_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                    const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                                    int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                                    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                    float scale, int partition_size, int max_context_len, void* workspace,
+                                    size_t workspace_bytes, pkv_dtype q_dtype, pkv_dtype out_dtype,
+                                    int32_t* dev_status, void* stream) {
+  pkv_status st = pkv_decode_partitions_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables,
+                                            max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                            head_dim, block_size, num_blocks, scale, partition_size, max_context_len,
+                                            workspace, workspace_bytes, q_dtype, out_dtype, dev_status, stream);
+  if (st != PKV_OK) return st;
+  return pkv_decode_reduce(out, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, partition_size,
+                           max_context_len, workspace, workspace_bytes, out_dtype, dev_status, stream);
 }
 
 const char* pkv_status_string(pkv_status s) {

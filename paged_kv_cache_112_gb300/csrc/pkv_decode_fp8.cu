@@ -24,15 +24,20 @@
 //    (gr = lane/4, tq = lane%4) needs exactly bytes [32tq, 32tq+32) of token
 //    rows gr and gr+8: two 16-byte shared loads per row, conflict-free under
 //    the swizzle.  For QK^T, k-step kk takes codes 32tq+4kk+{0,1} (A cols
-//    2tq, 2tq+1) and 32tq+4kk+{2,3} (cols 2tq+8, 2tq+9).  For PV, code pair
-//    j of a row (dims 32tq+2j, +1) is column pair tq of an 8x8 block, which
-//    movmatrix transposes into the V^T A fragment; M-tile mt covers pairs 2mt
-//    and 2mt+1, so accumulator row gr (+8) of mt is output dim
-//    32(gr/2) + 4mt + gr%2 (+2).
+//    2tq, 2tq+1) and 32tq+4kk+{2,3} (cols 2tq+8, 2tq+9).  For PV (A = V^T,
+//    k = tokens) lane (gr, tq) reads chunk gr (dims 16gr..16gr+15) of token
+//    rows 2tq, 2tq+1, 2tq+8, 2tq+9; a byte permute pairs each dim's codes of
+//    two tokens, which convert straight to the f16x2 A registers.  Row gr
+//    (gr+8) of M-tile mt is dim 16gr + 2mt (+1), so a lane ends up owning
+//    16 contiguous output dims of its two heads.
 //  * Scales: the K scale multiplies the tile's scores with the softmax scale
-//    (one multiplier per tile); the V scale multiplies the tile's P.V product
-//    as it is added to the accumulator.  Both are read with the table
-//    entries, one chunk of 32 tiles at a time.
+//    (one multiplier per tile); the V scale multiplies P before it is split
+//    into f16 hi + lo parts, in a per-warp power-of-two unit (raised, with
+//    the accumulator rescaled, when a chunk's largest V scale needs it) that
+//    keeps P * scale inside the f16 range.  Both scales are read with the
+//    table entries, one chunk of 32 tiles at a time.
+//  * The accumulator is rescaled only in tiles where some head's running
+//    max grows (a warp-uniform branch).
 #include "pkv_device.cuh"
 
 namespace pkv {
@@ -116,83 +121,107 @@ struct WarpAttentionFp8 : SoftmaxState<D / 16> {
     return down;
   }
 
-  // One tile: nv valid tokens (rows >= nv are masked, whatever they hold).
-  // sl2k = log2(e) * softmax scale * q prescale * K scale; vscale = V scale.
-  __device__ __forceinline__ void tile(uint32_t sK, uint32_t sV, int nv, float sl2k, float vscale, int lane) {
+  // NT tiles at once (independent chains interleave; one softmax update for
+  // all of them).  Tile t: K at sK[t], V at sK[t] + 2048, nv[t] valid
+  // tokens (rows >= nv are masked, whatever they hold), sl2k[t] = log2(e) *
+  // softmax scale * q prescale * K scale, pv[t] = V scale in the
+  // accumulator's unit (a power of two chosen per chunk of tiles).
+  template <int NT>
+  __device__ __forceinline__ void tiles(const uint32_t (&sK)[NT], const int (&nv)[NT], const float (&sl2k)[NT],
+                                        const float (&pv)[NT], int lane) {
     const int gr = lane >> 2, tq = lane & 3;
-    // Rows gr and gr+8 share the swizzle phase (row & 7 == gr).
+    // K: rows gr and gr+8 (same swizzle phase), chunks 2tq and 2tq+1.
     const uint32_t off0 = gr * 128 + (((2 * tq) ^ gr) << 4);
     const uint32_t off1 = gr * 128 + (((2 * tq + 1) ^ gr) << 4);
-    uint32_t k0[8], k1[8], v0[8], v1[8];  // rows gr, gr+8: words i = codes [32tq + 4i, +4)
-    lds128(k0, sK + off0);
-    lds128(k0 + 4, sK + off1);
-    lds128(k1, sK + 1024 + off0);
-    lds128(k1 + 4, sK + 1024 + off1);
-    lds128(v0, sV + off0);
-    lds128(v0 + 4, sV + off1);
-    lds128(v1, sV + 1024 + off0);
-    lds128(v1 + 4, sV + 1024 + off1);
-
-    // Scores S^T[token][head]; even and odd k-steps in separate chains.
-    float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t kw[NT][2][8];  // words i = codes [32tq + 4i, +4) of rows gr, gr+8
 #pragma unroll
-    for (int kk = 0; kk < KT; ++kk) {
-      uint32_t a[4];
-      e4m3x4_to_f16x4(k0[kk], a[0], a[2]);
-      e4m3x4_to_f16x4(k1[kk], a[1], a[3]);
-      if (kk & 1)
-        mma_16816<false>(c2, a, qf[kk][0], qf[kk][1]);
-      else
-        mma_16816<false>(c, a, qf[kk][0], qf[kk][1]);
+    for (int t = 0; t < NT; ++t) {
+      lds128(kw[t][0], sK[t] + off0);
+      lds128(kw[t][0] + 4, sK[t] + off1);
+      lds128(kw[t][1], sK[t] + 1024 + off0);
+      lds128(kw[t][1] + 4, sK[t] + 1024 + off1);
     }
-    float s0 = (c[0] + c2[0]) * sl2k, s1 = (c[1] + c2[1]) * sl2k;
-    float s2 = (c[2] + c2[2]) * sl2k, s3 = (c[3] + c2[3]) * sl2k;
-    if (gr >= nv) s0 = s1 = kNegInf;
-    if (gr + 8 >= nv) s2 = s3 = kNegInf;
-    float p0, p1, p2, p3;
-    this->online_update(s0, s1, s2, s3, p0, p1, p2, p3);
-
-    // P^T as f16 hi + lo parts (two MMAs), so the weights keep ~2^-22
-    // relative precision.
-    const uint32_t h0 = pack_f16(p0, p1), h1 = pack_f16(p2, p3);
-    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
-    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
-    const uint32_t pb0 = movmatrix_trans(h0), pb1 = movmatrix_trans(h1);
-    const uint32_t pl0 = movmatrix_trans(pack_f16(p0 - f0.x, p1 - f0.y));
-    const uint32_t pl1 = movmatrix_trans(pack_f16(p2 - f1.x, p3 - f1.y));
-
-    // V codes of tokens >= nv may be anything (NaN codes included): zero them.
-    if (nv < kBlockSize) {
-      if (gr >= nv) {
+    // Scores S^T[token][head]; per tile, even and odd k-steps in separate chains.
+    float c[NT][2][4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v0[i] = 0u;
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) c[t][0][j] = c[t][1][j] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk)
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        uint32_t a[4];
+        e4m3x4_to_f16x4(kw[t][0][kk], a[0], a[2]);
+        e4m3x4_to_f16x4(kw[t][1][kk], a[1], a[3]);
+        mma_16816<false>(c[t][kk & 1], a, qf[kk][0], qf[kk][1]);
       }
-      if (gr + 8 >= nv) {
+    // V: rows 2tq, 2tq+1, 2tq+8, 2tq+9, chunk gr (codes of dims 16gr .. 16gr+15).
+    const int r0 = 2 * tq;
+    const uint32_t voff[4] = {static_cast<uint32_t>(r0 * 128 + ((gr ^ r0) << 4)),
+                              static_cast<uint32_t>((r0 + 1) * 128 + ((gr ^ (r0 + 1)) << 4)),
+                              static_cast<uint32_t>((r0 + 8) * 128 + ((gr ^ r0) << 4)),
+                              static_cast<uint32_t>((r0 + 9) * 128 + ((gr ^ (r0 + 1)) << 4))};
+    uint32_t vw[NT][4][4];  // [tile][row 2tq, 2tq+1, 2tq+8, 2tq+9][word]
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v1[i] = 0u;
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) lds128(vw[t][r], sK[t] + 2048 + voff[r]);
+
+    float sc[4 * NT], p[4 * NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      sc[4 * t] = (c[t][0][0] + c[t][1][0]) * sl2k[t];
+      sc[4 * t + 1] = (c[t][0][1] + c[t][1][1]) * sl2k[t];
+      sc[4 * t + 2] = (c[t][0][2] + c[t][1][2]) * sl2k[t];
+      sc[4 * t + 3] = (c[t][0][3] + c[t][1][3]) * sl2k[t];
+      if (gr >= nv[t]) sc[4 * t] = sc[4 * t + 1] = kNegInf;
+      if (gr + 8 >= nv[t]) sc[4 * t + 2] = sc[4 * t + 3] = kNegInf;
+    }
+    this->template online_update_lazy<NT>(sc, p);
+
+    // P^T (times the V scale) as f16 hi + lo parts, two MMAs per tile, so
+    // the weights keep ~2^-22 relative precision.
+    uint32_t pb[NT][4];  // hi (tokens 0-7, 8-15), lo (tokens 0-7, 8-15)
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const float q0 = p[4 * t] * pv[t], q1 = p[4 * t + 1] * pv[t];
+      const float q2 = p[4 * t + 2] * pv[t], q3 = p[4 * t + 3] * pv[t];
+      const uint32_t h0 = pack_f16(q0, q1), h1 = pack_f16(q2, q3);
+      const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
+      const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
+      pb[t][0] = movmatrix_trans(h0);
+      pb[t][1] = movmatrix_trans(h1);
+      pb[t][2] = movmatrix_trans(pack_f16(q0 - f0.x, q1 - f0.y));
+      pb[t][3] = movmatrix_trans(pack_f16(q2 - f1.x, q3 - f1.y));
+      // V codes of tokens >= nv may be anything (NaN codes included): zero them.
+      if (nv[t] < kBlockSize) {
+        const int row[4] = {r0, r0 + 1, r0 + 8, r0 + 9};
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          if (row[r] >= nv[t]) vw[t][r][0] = vw[t][r][1] = vw[t][r][2] = vw[t][r][3] = 0u;
       }
     }
+    // V^T A fragment of M-tile mt: rows gr / gr+8 are dims 16gr+2mt / +1,
+    // k = tokens.  A byte permute pairs a dim's codes of tokens 2tq and
+    // 2tq+1 (and 2tq+8, 2tq+9), which convert to the f16x2 the MMA wants.
 #pragma unroll
     for (int mt = 0; mt < KT; ++mt) {
-      uint32_t x00, x01, x10, x11;  // 8x8 blocks (tokens 0-7 | 8-15) x (pair 2mt | 2mt+1)
-      e4m3x4_to_f16x4(v0[mt], x00, x01);
-      e4m3x4_to_f16x4(v1[mt], x10, x11);
-      uint32_t va[4];
-      va[0] = movmatrix_trans(x00);  // rows: pair 2mt, k: tokens 0-7
-      va[1] = movmatrix_trans(x01);  // rows: pair 2mt+1, k: tokens 0-7
-      va[2] = movmatrix_trans(x10);  // rows: pair 2mt, k: tokens 8-15
-      va[3] = movmatrix_trans(x11);
-      float t[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_16816<false>(t, va, pb0, pb1);
-      mma_16816<false>(t, va, pl0, pl1);
+      const int w = mt >> 1;
+      const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[mt][j] = fmaf(vscale, t[j], acc[mt][j]);
+      for (int t = 0; t < NT; ++t) {
+        uint32_t va[4];
+        e4m3x4_to_f16x4(__byte_perm(vw[t][0][w], vw[t][1][w], sel), va[0], va[1]);
+        e4m3x4_to_f16x4(__byte_perm(vw[t][2][w], vw[t][3][w], sel), va[2], va[3]);
+        mma_16816<false>(acc[mt], va, pb[t][0], pb[t][1]);
+        mma_16816<false>(acc[mt], va, pb[t][2], pb[t][3]);
+      }
     }
   }
 
-  // Output dim of accumulator row gr of M-tile mt (row gr+8: +2).
-  __device__ __forceinline__ static int out_dim(int mt, int gr) { return 32 * (gr >> 1) + 4 * mt + (gr & 1); }
-
+  // acc[mt][0..1] hold dim 16gr + 2mt of heads a, b; acc[mt][2..3] dim +1:
+  // a lane owns dims [16gr, 16gr+16) of its two heads.
   __device__ __forceinline__ void store_final(void* out, int64_t out_head0, int G, int dtype, int lane) const {
     const int gr = lane >> 2, tq = lane & 3;
     const int ha = 2 * tq, hb = ha + 1;
@@ -200,14 +229,14 @@ struct WarpAttentionFp8 : SoftmaxState<D / 16> {
     const float ib = this->l_b > 0.f ? 1.f / this->l_b : 0.f;
 #pragma unroll
     for (int mt = 0; mt < KT; ++mt) {
-      const int d = out_dim(mt, gr);
+      const int d = 16 * gr + 2 * mt;
       if (ha < G) {
         store_out(out, (out_head0 + ha) * D + d, acc[mt][0] * ia, dtype);
-        store_out(out, (out_head0 + ha) * D + d + 2, acc[mt][2] * ia, dtype);
+        store_out(out, (out_head0 + ha) * D + d + 1, acc[mt][2] * ia, dtype);
       }
       if (hb < G) {
         store_out(out, (out_head0 + hb) * D + d, acc[mt][1] * ib, dtype);
-        store_out(out, (out_head0 + hb) * D + d + 2, acc[mt][3] * ib, dtype);
+        store_out(out, (out_head0 + hb) * D + d + 1, acc[mt][3] * ib, dtype);
       }
     }
   }
@@ -218,16 +247,13 @@ struct WarpAttentionFp8 : SoftmaxState<D / 16> {
     const int ha = 2 * tq, hb = ha + 1;
     const int64_t ra = rec0 + ha * rec_stride, rb = rec0 + hb * rec_stride;
 #pragma unroll
-    for (int mt = 0; mt < KT; ++mt) {
-      const int d = out_dim(mt, gr);
-      if (ha < G) {
-        ws_acc[ra * D + d] = acc[mt][0];
-        ws_acc[ra * D + d + 2] = acc[mt][2];
-      }
-      if (hb < G) {
-        ws_acc[rb * D + d] = acc[mt][1];
-        ws_acc[rb * D + d + 2] = acc[mt][3];
-      }
+    for (int j = 0; j < KT / 2; ++j) {  // dims 16gr + 4j .. +3: M-tiles 2j, 2j+1
+      if (ha < G)
+        *reinterpret_cast<float4*>(ws_acc + ra * D + 16 * gr + 4 * j) =
+            make_float4(acc[2 * j][0], acc[2 * j][2], acc[2 * j + 1][0], acc[2 * j + 1][2]);
+      if (hb < G)
+        *reinterpret_cast<float4*>(ws_acc + rb * D + 16 * gr + 4 * j) =
+            make_float4(acc[2 * j][1], acc[2 * j][3], acc[2 * j + 1][1], acc[2 * j + 1][3]);
     }
     if (gr == 0) {
       if (ha < G) ws_ml[ra] = make_float2(this->m_a, this->l_a);
@@ -235,6 +261,20 @@ struct WarpAttentionFp8 : SoftmaxState<D / 16> {
     }
   }
 };
+
+// 2^e for an integer e in [-126, 127], exactly.
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
+
+// The accumulator's unit for a chunk of tiles: 2^-e with 2^e <= the
+// largest V scale of the chunk (over the warp) < 2^(e+1), so P * scale /
+// unit stays below 2 and well inside the f16 range.
+__device__ __forceinline__ int chunk_exponent(float vs) {
+  float m = vs;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  const int e = static_cast<int>((__float_as_uint(m) >> 23) & 0xff) - 127;
+  return min(max(e, -126), 126);
+}
 
 // One unit (sequence s, KV head g, partition p) served by U of the CTA's NW
 // warps; `raw_len` is the sequence's context length as read and `first` the
@@ -283,10 +323,16 @@ __device__ __forceinline__ void partition_unit_fp8(const DecodeArgs& a, const CU
   // Lane j holds the entry and scales of the warp's tile j of the current
   // chunk of 32 (the previous chunk's scales stay until its last tile, which
   // is consumed up to NST - 1 tiles after the next chunk's first issue).
+  // Lanes past the unit's tiles hold scale 0 (their entries are not used).
   int phys_cur = first;
   int phys_next = entry(32 + lane);
-  float ks_cur = ks_of(first), vs_cur = vs_of(first), ks_prev = 1.f, vs_prev = 1.f;
+  float ks_cur = lane < cnt ? ks_of(first) : 0.f, vs_cur = lane < cnt ? vs_of(first) : 0.f;
+  float ks_prev = 0.f, vs_prev = 0.f;
   int chunk_cur = 0;
+  // The accumulator holds (sum of P V) * 2^-vexp; vexp only grows, at the
+  // first tile of a chunk whose largest V scale needs it.
+  int vexp = -126, vexp_chunk = -1;
+  float inv_unit = exp2i(126);
 
   WarpRing<D, NST, 1> ring{smem_u32(smem + static_cast<size_t>(warp) * NST * Geom::kStageBytes),
                            smem_u32(smem + static_cast<size_t>(NW) * NST * Geom::kStageBytes) + 8 * NST * warp};
@@ -299,8 +345,9 @@ __device__ __forceinline__ void partition_unit_fp8(const DecodeArgs& a, const CU
       phys_next = entry(j + 32 + lane);
       ks_prev = ks_cur;
       vs_prev = vs_cur;
-      ks_cur = ks_of(phys_cur);
-      vs_cur = vs_of(phys_cur);
+      const bool mine = j + lane < cnt;
+      ks_cur = mine ? ks_of(phys_cur) : 0.f;
+      vs_cur = mine ? vs_of(phys_cur) : 0.f;
       chunk_cur = j >> 5;
     }
     const int st = j % NST;
@@ -318,27 +365,52 @@ __device__ __forceinline__ void partition_unit_fp8(const DecodeArgs& a, const CU
   at.reset();
   for (int j = 0; j < min(cnt, NST); ++j) issue(j);
 
-  for (int i = 0; i < cnt; ++i) {
-    if (!__all_sync(kFull, ring.wait(i, a.timeout_ns))) {
+  // Tiles are consumed two at a time (i even; both in the same chunk of
+  // 32).  A missing second tile reuses the first one's buffer with no valid
+  // token.
+  static_assert(NST % 2 == 0, "tile pairs take whole pairs of stages");
+  for (int i = 0; i < cnt; i += 2) {
+    const bool two = i + 1 < cnt;
+    const bool ok = ring.wait(i, a.timeout_ns) && (!two || ring.wait(i + 1, a.timeout_ns));
+    if (!__all_sync(kFull, ok)) {
       ring.drain(i, min(cnt, i + NST), a.timeout_ns);
       if (lane == 0) flag(a.dev_status, 16u);  // PKV_DEV_ERR_TIMEOUT; the output is undefined
       break;
     }
-    const int t = i * U + sub;
-    const int st = i % NST;
-    const int nv = ((bad_stage >> st) & 1) ? 0 : min(kBlockSize, ntok - t * kBlockSize);
+    if ((i >> 5) != vexp_chunk) {  // first pair of a chunk (its scales arrived NST tiles ago)
+      vexp_chunk = i >> 5;
+      const int e = chunk_exponent(vs_cur);
+      if (e > vexp) {
+        at.scale_acc(exp2i(vexp - e));
+        vexp = e;
+        inv_unit = exp2i(-e);
+      }
+    }
     const bool cur = (i >> 5) == chunk_cur;
-    const float ksc = __shfl_sync(kFull, cur ? ks_cur : ks_prev, i & 31);
-    const float vsc = __shfl_sync(kFull, cur ? vs_cur : vs_prev, i & 31);
-    const uint32_t sK = ring.k_tile(i);
-    at.tile(sK, sK + Geom::kTileBytes, nv, sl2q * ksc, vsc, lane);
+    const float ksel = cur ? ks_cur : ks_prev, vsel = cur ? vs_cur : vs_prev;
+    uint32_t sK[2];
+    int nv[2];
+    float sl2k[2], pv[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int j = two ? i + u : i;
+      const int st = j % NST;
+      const int t = j * U + sub;
+      nv[u] = (u == 1 && !two) || ((bad_stage >> st) & 1) ? 0 : min(kBlockSize, ntok - t * kBlockSize);
+      sK[u] = ring.k_tile(j);
+      sl2k[u] = sl2q * __shfl_sync(kFull, ksel, j & 31);
+      pv[u] = inv_unit * __shfl_sync(kFull, vsel, j & 31);
+    }
+    at.template tiles<2>(sK, nv, sl2k, pv, lane);
     __syncwarp();
     if (i + NST < cnt) {
       fence_proxy_async_smem();
       issue(i + NST);
+      if (i + 1 + NST < cnt) issue(i + 1 + NST);
     }
   }
 
+  at.scale_acc(exp2i(vexp));
   at.finish_sums();
   if constexpr (U > 1) {
     const uint32_t mine = smem_u32(smem + static_cast<size_t>(warp) * NST * Geom::kStageBytes);

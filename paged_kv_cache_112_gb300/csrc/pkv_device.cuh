@@ -139,6 +139,13 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t x) {
   return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
 }
 
+// 2^x by the MUFU approximation (relative error ~2^-22), subnormal results flushed to 0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void flag(int32_t* status, unsigned bit) {
   if (status) atomicOr(reinterpret_cast<unsigned*>(status), bit);
 }
@@ -374,6 +381,59 @@ struct SoftmaxState {
       acc[mt][2] *= al_a;
       acc[mt][3] *= al_b;
     }
+  }
+
+  // online_update over NT tiles at once (scores s[4t..4t+3] of tile t in
+  // the order of online_update), with the rescale of the accumulator
+  // skipped when no head's running max grows (the common case once a
+  // sequence is under way; a warp-uniform branch) and exponentials by
+  // ex2.approx.ftz (results below 2^-126 flush to 0).
+  template <int NT>
+  __device__ __forceinline__ void online_update_lazy(const float (&s)[4 * NT], float (&p)[4 * NT]) {
+    float mx_a = fmaxf(s[0], s[2]), mx_b = fmaxf(s[1], s[3]);
+#pragma unroll
+    for (int t = 1; t < NT; ++t) {
+      mx_a = fmaxf(mx_a, fmaxf(s[4 * t], s[4 * t + 2]));
+      mx_b = fmaxf(mx_b, fmaxf(s[4 * t + 1], s[4 * t + 3]));
+    }
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(kFull, mx_a, o));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(kFull, mx_b, o));
+    }
+    const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+    if (__any_sync(kFull, (mn_a > m_a) | (mn_b > m_b))) {
+      const float al_a = ex2_approx(m_a - mn_a), al_b = ex2_approx(m_b - mn_b);  // m = -inf: 0
+      l_a *= al_a;
+      l_b *= al_b;
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) {
+        acc[mt][0] *= al_a;
+        acc[mt][1] *= al_b;
+        acc[mt][2] *= al_a;
+        acc[mt][3] *= al_b;
+      }
+      m_a = mn_a;
+      m_b = mn_b;
+    }
+    const float u_a = (m_a == kNegInf) ? 0.f : m_a;
+    const float u_b = (m_b == kNegInf) ? 0.f : m_b;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      p[4 * t] = ex2_approx(s[4 * t] - u_a);
+      p[4 * t + 2] = ex2_approx(s[4 * t + 2] - u_a);
+      p[4 * t + 1] = ex2_approx(s[4 * t + 1] - u_b);
+      p[4 * t + 3] = ex2_approx(s[4 * t + 3] - u_b);
+      l_a += p[4 * t] + p[4 * t + 2];
+      l_b += p[4 * t + 1] + p[4 * t + 3];
+    }
+  }
+
+  __device__ __forceinline__ void scale_acc(float f) {
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[mt][j] *= f;
   }
 
   // Per-head sums over all lanes (lanes with the same lane%4 share heads).
