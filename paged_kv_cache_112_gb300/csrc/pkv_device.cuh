@@ -350,44 +350,13 @@ struct SoftmaxState {
     l_a = l_b = 0.f;
   }
 
-  // One tile of 16 tokens: this lane's scores s0 = (token gr, head a), s1 =
-  // (gr, b), s2 = (gr+8, a), s3 = (gr+8, b), masked ones -inf.  Updates the
-  // running max and sum, rescales the accumulator and returns the weights.
-  __device__ __forceinline__ void online_update(float s0, float s1, float s2, float s3, float& p0, float& p1,
-                                                float& p2, float& p3) {
-    // Block max per head over the 16 tokens (lanes with equal lane%4).
-    float mx_a = fmaxf(s0, s2), mx_b = fmaxf(s1, s3);
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(kFull, mx_a, o));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(kFull, mx_b, o));
-    }
-    const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-    const float u_a = (mn_a == kNegInf) ? 0.f : mn_a;
-    const float u_b = (mn_b == kNegInf) ? 0.f : mn_b;
-    const float al_a = exp2f(m_a - u_a), al_b = exp2f(m_b - u_b);
-    m_a = mn_a;
-    m_b = mn_b;
-    p0 = exp2f(s0 - u_a);
-    p2 = exp2f(s2 - u_a);
-    p1 = exp2f(s1 - u_b);
-    p3 = exp2f(s3 - u_b);
-    l_a = l_a * al_a + (p0 + p2);
-    l_b = l_b * al_b + (p1 + p3);
-#pragma unroll
-    for (int mt = 0; mt < KT; ++mt) {
-      acc[mt][0] *= al_a;
-      acc[mt][1] *= al_b;
-      acc[mt][2] *= al_a;
-      acc[mt][3] *= al_b;
-    }
-  }
-
-  // online_update over NT tiles at once (scores s[4t..4t+3] of tile t in
-  // the order of online_update), with the rescale of the accumulator
-  // skipped when no head's running max grows (the common case once a
-  // sequence is under way; a warp-uniform branch) and exponentials by
-  // ex2.approx.ftz (results below 2^-126 flush to 0).
+  // Online-softmax step over NT tiles of 16 tokens: this lane's scores of
+  // tile t are s[4t] = (token gr, head a), s[4t+1] = (gr, b), s[4t+2] =
+  // (gr+8, a), s[4t+3] = (gr+8, b), masked ones -inf.  Updates the running
+  // max and sum and returns the weights p.  The accumulator is rescaled
+  // only when some head's running max grows (the common case once a
+  // sequence is under way skips it; a warp-uniform branch).  Exponentials
+  // by ex2.approx.ftz (results below 2^-126 flush to 0).
   template <int NT>
   __device__ __forceinline__ void online_update_lazy(const float (&s)[4 * NT], float (&p)[4 * NT]) {
     float mx_a = fmaxf(s[0], s[2]), mx_b = fmaxf(s[1], s[3]);
@@ -562,8 +531,9 @@ struct WarpAttention : SoftmaxState<D / 16> {
     float s2 = (c[2] + c2[2]) * sl2, s3 = (c[3] + c2[3]) * sl2;
     if (gr >= nv) s0 = s1 = kNegInf;
     if (gr + 8 >= nv) s2 = s3 = kNegInf;
-    float p0, p1, p2, p3;
-    this->online_update(s0, s1, s2, s3, p0, p1, p2, p3);
+    float sc[4] = {s0, s1, s2, s3}, pw[4];
+    this->template online_update_lazy<1>(sc, pw);
+    const float p0 = pw[0], p1 = pw[1], p2 = pw[2], p3 = pw[3];
 
     uint32_t pb0, pb1, pl0 = 0, pl1 = 0;
     if constexpr (BF16) {
