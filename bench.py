@@ -17,9 +17,10 @@ divided by the device time of exactly K steps.  Between timed steps the K/V
 pools rotate over R device replicas whose total exceeds L2 several times.
 
 `--kv fp8` runs the same step over FP8 (e4m3) pools with one float scale per
-(block, KV head): copy-on-write, the quantising write and decode attention
-through the *_fp8 entry points; bytes count one byte per K/V element plus
-the scales.
+(block, KV head): copy-on-write, the quantising write kernel and decode
+attention through the *_fp8 entry points (--fused: the write fused into the
+partition kernel by pkv_decode_step_fp8, which measures no faster); bytes
+count one byte per K/V element plus the scales.
 
 `--impl reference` times the fp64 CPU oracle instead (a deliberately slow
 statement of the same computation) on a bounded sample of the workload.
@@ -234,18 +235,24 @@ def run_gpu(args):
     clone = lambda t: None if t is None else t.clone()
     pools = [(k0, v0, ks0, vs0)] + [(k0.clone(), v0.clone(), clone(ks0), clone(vs0)) for _ in range(replicas - 1)]
     max_len = wl.max_context_len
-    unfused = args.unfused or fp8
-    n_launch = (1 if unfused else 0) + 1 + (1 if ws_bytes else 0) + (1 if pairs.shape[0] else 0)
+    separate_write = (not args.fused) if fp8 else args.unfused
+    n_launch = (1 if separate_write else 0) + 1 + (1 if ws_bytes else 0) + (1 if pairs.shape[0] else 0)
 
     def step_fp8(i, ev=None):
         kp, vp, ksp, vsp = pools[i % replicas]
         if pairs.shape[0]:
             pkv.copy_blocks_fp8(kp, vp, ksp, vsp, pairs, status=status)
-        pkv.write_cache_fp8(k_new, v_new, kp, vp, ksp, vsp, sm, status=status)
+        if not args.fused:
+            pkv.write_cache_fp8(k_new, v_new, kp, vp, ksp, vsp, sm, status=status)
         if ev is not None:
             ev[0].record()
-        pkv.decode_partitions_fp8(out, q, kp, vp, ksp, vsp, bt, cl, wl.scale, partition_size=ps,
-                                  max_context_len=max_len, workspace=ws, status=status)
+        if not args.fused:
+            pkv.decode_partitions_fp8(out, q, kp, vp, ksp, vsp, bt, cl, wl.scale, partition_size=ps,
+                                      max_context_len=max_len, workspace=ws, status=status)
+        else:  # the quantising write of the new token fused into the partition kernel
+            pkv.decode_step_partitions_fp8(out, q, k_new, v_new, kp, vp, ksp, vsp, bt, cl, sm, wl.scale,
+                                           partition_size=ps, max_context_len=max_len, workspace=ws,
+                                           status=status)
         if ev is not None:
             ev[1].record()
         if ws is not None:
@@ -365,7 +372,8 @@ def run_gpu(args):
                    int(wl.context_lens.astype(np.int64).sum()), "num_blocks": wl.num_blocks,
                    "cow_pairs": int(wl.copy_pairs.shape[0]), "out_dtype": "f32",
                    "kv_cache": "e4m3 + per-(block, KV head) f32 scales" if fp8 else wl.dtype,
-                   "entry": ("pkv_copy_blocks_fp8 + pkv_write_cache_fp8 + pkv_decode_attention_fp8" if fp8 else
+                   "entry": (("pkv_decode_step_fp8" if args.fused else
+                              "pkv_write_cache_fp8 + pkv_decode_attention_fp8") if fp8 else
                              "pkv_write_cache + pkv_decode_attention" if args.unfused else "pkv_decode_step"),
                    "l2": f"inputs larger than L2: {replicas} pool replicas of {pool_bytes / 1e6:.0f} MB rotated "
                          f"(L2 {l2 / 1e6:.0f} MB)", "parallelism": f"replicas x{world}"},
@@ -541,6 +549,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused", action="store_true",
                     help="run write_cache and decode attention as separate calls instead of pkv_decode_step")
+    ap.add_argument("--fused", action="store_true",
+                    help="with --kv fp8: fuse the quantising write into the partition kernel (pkv_decode_step_fp8)")
     ap.add_argument("--kv", default="16bit", choices=["16bit", "fp8"],
                     help="KV pool format: the workload's 16-bit type, or e4m3 codes with per-(block, KV head) "
                          "scales (copy, write and attention through the *_fp8 entry points)")

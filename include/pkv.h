@@ -328,6 +328,41 @@ pkv_status pkv_decode_partitions_fp8(void* out, const void* q, const void* k_poo
                                      void* workspace, size_t workspace_bytes, pkv_dtype q_dtype,
                                      pkv_dtype out_dtype, int32_t* dev_status, void* stream);
 
+/*
+ * pkv_decode_step_fp8 -- one decode step over FP8 pools in one call, as
+ * pkv_decode_step: for every sequence s whose slot_mapping[s] is the slot of
+ * position L-1 through its block table, the result equals
+ * pkv_write_cache_fp8 (rows k_new[s], v_new[s], quantised with that
+ * block's scales) followed by pkv_decode_attention_fp8.  The write is fused
+ * into the partition kernel: the warp that reads the tile holding position
+ * L-1 quantises the rows, stores the codes and uses them directly.
+ * slot_mapping[s] == -1: no token; any other slot sets PKV_DEV_ERR_SLOT and
+ * is not written.  k_new, v_new have q_dtype, [num_seqs][num_kv_heads][128],
+ * rows 16-byte aligned, new_row_stride as in pkv_decode_step.
+ * pkv_decode_step_partitions_fp8 is its first kernel alone (follow it with
+ * pkv_decode_reduce).
+ */
+pkv_status pkv_decode_step_fp8(void* out, const void* q, const void* k_new, const void* v_new,
+                               int64_t new_row_stride, void* k_pool, void* v_pool, const float* k_scale,
+                               const float* v_scale, const int32_t* block_tables,
+                               int max_blocks_per_seq, const int32_t* context_lens,
+                               const int32_t* slot_mapping, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                               float scale, int partition_size, int max_context_len, void* workspace,
+                               size_t workspace_bytes, pkv_dtype q_dtype, pkv_dtype out_dtype,
+                               int32_t* dev_status, void* stream);
+
+pkv_status pkv_decode_step_partitions_fp8(void* out, const void* q, const void* k_new,
+                                          const void* v_new, int64_t new_row_stride, void* k_pool,
+                                          void* v_pool, const float* k_scale, const float* v_scale,
+                                          const int32_t* block_tables, int max_blocks_per_seq,
+                                          const int32_t* context_lens, const int32_t* slot_mapping,
+                                          int num_seqs, int num_q_heads, int num_kv_heads,
+                                          int head_dim, int block_size, int num_blocks, float scale,
+                                          int partition_size, int max_context_len, void* workspace,
+                                          size_t workspace_bytes, pkv_dtype q_dtype,
+                                          pkv_dtype out_dtype, int32_t* dev_status, void* stream);
+
 /* Static string naming a status code.  Host function. */
 const char* pkv_status_string(pkv_status status);
 

@@ -49,6 +49,10 @@ _SIGS["pkv_decode_attention_fp8"] = ([_c_void_p] * 7 + [_c_int, _c_void_p] + [_c
                                      [_c_float, _c_int, _c_int, _c_void_p, _c_size_t, _c_int, _c_int, _c_void_p,
                                       _c_void_p])
 _SIGS["pkv_decode_partitions_fp8"] = _SIGS["pkv_decode_attention_fp8"]
+_SIGS["pkv_decode_step_fp8"] = ([_c_void_p] * 4 + [_c_int64] + [_c_void_p] * 5 + [_c_int] + [_c_void_p] * 2 +
+                                [_c_int] * 6 + [_c_float, _c_int, _c_int, _c_void_p, _c_size_t, _c_int, _c_int,
+                                                _c_void_p, _c_void_p])
+_SIGS["pkv_decode_step_partitions_fp8"] = _SIGS["pkv_decode_step_fp8"]
 
 _LIB = None
 
@@ -290,3 +294,41 @@ def decode_partitions_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables
                                                               block_tables, context_lens, scale, partition_size,
                                                               max_context_len, workspace, status, stream)),
            "pkv_decode_partitions_fp8")
+
+
+def _step_fp8_args(out, q, k_new, v_new, k_pool, v_pool, k_scale, v_scale, block_tables, context_lens, slot_mapping,
+                   scale, partition_size, max_context_len, workspace, status, stream):
+    base = _decode_fp8_args(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, context_lens, scale,
+                            partition_size, max_context_len, workspace, status, stream)
+    _need_cuda(slot_mapping)
+    NB, B, Hkv, D = k_pool.shape
+    for t in (k_new, v_new):
+        if not t.is_cuda or t.dim() != 3 or t.shape != (q.shape[0], Hkv, D) or t.stride(2) != 1 or t.stride(1) != D:
+            raise PkvError("k_new/v_new must be CUDA [S, H_kv, D] with dense rows")
+    if k_new.stride(0) != v_new.stride(0) or k_new.dtype != q.dtype or v_new.dtype != q.dtype:
+        raise PkvError("k_new and v_new must share a row stride and the queries' dtype")
+    if slot_mapping.dtype != torch.int32 or slot_mapping.shape != (q.shape[0],):
+        raise PkvError("slot_mapping must be int32 [S]")
+    (o, qp, kp, vp, ksp, vsp, bt, maxb, cl, S, Hq, Hkv_, D_, B_, NB_, sc, ps, mcl, ws, wsb, qd, od, st, strm) = base
+    return (o, qp, _ptr(k_new), _ptr(v_new), int(k_new.stride(0)), kp, vp, ksp, vsp, bt, maxb, cl, _ptr(slot_mapping),
+            S, Hq, Hkv_, D_, B_, NB_, sc, ps, mcl, ws, wsb, qd, od, st, strm)
+
+
+def decode_step_fp8(out, q, k_new, v_new, k_pool, v_pool, k_scale, v_scale, block_tables, context_lens, slot_mapping,
+                    scale, *, partition_size=0, max_context_len, workspace=None, status=None, stream=None):
+    """pkv_decode_step_fp8: the quantising write of the new token fused into FP8 decode attention, then the reduce."""
+    _check(load().pkv_decode_step_fp8(*_step_fp8_args(out, q, k_new, v_new, k_pool, v_pool, k_scale, v_scale,
+                                                      block_tables, context_lens, slot_mapping, scale, partition_size,
+                                                      max_context_len, workspace, status, stream)),
+           "pkv_decode_step_fp8")
+
+
+def decode_step_partitions_fp8(out, q, k_new, v_new, k_pool, v_pool, k_scale, v_scale, block_tables, context_lens,
+                               slot_mapping, scale, *, partition_size=0, max_context_len, workspace=None, status=None,
+                               stream=None):
+    """pkv_decode_step_partitions_fp8: the first kernel of decode_step_fp8 alone."""
+    _check(load().pkv_decode_step_partitions_fp8(*_step_fp8_args(out, q, k_new, v_new, k_pool, v_pool, k_scale,
+                                                                 v_scale, block_tables, context_lens, slot_mapping,
+                                                                 scale, partition_size, max_context_len, workspace,
+                                                                 status, stream)),
+           "pkv_decode_step_partitions_fp8")

@@ -511,16 +511,20 @@ pkv_status pkv_copy_blocks_fp8(void* k_pool, void* v_pool, float* k_scale, float
   return launch_copy_blocks(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-pkv_status pkv_decode_partitions_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
-                                     const float* k_scale, const float* v_scale, const int32_t* block_tables,
-                                     int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
-                                     int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                                     float scale, int partition_size, int max_context_len, void* workspace,
-                                     size_t workspace_bytes, pkv_dtype q_dtype, pkv_dtype out_dtype,
-                                     int32_t* dev_status, void* stream) {
+}  // extern "C"
+
+namespace pkv {
+namespace {
+
+// Validation and descriptors shared by the FP8 decode entry points.
+pkv_status prepare_decode_fp8(DecodeCall* c, void* out, const void* q, const void* k_pool, const void* v_pool,
+                              const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                              int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads,
+                              int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                              int partition_size, int max_context_len, void* workspace, size_t workspace_bytes,
+                              pkv_dtype q_dtype, pkv_dtype out_dtype, int32_t* dev_status) {
   if (partition_size == PKV_PARTITION_BALANCED) return PKV_ERR_UNSUPPORTED;
-  DecodeCall c{};
-  pkv_status st = prepare_decode(&c, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+  pkv_status st = prepare_decode(c, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
                                  num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                                  partition_size, max_context_len, workspace, workspace_bytes, q_dtype, out_dtype,
                                  dev_status, false);
@@ -529,15 +533,85 @@ pkv_status pkv_decode_partitions_fp8(void* out, const void* q, const void* k_poo
   if (num_seqs == 0) return PKV_OK;
   if (!k_scale || !v_scale || !aligned(k_scale, 4) || !aligned(v_scale, 4) || !aligned(q, 16))
     return PKV_ERR_INVALID_ARG;
-  c.args.k_scale = k_scale;
-  c.args.v_scale = v_scale;
-  if (!encode_pool_map(&c.tmap_k, k_pool, num_blocks, num_kv_heads, head_dim, 1) ||
-      !encode_pool_map(&c.tmap_v, v_pool, num_blocks, num_kv_heads, head_dim, 1))
+  c->args.k_scale = k_scale;
+  c->args.v_scale = v_scale;
+  if (!encode_pool_map(&c->tmap_k, k_pool, num_blocks, num_kv_heads, head_dim, 1) ||
+      !encode_pool_map(&c->tmap_v, v_pool, num_blocks, num_kv_heads, head_dim, 1))
     return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status pkv_decode_partitions_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                     const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                                     int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                                     int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                     float scale, int partition_size, int max_context_len, void* workspace,
+                                     size_t workspace_bytes, pkv_dtype q_dtype, pkv_dtype out_dtype,
+                                     int32_t* dev_status, void* stream) {
+  DecodeCall c{};
+  const pkv_status st = prepare_decode_fp8(&c, out, q, k_pool, v_pool, k_scale, v_scale, block_tables,
+                                           max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                           head_dim, block_size, num_blocks, scale, partition_size, max_context_len,
+                                           workspace, workspace_bytes, q_dtype, out_dtype, dev_status);
+  if (st != PKV_OK || num_seqs == 0) return st;
   return launch_decode_partitions_fp8(c.args, c.tmap_k, c.tmap_v, head_dim, q_dtype == PKV_BF16,
                                       static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PKV_OK
              : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_decode_step_partitions_fp8(void* out, const void* q, const void* k_new, const void* v_new,
+                                          int64_t new_row_stride, void* k_pool, void* v_pool, const float* k_scale,
+                                          const float* v_scale, const int32_t* block_tables, int max_blocks_per_seq,
+                                          const int32_t* context_lens, const int32_t* slot_mapping, int num_seqs,
+                                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                          int num_blocks, float scale, int partition_size, int max_context_len,
+                                          void* workspace, size_t workspace_bytes, pkv_dtype q_dtype,
+                                          pkv_dtype out_dtype, int32_t* dev_status, void* stream) {
+  DecodeCall c{};
+  const pkv_status st = prepare_decode_fp8(&c, out, q, k_pool, v_pool, k_scale, v_scale, block_tables,
+                                           max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                           head_dim, block_size, num_blocks, scale, partition_size, max_context_len,
+                                           workspace, workspace_bytes, q_dtype, out_dtype, dev_status);
+  if (st != PKV_OK || num_seqs == 0) return st;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  const int64_t stride = new_row_stride ? new_row_stride : row;
+  if (!k_new || !v_new || !slot_mapping || new_row_stride < 0 || stride < row || stride % 8 != 0 ||
+      !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 4))
+    return PKV_ERR_INVALID_ARG;
+  DecodeArgs& a = c.args;
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.new_stride = stride;
+  a.slot_mapping = slot_mapping;
+  a.k_pool_w = static_cast<uint16_t*>(k_pool);  // written as bytes by the FP8 kernel
+  a.v_pool_w = static_cast<uint16_t*>(v_pool);
+  return launch_decode_partitions_fp8(a, c.tmap_k, c.tmap_v, head_dim, q_dtype == PKV_BF16,
+                                      static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_decode_step_fp8(void* out, const void* q, const void* k_new, const void* v_new,
+                               int64_t new_row_stride, void* k_pool, void* v_pool, const float* k_scale,
+                               const float* v_scale, const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, const int32_t* slot_mapping, int num_seqs,
+                               int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                               float scale, int partition_size, int max_context_len, void* workspace,
+                               size_t workspace_bytes, pkv_dtype q_dtype, pkv_dtype out_dtype, int32_t* dev_status,
+                               void* stream) {
+  const pkv_status st = pkv_decode_step_partitions_fp8(
+      out, q, k_new, v_new, new_row_stride, k_pool, v_pool, k_scale, v_scale, block_tables, max_blocks_per_seq,
+      context_lens, slot_mapping, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+      partition_size, max_context_len, workspace, workspace_bytes, q_dtype, out_dtype, dev_status, stream);
+  if (st != PKV_OK) return st;
+  return pkv_decode_reduce(out, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, partition_size,
+                           max_context_len, workspace, workspace_bytes, out_dtype, dev_status, stream);
 }
 
 pkv_status pkv_decode_attention_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,

@@ -13,8 +13,7 @@
 // threads move adjacent vectors of the same row (coalesced 128-byte lines on
 // both sides).  Grids are capped at a multiple of the SM count and
 // grid-stride over the work.
-#include <cuda_fp16.h>
-
+#include "pkv_fp8.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -93,19 +92,7 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(CopyBlocksArgs a) {
 
 // FP8 write path: each thread quantises 16 consecutive elements of one new
 // row (one head's slice) with the scale of the destination block and KV
-// head, e4m3(float32(x) / scale) rounded to nearest even and saturated to
-// the largest finite code, and stores the 16 codes as one vector.
-__device__ __forceinline__ float widen16(uint32_t bits, bool bf16) {
-  return bf16 ? __uint_as_float(bits << 16) : __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
-}
-
-// Two floats -> two e4m3 codes, `lo` in the low byte.
-__device__ __forceinline__ uint32_t e4m3x2_satfinite(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
+// head (fp8::quantize4) and stores the 16 codes as one vector.
 __global__ void __launch_bounds__(256) write_cache_fp8_kernel(WriteCacheFp8Args a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -131,13 +118,7 @@ __global__ void __launch_bounds__(256) write_cache_fp8_kernel(WriteCacheFp8Args 
     const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
     uint32_t c[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t e01 = e4m3x2_satfinite(__fdiv_rn(widen16(w[2 * i] & 0xffffu, bf16), sc),
-                                            __fdiv_rn(widen16(w[2 * i] >> 16, bf16), sc));
-      const uint32_t e23 = e4m3x2_satfinite(__fdiv_rn(widen16(w[2 * i + 1] & 0xffffu, bf16), sc),
-                                            __fdiv_rn(widen16(w[2 * i + 1] >> 16, bf16), sc));
-      c[i] = e01 | (e23 << 16);
-    }
+    for (int i = 0; i < 4; ++i) c[i] = fp8::quantize4(w[2 * i], w[2 * i + 1], sc, bf16);
     uint8_t* dst = (which ? a.v_pool : a.k_pool) + slot * row;
     reinterpret_cast<uint4*>(dst)[v] = make_uint4(c[0], c[1], c[2], c[3]);
   }

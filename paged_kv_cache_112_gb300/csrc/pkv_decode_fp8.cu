@@ -39,6 +39,7 @@
 //  * The accumulator is rescaled only in tiles where some head's running
 //    max grows (a warp-uniform branch).
 #include "pkv_device.cuh"
+#include "pkv_fp8.cuh"
 
 namespace pkv {
 namespace {
@@ -276,11 +277,69 @@ __device__ __forceinline__ int chunk_exponent(float vs) {
   return min(max(e, -126), 126);
 }
 
+// The token generated this step, for the warp that reads the tile holding
+// its position L-1 (fused decode step over FP8 pools).  Lanes [0, 16) hold
+// the 16-byte chunks (8 values) of the K row of KV head g, lanes [16, 32)
+// those of the V row.  The warp checks the slot against the table,
+// quantises the row with the block's scales (fp8::quantize4, as the write
+// kernel does), stores the codes to the pools and patches them into its
+// shared-memory tiles, so the attention reads the new token at once.
+template <int D>
+struct NewTokenFp8 {
+  static_assert(D == 128, "16 lanes x 8 values per row");
+  uint4 val;
+  uint2 code;
+  int row = -1;
+  int slot = -1;
+  int last_phys = -1;
+
+  __device__ __forceinline__ void prefetch(const DecodeArgs& a, int s, int g, int L, int lane) {
+    slot = a.slot_mapping[s];
+    last_phys = L > 0 ? __ldg(a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + (L - 1) / kBlockSize)
+                      : -1;
+    const uint16_t* src = (lane < 16 ? a.k_new : a.v_new) + static_cast<int64_t>(s) * a.new_stride + g * D +
+                          (lane & 15) * 8;
+    val = __ldg(reinterpret_cast<const uint4*>(src));
+    row = L > 0 ? (L - 1) % kBlockSize : -1;
+  }
+
+  // Whether the slot is position L-1 through the table; if not, flags
+  // PKV_DEV_ERR_SLOT (unless the slot is -1) and drops the token.
+  __device__ __forceinline__ bool check(const DecodeArgs& a, int lane) {
+    const bool ok = row >= 0 && slot != -1 && static_cast<unsigned>(last_phys) < static_cast<unsigned>(a.num_blocks) &&
+                    slot == last_phys * kBlockSize + row;
+    if (!ok) {
+      if (slot != -1 && lane == 0) flag(a.dev_status, 1u);
+      row = -1;
+    }
+    return ok;
+  }
+
+  // Quantises and stores this lane's 8 values (K scale for lanes < 16, V
+  // scale above) and keeps the codes for patch().
+  template <bool BF16>
+  __device__ __forceinline__ void store(const DecodeArgs& a, int g, float k_scale, float v_scale, int lane) {
+    const float sc = lane < 16 ? k_scale : v_scale;
+    code = make_uint2(fp8::quantize4(val.x, val.y, sc, BF16), fp8::quantize4(val.z, val.w, sc, BF16));
+    uint8_t* pool = reinterpret_cast<uint8_t*>(lane < 16 ? a.k_pool_w : a.v_pool_w);
+    *reinterpret_cast<uint2*>(pool + static_cast<int64_t>(slot) * a.num_kv_heads * D + g * D + (lane & 15) * 8) = code;
+  }
+
+  // Overwrites token `row` of the K and V tiles (128-byte swizzle: 8-byte
+  // half c & 1 of 16-byte chunk c / 2, chunk at position (c / 2) ^ (row & 7)).
+  __device__ __forceinline__ void patch(uint32_t k_tile, uint32_t v_tile, int lane) const {
+    const int c = lane & 15;
+    const uint32_t addr = (lane < 16 ? k_tile : v_tile) + row * 128 + ((((c >> 1) ^ (row & 7))) << 4) + ((c & 1) << 3);
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(code.x), "r"(code.y) : "memory");
+    __syncwarp();
+  }
+};
+
 // One unit (sequence s, KV head g, partition p) served by U of the CTA's NW
 // warps; `raw_len` is the sequence's context length as read and `first` the
 // warp's first table entries (first_entries<U>).  The control flow is the
 // 16-bit kernel's; the per-tile scales come with the table entries.
-template <int D, bool QBF16, int NW, int U, int NST>
+template <int D, bool QBF16, int NW, int U, int NST, bool FUSED>
 __device__ __forceinline__ void partition_unit_fp8(const DecodeArgs& a, const CUtensorMap* tmap_k,
                                                    const CUtensorMap* tmap_v, uint8_t* smem, int64_t unit,
                                                    int raw_len, int first, int warp, int lane) {
@@ -365,6 +424,15 @@ __device__ __forceinline__ void partition_unit_fp8(const DecodeArgs& a, const CU
   at.reset();
   for (int j = 0; j < min(cnt, NST); ++j) issue(j);
 
+  // Fused decode step: the last block of the last partition of (s, g) holds
+  // position L-1.
+  NewTokenFp8<D> nt;
+  const bool owns_new = FUSED && part == nparts - 1 && sub == (nblk > 0 ? (nblk - 1) % U : 0);
+  if (owns_new) {
+    nt.prefetch(a, s, g, L, lane);
+    if (nblk == 0) nt.check(a, lane);  // empty sequence: only checks the slot
+  }
+
   // Tiles are consumed two at a time (i even; both in the same chunk of
   // 32).  A missing second tile reuses the first one's buffer with no valid
   // token.
@@ -398,8 +466,13 @@ __device__ __forceinline__ void partition_unit_fp8(const DecodeArgs& a, const CU
       const int t = j * U + sub;
       nv[u] = (u == 1 && !two) || ((bad_stage >> st) & 1) ? 0 : min(kBlockSize, ntok - t * kBlockSize);
       sK[u] = ring.k_tile(j);
-      sl2k[u] = sl2q * __shfl_sync(kFull, ksel, j & 31);
-      pv[u] = inv_unit * __shfl_sync(kFull, vsel, j & 31);
+      const float ksc = __shfl_sync(kFull, ksel, j & 31), vsc = __shfl_sync(kFull, vsel, j & 31);
+      if (owns_new && (u == 0 || two) && t == nblk - 1 && nt.check(a, lane)) {
+        nt.template store<QBF16>(a, g, ksc, vsc, lane);
+        nt.patch(sK[u], sK[u] + Geom::kTileBytes, lane);
+      }
+      sl2k[u] = sl2q * ksc;
+      pv[u] = inv_unit * vsc;
     }
     at.template tiles<2>(sK, nv, sl2k, pv, lane);
     __syncwarp();
@@ -430,7 +503,7 @@ __device__ __forceinline__ void partition_unit_fp8(const DecodeArgs& a, const CU
 // Two-warp CTAs, units assigned as in the 16-bit kernel.  Six per SM (12
 // warps x 4 stages x 4 KB = 192 KB of tiles in flight); the bound lets the
 // tile's loads and conversions keep all their registers (154, no spills).
-template <int D, bool QBF16, int NST>
+template <int D, bool QBF16, int NST, bool FUSED>
 __global__ void __launch_bounds__(64, 6) decode_partitions_fp8_kernel(
     const DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
     const __grid_constant__ CUtensorMap tmap_v) {
@@ -444,11 +517,13 @@ __global__ void __launch_bounds__(64, 6) decode_partitions_fp8_kernel(
   auto seq_of = [&](int64_t u) { return static_cast<int>((u / a.num_kv_heads) % a.num_seqs); };
   if (a.unit_warps == 2) {
     if (unit2 < units)
-      partition_unit_fp8<D, QBF16, 2, 2, NST>(a, &tmap_k, &tmap_v, smem, unit2, a.context_lens[seq_of(unit2)],
-                                              first_entries<2>(a, unit2, warp, lane), warp, lane);
+      partition_unit_fp8<D, QBF16, 2, 2, NST, FUSED>(a, &tmap_k, &tmap_v, smem, unit2,
+                                                     a.context_lens[seq_of(unit2)],
+                                                     first_entries<2>(a, unit2, warp, lane), warp, lane);
   } else if (unit1 < units) {
-    partition_unit_fp8<D, QBF16, 2, 1, NST>(a, &tmap_k, &tmap_v, smem, unit1, a.context_lens[seq_of(unit1)],
-                                            first_entries<1>(a, unit1, 0, lane), warp, lane);
+    partition_unit_fp8<D, QBF16, 2, 1, NST, FUSED>(a, &tmap_k, &tmap_v, smem, unit1,
+                                                   a.context_lens[seq_of(unit1)],
+                                                   first_entries<1>(a, unit1, 0, lane), warp, lane);
   }
 }
 
@@ -477,12 +552,12 @@ int fp8_warp_slots(const void* kern, size_t smem) {
   return slots;
 }
 
-template <int D, bool QBF16>
+template <int D, bool QBF16, bool FUSED>
 cudaError_t launch_fp8_t(const DecodeArgs& a_in, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
   using Geom = TileGeom<D, 1>;
   constexpr int NST = kFp8Stages;
   const size_t smem = 2 * NST * Geom::kStageBytes + 2 * NST * 8;
-  auto kern = decode_partitions_fp8_kernel<D, QBF16, NST>;
+  auto kern = decode_partitions_fp8_kernel<D, QBF16, NST, FUSED>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   DecodeArgs a = a_in;
@@ -500,8 +575,11 @@ cudaError_t launch_fp8_t(const DecodeArgs& a_in, const CUtensorMap& tk, const CU
 cudaError_t launch_decode_partitions_fp8(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                          int head_dim, int q_bf16, cudaStream_t stream) {
   if (head_dim != 128) return cudaErrorInvalidValue;
-  return q_bf16 ? launch_fp8_t<128, true>(a, tmap_k, tmap_v, stream)
-                : launch_fp8_t<128, false>(a, tmap_k, tmap_v, stream);
+  if (a.k_new)
+    return q_bf16 ? launch_fp8_t<128, true, true>(a, tmap_k, tmap_v, stream)
+                  : launch_fp8_t<128, false, true>(a, tmap_k, tmap_v, stream);
+  return q_bf16 ? launch_fp8_t<128, true, false>(a, tmap_k, tmap_v, stream)
+                : launch_fp8_t<128, false, false>(a, tmap_k, tmap_v, stream);
 }
 
 }  // namespace pkv

@@ -129,6 +129,16 @@ class DeviceStepFp8:
         torch.cuda.synchronize()
         return self.out
 
+    def fused_step(self, out=None):
+        """copy_blocks_fp8, then the quantising write fused into attention (pkv_decode_step_fp8)."""
+        self.copy()
+        pkv.decode_step_fp8(self.out if out is None else out, self.q, self.k_new, self.v_new, self.k8, self.v8,
+                            self.k_scale, self.v_scale, self.block_tables, self.context_lens, self.slot_mapping,
+                            self.wl.scale, partition_size=self.partition_size, max_context_len=self.max_context_len,
+                            workspace=self.workspace, status=self.status)
+        torch.cuda.synchronize()
+        return self.out if out is None else out
+
     def status_bits(self) -> int:
         torch.cuda.synchronize()
         return int(self.status.item())

@@ -79,6 +79,49 @@ def test_fp8_step_matches_oracle(case, dtype):
     assert err <= ATOL, err
 
 
+@pytest.mark.parametrize("case", sorted(SMALL))
+def test_fp8_fused_step_equals_write_then_attend(case):
+    """The write fused into the partition kernel stores the same codes and
+    gives the same output, bit for bit, as the write kernel followed by
+    attention."""
+    for dtype in (["f16", "bf16"] if case == "c2_ps16" else [None]):
+        wl, pools = _small(case, dtype)
+        a, b = DeviceStepFp8(wl, pools), DeviceStepFp8(wl, pools)
+        out_a = a.step().clone()
+        out_b = b.fused_step().clone()
+        assert a.status_bits() == 0 and b.status_bits() == 0
+        assert torch.equal(out_a.view(torch.int32), out_b.view(torch.int32))
+        assert torch.equal(a.k8, b.k8) and torch.equal(a.v8, b.v8)
+        assert torch.equal(a.k_scale.view(torch.int32), b.k_scale.view(torch.int32))
+
+
+def test_fp8_fused_step_slot_checks():
+    """slot -1: no write, no flag; a slot that is not position L-1 through
+    the table: PKV_DEV_ERR_SLOT and no write; everything else as the oracle."""
+    wl, pools = _small("c2_ps64", "f16")
+    sm = wl.slot_mapping.copy()
+    s_skip, s_bad = 0, 1
+    sm[s_skip] = -1
+    sm[s_bad] = sm[s_bad] ^ 1 if wl.context_lens[s_bad] > 1 else sm[s_bad] + 1  # another slot of the pool
+    wl.slot_mapping = sm
+    ds = DeviceStepFp8(wl, pools)
+    ds.fused_step()
+    assert ds.status_bits() == pkv.DEV_ERR_SLOT
+    k8 = ds.k8.cpu().numpy()
+    for s in (s_skip, s_bad):
+        b, o = divmod(int(sm[s]) if sm[s] >= 0 else 0, 16)
+        if sm[s] >= 0:
+            assert np.array_equal(k8[b, o], pools.k8[b, o])  # untouched
+    # the other sequences' rows were written as the oracle writes them
+    keep = [s for s in range(wl.num_seqs) if s not in (s_skip, s_bad)]
+    ks = pools.k_scale.copy()
+    for s in keep:
+        b, o = divmod(int(sm[s]), 16)
+        x = P.bits_to_f32(wl.k_new[s], wl.dtype)
+        want = oracle.e4m3_encode(x / ks[b][:, None])
+        assert np.array_equal(k8[b, o], want)
+
+
 def test_fp8_write_saturates_and_rounds_like_the_oracle():
     """New rows scaled up so that many quotients pass 448: saturated codes
     and round-to-nearest-even agree with the oracle bit for bit."""
