@@ -25,6 +25,10 @@ count one byte per K/V element plus the scales.
 `--impl reference` times the fp64 CPU oracle instead (a deliberately slow
 statement of the same computation) on a bounded sample of the workload.
 
+`--layers N` times every layer of a decode step over an all-layer pool
+[2][NB][N][16][H_kv][D], the step captured once as a CUDA graph and replayed
+(eager time reported beside it).
+
 Multi-GPU (torchrun): every rank runs the same per-GPU workload (replicas,
 weak scaling); time is the max over ranks, value the sum of bytes / that time.
 """
@@ -396,6 +400,165 @@ def run_gpu(args):
     return line
 
 
+def run_layers(args):
+    """Every layer of one decode step (--layers N) over an all-layer pool
+    [2][NB][N][16][H_kv][D] ("KV Cache & PagedAttention" section 4), the
+    step captured once as a CUDA graph and replayed.  Copy-on-write moves
+    whole blocks (all layers); each layer runs the fused write + attention
+    and the reduce on its view of the pool.  Values are seeded N(0,1) drawn
+    on the device; tables, lengths and slots are the recipe's."""
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_112_gb300 as pkv
+    import pkv_inputs as P
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    pkv.load()
+    wl = P.make_workload(args.config, poison=False)
+    ps = wl.partition_size if args.partition_size is None else args.partition_size
+    dt = {"f16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
+    n_layers = args.layers
+    S, Hq, Hkv, D, NB = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.num_blocks
+    gen = torch.Generator(device=dev).manual_seed(7919 * args.config + n_layers)
+    pool = torch.empty((2, NB, n_layers, 16, Hkv, D), dtype=dt, device=dev)
+    for kv in range(2):
+        for layer in range(n_layers):
+            pool[kv, :, layer].normal_(generator=gen)
+    q = torch.randn((n_layers, S, Hq, D), generator=gen, device=dev).to(dt)
+    k_new = torch.randn((n_layers, S, Hkv, D), generator=gen, device=dev).to(dt)
+    v_new = torch.randn((n_layers, S, Hkv, D), generator=gen, device=dev).to(dt)
+    bt = torch.from_numpy(wl.block_tables).to(dev)
+    cl = torch.from_numpy(wl.context_lens).to(dev)
+    sm = torch.from_numpy(wl.slot_mapping).to(dev)
+    pairs = torch.from_numpy(np.ascontiguousarray(wl.copy_pairs, dtype=np.int32)).to(dev)
+    out = torch.empty((n_layers, S, Hq, D), dtype=torch.float32, device=dev)
+    max_len = wl.max_context_len
+    ws_bytes = pkv.decode_workspace_bytes(S, Hq, D, max_len, ps)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(evs=None):
+        if pairs.shape[0]:
+            pkv.copy_blocks(pool[0], pool[1], pairs, status=status)
+        for layer in range(n_layers):
+            kp, vp = pool[0, :, layer], pool[1, :, layer]
+            if evs is not None:
+                evs[layer][0].record()
+            pkv.decode_step_partitions(out[layer], q[layer], k_new[layer], v_new[layer], kp, vp, bt, cl, sm, wl.scale,
+                                       partition_size=ps, max_context_len=max_len, workspace=ws, status=status)
+            if evs is not None:
+                evs[layer][1].record()
+            if ws is not None:
+                pkv.decode_reduce(out[layer], cl, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, partition_size=ps,
+                                  max_context_len=max_len, workspace=ws, status=status)
+
+    K, W = args.steps, args.warmup
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def timed(fn, k):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        a.record()
+        for _ in range(k):
+            fn()
+        b.record()
+        barrier()
+        return a.elapsed_time(b)
+
+    for _ in range(W):
+        step()
+    eager_ms = timed(step, K)
+    # the partition kernels' own durations (events between launches stop PDL overlap; eager)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_layers)]
+    kern = []
+    for _ in range(min(K, 20)):
+        step(evs)
+        torch.cuda.synchronize()
+        kern += [x.elapsed_time(y) for x, y in evs]
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(W):
+        graph.replay()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    graph_ms = timed(graph.replay, K)
+    clocks = sampler.stop() if sampler else None
+    graph_ms = max_over_ranks(graph_ms, dev)
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed steps")
+
+    # end to end: every layer's queries and new rows from pinned host memory, outputs back, each step
+    h_q, h_k, h_v = q.cpu().pin_memory(), k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(h_q, non_blocking=True)
+        k_new.copy_(h_k, non_blocking=True)
+        v_new.copy_(h_v, non_blocking=True)
+        graph.replay()
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    Ke = max(1, min(K, args.e2e_steps))
+    e_ms = max_over_ranks(timed(e2e_step, Ke), dev)
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+    peak, peak_kind = _peaks()
+    nb = step_bytes(wl)
+    per_step = n_layers * nb["step"]
+    value = job_gbs(per_step, world, K, graph_ms)
+    kern_avg_ms = statistics.mean(kern)
+    achieved = nb["attention"] / (kern_avg_ms * 1e-3) / 1e9
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v))
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(graph_ms / K, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "layers": n_layers, "pool": "all-layer [2, NB, layers, 16, H_kv, D]",
+                   "graph": "one CUDA graph per step, replayed", "num_seqs": S, "num_q_heads": Hq,
+                   "num_kv_heads": Hkv, "head_dim": D, "partition_size": ps, "max_context_len": max_len,
+                   "cow_pairs": int(wl.copy_pairs.shape[0]), "entry": "pkv_copy_blocks + pkv_decode_step per layer",
+                   "l2": f"inputs larger than L2: {n_layers} layers x {2 * pool[0, :, 0].numel() * 2 / 1e6:.0f} MB",
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_hbm_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_hbm_measured": round(100 * value / world / peak, 2),
+        "seq_layers_per_s": round(world * S * n_layers / (graph_ms / K * 1e-3), 1),
+        "eager_ms_per_step": round(eager_ms / K, 5), "graph_ms_per_step": round(graph_ms / K, 5),
+        "step_bytes": per_step,
+        "roofline": {"bound": "hbm", "kernel": "decode_partitions_kernel", "achieved": round(achieved, 2),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None, "bytes_per_launch": nb["attention"], "avg_launch_ms": round(kern_avg_ms, 5)},
+        "gpu_launches": ((1 if pairs.shape[0] else 0) + n_layers * (1 + (1 if ws_bytes else 0))) * K,
+        "clocks": clocks,
+        "e2e": {"value": round(job_gbs(per_step, world, Ke, e_ms), 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(h_out.numel() * h_out.element_size()), "steps": Ke,
+                "ms_per_step": round(e_ms / Ke, 5)},
+    }
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
 def _recorded_traffic(cfg, kernel):
     """DRAM bytes per launch of the partition kernel from the committed ncu
     summary, if it was taken on the current kernel sources; else None."""
@@ -549,6 +712,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused", action="store_true",
                     help="run write_cache and decode attention as separate calls instead of pkv_decode_step")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="time every layer of a decode step (this many) over an all-layer pool, as a CUDA graph")
     ap.add_argument("--fused", action="store_true",
                     help="with --kv fp8: fuse the quantising write into the partition kernel (pkv_decode_step_fp8)")
     ap.add_argument("--kv", default="16bit", choices=["16bit", "fp8"],
@@ -561,7 +726,12 @@ def main(argv=None):
         args.warmup = 20 if args.impl == "ours" else 3
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if args.impl == "reference":
+        line = run_reference(args)
+    elif args.layers > 0:
+        line = run_layers(args)
+    else:
+        line = run_gpu(args)
     if line is not None:
         print(json.dumps(line), flush=True)
 

@@ -16,12 +16,22 @@
  *     launches its kernels only on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream).  Calls are asynchronous: a PKV_OK return means
  *     the arguments were valid and the kernels were launched.
- *   - KV pools are one K and one V tensor per layer [P1 "Sizing the pool"],
- *     laid out [num_blocks][block_size][num_kv_heads][head_dim], head_dim
- *     innermost and contiguous [P1 "The write path"], block-major as in the
- *     numpy sketch of [P4 section 4] without its layer axis.  A "slot" is
- *     one row of num_kv_heads * head_dim elements; slot = block * block_size
- *     + offset [P1 "The write path"].
+ *   - A KV pool holds blocks of [block_size][num_kv_heads][head_dim]
+ *     elements, head_dim innermost and contiguous [P1 "The write path"].  A
+ *     "slot" is one row of num_kv_heads * head_dim elements; slot = block *
+ *     block_size + offset [P1 "The write path"].  Consecutive blocks are
+ *     block_stride elements apart:
+ *       - block_stride = 0 (dense, block_size * num_kv_heads * head_dim):
+ *         one K and one V tensor per layer [P1 "Sizing the pool"],
+ *         [num_blocks][block_size][num_kv_heads][head_dim];
+ *       - block_stride = num_layers * block_size * num_kv_heads * head_dim:
+ *         one layer's view of a pool that keeps all layers of a block
+ *         together, [num_blocks][num_layers][block_size][num_kv_heads]
+ *         [head_dim] per K and per V as in the numpy sketch of [P4 section
+ *         4]; the layer-l pool pointer is base + l * block_size *
+ *         num_kv_heads * head_dim.
+ *     Any other block_stride >= the dense one and a multiple of 8 elements
+ *     works too.  Pool pointers are 16-byte aligned.
  *   - block_size must be 16 [P1 "Fixed-size blocks"; P2 section 02].
  *   - Elements are IEEE binary16 (PKV_F16) or bfloat16 (PKV_BF16).  Queries
  *     have the pools' type.
@@ -71,12 +81,15 @@ typedef enum pkv_dtype { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 } pkv_dtype;
  *                  are new_row_stride elements apart (0 = dense, i.e.
  *                  num_kv_heads*head_dim), so rows of a fused QKV projection
  *                  can be passed directly.  Rows must be 16-byte aligned.
- *   k_pool, v_pool : pools as above, 16-byte aligned.
+ *   k_pool, v_pool, block_stride : pools as above (one layer).
  *   slot_mapping : int32[num_tokens].
  * num_tokens == 0 is a no-op.  Out-of-range slots set PKV_DEV_ERR_SLOT.
+ * num_tokens may be a whole prompt (the bulk write of prefill, [P3
+ * "End-to-end flow"]: a 300-token prompt fills 19 blocks).
  */
 pkv_status pkv_write_cache(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
-                           const int32_t* slot_mapping, int num_tokens, int64_t new_row_stride,
+                           int64_t block_stride, const int32_t* slot_mapping, int num_tokens,
+                           int64_t new_row_stride,
                            int num_kv_heads, int head_dim, int block_size, int num_blocks,
                            pkv_dtype kv_dtype, int32_t* dev_status, void* stream);
 
@@ -84,7 +97,10 @@ pkv_status pkv_write_cache(const void* k_new, const void* v_new, void* k_pool, v
  * pkv_copy_blocks -- the copy-on-write block copy [P1 "Prefix sharing,
  * reference counts, and copy-on-write"; P2 section 03; P3 "The
  * architecture"]: for each pair i, block pairs[2i+1] := block pairs[2i] in
- * both pools, bitwise, device to device.
+ * both pools, bitwise, device to device.  A block is num_layers consecutive
+ * [block_size][num_kv_heads][head_dim] slices: 1 for per-layer pools; the
+ * layer count for the all-layer layout, whose copy-on-write moves every
+ * layer of the block at once (k_pool, v_pool: the K and V bases).
  *   pairs : int32[num_pairs][2] = (src, dst).  dsts must be distinct and no
  *           dst may also be a src in the same call (a copy-on-write target is
  *           always a freshly allocated block).
@@ -92,8 +108,8 @@ pkv_status pkv_write_cache(const void* k_new, const void* v_new, void* k_pool, v
  * skipped.
  */
 pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int num_pairs,
-                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                           pkv_dtype kv_dtype, int32_t* dev_status, void* stream);
+                           int num_layers, int num_kv_heads, int head_dim, int block_size,
+                           int num_blocks, pkv_dtype kv_dtype, int32_t* dev_status, void* stream);
 
 /* partition_size value selecting the balanced split (see pkv_decode_attention). */
 #define PKV_PARTITION_BALANCED (-1)
@@ -123,9 +139,10 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, i
  * restructuring of [P1 "Inside the paged attention kernel"]).
  *   out          : [num_seqs][num_q_heads][head_dim], out_dtype F32/F16/BF16.
  *   q            : [num_seqs][num_q_heads][head_dim], kv_dtype, 4-byte aligned.
- *   k_pool, v_pool : pools as above (16-byte aligned).
+ *   k_pool, v_pool, block_stride : pools as above (one layer).
  *   block_tables : int32[num_seqs][max_blocks_per_seq], row-major; entries at
- *                  and past ceil(L/16) are never read.
+ *                  and past ceil(L/16) are not used (those within the row
+ *                  may be read).
  *   context_lens : int32[num_seqs].
  *   scale        : softmax scale (typically 1/sqrt(head_dim)).
  *   partition_size : tokens per split-K partition, a multiple of 16; 0 for
@@ -148,7 +165,7 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, i
  * pkv_decode_reduce below expose them separately.
  */
 pkv_status pkv_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
-                                const int32_t* block_tables, int max_blocks_per_seq,
+                                int64_t block_stride, const int32_t* block_tables, int max_blocks_per_seq,
                                 const int32_t* context_lens, int num_seqs, int num_q_heads,
                                 int num_kv_heads, int head_dim, int block_size, int num_blocks,
                                 float scale, int partition_size, int max_context_len,
@@ -163,7 +180,7 @@ pkv_status pkv_decode_attention(void* out, const void* q, const void* k_pool, co
  * pkv_decode_reduce.
  */
 pkv_status pkv_decode_partitions(void* out, const void* q, const void* k_pool, const void* v_pool,
-                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 int64_t block_stride, const int32_t* block_tables, int max_blocks_per_seq,
                                  const int32_t* context_lens, int num_seqs, int num_q_heads,
                                  int num_kv_heads, int head_dim, int block_size, int num_blocks,
                                  float scale, int partition_size, int max_context_len,
@@ -200,13 +217,13 @@ pkv_status pkv_decode_reduce(void* out, const int32_t* context_lens, int num_seq
  *   k_new, v_new : [num_seqs][num_kv_heads][head_dim], consecutive sequences
  *                  new_row_stride elements apart (0 = dense), rows 16-byte
  *                  aligned.
- *   k_pool, v_pool : pools (read and written).
+ *   k_pool, v_pool, block_stride : pools (read and written).
  *   other arguments as in pkv_decode_attention.
  * pkv_decode_step_partitions is its first kernel alone (follow it with
  * pkv_decode_reduce, as for pkv_decode_partitions).
  */
 pkv_status pkv_decode_step(void* out, const void* q, const void* k_new, const void* v_new,
-                           int64_t new_row_stride, void* k_pool, void* v_pool,
+                           int64_t new_row_stride, void* k_pool, void* v_pool, int64_t block_stride,
                            const int32_t* block_tables, int max_blocks_per_seq,
                            const int32_t* context_lens, const int32_t* slot_mapping, int num_seqs,
                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
@@ -215,7 +232,7 @@ pkv_status pkv_decode_step(void* out, const void* q, const void* k_new, const vo
                            pkv_dtype out_dtype, int32_t* dev_status, void* stream);
 
 pkv_status pkv_decode_step_partitions(void* out, const void* q, const void* k_new, const void* v_new,
-                                      int64_t new_row_stride, void* k_pool, void* v_pool,
+                                      int64_t new_row_stride, void* k_pool, void* v_pool, int64_t block_stride,
                                       const int32_t* block_tables, int max_blocks_per_seq,
                                       const int32_t* context_lens, const int32_t* slot_mapping,
                                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -246,8 +263,8 @@ pkv_status pkv_decode_step_partitions(void* out, const void* q, const void* k_ne
  */
 #define PKV_STATIC_WORKSPACE_BYTES (16u << 20)
 pkv_status pkv_decode_attention_static_workspace(
-    void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
-    int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+    void* out, const void* q, const void* k_pool, const void* v_pool, int64_t block_stride,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
     int head_dim, int block_size, int num_blocks, float scale, int partition_size, int max_context_len,
     pkv_dtype kv_dtype, pkv_dtype out_dtype, int32_t* dev_status, void* stream);
 
@@ -256,8 +273,8 @@ pkv_status pkv_decode_attention_static_workspace(
  *
  * Pools of 8-bit e4m3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa
  * bits; largest finite magnitude 448; codes 0x7F/0xFF are NaN; no infinity)
- * in the same [num_blocks][block_size][num_kv_heads][head_dim] layout, one
- * byte per element, halving the bytes decode reads ([P4 section 5]: K, V
+ * in the dense per-layer [num_blocks][block_size][num_kv_heads][head_dim]
+ * layout, one byte per element, halving the bytes decode reads ([P4 section 5]: K, V
  * stored in FP8).  The 16-token block is the quantisation group and its
  * scales ride with it, through copy-on-write included [P2 section 06,
  * "Blocks as quantization groups"]:

@@ -26,22 +26,20 @@ _KV_DTYPES = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
 _c_void_p, _c_int, _c_int64, _c_size_t, _c_float = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
                                                     ctypes.c_size_t, ctypes.c_float)
 _SIGS = {
-    "pkv_write_cache": [_c_void_p] * 5 + [_c_int, _c_int64] + [_c_int] * 5 + [_c_void_p, _c_void_p],
-    "pkv_copy_blocks": [_c_void_p] * 3 + [_c_int] * 6 + [_c_void_p, _c_void_p],
+    "pkv_write_cache": [_c_void_p] * 4 + [_c_int64, _c_void_p, _c_int, _c_int64] + [_c_int] * 5 + [_c_void_p] * 2,
+    "pkv_copy_blocks": [_c_void_p] * 3 + [_c_int] * 7 + [_c_void_p, _c_void_p],
     "pkv_decode_workspace_bytes": [_c_int] * 5,
-    "pkv_decode_attention": [_c_void_p] * 5 + [_c_int, _c_void_p] + [_c_int] * 6 + [_c_float, _c_int, _c_int,
-                                                                                      _c_void_p, _c_size_t,
-                                                                                      _c_int, _c_int, _c_void_p,
-                                                                                      _c_void_p],
+    "pkv_decode_attention": [_c_void_p] * 4 + [_c_int64, _c_void_p, _c_int, _c_void_p] + [_c_int] * 6 + [
+        _c_float, _c_int, _c_int, _c_void_p, _c_size_t, _c_int, _c_int, _c_void_p, _c_void_p],
     "pkv_decode_reduce": [_c_void_p, _c_void_p] + [_c_int] * 6 + [_c_void_p, _c_size_t, _c_int, _c_void_p,
                                                                   _c_void_p],
     "pkv_status_string": [_c_int],
     "pkv_version": [],
 }
 _SIGS["pkv_decode_partitions"] = _SIGS["pkv_decode_attention"]
-_SIGS["pkv_decode_step"] = ([_c_void_p] * 4 + [_c_int64] + [_c_void_p] * 3 + [_c_int] + [_c_void_p] * 2 +
-                            [_c_int] * 6 + [_c_float, _c_int, _c_int, _c_void_p, _c_size_t, _c_int, _c_int,
-                                            _c_void_p, _c_void_p])
+_SIGS["pkv_decode_step"] = ([_c_void_p] * 4 + [_c_int64] + [_c_void_p] * 2 + [_c_int64, _c_void_p, _c_int] +
+                            [_c_void_p] * 2 + [_c_int] * 6 + [_c_float, _c_int, _c_int, _c_void_p, _c_size_t, _c_int,
+                                                              _c_int, _c_void_p, _c_void_p])
 _SIGS["pkv_decode_step_partitions"] = _SIGS["pkv_decode_step"]
 _SIGS["pkv_write_cache_fp8"] = [_c_void_p] * 7 + [_c_int, _c_int64] + [_c_int] * 5 + [_c_void_p, _c_void_p]
 _SIGS["pkv_copy_blocks_fp8"] = [_c_void_p] * 5 + [_c_int] * 5 + [_c_void_p, _c_void_p]
@@ -110,6 +108,21 @@ def _need_cuda(*ts):
             raise PkvError("tensors must be contiguous CUDA tensors")
 
 
+def _pool_stride(k_pool, v_pool) -> int:
+    """Block stride (elements) of a pool given as [NB, 16, H_kv, D] with dense
+    blocks: a per-layer tensor, or one layer's view of an all-layer pool
+    (e.g. pool[0, :, layer] of a [2, NB, layers, 16, H_kv, D] tensor)."""
+    for t in (k_pool, v_pool):
+        if not t.is_cuda or t.dim() != 4:
+            raise PkvError("pools must be CUDA tensors [NB, 16, H_kv, D]")
+        NB, B, Hkv, D = t.shape
+        if t.stride(3) != 1 or t.stride(2) != D or t.stride(1) != Hkv * D or t.stride(0) < B * Hkv * D:
+            raise PkvError("pool blocks must be dense [16, H_kv, D] slices")
+    if k_pool.stride(0) != v_pool.stride(0) or k_pool.shape != v_pool.shape:
+        raise PkvError("k_pool and v_pool must share shape and block stride")
+    return int(k_pool.stride(0))
+
+
 def _kv_dtype(t) -> int:
     if t.dtype not in _KV_DTYPES:
         raise PkvError(f"KV dtype must be float16 or bfloat16, got {t.dtype}")
@@ -117,8 +130,10 @@ def _kv_dtype(t) -> int:
 
 
 def write_cache(k_new, v_new, k_pool, v_pool, slot_mapping, *, status=None, stream=None):
-    """pkv_write_cache: k_new/v_new [T, H_kv, D] (rows may be strided), pools [NB, 16, H_kv, D]."""
-    _need_cuda(k_pool, v_pool, slot_mapping, status)
+    """pkv_write_cache: k_new/v_new [T, H_kv, D] (rows may be strided), pools [NB, 16, H_kv, D]
+    (per-layer tensors or layer views of an all-layer pool)."""
+    bstride = _pool_stride(k_pool, v_pool)
+    _need_cuda(slot_mapping, status)
     NB, B, Hkv, D = k_pool.shape
     T = k_new.shape[0]
     for t in (k_new, v_new):
@@ -126,17 +141,22 @@ def write_cache(k_new, v_new, k_pool, v_pool, slot_mapping, *, status=None, stre
             raise PkvError("k_new/v_new must be CUDA [T, H_kv, D] with dense rows")
     if k_new.stride(0) != v_new.stride(0):
         raise PkvError("k_new and v_new must share a row stride")
-    _check(load().pkv_write_cache(_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(slot_mapping), T,
-                                  int(k_new.stride(0)), Hkv, D, B, NB, _kv_dtype(k_pool), _ptr(status),
+    _check(load().pkv_write_cache(_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), bstride, _ptr(slot_mapping),
+                                  T, int(k_new.stride(0)), Hkv, D, B, NB, _kv_dtype(k_pool), _ptr(status),
                                   _stream(stream)), "pkv_write_cache")
 
 
 def copy_blocks(k_pool, v_pool, pairs, *, status=None, stream=None):
-    """pkv_copy_blocks: pairs int32 [P, 2] (src, dst)."""
+    """pkv_copy_blocks: pairs int32 [P, 2] (src, dst).  Pools are contiguous per-layer
+    [NB, 16, H_kv, D] tensors, or the K and V halves [NB, layers, 16, H_kv, D] of an
+    all-layer pool, whose blocks are copied with every layer."""
     _need_cuda(k_pool, v_pool, pairs, status)
-    NB, B, Hkv, D = k_pool.shape
-    _check(load().pkv_copy_blocks(_ptr(k_pool), _ptr(v_pool), _ptr(pairs), int(pairs.shape[0]), Hkv, D, B, NB,
-                                  _kv_dtype(k_pool), _ptr(status), _stream(stream)), "pkv_copy_blocks")
+    if k_pool.shape != v_pool.shape or k_pool.dim() not in (4, 5):
+        raise PkvError("pools must be [NB, 16, H_kv, D] or [NB, layers, 16, H_kv, D], K and V alike")
+    layers = 1 if k_pool.dim() == 4 else int(k_pool.shape[1])
+    NB, B, Hkv, D = k_pool.shape[0], k_pool.shape[-3], k_pool.shape[-2], k_pool.shape[-1]
+    _check(load().pkv_copy_blocks(_ptr(k_pool), _ptr(v_pool), _ptr(pairs), int(pairs.shape[0]), layers, Hkv, D, B,
+                                  NB, _kv_dtype(k_pool), _ptr(status), _stream(stream)), "pkv_copy_blocks")
 
 
 def decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len, partition_size) -> int:
@@ -145,7 +165,8 @@ def decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len, par
 
 def _decode_args(out, q, k_pool, v_pool, block_tables, context_lens, scale, partition_size, max_context_len,
                  workspace, status, stream):
-    _need_cuda(out, q, k_pool, v_pool, block_tables, context_lens, workspace, status)
+    bstride = _pool_stride(k_pool, v_pool)
+    _need_cuda(out, q, block_tables, context_lens, workspace, status)
     S, Hq, D = q.shape
     NB, B, Hkv, D2 = k_pool.shape
     if D2 != D or v_pool.shape != k_pool.shape or q.dtype != k_pool.dtype or v_pool.dtype != k_pool.dtype:
@@ -155,7 +176,7 @@ def _decode_args(out, q, k_pool, v_pool, block_tables, context_lens, scale, part
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise PkvError("block_tables and context_lens must be int32")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    return (_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), int(block_tables.shape[1]),
+    return (_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), bstride, _ptr(block_tables), int(block_tables.shape[1]),
             _ptr(context_lens), S, Hq, Hkv, D, B, NB, float(scale), int(partition_size), int(max_context_len),
             _ptr(workspace), ws_bytes, _kv_dtype(k_pool), _DTYPES[out.dtype], _ptr(status), _stream(stream))
 
@@ -200,9 +221,9 @@ def _step_args(out, q, k_new, v_new, k_pool, v_pool, block_tables, context_lens,
         raise PkvError("k_new and v_new must share a row stride and the pools' dtype")
     if slot_mapping.dtype != torch.int32 or slot_mapping.shape != (q.shape[0],):
         raise PkvError("slot_mapping must be int32 [S]")
-    (o, qp, kp, vp, bt, maxb, cl, S, Hq, Hkv_, D_, B_, NB_, sc, ps, mcl, ws, wsb, kvd, od, st, strm) = base
-    return (o, qp, _ptr(k_new), _ptr(v_new), int(k_new.stride(0)), kp, vp, bt, maxb, cl, _ptr(slot_mapping), S, Hq,
-            Hkv_, D_, B_, NB_, sc, ps, mcl, ws, wsb, kvd, od, st, strm)
+    (o, qp, kp, vp, bs, bt, maxb, cl, S, Hq, Hkv_, D_, B_, NB_, sc, ps, mcl, ws, wsb, kvd, od, st, strm) = base
+    return (o, qp, _ptr(k_new), _ptr(v_new), int(k_new.stride(0)), kp, vp, bs, bt, maxb, cl, _ptr(slot_mapping), S,
+            Hq, Hkv_, D_, B_, NB_, sc, ps, mcl, ws, wsb, kvd, od, st, strm)
 
 
 def decode_step(out, q, k_new, v_new, k_pool, v_pool, block_tables, context_lens, slot_mapping, scale, *,

@@ -102,22 +102,25 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Describes a pool of `eb`-byte elements as [num_blocks * 16 rows]
-// [num_kv_heads * head_dim * eb / 128 lines][128 bytes] so that one box is
-// the 16 token rows of one 128-byte line of one head: a (block, head) tile
-// is head_dim * eb / 128 boxes (16-bit: 2 at head_dim 128, 1 at 64; FP8: 1
-// at head_dim 128).
+// Describes a pool of `eb`-byte elements, blocks `block_stride` elements
+// apart, as [num_blocks][16 rows][num_kv_heads * head_dim * eb / 128 lines]
+// [128 bytes], so that one box {128 bytes, 1, 16, 1} is the 16 token rows
+// of one 128-byte line of one head of one block: a (block, head) tile is
+// head_dim * eb / 128 boxes (16-bit: 2 at head_dim 128, 1 at 64; FP8: 1 at
+// head_dim 128).  A block stride above 16 rows is a layer slice of a pool
+// that keeps all layers of a block together.
 bool encode_pool_map_uncached(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, int head_dim,
-                              int eb) {
+                              int eb, int64_t block_stride) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint32_t line = 128 / eb;  // elements per 128-byte line
-  const cuuint64_t dims[3] = {line, static_cast<cuuint64_t>(num_kv_heads) * (head_dim / line),
-                              static_cast<cuuint64_t>(num_blocks) * kBlockSize};
-  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(num_kv_heads) * head_dim * eb};
-  const cuuint32_t box[3] = {line, 1, kBlockSize};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = fn(map, eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
+  const cuuint64_t dims[4] = {line, static_cast<cuuint64_t>(num_kv_heads) * (head_dim / line), kBlockSize,
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(num_kv_heads) * head_dim * eb,
+                                 static_cast<cuuint64_t>(block_stride) * eb};
+  const cuuint32_t box[4] = {line, 1, kBlockSize, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
                         const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B,
                         head_dim * eb >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -127,30 +130,41 @@ bool encode_pool_map_uncached(CUtensorMap* map, const void* pool, int num_blocks
 
 // Descriptors depend only on the pool address and geometry, so recent ones
 // are kept (a small round-robin cache) instead of re-encoded every call.
-bool encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, int head_dim,
-                     int eb = 2) {
+bool encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, int head_dim, int eb,
+                     int64_t block_stride) {
   struct Entry {
     const void* pool;
     int num_blocks, num_kv_heads, head_dim, eb;
+    int64_t block_stride;
     CUtensorMap map;
   };
-  static Entry cache[32];
+  static Entry cache[64];
   static int next = 0;
   static std::mutex mu;
   {
     std::lock_guard<std::mutex> lock(mu);
     for (const Entry& e : cache)
       if (e.pool == pool && e.num_blocks == num_blocks && e.num_kv_heads == num_kv_heads &&
-          e.head_dim == head_dim && e.eb == eb) {
+          e.head_dim == head_dim && e.eb == eb && e.block_stride == block_stride) {
         *map = e.map;
         return true;
       }
   }
-  if (!encode_pool_map_uncached(map, pool, num_blocks, num_kv_heads, head_dim, eb)) return false;
+  if (!encode_pool_map_uncached(map, pool, num_blocks, num_kv_heads, head_dim, eb, block_stride)) return false;
   std::lock_guard<std::mutex> lock(mu);
-  cache[next] = Entry{pool, num_blocks, num_kv_heads, head_dim, eb, *map};
-  next = (next + 1) % 32;
+  cache[next] = Entry{pool, num_blocks, num_kv_heads, head_dim, eb, block_stride, *map};
+  next = (next + 1) % 64;
   return true;
+}
+
+// Block stride of a pool: 0 means dense (block_size * num_kv_heads *
+// head_dim); otherwise at least that and a multiple of 8 elements (16 bytes
+// at 16 bits).  Returns -1 when invalid.
+int64_t resolve_block_stride(int64_t block_stride, int num_kv_heads, int head_dim) {
+  const int64_t dense = static_cast<int64_t>(kBlockSize) * num_kv_heads * head_dim;
+  if (block_stride == 0) return dense;
+  if (block_stride < dense || block_stride % 8 != 0) return -1;
+  return block_stride;
 }
 
 int parts_for(int max_context_len, int partition_size, int* ps_out) {
@@ -183,7 +197,8 @@ struct DecodeCall {
 };
 
 pkv_status prepare_decode(DecodeCall* c, void* out, const void* q, const void* k_pool, const void* v_pool,
-                          const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                          int64_t block_stride, const int32_t* block_tables, int max_blocks_per_seq,
+                          const int32_t* context_lens,
                           int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                           int num_blocks, float scale, int partition_size, int max_context_len, void* workspace,
                           size_t workspace_bytes, pkv_dtype kv_dtype, pkv_dtype out_dtype, int32_t* dev_status,
@@ -206,6 +221,8 @@ pkv_status prepare_decode(DecodeCall* c, void* out, const void* q, const void* k
   if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(q, 4) ||
       !aligned(out, out_dtype == PKV_F32 ? 4 : 2) || !aligned(block_tables, 4) || !aligned(context_lens, 4))
     return PKV_ERR_INVALID_ARG;
+  const int64_t bstride = resolve_block_stride(block_stride, num_kv_heads, head_dim);
+  if (bstride < 0) return PKV_ERR_INVALID_ARG;
   const int sms = balanced ? current_sm_count(0) : 0;
   if (balanced && sms <= 0) return PKV_ERR_CUDA;
   int max_parts = 1, ps = 0;
@@ -236,12 +253,13 @@ pkv_status prepare_decode(DecodeCall* c, void* out, const void* q, const void* k
   a.partition_size = ps;
   a.max_parts = max_parts;
   a.max_context_len = max_context_len;
+  a.block_stride = bstride;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out_dtype = static_cast<int>(out_dtype);
   a.timeout_ns = kWaitTimeoutNs;
   if (need_maps && num_seqs > 0) {
-    if (!encode_pool_map(&c->tmap_k, k_pool, num_blocks, num_kv_heads, head_dim) ||
-        !encode_pool_map(&c->tmap_v, v_pool, num_blocks, num_kv_heads, head_dim))
+    if (!encode_pool_map(&c->tmap_k, k_pool, num_blocks, num_kv_heads, head_dim, 2, bstride) ||
+        !encode_pool_map(&c->tmap_v, v_pool, num_blocks, num_kv_heads, head_dim, 2, bstride))
       return PKV_ERR_CUDA;
   }
   return PKV_OK;
@@ -254,7 +272,7 @@ using namespace pkv;
 
 extern "C" {
 
-pkv_status pkv_write_cache(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+pkv_status pkv_write_cache(const void* k_new, const void* v_new, void* k_pool, void* v_pool, int64_t block_stride,
                            const int32_t* slot_mapping, int num_tokens, int64_t new_row_stride, int num_kv_heads,
                            int head_dim, int block_size, int num_blocks, pkv_dtype kv_dtype, int32_t* dev_status,
                            void* stream) {
@@ -264,6 +282,8 @@ pkv_status pkv_write_cache(const void* k_new, const void* v_new, void* k_pool, v
   if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
   const int row = num_kv_heads * head_dim;
   if (row % 8 != 0) return PKV_ERR_UNSUPPORTED;  // 16-byte vectors
+  const int64_t bstride = resolve_block_stride(block_stride, num_kv_heads, head_dim);
+  if (bstride < 0) return PKV_ERR_INVALID_ARG;
   if (num_tokens == 0) return PKV_OK;
   if (!k_new || !v_new || !k_pool || !v_pool || !slot_mapping) return PKV_ERR_INVALID_ARG;
   const int64_t stride = new_row_stride ? new_row_stride : row;
@@ -281,15 +301,17 @@ pkv_status pkv_write_cache(const void* k_new, const void* v_new, void* k_pool, v
   a.k_stride = stride;
   a.v_stride = stride;
   a.num_slots = static_cast<int64_t>(num_blocks) * kBlockSize;
+  a.block_stride = bstride;
   a.num_tokens = num_tokens;
   a.row_elems = row;
   return launch_write_cache(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int num_pairs, int num_kv_heads,
-                           int head_dim, int block_size, int num_blocks, pkv_dtype kv_dtype, int32_t* dev_status,
-                           void* stream) {
-  if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int num_pairs, int num_layers,
+                           int num_kv_heads, int head_dim, int block_size, int num_blocks, pkv_dtype kv_dtype,
+                           int32_t* dev_status, void* stream) {
+  if (num_pairs < 0 || num_layers <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0)
+    return PKV_ERR_INVALID_ARG;
   if (!kv_dtype_ok(kv_dtype)) return PKV_ERR_INVALID_ARG;
   if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
   if ((num_kv_heads * head_dim) % 8 != 0) return PKV_ERR_UNSUPPORTED;
@@ -301,7 +323,7 @@ pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int
   a.v_pool = static_cast<uint16_t*>(v_pool);
   a.pairs = pairs;
   a.dev_status = dev_status;
-  a.block_elems = static_cast<int64_t>(kBlockSize) * num_kv_heads * head_dim;
+  a.block_elems = static_cast<int64_t>(num_layers) * kBlockSize * num_kv_heads * head_dim;
   a.num_pairs = num_pairs;
   a.num_blocks = num_blocks;
   return launch_copy_blocks(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
@@ -320,13 +342,15 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, i
 }
 
 pkv_status pkv_decode_partitions(void* out, const void* q, const void* k_pool, const void* v_pool,
-                                 const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                                 int64_t block_stride, const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* context_lens,
                                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                  int num_blocks, float scale, int partition_size, int max_context_len,
                                  void* workspace, size_t workspace_bytes, pkv_dtype kv_dtype, pkv_dtype out_dtype,
                                  int32_t* dev_status, void* stream) {
   DecodeCall c{};
-  pkv_status st = prepare_decode(&c, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+  pkv_status st = prepare_decode(&c, out, q, k_pool, v_pool, block_stride, block_tables, max_blocks_per_seq,
+                                 context_lens,
                                  num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                                  partition_size, max_context_len, workspace, workspace_bytes, kv_dtype, out_dtype,
                                  dev_status, true);
@@ -385,7 +409,7 @@ pkv_status pkv_decode_reduce(void* out, const int32_t* context_lens, int num_seq
 }
 
 pkv_status pkv_decode_step_partitions(void* out, const void* q, const void* k_new, const void* v_new,
-                                      int64_t new_row_stride, void* k_pool, void* v_pool,
+                                      int64_t new_row_stride, void* k_pool, void* v_pool, int64_t block_stride,
                                       const int32_t* block_tables, int max_blocks_per_seq,
                                       const int32_t* context_lens, const int32_t* slot_mapping, int num_seqs,
                                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
@@ -393,7 +417,8 @@ pkv_status pkv_decode_step_partitions(void* out, const void* q, const void* k_ne
                                       void* workspace, size_t workspace_bytes, pkv_dtype kv_dtype,
                                       pkv_dtype out_dtype, int32_t* dev_status, void* stream) {
   DecodeCall c{};
-  pkv_status st = prepare_decode(&c, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+  pkv_status st = prepare_decode(&c, out, q, k_pool, v_pool, block_stride, block_tables, max_blocks_per_seq,
+                                 context_lens,
                                  num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                                  partition_size, max_context_len, workspace, workspace_bytes, kv_dtype, out_dtype,
                                  dev_status, true);
@@ -419,12 +444,14 @@ pkv_status pkv_decode_step_partitions(void* out, const void* q, const void* k_ne
 }
 
 pkv_status pkv_decode_step(void* out, const void* q, const void* k_new, const void* v_new, int64_t new_row_stride,
-                           void* k_pool, void* v_pool, const int32_t* block_tables, int max_blocks_per_seq,
+                           void* k_pool, void* v_pool, int64_t block_stride, const int32_t* block_tables,
+                           int max_blocks_per_seq,
                            const int32_t* context_lens, const int32_t* slot_mapping, int num_seqs, int num_q_heads,
                            int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
                            int partition_size, int max_context_len, void* workspace, size_t workspace_bytes,
                            pkv_dtype kv_dtype, pkv_dtype out_dtype, int32_t* dev_status, void* stream) {
-  pkv_status st = pkv_decode_step_partitions(out, q, k_new, v_new, new_row_stride, k_pool, v_pool, block_tables,
+  pkv_status st = pkv_decode_step_partitions(out, q, k_new, v_new, new_row_stride, k_pool, v_pool, block_stride,
+                                             block_tables,
                                              max_blocks_per_seq, context_lens, slot_mapping, num_seqs, num_q_heads,
                                              num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size,
                                              max_context_len, workspace, workspace_bytes, kv_dtype, out_dtype,
@@ -435,12 +462,14 @@ pkv_status pkv_decode_step(void* out, const void* q, const void* k_new, const vo
 }
 
 pkv_status pkv_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
-                                const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                                int64_t block_stride, const int32_t* block_tables, int max_blocks_per_seq,
+                                const int32_t* context_lens,
                                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                 int num_blocks, float scale, int partition_size, int max_context_len, void* workspace,
                                 size_t workspace_bytes, pkv_dtype kv_dtype, pkv_dtype out_dtype, int32_t* dev_status,
                                 void* stream) {
-  pkv_status st = pkv_decode_partitions(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+  pkv_status st = pkv_decode_partitions(out, q, k_pool, v_pool, block_stride, block_tables, max_blocks_per_seq,
+                                        context_lens,
                                         num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                                         partition_size, max_context_len, workspace, workspace_bytes, kv_dtype,
                                         out_dtype, dev_status, stream);
@@ -524,7 +553,7 @@ pkv_status prepare_decode_fp8(DecodeCall* c, void* out, const void* q, const voi
                               int partition_size, int max_context_len, void* workspace, size_t workspace_bytes,
                               pkv_dtype q_dtype, pkv_dtype out_dtype, int32_t* dev_status) {
   if (partition_size == PKV_PARTITION_BALANCED) return PKV_ERR_UNSUPPORTED;
-  pkv_status st = prepare_decode(c, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+  pkv_status st = prepare_decode(c, out, q, k_pool, v_pool, 0, block_tables, max_blocks_per_seq, context_lens,
                                  num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                                  partition_size, max_context_len, workspace, workspace_bytes, q_dtype, out_dtype,
                                  dev_status, false);
@@ -535,8 +564,9 @@ pkv_status prepare_decode_fp8(DecodeCall* c, void* out, const void* q, const voi
     return PKV_ERR_INVALID_ARG;
   c->args.k_scale = k_scale;
   c->args.v_scale = v_scale;
-  if (!encode_pool_map(&c->tmap_k, k_pool, num_blocks, num_kv_heads, head_dim, 1) ||
-      !encode_pool_map(&c->tmap_v, v_pool, num_blocks, num_kv_heads, head_dim, 1))
+  // FP8 pools are dense (one layer): the same block stride, in bytes.
+  if (!encode_pool_map(&c->tmap_k, k_pool, num_blocks, num_kv_heads, head_dim, 1, c->args.block_stride) ||
+      !encode_pool_map(&c->tmap_v, v_pool, num_blocks, num_kv_heads, head_dim, 1, c->args.block_stride))
     return PKV_ERR_CUDA;
   return PKV_OK;
 }

@@ -322,7 +322,8 @@ struct NewTokenFp8 {
     const float sc = lane < 16 ? k_scale : v_scale;
     code = make_uint2(fp8::quantize4(val.x, val.y, sc, BF16), fp8::quantize4(val.z, val.w, sc, BF16));
     uint8_t* pool = reinterpret_cast<uint8_t*>(lane < 16 ? a.k_pool_w : a.v_pool_w);
-    *reinterpret_cast<uint2*>(pool + static_cast<int64_t>(slot) * a.num_kv_heads * D + g * D + (lane & 15) * 8) = code;
+    *reinterpret_cast<uint2*>(pool + (slot / kBlockSize) * a.block_stride +
+                              static_cast<int64_t>(row) * a.num_kv_heads * D + g * D + (lane & 15) * 8) = code;
   }
 
   // Overwrites token `row` of the K and V tiles (128-byte swizzle: 8-byte

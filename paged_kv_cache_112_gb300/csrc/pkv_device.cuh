@@ -61,12 +61,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
                                             uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
       : "memory");
 }
 
@@ -218,7 +218,8 @@ struct WarpRing {
   }
 
   // Lane 0 issues the K and V copies of tile number j (stage j % NST) for
-  // physical block `phys`, KV head g.
+  // physical block `phys`, KV head g (tensor maps: {element line, head
+  // line, row in block, block}).
   __device__ __forceinline__ void issue(int j, int phys, int g, const CUtensorMap* tk, const CUtensorMap* tv,
                                         int lane) const {
     if (lane != 0) return;
@@ -228,8 +229,8 @@ struct WarpRing {
     mbar_arrive_expect_tx(b, Geom::kStageBytes);
 #pragma unroll
     for (int h = 0; h < Geom::kHalves; ++h) {
-      tma_load_3d(dst + h * 2048, tk, 0, g * Geom::kHalves + h, phys * kBlockSize, b);
-      tma_load_3d(dst + Geom::kTileBytes + h * 2048, tv, 0, g * Geom::kHalves + h, phys * kBlockSize, b);
+      tma_load_4d(dst + h * 2048, tk, 0, g * Geom::kHalves + h, 0, phys, b);
+      tma_load_4d(dst + Geom::kTileBytes + h * 2048, tv, 0, g * Geom::kHalves + h, 0, phys, b);
     }
   }
 
@@ -308,8 +309,8 @@ struct NewToken {
     }
     const int c = lane & 15;
     if (c < D / 8) {
-      uint16_t* dst = (lane < 16 ? a.k_pool_w : a.v_pool_w) +
-                      static_cast<int64_t>(slot) * a.num_kv_heads * D + g * D + c * 8;
+      uint16_t* dst = (lane < 16 ? a.k_pool_w : a.v_pool_w) + (slot / kBlockSize) * a.block_stride +
+                      static_cast<int64_t>(row) * a.num_kv_heads * D + g * D + c * 8;
       *reinterpret_cast<uint4*>(dst) = val;
     }
     return true;

@@ -22,6 +22,7 @@ struct WriteCacheArgs {
   int64_t k_stride;   // elements between consecutive new tokens
   int64_t v_stride;
   int64_t num_slots;  // num_blocks * block_size
+  int64_t block_stride;  // pool elements between consecutive blocks (>= block_size * row_elems)
   int num_tokens;
   int row_elems;      // num_kv_heads * head_dim
 };
@@ -51,7 +52,8 @@ struct CopyBlocksArgs {
   uint16_t* v_pool;
   const int32_t* pairs;
   int32_t* dev_status;
-  int64_t block_elems;  // block bytes / 2 (block_size * num_kv_heads * head_dim for 16-bit pools)
+  int64_t block_elems;  // 16-bit units per block: num_layers * block_size * num_kv_heads * head_dim
+                        // (FP8 pools: half the block's bytes)
   int num_pairs;
   int num_blocks;
   // FP8 pools only (null otherwise): per-block scales copied with the block.
@@ -78,6 +80,7 @@ struct DecodeArgs {
   int partition_size;  // tokens, multiple of 16
   int max_parts;
   int max_context_len;
+  int64_t block_stride;  // pool elements between consecutive blocks (the fused write's addressing)
   float scale_log2;    // scale * log2(e)
   int out_dtype;       // pkv_dtype
   int balanced_ctas;   // balanced split: persistent CTAs (one per SM); 0 otherwise

@@ -56,7 +56,7 @@ pkv_status static_workspace_address(void** addr) {
 }  // namespace
 
 extern "C" pkv_status pkv_decode_attention_static_workspace(
-    void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+    void* out, const void* q, const void* k_pool, const void* v_pool, int64_t block_stride, const int32_t* block_tables,
     int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
     int head_dim, int block_size, int num_blocks, float scale, int partition_size, int max_context_len,
     pkv_dtype kv_dtype, pkv_dtype out_dtype, int32_t* dev_status, void* stream) {
@@ -68,8 +68,8 @@ extern "C" pkv_status pkv_decode_attention_static_workspace(
     const pkv_status st = static_workspace_address(&ws);
     if (st != PKV_OK) return st;
   }
-  return pkv_decode_attention(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-                              num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size,
+  return pkv_decode_attention(out, q, k_pool, v_pool, block_stride, block_tables, max_blocks_per_seq, context_lens,
+                              num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size,
                               max_context_len, ws, need > 0 ? static_cast<size_t>(PKV_STATIC_WORKSPACE_BYTES) : 0,
                               kv_dtype, out_dtype, dev_status, stream);
 }

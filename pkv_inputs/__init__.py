@@ -405,3 +405,49 @@ def make_fp8_pools(wl: Workload, *, seed: int | None = None, exact: bool = False
         ks[dead] = np.nan
         vs[dead] = np.nan
     return Fp8Pools(k8=k8, v8=v8, k_scale=ks, v_scale=vs)
+
+
+# ------------------------------------------------------------------ all-layer pools
+#
+# A model's layers share the block tables, lengths, slot mapping and
+# copy-on-write pairs of a step; each layer has its own queries, new rows and
+# pool contents.  "KV Cache & PagedAttention" section 4 keeps every layer of
+# a block together: [2 (K, V)][num_blocks][num_layers][block_size][H_kv][D].
+
+
+@dataclass
+class LayerData:
+    q: np.ndarray      # uint16 [L, S, H_q, D]
+    k_new: np.ndarray  # uint16 [L, S, H_kv, D]
+    v_new: np.ndarray
+    pool: np.ndarray   # uint16 [2, NB, L, B, H_kv, D]
+
+
+def make_layers(wl: Workload, num_layers: int, *, seed: int | None = None) -> LayerData:
+    """Per-layer values for workload `wl` (its tables and bookkeeping are
+    shared): layer 0 is wl's own arrays, the others are seeded N(0,1) draws
+    rounded to wl.dtype, poisoned like wl (NaN in every slot no sequence
+    owns)."""
+    import torch
+
+    gen = torch.Generator().manual_seed(wl.cfg * 1000003 + 11 if seed is None else seed)
+    L, S, NB, B = num_layers, wl.num_seqs, wl.num_blocks, wl.block_size
+    Hq, Hkv, D = wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    q = np.empty((L, S, Hq, D), dtype=np.uint16)
+    k_new = np.empty((L, S, Hkv, D), dtype=np.uint16)
+    v_new = np.empty_like(k_new)
+    pool = np.empty((2, NB, L, B, Hkv, D), dtype=np.uint16)
+    for layer in range(L):
+        if layer == 0:
+            q[0], k_new[0], v_new[0] = wl.q, wl.k_new, wl.v_new
+            pool[0, :, 0], pool[1, :, 0] = wl.k_pool, wl.v_pool
+            continue
+        q[layer] = _fill_normal((S, Hq, D), wl.dtype, gen)
+        k_new[layer] = _fill_normal((S, Hkv, D), wl.dtype, gen)
+        v_new[layer] = _fill_normal((S, Hkv, D), wl.dtype, gen)
+        for kv in range(2):
+            blk = _fill_normal((NB, B, Hkv, D), wl.dtype, gen)
+            if wl.poisoned:
+                blk[~wl.live] = NAN_BITS[wl.dtype]
+            pool[kv, :, layer] = blk
+    return LayerData(q=q, k_new=k_new, v_new=v_new, pool=pool)

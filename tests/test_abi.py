@@ -70,10 +70,11 @@ FAKE = 0x10000  # never dereferenced: validation fails before any device work
 
 
 def _decode(lib, **kw):
-    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, maxb=4, cl=FAKE, S=2, Hq=8, Hkv=2, D=128, B=16, NB=10,
+    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bs=0, bt=FAKE, maxb=4, cl=FAKE, S=2, Hq=8, Hkv=2, D=128, B=16, NB=10,
              scale=0.1, ps=0, maxlen=64, ws=None, wsb=0, kvd=pkv.PKV_BF16, od=pkv.PKV_F32)
     a.update(kw)
-    return lib.pkv_decode_attention(a["out"], a["q"], a["k"], a["v"], a["bt"], a["maxb"], a["cl"], a["S"], a["Hq"],
+    return lib.pkv_decode_attention(a["out"], a["q"], a["k"], a["v"], a["bs"], a["bt"], a["maxb"], a["cl"], a["S"],
+                                    a["Hq"],
                                     a["Hkv"], a["D"], a["B"], a["NB"], a["scale"], a["ps"], a["maxlen"], a["ws"],
                                     a["wsb"], a["kvd"], a["od"], None, None)
 
@@ -89,6 +90,9 @@ def test_decode_argument_validation(lib):
     assert _decode(lib, kvd=pkv.PKV_F32) == pkv.PKV_ERR_INVALID_ARG
     assert _decode(lib, S=-1) == pkv.PKV_ERR_INVALID_ARG
     assert _decode(lib, scale=float("nan")) == pkv.PKV_ERR_INVALID_ARG
+    # block stride: below a dense block, or not a whole 16-byte vector
+    assert _decode(lib, bs=16 * 2 * 128 - 8) == pkv.PKV_ERR_INVALID_ARG
+    assert _decode(lib, bs=3 * 16 * 2 * 128 + 4) == pkv.PKV_ERR_INVALID_ARG
     # split needs a workspace
     assert _decode(lib, ps=16, maxlen=64) == pkv.PKV_ERR_WORKSPACE
     need = pkv.decode_workspace_bytes(2, 8, 128, 64, 16)
@@ -96,9 +100,9 @@ def test_decode_argument_validation(lib):
 
 
 def test_write_and_copy_argument_validation(lib):
-    w = lambda **kw: lib.pkv_write_cache(kw.get("kn", FAKE), kw.get("vn", FAKE), FAKE, FAKE, FAKE, kw.get("T", 4),
-                                         kw.get("stride", 0), kw.get("Hkv", 8), kw.get("D", 128), kw.get("B", 16),
-                                         100, kw.get("dt", pkv.PKV_F16), None, None)
+    w = lambda **kw: lib.pkv_write_cache(kw.get("kn", FAKE), kw.get("vn", FAKE), FAKE, FAKE, kw.get("bs", 0), FAKE,
+                                         kw.get("T", 4), kw.get("stride", 0), kw.get("Hkv", 8), kw.get("D", 128),
+                                         kw.get("B", 16), 100, kw.get("dt", pkv.PKV_F16), None, None)
     assert w(B=32) == pkv.PKV_ERR_UNSUPPORTED
     assert w(T=-1) == pkv.PKV_ERR_INVALID_ARG
     assert w(kn=None) == pkv.PKV_ERR_INVALID_ARG
@@ -106,9 +110,11 @@ def test_write_and_copy_argument_validation(lib):
     assert w(stride=100) == pkv.PKV_ERR_INVALID_ARG  # stride below a row
     assert w(Hkv=1, D=4) == pkv.PKV_ERR_UNSUPPORTED  # row not a whole 16-byte vector
     assert w(T=0) == pkv.PKV_OK  # no-op, no launch
-    c = lambda **kw: lib.pkv_copy_blocks(FAKE, FAKE, kw.get("pairs", FAKE), kw.get("P", 3), 8, 128,
-                                         kw.get("B", 16), 100, pkv.PKV_BF16, None, None)
+    assert w(bs=16 * 8 * 128 - 8) == pkv.PKV_ERR_INVALID_ARG  # block stride below a dense block
+    c = lambda **kw: lib.pkv_copy_blocks(FAKE, FAKE, kw.get("pairs", FAKE), kw.get("P", 3), kw.get("layers", 1), 8,
+                                         128, kw.get("B", 16), 100, pkv.PKV_BF16, None, None)
     assert c(B=8) == pkv.PKV_ERR_UNSUPPORTED
+    assert c(layers=0) == pkv.PKV_ERR_INVALID_ARG
     assert c(pairs=None) == pkv.PKV_ERR_INVALID_ARG
     assert c(P=0) == pkv.PKV_OK
 

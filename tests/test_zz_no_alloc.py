@@ -29,7 +29,8 @@ def entry():
     lib = pkv.load(build_if_missing=True)
     fn = lib.pkv_decode_attention_static_workspace
     fn.restype = ctypes.c_int
-    fn.argtypes = ([ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_void_p] + [ctypes.c_int] * 6 +
+    fn.argtypes = ([ctypes.c_void_p] * 4 + [ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p] +
+                   [ctypes.c_int] * 6 +
                    [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                     ctypes.c_void_p])
     return fn
@@ -39,7 +40,7 @@ def _call(fn, ds, out):
     kv = pkv.PKV_BF16 if ds.k_pool.dtype == torch.bfloat16 else pkv.PKV_F16
     NB, B, Hkv, D = ds.k_pool.shape
     S, Hq, _ = ds.q.shape
-    return fn(out.data_ptr(), ds.q.data_ptr(), ds.k_pool.data_ptr(), ds.v_pool.data_ptr(),
+    return fn(out.data_ptr(), ds.q.data_ptr(), ds.k_pool.data_ptr(), ds.v_pool.data_ptr(), 0,
               ds.block_tables.data_ptr(), ds.block_tables.shape[1], ds.context_lens.data_ptr(), S, Hq, Hkv, D, B,
               NB, ds.wl.scale, ds.partition_size, ds.max_context_len, kv, pkv.PKV_F32, ds.status.data_ptr(),
               torch.cuda.current_stream().cuda_stream)
