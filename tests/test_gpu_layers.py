@@ -3,8 +3,8 @@
 "KV Cache & PagedAttention" section 4 keeps every layer of a block
 together, [2][num_blocks][num_layers][16][H_kv][D]; a layer's pool is then a
 view whose blocks are num_layers slices apart, which the library takes as a
-block stride.  "gpu_paged_kv_cache" ("Fixed-size blocks and the block-table
-indirection") keeps the tables at fixed addresses, updated in place, so a
+block stride.  "gpu_paged_kv_cache" ("The write path: slot mapping and
+scatter") keeps the tables at fixed addresses, updated in place, so a
 captured decode step replays with new contents.  Each layer is checked
 against the oracle run on that layer's own contiguous pool."""
 import numpy as np
