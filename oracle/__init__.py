@@ -46,8 +46,8 @@ import numpy as np
 
 from . import build as _build
 
-__all__ = ["write_cache", "copy_blocks", "decode_attention", "hardware_threads", "e4m3_decode", "e4m3_encode",
-           "write_cache_fp8", "copy_blocks_fp8", "decode_attention_fp8", "apply_step_fp8"]
+__all__ = ["write_cache", "copy_blocks", "swap_blocks", "decode_attention", "hardware_threads", "e4m3_decode",
+           "e4m3_encode", "write_cache_fp8", "copy_blocks_fp8", "decode_attention_fp8", "apply_step_fp8"]
 
 _LIB = None
 
@@ -94,6 +94,20 @@ def copy_blocks(k_pool: np.ndarray, v_pool: np.ndarray, pairs: np.ndarray) -> No
     for src, dst in np.asarray(pairs).reshape(-1, 2).tolist():
         k_pool[dst] = k_pool[src]
         v_pool[dst] = v_pool[src]
+
+
+def swap_blocks(dst_k: np.ndarray, dst_v: np.ndarray, src_k: np.ndarray, src_v: np.ndarray,
+                pairs: np.ndarray) -> None:
+    """In place: for each (s, d) pair, dst block d := src block s (K and V), byte for byte.
+
+    Swap out: src = the device pool, dst = a host pool ("gpu_paged_kv_cache",
+    "Reclaiming memory: swap versus recompute": the victim's blocks are copied
+    to pinned host memory and freed); swap in: the reverse, to whatever free
+    device blocks the block manager picks ("PagedAttention internals" section
+    05: copied back on resume).  Blocks are the arrays' first axis."""
+    for s_idx, d_idx in np.asarray(pairs).reshape(-1, 2).tolist():
+        dst_k[d_idx] = src_k[s_idx]
+        dst_v[d_idx] = src_v[s_idx]
 
 
 def decode_attention(q: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray, block_tables: np.ndarray,
