@@ -25,6 +25,9 @@ count one byte per K/V element plus the scales.
 `--impl reference` times the fp64 CPU oracle instead (a deliberately slow
 statement of the same computation) on a bounded sample of the workload.
 
+`--swap-gib X` times swapping X GiB of a preempted sequence's blocks out to
+pinned host memory and back in (pkv_swap_blocks).
+
 `--layers N` times every layer of a decode step over an all-layer pool
 [2][NB][N][16][H_kv][D], the step captured once as a CUDA graph and replayed
 (eager time reported beside it).
@@ -559,6 +562,87 @@ def run_layers(args):
     return line
 
 
+def run_swap(args):
+    """Swap out / in of a preempted victim's blocks (--swap-gib X): the pages'
+    example of 1.25 GiB of an 8B-class model's KV ("PagedAttention internals"
+    section 05: 32 layers, 8 KV heads, head_dim 128, fp16, 16-token blocks of
+    2 MiB over all layers, ~50 ms each way over PCIe 4.0 at ~25 GB/s).  The
+    victim's blocks are scattered over an all-layer device pool; the host
+    pool is pinned memory, reached by the kernel over NVLink-C2C."""
+    import torch
+
+    import paged_kv_cache_112_gb300 as pkv
+
+    _, _, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkv.load()
+    layers, hkv, d = 32, 8, 128
+    block_bytes = 2 * layers * 16 * hkv * d * 2  # K + V, all layers
+    n = max(1, int(round(args.swap_gib * 2 ** 30 / block_bytes)))
+    nb_dev = max(4 * n, 1024)
+    gen = torch.Generator(device=dev).manual_seed(1250)
+    pool = torch.empty((2, nb_dev, layers, 16, hkv, d), dtype=torch.float16, device=dev)
+    pool.normal_(generator=gen)
+    host = torch.empty((2, n, layers, 16, hkv, d), dtype=torch.float16).pin_memory()
+    rng = np.random.default_rng(1250)
+    victim = rng.permutation(nb_dev)[:n].astype(np.int32)
+    target = rng.permutation(nb_dev)[:n].astype(np.int32)
+    out_pairs = torch.from_numpy(np.stack([victim, np.arange(n, dtype=np.int32)], 1)).to(dev)
+    in_pairs = torch.from_numpy(np.stack([np.arange(n, dtype=np.int32), target], 1)).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def swap_out():
+        pkv.swap_blocks(host[0], host[1], pool[0], pool[1], out_pairs, status=status)
+
+    def swap_in():
+        pkv.swap_blocks(pool[0], pool[1], host[0], host[1], in_pairs, status=status)
+
+    res = {}
+    for name, fn in (("out", swap_out), ("in", swap_in)):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / args.steps
+        res[name] = {"ms": round(ms, 4), "GB/s": round(n * block_bytes / (ms * 1e-3) / 1e9, 2)}
+    # the link's bulk rate for comparison: one contiguous copy of the same bytes each way (copy engine)
+    flat_dev = pool.view(-1)[: host.numel()]
+    flat_host = host.view(-1)
+    for name, fn in (("bulk_d2h", lambda: flat_host.copy_(flat_dev, non_blocking=True)),
+                     ("bulk_h2d", lambda: flat_dev.copy_(flat_host, non_blocking=True))):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / args.steps
+        res[name] = {"ms": round(ms, 4), "GB/s": round(n * block_bytes / (ms * 1e-3) / 1e9, 2)}
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    moved = n * block_bytes
+    value = 2 * moved / ((res["out"]["ms"] + res["in"]["ms"]) * 1e-3) / 1e9
+    return {"metric": "swap out + in of a preempted sequence's blocks, GB/s (device <-> pinned host)",
+            "value": round(value, 2), "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(res["out"]["ms"] + res["in"]["ms"], 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": "8B-class all-layer blocks (32 layers, 8 KV heads, head_dim 128, fp16), "
+                                   f"{n} blocks of 2 MiB scattered over {nb_dev}",
+                       "bytes_each_way": moved, "entry": "pkv_swap_blocks"},
+            "swap_out": res["out"], "swap_in": res["in"],
+            "contiguous_copy_engine": {"d2h": res["bulk_d2h"], "h2d": res["bulk_h2d"]},
+            "pages_figure": "1.25 GiB over PCIe 4.0 x16 at ~25 GB/s: ~50 ms each way"}
+
+
 def _recorded_traffic(cfg, kernel):
     """DRAM bytes per launch of the partition kernel from the committed ncu
     summary, if it was taken on the current kernel sources; else None."""
@@ -712,6 +796,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused", action="store_true",
                     help="run write_cache and decode attention as separate calls instead of pkv_decode_step")
+    ap.add_argument("--swap-gib", type=float, default=0.0,
+                    help="time swapping this many GiB of a victim's blocks out to pinned host memory and back")
     ap.add_argument("--layers", type=int, default=0,
                     help="time every layer of a decode step (this many) over an all-layer pool, as a CUDA graph")
     ap.add_argument("--fused", action="store_true",
@@ -728,6 +814,8 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         line = run_reference(args)
+    elif args.swap_gib > 0:
+        line = run_swap(args)
     elif args.layers > 0:
         line = run_layers(args)
     else:

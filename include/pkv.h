@@ -111,6 +111,36 @@ pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int
                            int num_layers, int num_kv_heads, int head_dim, int block_size,
                            int num_blocks, pkv_dtype kv_dtype, int32_t* dev_status, void* stream);
 
+/*
+ * pkv_swap_blocks -- swap out / swap in of block lists ["gpu_paged_kv_cache",
+ * "Reclaiming memory: swap versus recompute": a preempted victim's blocks
+ * are copied to pinned host memory, freed, and copied back on resume; P2
+ * section 05]: for each pair i, block pairs[2i+1] of the destination pool
+ * := block pairs[2i] of the source pool, for K and for V, block_bytes bytes
+ * each.  Swap out: source = the device pool, destination = a pool in
+ * pinned host memory; swap in: the reverse, to whatever free device blocks
+ * the block manager picked (the caller repoints the tables).  One kernel
+ * moves the whole list, reading or writing the host pool through its
+ * device mapping (NVLink-C2C on GB300).
+ *   dst_k, dst_v / src_k, src_v : block 0 of each pool, 16-byte aligned,
+ *                  device memory, managed memory or pinned (page-locked or
+ *                  registered) host memory; pageable host memory is
+ *                  rejected (PKV_ERR_INVALID_ARG).
+ *   *_block_stride : bytes between consecutive blocks of that pool, a
+ *                  multiple of 16 and >= block_bytes.
+ *   *_num_blocks : blocks in that pool (pair indices are checked against it).
+ *   block_bytes  : bytes per block and per K / V, a multiple of 16: one
+ *                  layer's block (16 * H_kv * D * elem), a whole all-layer
+ *                  block (times num_layers), or an FP8 pool's codes or scales.
+ *   pairs        : int32[num_pairs][2] = (source block, destination block),
+ *                  device or pinned host memory; destination blocks distinct.
+ * Out-of-range pairs set PKV_DEV_ERR_PAIR and are skipped.
+ */
+pkv_status pkv_swap_blocks(void* dst_k, void* dst_v, int64_t dst_block_stride, int dst_num_blocks,
+                           const void* src_k, const void* src_v, int64_t src_block_stride,
+                           int src_num_blocks, int64_t block_bytes, const int32_t* pairs, int num_pairs,
+                           int32_t* dev_status, void* stream);
+
 /* partition_size value selecting the balanced split (see pkv_decode_attention). */
 #define PKV_PARTITION_BALANCED (-1)
 

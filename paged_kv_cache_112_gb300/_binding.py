@@ -47,6 +47,9 @@ _SIGS["pkv_decode_attention_fp8"] = ([_c_void_p] * 7 + [_c_int, _c_void_p] + [_c
                                      [_c_float, _c_int, _c_int, _c_void_p, _c_size_t, _c_int, _c_int, _c_void_p,
                                       _c_void_p])
 _SIGS["pkv_decode_partitions_fp8"] = _SIGS["pkv_decode_attention_fp8"]
+_SIGS["pkv_swap_blocks"] = ([_c_void_p] * 2 + [_c_int64, _c_int] + [_c_void_p] * 2 + [_c_int64, _c_int, _c_int64,
+                                                                                     _c_void_p, _c_int, _c_void_p,
+                                                                                     _c_void_p])
 _SIGS["pkv_decode_step_fp8"] = ([_c_void_p] * 4 + [_c_int64] + [_c_void_p] * 5 + [_c_int] + [_c_void_p] * 2 +
                                 [_c_int] * 6 + [_c_float, _c_int, _c_int, _c_void_p, _c_size_t, _c_int, _c_int,
                                                 _c_void_p, _c_void_p])
@@ -353,3 +356,44 @@ def decode_step_partitions_fp8(out, q, k_new, v_new, k_pool, v_pool, k_scale, v_
                                                                  scale, partition_size, max_context_len, workspace,
                                                                  status, stream)),
            "pkv_decode_step_partitions_fp8")
+
+
+# ------------------------------------------------------------------ swap
+
+
+def _block_layout(t):
+    """(bytes between blocks, bytes per block) of a pool whose blocks are dense slices along dim 0."""
+    esz = t.element_size()
+    inner = 1
+    expect = 1
+    for d in range(t.dim() - 1, 0, -1):
+        if t.stride(d) != expect:
+            raise PkvError("pool blocks must be dense slices along the first axis")
+        expect *= t.shape[d]
+        inner *= t.shape[d]
+    if t.stride(0) < inner:
+        raise PkvError("pool blocks overlap")
+    return int(t.stride(0)) * esz, inner * esz
+
+
+def swap_blocks(dst_k, dst_v, src_k, src_v, pairs, *, status=None, stream=None):
+    """pkv_swap_blocks: for each (s, d) in pairs, dst block d := src block s (K and V).
+
+    Pools are tensors whose first axis is the block ([NB, 16, H_kv, D] per layer,
+    [NB, layers, 16, H_kv, D] all layers, FP8 codes, or [NB, H_kv] scales), each on
+    the GPU or in pinned host memory (tensor.pin_memory()); pairs int32 [P, 2]."""
+    for t in (dst_k, dst_v, src_k, src_v, pairs):
+        if not (t.is_cuda or t.is_pinned()):
+            raise PkvError("swap operands must be CUDA tensors or pinned host tensors")
+    if pairs.dtype != torch.int32 or not pairs.is_contiguous():
+        raise PkvError("pairs must be a contiguous int32 [P, 2] tensor")
+    d_stride, d_bytes = _block_layout(dst_k)
+    s_stride, s_bytes = _block_layout(src_k)
+    if _block_layout(dst_v) != (d_stride, d_bytes) or _block_layout(src_v) != (s_stride, s_bytes):
+        raise PkvError("K and V pools must share their block layout")
+    if d_bytes != s_bytes or dst_k.shape[0] != dst_v.shape[0] or src_k.shape[0] != src_v.shape[0]:
+        raise PkvError("source and destination blocks must have the same size")
+    _need_cuda(status)
+    _check(load().pkv_swap_blocks(_ptr(dst_k), _ptr(dst_v), d_stride, int(dst_k.shape[0]), _ptr(src_k), _ptr(src_v),
+                                  s_stride, int(src_k.shape[0]), d_bytes, _ptr(pairs), int(pairs.shape[0]),
+                                  _ptr(status), _stream(stream)), "pkv_swap_blocks")

@@ -660,6 +660,66 @@ pkv_status pkv_decode_attention_fp8(void* out, const void* q, const void* k_pool
                            max_context_len, workspace, workspace_bytes, out_dtype, dev_status, stream);
 }
 
+}  // extern "C"
+
+namespace pkv {
+namespace {
+
+// The address the device dereferences for `p`: device and managed memory as
+// is, pinned (page-locked, registered) host memory through its mapping.
+// Returns nullptr for memory the device cannot reach (pageable host memory).
+const void* device_view(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+      return p;
+    case cudaMemoryTypeHost:
+      return at.devicePointer;
+    default:
+      return nullptr;
+  }
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status pkv_swap_blocks(void* dst_k, void* dst_v, int64_t dst_block_stride, int dst_num_blocks,
+                           const void* src_k, const void* src_v, int64_t src_block_stride, int src_num_blocks,
+                           int64_t block_bytes, const int32_t* pairs, int num_pairs, int32_t* dev_status,
+                           void* stream) {
+  if (num_pairs < 0 || dst_num_blocks <= 0 || src_num_blocks <= 0 || block_bytes <= 0 || block_bytes % 16 != 0 ||
+      dst_block_stride < block_bytes || src_block_stride < block_bytes || dst_block_stride % 16 != 0 ||
+      src_block_stride % 16 != 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PKV_OK;
+  if (!dst_k || !dst_v || !src_k || !src_v || !pairs) return PKV_ERR_INVALID_ARG;
+  if (!aligned(dst_k, 16) || !aligned(dst_v, 16) || !aligned(src_k, 16) || !aligned(src_v, 16) ||
+      !aligned(pairs, 4))
+    return PKV_ERR_INVALID_ARG;
+  SwapBlocksArgs a{};
+  a.dst_k = static_cast<uint8_t*>(const_cast<void*>(device_view(dst_k)));
+  a.dst_v = static_cast<uint8_t*>(const_cast<void*>(device_view(dst_v)));
+  a.src_k = static_cast<const uint8_t*>(device_view(src_k));
+  a.src_v = static_cast<const uint8_t*>(device_view(src_v));
+  a.pairs = static_cast<const int32_t*>(device_view(pairs));
+  if (!a.dst_k || !a.dst_v || !a.src_k || !a.src_v || !a.pairs) return PKV_ERR_INVALID_ARG;  // pageable memory
+  a.dev_status = dev_status;
+  a.dst_stride = dst_block_stride;
+  a.src_stride = src_block_stride;
+  a.block_bytes = block_bytes;
+  a.num_pairs = num_pairs;
+  a.dst_num_blocks = dst_num_blocks;
+  a.src_num_blocks = src_num_blocks;
+  return launch_swap_blocks(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 const char* pkv_status_string(pkv_status s) {
   switch (s) {
     case PKV_OK: return "PKV_OK";

@@ -124,6 +124,36 @@ __global__ void __launch_bounds__(256) write_cache_fp8_kernel(WriteCacheFp8Args 
   }
 }
 
+// Swap out / in ("gpu_paged_kv_cache", "Reclaiming memory: swap versus
+// recompute"; "PagedAttention internals", section 05): for each pair (s, d),
+// block d of the destination pool := block s of the source pool, K and V.
+// One side is pinned host memory, read or written directly by the kernel
+// through its mapped address (on GB300 over NVLink-C2C), so a whole block
+// list moves in one launch.  Each thread moves 16-byte vectors; adjacent
+// threads move adjacent vectors of one block.
+__global__ void __launch_bounds__(256) swap_blocks_kernel(SwapBlocksArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int64_t vec_per_block = a.block_bytes / 16;
+  const int64_t total = static_cast<int64_t>(a.num_pairs) * 2 * vec_per_block;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t v = idx % vec_per_block;
+    const int64_t r = idx / vec_per_block;
+    const int which = static_cast<int>(r & 1);
+    const int64_t pair = r >> 1;
+    const int src = a.pairs[2 * pair];
+    const int dst = a.pairs[2 * pair + 1];
+    if (src < 0 || src >= a.src_num_blocks || dst < 0 || dst >= a.dst_num_blocks) {
+      if (v == 0 && which == 0) flag(a.dev_status, 2u);  // PKV_DEV_ERR_PAIR
+      continue;
+    }
+    const uint8_t* from = (which ? a.src_v : a.src_k) + src * a.src_stride;
+    uint8_t* to = (which ? a.dst_v : a.dst_k) + dst * a.dst_stride;
+    reinterpret_cast<uint4*>(to)[v] = reinterpret_cast<const uint4*>(from)[v];
+  }
+}
+
 int grid_for(int64_t work_items, int threads) {
   const int sms = current_sm_count(148);
   const int64_t want = (work_items + threads - 1) / threads;
@@ -143,6 +173,12 @@ cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream) {
   const int64_t work = static_cast<int64_t>(a.num_pairs) * 2 * (a.block_elems / 8);
   if (work == 0) return cudaSuccess;
   return launch_pdl(copy_blocks_kernel, dim3(grid_for(work, 256)), dim3(256), 0, stream, a);
+}
+
+cudaError_t launch_swap_blocks(const SwapBlocksArgs& a, cudaStream_t stream) {
+  const int64_t work = static_cast<int64_t>(a.num_pairs) * 2 * (a.block_bytes / 16);
+  if (work == 0) return cudaSuccess;
+  return launch_pdl(swap_blocks_kernel, dim3(grid_for(work, 256)), dim3(256), 0, stream, a);
 }
 
 cudaError_t launch_write_cache_fp8(const WriteCacheFp8Args& a, cudaStream_t stream) {

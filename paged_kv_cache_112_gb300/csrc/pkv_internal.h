@@ -47,6 +47,23 @@ struct WriteCacheFp8Args {
   int new_bf16;          // new rows: 0 = f16, 1 = bf16
 };
 
+// Block lists moved between two pools, each in device memory or in pinned
+// host memory reached through its device-mapped address (swap out / in).
+struct SwapBlocksArgs {
+  uint8_t* dst_k;
+  uint8_t* dst_v;
+  const uint8_t* src_k;
+  const uint8_t* src_v;
+  const int32_t* pairs;  // [num_pairs][2] = (src block, dst block)
+  int32_t* dev_status;
+  int64_t dst_stride;    // bytes between consecutive blocks
+  int64_t src_stride;
+  int64_t block_bytes;   // bytes moved per block (multiple of 16)
+  int num_pairs;
+  int dst_num_blocks;
+  int src_num_blocks;
+};
+
 struct CopyBlocksArgs {
   uint16_t* k_pool;
   uint16_t* v_pool;
@@ -152,6 +169,7 @@ cudaError_t launch_decode_partitions_fp8(const DecodeArgs& a, const CUtensorMap&
                                          const CUtensorMap& tmap_v, int head_dim, int q_bf16,
                                          cudaStream_t stream);
 cudaError_t launch_write_cache_fp8(const WriteCacheFp8Args& a, cudaStream_t stream);
+cudaError_t launch_swap_blocks(const SwapBlocksArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_balanced(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                    int head_dim, int kv_bf16, cudaStream_t stream);
 cudaError_t launch_decode_reduce_balanced(const DecodeArgs& a, int head_dim, cudaStream_t stream);

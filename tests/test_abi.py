@@ -32,7 +32,7 @@ def test_header_declares_the_entry_points():
     names = _declared()
     for n in ["pkv_write_cache", "pkv_copy_blocks", "pkv_decode_attention", "pkv_decode_partitions",
               "pkv_decode_reduce", "pkv_decode_workspace_bytes", "pkv_status_string", "pkv_version",
-              "pkv_write_cache_fp8", "pkv_copy_blocks_fp8", "pkv_decode_attention_fp8"]:
+              "pkv_write_cache_fp8", "pkv_copy_blocks_fp8", "pkv_decode_attention_fp8", "pkv_swap_blocks"]:
         assert n in names
 
 
@@ -151,6 +151,24 @@ def test_fp8_argument_validation(lib):
     assert c(B=8) == pkv.PKV_ERR_UNSUPPORTED
     assert c(ks=None) == pkv.PKV_ERR_INVALID_ARG
     assert c(P=0) == pkv.PKV_OK
+
+
+def test_swap_argument_validation(lib):
+    def sw(**kw):
+        return lib.pkv_swap_blocks(kw.get("dk", FAKE), FAKE, kw.get("ds", 4096), 10, FAKE, FAKE, kw.get("ss", 4096), 10,
+                                   kw.get("bb", 4096), kw.get("pairs", FAKE), kw.get("P", 3), None, None)
+
+    assert sw(bb=4000) == pkv.PKV_ERR_INVALID_ARG  # not a whole 16-byte vector
+    assert sw(ds=2048) == pkv.PKV_ERR_INVALID_ARG  # stride below a block
+    assert sw(ss=4104) == pkv.PKV_ERR_INVALID_ARG  # stride not a 16-byte multiple
+    assert sw(dk=FAKE + 8) == pkv.PKV_ERR_INVALID_ARG
+    assert sw(pairs=None) == pkv.PKV_ERR_INVALID_ARG
+    assert sw(P=-1) == pkv.PKV_ERR_INVALID_ARG
+    assert sw(P=0) == pkv.PKV_OK
+    # pointers the device cannot reach (here: no device at all, or plain host memory) are refused
+    host = ctypes.create_string_buffer(8192 + 16)
+    addr = (ctypes.addressof(host) + 15) // 16 * 16
+    assert sw(dk=addr) == pkv.PKV_ERR_INVALID_ARG
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
