@@ -101,14 +101,15 @@ def step_bytes(wl, out_bytes_per_elem=4):
     S, Hq, Hkv, D = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
     L = wl.context_lens.astype(np.int64)
     kv = int(L.sum()) * Hkv * D * 2 * 2
-    tables = int(np.sum((L + 15) // 16)) * 4
+    B = wl.block_size
+    tables = int(np.sum((L + B - 1) // B)) * 4
     q = S * Hq * D * 2
     out = S * Hq * D * out_bytes_per_elem
     lens = S * 4
     attn = kv + tables + q + out + lens
     T = wl.slot_mapping.shape[0]
     write = 2 * T * Hkv * D * 2 * 2 + T * 4  # read new rows + write pool rows, K and V; slots
-    cow = wl.copy_pairs.shape[0] * (2 * 16 * Hkv * D * 2 * 2 + 8)
+    cow = wl.copy_pairs.shape[0] * (2 * B * Hkv * D * 2 * 2 + 8)
     return {"attention": attn, "kv": kv, "write": write, "copy": cow, "step": attn + write + cow}
 
 
@@ -194,7 +195,7 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=dev)
     pkv.load()
 
-    wl = P.make_workload(args.config, poison=False)
+    wl = P.make_workload(args.config, poison=False, block_size=args.block_size)
     ps = wl.partition_size if args.partition_size is None else args.partition_size
     dt = {"f16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
 
@@ -374,7 +375,7 @@ def run_gpu(args):
         "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": f"e4m3 KV, {wl.dtype} q" if fp8 else wl.dtype, "data": "synthetic",
         "config": {"workload": wl.name, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
-                   "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": 16,
+                   "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
                    "partition_size": ps, "max_context_len": max_len, "total_context_tokens":
                    int(wl.context_lens.astype(np.int64).sum()), "num_blocks": wl.num_blocks,
                    "cow_pairs": int(wl.copy_pairs.shape[0]), "out_dtype": "f32",
@@ -796,6 +797,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused", action="store_true",
                     help="run write_cache and decode attention as separate calls instead of pkv_decode_step")
+    ap.add_argument("--block-size", type=int, default=16, choices=[8, 16, 32, 64],
+                    help="tokens per KV block (16-bit pools; the recipes use 16)")
     ap.add_argument("--swap-gib", type=float, default=0.0,
                     help="time swapping this many GiB of a victim's blocks out to pinned host memory and back")
     ap.add_argument("--layers", type=int, default=0,

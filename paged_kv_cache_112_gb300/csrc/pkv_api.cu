@@ -109,16 +109,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // head_dim * eb / 128 boxes (16-bit: 2 at head_dim 128, 1 at 64; FP8: 1 at
 // head_dim 128).  A block stride above 16 rows is a layer slice of a pool
 // that keeps all layers of a block together.
-bool encode_pool_map_uncached(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, int head_dim,
-                              int eb, int64_t block_stride) {
+bool encode_pool_map_uncached(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int num_kv_heads,
+                              int head_dim, int eb, int64_t block_stride) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint32_t line = 128 / eb;  // elements per 128-byte line
-  const cuuint64_t dims[4] = {line, static_cast<cuuint64_t>(num_kv_heads) * (head_dim / line), kBlockSize,
-                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t dims[4] = {line, static_cast<cuuint64_t>(num_kv_heads) * (head_dim / line),
+                              static_cast<cuuint64_t>(block_size), static_cast<cuuint64_t>(num_blocks)};
   const cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(num_kv_heads) * head_dim * eb,
                                  static_cast<cuuint64_t>(block_stride) * eb};
-  const cuuint32_t box[4] = {line, 1, kBlockSize, 1};
+  // A box is one 16-row tile, or one 8-token block (two boxes per tile).
+  const cuuint32_t box[4] = {line, 1, static_cast<cuuint32_t>(block_size < kTile ? block_size : kTile), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = fn(map, eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
                         const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -130,11 +131,11 @@ bool encode_pool_map_uncached(CUtensorMap* map, const void* pool, int num_blocks
 
 // Descriptors depend only on the pool address and geometry, so recent ones
 // are kept (a small round-robin cache) instead of re-encoded every call.
-bool encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads, int head_dim, int eb,
-                     int64_t block_stride) {
+bool encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int num_kv_heads,
+                     int head_dim, int eb, int64_t block_stride) {
   struct Entry {
     const void* pool;
-    int num_blocks, num_kv_heads, head_dim, eb;
+    int num_blocks, block_size, num_kv_heads, head_dim, eb;
     int64_t block_stride;
     CUtensorMap map;
   };
@@ -144,24 +145,36 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int num
   {
     std::lock_guard<std::mutex> lock(mu);
     for (const Entry& e : cache)
-      if (e.pool == pool && e.num_blocks == num_blocks && e.num_kv_heads == num_kv_heads &&
-          e.head_dim == head_dim && e.eb == eb && e.block_stride == block_stride) {
+      if (e.pool == pool && e.num_blocks == num_blocks && e.block_size == block_size &&
+          e.num_kv_heads == num_kv_heads && e.head_dim == head_dim && e.eb == eb && e.block_stride == block_stride) {
         *map = e.map;
         return true;
       }
   }
-  if (!encode_pool_map_uncached(map, pool, num_blocks, num_kv_heads, head_dim, eb, block_stride)) return false;
+  if (!encode_pool_map_uncached(map, pool, num_blocks, block_size, num_kv_heads, head_dim, eb, block_stride))
+    return false;
   std::lock_guard<std::mutex> lock(mu);
-  cache[next] = Entry{pool, num_blocks, num_kv_heads, head_dim, eb, block_stride, *map};
+  cache[next] = Entry{pool, num_blocks, block_size, num_kv_heads, head_dim, eb, block_stride, *map};
   next = (next + 1) % 64;
   return true;
+}
+
+// log2 of a supported block size (8, 16, 32 or 64 tokens), else -1.
+int block_shift_of(int block_size) {
+  switch (block_size) {
+    case 8: return 3;
+    case 16: return 4;
+    case 32: return 5;
+    case 64: return 6;
+    default: return -1;
+  }
 }
 
 // Block stride of a pool: 0 means dense (block_size * num_kv_heads *
 // head_dim); otherwise at least that and a multiple of 8 elements (16 bytes
 // at 16 bits).  Returns -1 when invalid.
-int64_t resolve_block_stride(int64_t block_stride, int num_kv_heads, int head_dim) {
-  const int64_t dense = static_cast<int64_t>(kBlockSize) * num_kv_heads * head_dim;
+int64_t resolve_block_stride(int64_t block_stride, int block_size, int num_kv_heads, int head_dim) {
+  const int64_t dense = static_cast<int64_t>(block_size) * num_kv_heads * head_dim;
   if (block_stride == 0) return dense;
   if (block_stride < dense || block_stride % 8 != 0) return -1;
   return block_stride;
@@ -171,7 +184,7 @@ int parts_for(int max_context_len, int partition_size, int* ps_out) {
   int ps = partition_size;
   if (ps <= 0) {  // one partition per sequence
     const int len = max_context_len > 0 ? max_context_len : 1;
-    ps = ((len + kBlockSize - 1) / kBlockSize) * kBlockSize;
+    ps = ((len + kTile - 1) / kTile) * kTile;
   }
   *ps_out = ps;
   const int len = max_context_len > 0 ? max_context_len : 1;
@@ -207,12 +220,13 @@ pkv_status prepare_decode(DecodeCall* c, void* out, const void* q, const void* k
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq < 0 || num_blocks <= 0 ||
       max_context_len < 0 || (partition_size < 0 && !balanced) || !std::isfinite(scale))
     return PKV_ERR_INVALID_ARG;
-  if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  const int shift = block_shift_of(block_size);
+  if (shift < 0 || (balanced && block_size != kBlockSize)) return PKV_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
   if (num_q_heads % num_kv_heads != 0) return PKV_ERR_UNSUPPORTED;
   const int group = num_q_heads / num_kv_heads;
   if (group > 8) return PKV_ERR_UNSUPPORTED;
-  if (!balanced && partition_size % kBlockSize != 0) return PKV_ERR_UNSUPPORTED;
+  if (!balanced && partition_size % kTile != 0) return PKV_ERR_UNSUPPORTED;
   if (balanced && num_seqs > kBalancedMaxSeqs) return PKV_ERR_UNSUPPORTED;
   if (!kv_dtype_ok(kv_dtype) || (out_dtype != PKV_F32 && out_dtype != PKV_F16 && out_dtype != PKV_BF16))
     return PKV_ERR_INVALID_ARG;
@@ -221,7 +235,7 @@ pkv_status prepare_decode(DecodeCall* c, void* out, const void* q, const void* k
   if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(q, 4) ||
       !aligned(out, out_dtype == PKV_F32 ? 4 : 2) || !aligned(block_tables, 4) || !aligned(context_lens, 4))
     return PKV_ERR_INVALID_ARG;
-  const int64_t bstride = resolve_block_stride(block_stride, num_kv_heads, head_dim);
+  const int64_t bstride = resolve_block_stride(block_stride, block_size, num_kv_heads, head_dim);
   if (bstride < 0) return PKV_ERR_INVALID_ARG;
   const int sms = balanced ? current_sm_count(0) : 0;
   if (balanced && sms <= 0) return PKV_ERR_CUDA;
@@ -253,13 +267,14 @@ pkv_status prepare_decode(DecodeCall* c, void* out, const void* q, const void* k
   a.partition_size = ps;
   a.max_parts = max_parts;
   a.max_context_len = max_context_len;
+  a.block_shift = shift;
   a.block_stride = bstride;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out_dtype = static_cast<int>(out_dtype);
   a.timeout_ns = kWaitTimeoutNs;
   if (need_maps && num_seqs > 0) {
-    if (!encode_pool_map(&c->tmap_k, k_pool, num_blocks, num_kv_heads, head_dim, 2, bstride) ||
-        !encode_pool_map(&c->tmap_v, v_pool, num_blocks, num_kv_heads, head_dim, 2, bstride))
+    if (!encode_pool_map(&c->tmap_k, k_pool, num_blocks, block_size, num_kv_heads, head_dim, 2, bstride) ||
+        !encode_pool_map(&c->tmap_v, v_pool, num_blocks, block_size, num_kv_heads, head_dim, 2, bstride))
       return PKV_ERR_CUDA;
   }
   return PKV_OK;
@@ -279,10 +294,11 @@ pkv_status pkv_write_cache(const void* k_new, const void* v_new, void* k_pool, v
   if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || new_row_stride < 0)
     return PKV_ERR_INVALID_ARG;
   if (!kv_dtype_ok(kv_dtype)) return PKV_ERR_INVALID_ARG;
-  if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  const int shift = block_shift_of(block_size);
+  if (shift < 0) return PKV_ERR_UNSUPPORTED;
   const int row = num_kv_heads * head_dim;
   if (row % 8 != 0) return PKV_ERR_UNSUPPORTED;  // 16-byte vectors
-  const int64_t bstride = resolve_block_stride(block_stride, num_kv_heads, head_dim);
+  const int64_t bstride = resolve_block_stride(block_stride, block_size, num_kv_heads, head_dim);
   if (bstride < 0) return PKV_ERR_INVALID_ARG;
   if (num_tokens == 0) return PKV_OK;
   if (!k_new || !v_new || !k_pool || !v_pool || !slot_mapping) return PKV_ERR_INVALID_ARG;
@@ -300,8 +316,9 @@ pkv_status pkv_write_cache(const void* k_new, const void* v_new, void* k_pool, v
   a.dev_status = dev_status;
   a.k_stride = stride;
   a.v_stride = stride;
-  a.num_slots = static_cast<int64_t>(num_blocks) * kBlockSize;
+  a.num_slots = static_cast<int64_t>(num_blocks) << shift;
   a.block_stride = bstride;
+  a.block_shift = shift;
   a.num_tokens = num_tokens;
   a.row_elems = row;
   return launch_write_cache(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
@@ -313,7 +330,7 @@ pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int
   if (num_pairs < 0 || num_layers <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0)
     return PKV_ERR_INVALID_ARG;
   if (!kv_dtype_ok(kv_dtype)) return PKV_ERR_INVALID_ARG;
-  if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  if (block_shift_of(block_size) < 0) return PKV_ERR_UNSUPPORTED;
   if ((num_kv_heads * head_dim) % 8 != 0) return PKV_ERR_UNSUPPORTED;
   if (num_pairs == 0) return PKV_OK;
   if (!k_pool || !v_pool || !pairs) return PKV_ERR_INVALID_ARG;
@@ -323,7 +340,7 @@ pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int
   a.v_pool = static_cast<uint16_t*>(v_pool);
   a.pairs = pairs;
   a.dev_status = dev_status;
-  a.block_elems = static_cast<int64_t>(num_layers) * kBlockSize * num_kv_heads * head_dim;
+  a.block_elems = static_cast<int64_t>(num_layers) * block_size * num_kv_heads * head_dim;
   a.num_pairs = num_pairs;
   a.num_blocks = num_blocks;
   return launch_copy_blocks(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
@@ -333,7 +350,7 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, i
                                   int partition_size) {
   const bool balanced = partition_size == PKV_PARTITION_BALANCED;
   if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||
-      (!balanced && (partition_size < 0 || partition_size % kBlockSize != 0)))
+      (!balanced && (partition_size < 0 || partition_size % kTile != 0)))
     return 0;
   int parts = 1;
   return decode_layout(num_seqs, num_q_heads, head_dim, max_context_len, partition_size,
@@ -372,7 +389,7 @@ pkv_status pkv_decode_reduce(void* out, const int32_t* context_lens, int num_seq
     return PKV_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
   if (num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > 8) return PKV_ERR_UNSUPPORTED;
-  if (!balanced && partition_size % kBlockSize != 0) return PKV_ERR_UNSUPPORTED;
+  if (!balanced && partition_size % kTile != 0) return PKV_ERR_UNSUPPORTED;
   if (out_dtype != PKV_F32 && out_dtype != PKV_F16 && out_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
   const int sms = balanced ? current_sm_count(0) : 0;
   if (balanced && sms <= 0) return PKV_ERR_CUDA;
@@ -400,7 +417,8 @@ pkv_status pkv_decode_reduce(void* out, const int32_t* context_lens, int num_seq
   a.max_context_len = max_context_len;
   // Lengths are clamped as in the partition kernel; beyond max_context_len the
   // table width does not matter here.
-  a.max_blocks_per_seq = (max_context_len + kBlockSize - 1) / kBlockSize;
+  a.max_blocks_per_seq = (max_context_len + kTile - 1) / kTile;
+  a.block_shift = 4;  // with the line above: lengths are clamped to max_context_len alone
   a.out_dtype = static_cast<int>(out_dtype);
   a.balanced_ctas = balanced ? sms : 0;
   const cudaError_t e = balanced ? launch_decode_reduce_balanced(a, head_dim, static_cast<cudaStream_t>(stream))
@@ -552,7 +570,7 @@ pkv_status prepare_decode_fp8(DecodeCall* c, void* out, const void* q, const voi
                               int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
                               int partition_size, int max_context_len, void* workspace, size_t workspace_bytes,
                               pkv_dtype q_dtype, pkv_dtype out_dtype, int32_t* dev_status) {
-  if (partition_size == PKV_PARTITION_BALANCED) return PKV_ERR_UNSUPPORTED;
+  if (partition_size == PKV_PARTITION_BALANCED || block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
   pkv_status st = prepare_decode(c, out, q, k_pool, v_pool, 0, block_tables, max_blocks_per_seq, context_lens,
                                  num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                                  partition_size, max_context_len, workspace, workspace_bytes, q_dtype, out_dtype,
@@ -565,8 +583,8 @@ pkv_status prepare_decode_fp8(DecodeCall* c, void* out, const void* q, const voi
   c->args.k_scale = k_scale;
   c->args.v_scale = v_scale;
   // FP8 pools are dense (one layer): the same block stride, in bytes.
-  if (!encode_pool_map(&c->tmap_k, k_pool, num_blocks, num_kv_heads, head_dim, 1, c->args.block_stride) ||
-      !encode_pool_map(&c->tmap_v, v_pool, num_blocks, num_kv_heads, head_dim, 1, c->args.block_stride))
+  if (!encode_pool_map(&c->tmap_k, k_pool, num_blocks, kBlockSize, num_kv_heads, head_dim, 1, c->args.block_stride) ||
+      !encode_pool_map(&c->tmap_v, v_pool, num_blocks, kBlockSize, num_kv_heads, head_dim, 1, c->args.block_stride))
     return PKV_ERR_CUDA;
   return PKV_OK;
 }

@@ -46,7 +46,8 @@ __global__ void __launch_bounds__(256) write_cache_kernel(WriteCacheArgs a) {
       if (v == 0 && which == 0) flag(a.dev_status, 1u);
       continue;
     }
-    uint16_t* dst = (which ? a.v_pool : a.k_pool) + (slot / kBlockSize) * a.block_stride + (slot % kBlockSize) * a.row_elems;
+    uint16_t* dst = (which ? a.v_pool : a.k_pool) + (slot >> a.block_shift) * a.block_stride +
+                    (slot & ((1 << a.block_shift) - 1)) * a.row_elems;
     reinterpret_cast<uint4*>(dst)[v] = val;
   }
 }

@@ -35,10 +35,13 @@ using namespace dev;
 // One unit (sequence s, KV head g, partition p) served by U of the CTA's NW
 // warps; `raw_len` is the sequence's context length as read and `first`
 // the warp's first table entries (first_entries<U>).
-template <int D, bool BF16, int NW, int U, int NST, bool FUSED>
+// B8: 8-token blocks (a tile spans two blocks: `first2` holds the second
+// entries); otherwise blocks of 16 tokens or more (a tile is rows
+// [row0, row0 + 16) of one block).
+template <int D, bool BF16, int NW, int U, int NST, bool FUSED, bool B8>
 __device__ __forceinline__ void partition_unit(const DecodeArgs& a, const CUtensorMap* tmap_k,
                                                const CUtensorMap* tmap_v, uint8_t* smem, int64_t unit,
-                                               int raw_len, int first, int warp, int lane) {
+                                               int raw_len, int first, int first2, int warp, int lane) {
   using Geom = TileGeom<D>;
   using Att = WarpAttention<D, BF16>;
   static_assert(NW % U == 0 && NW / U <= 15, "named barriers 1..15, one per unit of the CTA");
@@ -64,15 +67,16 @@ __device__ __forceinline__ void partition_unit(const DecodeArgs& a, const CUtens
   at.load_q(a.q + (static_cast<int64_t>(s) * a.num_q_heads + g * G) * D, G, lane);
   const int tok0 = part * PS;
   const int ntok = max(0, min(L - tok0, PS));
-  const int nblk = (ntok + kBlockSize - 1) / kBlockSize;
-  // The warp's tiles are the partition's blocks sub, sub + U, sub + 2U, ...
+  const int nblk = (ntok + kTile - 1) / kTile;  // 16-token tiles of the partition
+  // The warp's tiles are the partition's tiles sub, sub + U, sub + 2U, ...
   // Their table entries sit in registers 32 at a time (lane j: the warp's
   // tile j of the chunk); the next chunk is fetched one chunk ahead of use.
   const int cnt = nblk > sub ? (nblk - sub + U - 1) / U : 0;
-  const int32_t* tbl = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + tok0 / kBlockSize;
-  auto entry = [&](int i) { return i < cnt ? __ldg(tbl + i * U + sub) : 0; };
+  const int tile0 = tok0 / kTile;
+  auto entry = [&](int i, int second) { return i < cnt ? tile_entry(a, s, tile0 + i * U + sub, second) : 0; };
   int phys_cur = first;
-  int phys_next = entry(32 + lane);
+  int phys_next = entry(32 + lane, 0);
+  int phys2_cur = first2, phys2_next = B8 ? entry(32 + lane, 1) : 0;
 
   WarpRing<D, NST> ring{smem_u32(smem + static_cast<size_t>(warp) * NST * Geom::kStageBytes),
                         smem_u32(smem + static_cast<size_t>(NW) * NST * Geom::kStageBytes) + 8 * NST * warp};
@@ -82,18 +86,37 @@ __device__ __forceinline__ void partition_unit(const DecodeArgs& a, const CUtens
   auto issue = [&](int j) {  // all lanes call
     if ((j & 31) == 0 && j > 0) {
       phys_cur = phys_next;
-      phys_next = entry(j + 32 + lane);
+      phys_next = entry(j + 32 + lane, 0);
+      if constexpr (B8) {
+        phys2_cur = phys2_next;
+        phys2_next = entry(j + 32 + lane, 1);
+      }
     }
     const int st = j % NST;
+    const int t = j * U + sub;  // tile index within the partition
     int phys = __shfl_sync(kFull, phys_cur, j & 31);
-    if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
+    int phys2 = -1, row0 = 0;
+    bool bad = static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks);
+    if constexpr (B8) {
+      // The tile's rows 8-15 come from the next block when the sequence
+      // reaches them; otherwise the first block is loaded again (masked).
+      phys2 = __shfl_sync(kFull, phys2_cur, j & 31);
+      if (ntok - t * kTile > 8)
+        bad |= static_cast<unsigned>(phys2) >= static_cast<unsigned>(a.num_blocks);
+      else
+        phys2 = phys;
+    } else {
+      row0 = ((tile0 + t) * kTile) & ((1 << a.block_shift) - 1);
+    }
+    if (bad) {
       if (lane == 0) flag(a.dev_status, 4u);  // PKV_DEV_ERR_BLOCK
       phys = 0;
+      if constexpr (B8) phys2 = 0;
       bad_stage |= 1u << st;
     } else {
       bad_stage &= ~(1u << st);
     }
-    ring.issue(j, phys, g, tmap_k, tmap_v, lane);
+    ring.issue(j, phys, phys2, row0, g, tmap_k, tmap_v, lane);
   };
 
   at.reset();
@@ -114,9 +137,9 @@ __device__ __forceinline__ void partition_unit(const DecodeArgs& a, const CUtens
       if (lane == 0) flag(a.dev_status, 16u);  // PKV_DEV_ERR_TIMEOUT; the output is undefined
       break;
     }
-    const int t = i * U + sub;  // block index within the partition
+    const int t = i * U + sub;  // tile index within the partition
     const int st = i % NST;
-    const int nv = ((bad_stage >> st) & 1) ? 0 : min(kBlockSize, ntok - t * kBlockSize);
+    const int nv = ((bad_stage >> st) & 1) ? 0 : min(kTile, ntok - t * kTile);
     const uint32_t sK = ring.k_tile(i);
     if (owns_new && t == nblk - 1 && nt.commit(a, g, lane)) nt.patch(sK, sK + Geom::kTileBytes, lane);
     at.tile(sK, sK + Geom::kTileBytes, nv, a.scale_log2, lane);
@@ -148,7 +171,7 @@ __device__ __forceinline__ void partition_unit(const DecodeArgs& a, const CUtens
 // Two-warp CTAs.  With one warp per unit (a.unit_warps == 1) CTA b serves
 // units 2b and 2b + 1; with two (== 2) it serves unit b with both warps.
 // A unit's length and first table entries go out together.
-template <int D, bool BF16, int NST, bool FUSED>
+template <int D, bool BF16, int NST, bool FUSED, bool B8>
 __global__ void __launch_bounds__(64) decode_partitions_kernel(
     const DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
     const __grid_constant__ CUtensorMap tmap_v) {
@@ -162,11 +185,13 @@ __global__ void __launch_bounds__(64) decode_partitions_kernel(
   auto seq_of = [&](int64_t u) { return static_cast<int>((u / a.num_kv_heads) % a.num_seqs); };
   if (a.unit_warps == 2) {
     if (unit2 < units)
-      partition_unit<D, BF16, 2, 2, NST, FUSED>(a, &tmap_k, &tmap_v, smem, unit2, a.context_lens[seq_of(unit2)],
-                                                first_entries<2>(a, unit2, warp, lane), warp, lane);
+      partition_unit<D, BF16, 2, 2, NST, FUSED, B8>(a, &tmap_k, &tmap_v, smem, unit2, a.context_lens[seq_of(unit2)],
+                                                    first_entries<2>(a, unit2, warp, lane),
+                                                    B8 ? first_entries<2>(a, unit2, warp, lane, 1) : 0, warp, lane);
   } else if (unit1 < units) {
-    partition_unit<D, BF16, 2, 1, NST, FUSED>(a, &tmap_k, &tmap_v, smem, unit1, a.context_lens[seq_of(unit1)],
-                                              first_entries<1>(a, unit1, 0, lane), warp, lane);
+    partition_unit<D, BF16, 2, 1, NST, FUSED, B8>(a, &tmap_k, &tmap_v, smem, unit1, a.context_lens[seq_of(unit1)],
+                                                  first_entries<1>(a, unit1, 0, lane),
+                                                  B8 ? first_entries<1>(a, unit1, 0, lane, 1) : 0, warp, lane);
   }
 }
 
@@ -274,13 +299,13 @@ int partition_warp_slots(const void* kern, size_t smem) {
   return slots;
 }
 
-template <int D, bool BF16, bool FUSED>
+template <int D, bool BF16, bool FUSED, bool B8>
 cudaError_t launch_partitions_t(const DecodeArgs& a_in, const CUtensorMap& tk, const CUtensorMap& tv,
                                 cudaStream_t stream) {
   using Geom = TileGeom<D>;
   constexpr int NST = kStages;
   const size_t smem = 2 * NST * Geom::kStageBytes + 2 * NST * 8;
-  auto kern = decode_partitions_kernel<D, BF16, NST, FUSED>;
+  auto kern = decode_partitions_kernel<D, BF16, NST, FUSED, B8>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   DecodeArgs a = a_in;
@@ -301,8 +326,11 @@ cudaError_t launch_partitions_t(const DecodeArgs& a_in, const CUtensorMap& tk, c
 template <int D, bool BF16>
 cudaError_t launch_partitions_f(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                 cudaStream_t stream) {
-  return a.k_new ? launch_partitions_t<D, BF16, true>(a, tk, tv, stream)
-                 : launch_partitions_t<D, BF16, false>(a, tk, tv, stream);
+  if (a.block_shift == 3)
+    return a.k_new ? launch_partitions_t<D, BF16, true, true>(a, tk, tv, stream)
+                   : launch_partitions_t<D, BF16, false, true>(a, tk, tv, stream);
+  return a.k_new ? launch_partitions_t<D, BF16, true, false>(a, tk, tv, stream)
+                 : launch_partitions_t<D, BF16, false, false>(a, tk, tv, stream);
 }
 
 }  // namespace

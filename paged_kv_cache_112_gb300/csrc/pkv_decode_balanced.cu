@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     } else {
       bad_stage &= ~(1u << st);
     }
-    ring.issue(j, phys, ic.g, &tmap_k, &tmap_v, lane);
+    ring.issue(j, phys, -1, 0, ic.g, &tmap_k, &tmap_v, lane);
     advance(ic, pre, S, Hkv);
   };
 

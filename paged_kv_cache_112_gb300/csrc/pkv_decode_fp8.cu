@@ -419,7 +419,7 @@ __device__ __forceinline__ void partition_unit_fp8(const DecodeArgs& a, const CU
     } else {
       bad_stage &= ~(1u << st);
     }
-    ring.issue(j, phys, g, tmap_k, tmap_v, lane);
+    ring.issue(j, phys, -1, 0, g, tmap_k, tmap_v, lane);
   };
 
   at.reset();

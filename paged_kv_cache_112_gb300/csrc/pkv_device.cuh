@@ -163,7 +163,7 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, float v, int d
 // Context length of sequence s clamped to what the table and the host bound
 // allow; out-of-range values set PKV_DEV_ERR_LENGTH when `report`.
 __device__ __forceinline__ int clamped_len(const DecodeArgs& a, int s, bool report) {
-  const int cap = min(a.max_context_len, a.max_blocks_per_seq * kBlockSize);
+  const int cap = min(a.max_context_len, a.max_blocks_per_seq << a.block_shift);
   const int L = a.context_lens[s];
   if (L >= 0 && L <= cap) return L;
   if (report) flag(a.dev_status, 8u);
@@ -172,7 +172,7 @@ __device__ __forceinline__ int clamped_len(const DecodeArgs& a, int s, bool repo
 
 // The same for a length already read.
 __device__ __forceinline__ int clamp_len(const DecodeArgs& a, int L, bool report) {
-  const int cap = min(a.max_context_len, a.max_blocks_per_seq * kBlockSize);
+  const int cap = min(a.max_context_len, a.max_blocks_per_seq << a.block_shift);
   if (L >= 0 && L <= cap) return L;
   if (report) flag(a.dev_status, 8u);
   return L < 0 ? 0 : cap;
@@ -197,7 +197,7 @@ template <int D, int EB = 2>
 struct TileGeom {
   static_assert((D * EB) % 128 == 0, "a head row is whole 128-byte lines");
   static constexpr int kHalves = D * EB / 128;  // 128-byte lines per head row
-  static constexpr int kTileBytes = kBlockSize * D * EB;
+  static constexpr int kTileBytes = kTile * D * EB;
   static constexpr int kStageBytes = 2 * kTileBytes;
 };
 
@@ -217,11 +217,14 @@ struct WarpRing {
     __syncwarp();
   }
 
-  // Lane 0 issues the K and V copies of tile number j (stage j % NST) for
-  // physical block `phys`, KV head g (tensor maps: {element line, head
-  // line, row in block, block}).
-  __device__ __forceinline__ void issue(int j, int phys, int g, const CUtensorMap* tk, const CUtensorMap* tv,
-                                        int lane) const {
+  // Lane 0 issues the K and V copies of tile number j (stage j % NST), KV
+  // head g (tensor maps: {element line, head line, row in block, block}):
+  // rows [row0, row0 + 16) of block `phys` (blocks of >= 16 tokens; box of
+  // 16 rows), or, when phys2 >= 0 (8-token blocks; box of 8 rows), block
+  // phys then block phys2, the second landing 8 rows (1024 bytes) further,
+  // in the same swizzle phase as a 16-row box.
+  __device__ __forceinline__ void issue(int j, int phys, int phys2, int row0, int g, const CUtensorMap* tk,
+                                        const CUtensorMap* tv, int lane) const {
     if (lane != 0) return;
     const int st = j % NST;
     const uint32_t b = bar + 8 * st;
@@ -229,8 +232,12 @@ struct WarpRing {
     mbar_arrive_expect_tx(b, Geom::kStageBytes);
 #pragma unroll
     for (int h = 0; h < Geom::kHalves; ++h) {
-      tma_load_4d(dst + h * 2048, tk, 0, g * Geom::kHalves + h, 0, phys, b);
-      tma_load_4d(dst + Geom::kTileBytes + h * 2048, tv, 0, g * Geom::kHalves + h, 0, phys, b);
+      tma_load_4d(dst + h * 2048, tk, 0, g * Geom::kHalves + h, row0, phys, b);
+      tma_load_4d(dst + Geom::kTileBytes + h * 2048, tv, 0, g * Geom::kHalves + h, row0, phys, b);
+      if (phys2 >= 0) {
+        tma_load_4d(dst + h * 2048 + 1024, tk, 0, g * Geom::kHalves + h, 0, phys2, b);
+        tma_load_4d(dst + Geom::kTileBytes + h * 2048 + 1024, tv, 0, g * Geom::kHalves + h, 0, phys2, b);
+      }
     }
   }
 
@@ -246,20 +253,27 @@ struct WarpRing {
   __device__ __forceinline__ uint32_t k_tile(int i) const { return buf + (i % NST) * Geom::kStageBytes; }
 };
 
+// Table entry of tile T (16 tokens from 16T) of sequence s: the block
+// holding its first token (second = 1: the block holding its token 8, for
+// 8-token blocks).  0 for an index past the table row (such a tile's
+// tokens are beyond the length; the entry is not used).
+__device__ __forceinline__ int tile_entry(const DecodeArgs& a, int s, int T, int second) {
+  const int blk = ((T * kTile) >> a.block_shift) + second;
+  return blk < a.max_blocks_per_seq ? __ldg(a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + blk)
+                                    : 0;
+}
+
 // The warp's first 32 table entries of unit `unit` (KV head, sequence,
 // partition; partition-major) served by U warps (lane j: the partition's
-// block j * U + sub), read before the length is known: every read index lies
-// in the partition and in the table row; entries past the sequence's blocks
-// are never used.
+// tile j * U + sub), read before the length is known: every read index lies
+// in the table row; entries past the sequence's tiles are never used.
 template <int U>
-__device__ __forceinline__ int first_entries(const DecodeArgs& a, int64_t unit, int sub, int lane) {
+__device__ __forceinline__ int first_entries(const DecodeArgs& a, int64_t unit, int sub, int lane, int second = 0) {
   const int Hkv = a.num_kv_heads;
   const int s = static_cast<int>((unit / Hkv) % a.num_seqs);
   const int part = static_cast<int>(unit / Hkv / a.num_seqs);
-  const int blk = part * (a.partition_size / kBlockSize), e = lane * U + sub;
-  return (e < a.partition_size / kBlockSize && blk + e < a.max_blocks_per_seq)
-             ? __ldg(a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + blk + e)
-             : 0;
+  const int tiles = a.partition_size / kTile, e = lane * U + sub;
+  return e < tiles ? tile_entry(a, s, part * tiles + e, second) : 0;
 }
 
 // ---------------------------------------------------- fused new-token write
@@ -275,7 +289,8 @@ __device__ __forceinline__ int first_entries(const DecodeArgs& a, int64_t unit, 
 template <int D>
 struct NewToken {
   uint4 val;
-  int row = -1;
+  int row = -1;     // row of position L-1 in its 16-token tile
+  int offset = -1;  // offset of position L-1 in its block
   int slot = -1;
   int last_phys = -1;
 
@@ -283,12 +298,14 @@ struct NewToken {
   // behind the tiles the warp streams meanwhile).
   __device__ __forceinline__ void prefetch(const DecodeArgs& a, int s, int g, int L, int lane) {
     slot = a.slot_mapping[s];
-    last_phys = L > 0 ? __ldg(a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + (L - 1) / kBlockSize)
+    last_phys = L > 0 ? __ldg(a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq +
+                              ((L - 1) >> a.block_shift))
                       : -1;
     const int c = lane & 15;
     const uint16_t* src = (lane < 16 ? a.k_new : a.v_new) + static_cast<int64_t>(s) * a.new_stride + g * D + c * 8;
     val = (c < D / 8) ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
-    row = L > 0 ? (L - 1) % kBlockSize : -1;
+    row = L > 0 ? (L - 1) % kTile : -1;
+    offset = L > 0 ? (L - 1) & ((1 << a.block_shift) - 1) : -1;
   }
 
   // Checks that the slot is position L-1 through the table; if so stores the
@@ -301,7 +318,7 @@ struct NewToken {
       return false;
     }
     const bool ok = static_cast<unsigned>(last_phys) < static_cast<unsigned>(a.num_blocks) &&
-                    slot == last_phys * kBlockSize + row;
+                    slot == (last_phys << a.block_shift) + offset;
     if (!ok) {
       if (lane == 0) flag(a.dev_status, 1u);  // PKV_DEV_ERR_SLOT
       row = -1;
@@ -309,8 +326,8 @@ struct NewToken {
     }
     const int c = lane & 15;
     if (c < D / 8) {
-      uint16_t* dst = (lane < 16 ? a.k_pool_w : a.v_pool_w) + (slot / kBlockSize) * a.block_stride +
-                      static_cast<int64_t>(row) * a.num_kv_heads * D + g * D + c * 8;
+      uint16_t* dst = (lane < 16 ? a.k_pool_w : a.v_pool_w) + (slot >> a.block_shift) * a.block_stride +
+                      static_cast<int64_t>(offset) * a.num_kv_heads * D + g * D + c * 8;
       *reinterpret_cast<uint4*>(dst) = val;
     }
     return true;
@@ -552,7 +569,7 @@ struct WarpAttention : SoftmaxState<D / 16> {
     // V rows past the valid tokens may hold anything (even NaN): zero them in
     // the A fragment (lane holds tokens 2tq, 2tq+1 and 8+2tq, 9+2tq).
     uint32_t m01 = kFull, m23 = kFull;
-    if (nv < kBlockSize) {
+    if (nv < kTile) {
       m01 = (2 * tq < nv ? 0x0000ffffu : 0u) | (2 * tq + 1 < nv ? 0xffff0000u : 0u);
       m23 = (2 * tq + 8 < nv ? 0x0000ffffu : 0u) | (2 * tq + 9 < nv ? 0xffff0000u : 0u);
     }

@@ -10,7 +10,10 @@
 
 namespace pkv {
 
-constexpr int kBlockSize = 16;  // tokens per KV block
+constexpr int kBlockSize = 16;  // tokens per KV block: the default, and the only size of FP8 pools and the
+                                // balanced split
+constexpr int kTile = 16;       // tokens per shared-memory tile (the MMA's 16 rows); a block of B tokens
+                                // is B/16 tiles (B >= 16) or half a tile (B = 8)
 
 struct WriteCacheArgs {
   const uint16_t* k_new;
@@ -25,6 +28,7 @@ struct WriteCacheArgs {
   int64_t block_stride;  // pool elements between consecutive blocks (>= block_size * row_elems)
   int num_tokens;
   int row_elems;      // num_kv_heads * head_dim
+  int block_shift;    // log2(block_size)
 };
 
 // FP8 pools: e4m3 codes plus one float scale per (block, KV head) for K and
@@ -97,6 +101,7 @@ struct DecodeArgs {
   int partition_size;  // tokens, multiple of 16
   int max_parts;
   int max_context_len;
+  int block_shift;       // log2(tokens per block): 3, 4, 5 or 6
   int64_t block_stride;  // pool elements between consecutive blocks (the fused write's addressing)
   float scale_log2;    // scale * log2(e)
   int out_dtype;       // pkv_dtype

@@ -227,8 +227,9 @@ def make_workload(cfg: int, *, poison: bool = False, seed: int | None = None, **
     """Build the seeded workload of recipe `cfg` (1..5).
 
     Seed defaults to the recipe number.  `overrides` may change num_seqs,
-    lens, head counts, head_dim, dtype, num_blocks, pool_factor or
-    partition_size (used by tests for small variants of a recipe).
+    lens, head counts, head_dim, dtype, num_blocks, pool_factor,
+    partition_size or block_size (used by tests for small variants of a
+    recipe; the recipes use 16-token blocks).
     With poison=True every pool slot that holds no live token (unused blocks,
     tail slots past a sequence's length, the slot the new token goes to) is
     filled with NaN.
@@ -236,7 +237,7 @@ def make_workload(cfg: int, *, poison: bool = False, seed: int | None = None, **
     spec = dict(CONFIGS[cfg])
     spec.update(overrides)
     rng = np.random.default_rng(cfg if seed is None else seed)
-    B = BLOCK_SIZE
+    B = int(spec.get("block_size", BLOCK_SIZE))
     S = spec["num_seqs"]
     Hq, Hkv, D = spec["num_q_heads"], spec["num_kv_heads"], spec["head_dim"]
     dtype = spec["dtype"]

@@ -28,9 +28,10 @@ def _wid(b, dtype):
     return P.bits_to_f32(b, dtype).astype(np.float64)
 
 
-def paged_from_contiguous(K, V, num_blocks, rng, dtype):
+def paged_from_contiguous(K, V, num_blocks, rng, dtype, B=B):
     """Scatter per-sequence contiguous K/V ([L, H_kv, D] bit arrays) into a pool
-    through randomly drawn physical blocks.  Unused slots hold NaN."""
+    of B-token blocks through randomly drawn physical blocks.  Unused slots
+    hold NaN."""
     Hkv, D = K[0].shape[1], K[0].shape[2]
     nan = P.NAN_BITS[dtype]
     kp = np.full((num_blocks, B, Hkv, D), nan, dtype=np.uint16)
@@ -49,13 +50,32 @@ def paged_from_contiguous(K, V, num_blocks, rng, dtype):
     return kp, vp, tables, np.asarray(lens, dtype=np.int32)
 
 
-def _rand_problem(rng, lens, Hq, Hkv, D, dtype, nb_extra=5):
+def _rand_problem(rng, lens, Hq, Hkv, D, dtype, nb_extra=5, B=B):
     K = [_bits(rng.standard_normal((L, Hkv, D)), dtype) for L in lens]
     V = [_bits(rng.standard_normal((L, Hkv, D)), dtype) for L in lens]
     q = _bits(rng.standard_normal((len(lens), Hq, D)), dtype)
     nb = sum(-(-L // B) for L in lens) + nb_extra
-    kp, vp, bt, cl = paged_from_contiguous(K, V, nb, rng, dtype)
+    kp, vp, bt, cl = paged_from_contiguous(K, V, nb, rng, dtype, B)
     return q, K, V, kp, vp, bt, cl
+
+
+def pin_block_sizes(attn, dtype="bf16"):
+    """Blocks of 8, 32 and 64 tokens: torch SDPA in fp64 on the contiguous K/V
+    the pool was built from ("gpu_paged_kv_cache", "Fixed-size blocks": the
+    table, not address arithmetic, resolves position, whatever B is)."""
+    rng = np.random.default_rng(17)
+    lens = [1, 7, 8, 9, 33, 64, 65, 130]
+    Hq, Hkv, D = 4, 2, 32
+    for bs in (8, 32, 64):
+        q, K, V, kp, vp, bt, cl = _rand_problem(rng, lens, Hq, Hkv, D, dtype, B=bs)
+        got = attn(q, kp, vp, bt, cl, 0.3, dtype)
+        G = Hq // Hkv
+        for s, L in enumerate(lens):
+            qs = torch.from_numpy(_wid(q[s], dtype)).reshape(1, Hq, 1, D)
+            ks = torch.from_numpy(_wid(K[s], dtype)).permute(1, 0, 2).repeat_interleave(G, 0).unsqueeze(0)
+            vs = torch.from_numpy(_wid(V[s], dtype)).permute(1, 0, 2).repeat_interleave(G, 0).unsqueeze(0)
+            ref = torch.nn.functional.scaled_dot_product_attention(qs, ks, vs, scale=0.3)[0, :, 0].numpy()
+            assert np.max(np.abs(got[s] - ref)) <= 1e-12, (bs, s)
 
 
 def pin_brute_force(attn):
@@ -228,6 +248,6 @@ def pin_poison(attn):
     assert np.array_equal(a, b)
 
 
-ALL_PINS = [pin_brute_force, pin_sdpa, pin_single_token, pin_zero_scale_mean, pin_equal_keys_mean,
+ALL_PINS = [pin_brute_force, pin_sdpa, pin_block_sizes, pin_single_token, pin_zero_scale_mean, pin_equal_keys_mean,
             pin_dominant_key, pin_grouping, pin_len_boundary, pin_permutation_invariance,
             pin_shared_prefix, pin_poison]

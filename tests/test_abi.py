@@ -80,7 +80,9 @@ def _decode(lib, **kw):
 
 
 def test_decode_argument_validation(lib):
-    assert _decode(lib, B=8) == pkv.PKV_ERR_UNSUPPORTED
+    assert _decode(lib, B=24) == pkv.PKV_ERR_UNSUPPORTED  # block sizes: 8, 16, 32, 64
+    assert _decode(lib, B=128) == pkv.PKV_ERR_UNSUPPORTED
+    assert _decode(lib, B=32, ps=pkv.PARTITION_BALANCED) == pkv.PKV_ERR_UNSUPPORTED  # balanced split: 16 only
     assert _decode(lib, D=96) == pkv.PKV_ERR_UNSUPPORTED
     assert _decode(lib, Hq=6, Hkv=4) == pkv.PKV_ERR_UNSUPPORTED  # not a whole group
     assert _decode(lib, Hq=32, Hkv=2) == pkv.PKV_ERR_UNSUPPORTED  # group 16 > 8
@@ -103,7 +105,7 @@ def test_write_and_copy_argument_validation(lib):
     w = lambda **kw: lib.pkv_write_cache(kw.get("kn", FAKE), kw.get("vn", FAKE), FAKE, FAKE, kw.get("bs", 0), FAKE,
                                          kw.get("T", 4), kw.get("stride", 0), kw.get("Hkv", 8), kw.get("D", 128),
                                          kw.get("B", 16), 100, kw.get("dt", pkv.PKV_F16), None, None)
-    assert w(B=32) == pkv.PKV_ERR_UNSUPPORTED
+    assert w(B=12) == pkv.PKV_ERR_UNSUPPORTED
     assert w(T=-1) == pkv.PKV_ERR_INVALID_ARG
     assert w(kn=None) == pkv.PKV_ERR_INVALID_ARG
     assert w(kn=FAKE + 2) == pkv.PKV_ERR_INVALID_ARG  # rows must be 16-byte aligned
@@ -113,7 +115,7 @@ def test_write_and_copy_argument_validation(lib):
     assert w(bs=16 * 8 * 128 - 8) == pkv.PKV_ERR_INVALID_ARG  # block stride below a dense block
     c = lambda **kw: lib.pkv_copy_blocks(FAKE, FAKE, kw.get("pairs", FAKE), kw.get("P", 3), kw.get("layers", 1), 8,
                                          128, kw.get("B", 16), 100, pkv.PKV_BF16, None, None)
-    assert c(B=8) == pkv.PKV_ERR_UNSUPPORTED
+    assert c(B=12) == pkv.PKV_ERR_UNSUPPORTED
     assert c(layers=0) == pkv.PKV_ERR_INVALID_ARG
     assert c(pairs=None) == pkv.PKV_ERR_INVALID_ARG
     assert c(P=0) == pkv.PKV_OK
