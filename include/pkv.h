@@ -56,7 +56,8 @@ typedef enum pkv_status {
   PKV_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned pointer */
   PKV_ERR_UNSUPPORTED = 2,   /* block_size != 16, head_dim not 64/128, group > 8 ... */
   PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than pkv_decode_workspace_bytes */
-  PKV_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed */
+  PKV_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+  PKV_ERR_OUT_OF_BLOCKS = 5  /* block manager: not enough free blocks (pool exhausted) */
 } pkv_status;
 
 typedef enum pkv_dtype { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 } pkv_dtype;
@@ -409,6 +410,87 @@ pkv_status pkv_decode_step_partitions_fp8(void* out, const void* q, const void* 
                                           int partition_size, int max_context_len, void* workspace,
                                           size_t workspace_bytes, pkv_dtype q_dtype,
                                           pkv_dtype out_dtype, int32_t* dev_status, void* stream);
+
+/*
+ * ------------------------------------------------------------ block manager
+ *
+ * Host-side allocator of a pool's blocks (host functions, no GPU call): the
+ * free list and reference counts of [P4 section 4]; prefix sharing by a
+ * chained block hash [P1 "Prefix sharing, reference counts, and
+ * copy-on-write"; P2 section 04]; copy-on-write of a shared tail block;
+ * LRU eviction of cached blocks nobody references [P2 section 04]; a
+ * watermark of blocks admissions may not take and swap bookkeeping [P1
+ * "Reclaiming memory: swap versus recompute"].  It produces what the device
+ * entry points consume: block-table rows, slot mappings and copy-on-write
+ * pairs.  Calls on one manager are serialised by an internal lock.
+ *
+ * Functions returning int return a count (>= 0) on success or a negative
+ * pkv_status: -PKV_ERR_INVALID_ARG (unknown or duplicate sequence, null or
+ * short buffer, wrong state) or -PKV_ERR_OUT_OF_BLOCKS (nothing was changed).
+ *
+ * Prefix cache: a full block (block_size tokens) is keyed by a hash of its
+ * tokens chained onto the previous block's key, starting from the
+ * request's extra_key (adapter identity, multimodal inputs: anything else
+ * that changes the KV values), so a match means an identical history from
+ * position 0.  A hit is also compared token for token.  Cached blocks with
+ * no reference stay reusable until allocation needs them, least recently
+ * used first; referenced blocks are never evicted.
+ */
+typedef struct pkv_bm pkv_bm;
+
+/* A manager of num_blocks blocks of block_size tokens; watermark_blocks are
+ * kept back from admissions (add_sequence, swap_in).  NULL on bad sizes. */
+pkv_bm* pkv_bm_create(int num_blocks, int block_size, int watermark_blocks);
+void pkv_bm_destroy(pkv_bm* bm);
+
+/* Blocks that can be handed out (free + cached with no reference). */
+int pkv_bm_available_blocks(pkv_bm* bm);
+/* Blocks registered in the prefix cache (referenced or not). */
+int pkv_bm_cached_blocks(pkv_bm* bm);
+/* Reference count of a block. */
+int pkv_bm_block_refcount(pkv_bm* bm, int block);
+
+/*
+ * Admits sequence seq_id with its prompt (host int32 tokens[num_tokens]):
+ * the longest run of whole blocks from position 0 found in the prefix cache
+ * is shared (refcount bump), the rest is allocated.  slots[num_tokens]
+ * (host) receives each token's slot for pkv_write_cache (block * block_size
+ * + offset), or -1 for a token already cached.  Returns the number of
+ * cached prompt tokens (a multiple of block_size).
+ */
+int pkv_bm_add_sequence(pkv_bm* bm, int64_t seq_id, const int32_t* tokens, int num_tokens,
+                        uint64_t extra_key, int32_t* slots);
+
+/* child := a copy of parent sharing every block (parallel sampling, beams). */
+int pkv_bm_fork(pkv_bm* bm, int64_t parent, int64_t child);
+
+/*
+ * Appends one token (decode): *slot receives its slot; a fresh block is
+ * taken when the tail is full; when the tail is shared (refcount > 1) it is
+ * copied on write: a fresh block replaces it in the table and (*cow_src,
+ * *cow_dst) is the pair for pkv_copy_blocks (else both -1).  A block that
+ * becomes full is registered in the prefix cache.
+ */
+int pkv_bm_append(pkv_bm* bm, int64_t seq_id, int32_t token, int32_t* slot, int32_t* cow_src,
+                  int32_t* cow_dst);
+
+/* Releases a sequence (its blocks' references). */
+int pkv_bm_free_sequence(pkv_bm* bm, int64_t seq_id);
+
+/* Tokens in a sequence; its block-table row into out[capacity] (returns the
+ * number of blocks). */
+int pkv_bm_seq_len(pkv_bm* bm, int64_t seq_id);
+int pkv_bm_block_table(pkv_bm* bm, int64_t seq_id, int32_t* out, int capacity);
+
+/*
+ * Swap: pkv_bm_swap_out lists the sequence's blocks in blocks[] (logical
+ * order; move them to host memory with pkv_swap_blocks before they are
+ * reused) and releases them; the sequence keeps its tokens.
+ * pkv_bm_swap_in takes fresh blocks for it (blocks[i] receives logical
+ * block i: move host block i there) and returns their number.
+ */
+int pkv_bm_swap_out(pkv_bm* bm, int64_t seq_id, int32_t* blocks, int capacity);
+int pkv_bm_swap_in(pkv_bm* bm, int64_t seq_id, int32_t* blocks, int capacity);
 
 /* Static string naming a status code.  Host function. */
 const char* pkv_status_string(pkv_status status);

@@ -15,7 +15,7 @@ import torch
 
 from . import build as _build
 
-PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA = range(5)
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA, PKV_ERR_OUT_OF_BLOCKS = range(6)
 PKV_F32, PKV_F16, PKV_BF16 = 0, 1, 2
 PARTITION_BALANCED = -1  # partition_size selecting the library's balanced split
 DEV_ERR_SLOT, DEV_ERR_PAIR, DEV_ERR_BLOCK, DEV_ERR_LENGTH, DEV_ERR_TIMEOUT, DEV_ERR_SMEM = 1, 2, 4, 8, 16, 32
@@ -55,6 +55,24 @@ _SIGS["pkv_decode_step_fp8"] = ([_c_void_p] * 4 + [_c_int64] + [_c_void_p] * 5 +
                                                 _c_void_p, _c_void_p])
 _SIGS["pkv_decode_step_partitions_fp8"] = _SIGS["pkv_decode_step_fp8"]
 
+_BM_SIGS = {
+    "pkv_bm_create": ([ctypes.c_int] * 3, ctypes.c_void_p),
+    "pkv_bm_destroy": ([ctypes.c_void_p], None),
+    "pkv_bm_available_blocks": ([ctypes.c_void_p], ctypes.c_int),
+    "pkv_bm_cached_blocks": ([ctypes.c_void_p], ctypes.c_int),
+    "pkv_bm_block_refcount": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
+    "pkv_bm_add_sequence": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64,
+                             ctypes.c_void_p], ctypes.c_int),
+    "pkv_bm_fork": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64], ctypes.c_int),
+    "pkv_bm_append": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32] + [ctypes.POINTER(ctypes.c_int32)] * 3,
+                      ctypes.c_int),
+    "pkv_bm_free_sequence": ([ctypes.c_void_p, ctypes.c_int64], ctypes.c_int),
+    "pkv_bm_seq_len": ([ctypes.c_void_p, ctypes.c_int64], ctypes.c_int),
+    "pkv_bm_block_table": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
+    "pkv_bm_swap_out": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
+    "pkv_bm_swap_in": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
+}
+
 _LIB = None
 
 
@@ -82,6 +100,10 @@ def load(build_if_missing: bool = False):
         fn.argtypes = argtypes
         fn.restype = ctypes.c_size_t if name == "pkv_decode_workspace_bytes" else (
             ctypes.c_char_p if name == "pkv_status_string" else ctypes.c_int)
+    for name, (argtypes, restype) in _BM_SIGS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = argtypes
+        fn.restype = restype
     _LIB = lib
     return lib
 
@@ -397,3 +419,99 @@ def swap_blocks(dst_k, dst_v, src_k, src_v, pairs, *, status=None, stream=None):
     _check(load().pkv_swap_blocks(_ptr(dst_k), _ptr(dst_v), d_stride, int(dst_k.shape[0]), _ptr(src_k), _ptr(src_v),
                                   s_stride, int(src_k.shape[0]), d_bytes, _ptr(pairs), int(pairs.shape[0]),
                                   _ptr(status), _stream(stream)), "pkv_swap_blocks")
+
+
+# ------------------------------------------------------------------ block manager
+
+
+class OutOfBlocks(PkvError):
+    """The block manager has not enough free blocks (nothing was changed)."""
+
+
+class BlockManager:
+    """The host block manager of libpkv (pkv_bm_*): free list, reference
+    counts, chained-hash prefix cache with LRU eviction, copy-on-write,
+    watermark and swap bookkeeping.  Produces block-table rows, slot
+    mappings and copy-on-write pairs for the device entry points."""
+
+    def __init__(self, num_blocks: int, block_size: int = 16, watermark_blocks: int = 0):
+        import numpy as np
+
+        self._np = np
+        self._lib = load()
+        self._h = self._lib.pkv_bm_create(int(num_blocks), int(block_size), int(watermark_blocks))
+        if not self._h:
+            raise PkvError("pkv_bm_create: invalid sizes")
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+
+    def close(self):
+        if self._h:
+            self._lib.pkv_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _rc(self, rc: int, what: str) -> int:
+        if rc >= 0:
+            return rc
+        if -rc == PKV_ERR_OUT_OF_BLOCKS:
+            raise OutOfBlocks(what)
+        raise PkvError(f"{what}: {status_string(-rc)}")
+
+    @property
+    def available_blocks(self) -> int:
+        return self._lib.pkv_bm_available_blocks(self._h)
+
+    @property
+    def cached_blocks(self) -> int:
+        return self._lib.pkv_bm_cached_blocks(self._h)
+
+    def refcount(self, block: int) -> int:
+        return self._rc(self._lib.pkv_bm_block_refcount(self._h, int(block)), "refcount")
+
+    def add_sequence(self, seq_id: int, tokens, extra_key: int = 0):
+        """Admits a prompt; returns (cached_tokens, slots int32[n]; -1 for cached tokens)."""
+        np = self._np
+        t = np.ascontiguousarray(tokens, dtype=np.int32).reshape(-1)
+        slots = np.empty(t.size, dtype=np.int32)
+        rc = self._lib.pkv_bm_add_sequence(self._h, int(seq_id), t.ctypes.data, int(t.size),
+                                           int(extra_key) & 0xFFFFFFFFFFFFFFFF, slots.ctypes.data)
+        return self._rc(rc, "add_sequence"), slots
+
+    def fork(self, parent: int, child: int) -> None:
+        self._rc(self._lib.pkv_bm_fork(self._h, int(parent), int(child)), "fork")
+
+    def append(self, seq_id: int, token: int):
+        """Appends one token; returns (slot, (cow_src, cow_dst) or None)."""
+        slot, src, dst = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        self._rc(self._lib.pkv_bm_append(self._h, int(seq_id), int(token), ctypes.byref(slot), ctypes.byref(src),
+                                         ctypes.byref(dst)), "append")
+        return slot.value, ((src.value, dst.value) if src.value >= 0 else None)
+
+    def free(self, seq_id: int) -> None:
+        self._rc(self._lib.pkv_bm_free_sequence(self._h, int(seq_id)), "free_sequence")
+
+    def seq_len(self, seq_id: int) -> int:
+        return self._rc(self._lib.pkv_bm_seq_len(self._h, int(seq_id)), "seq_len")
+
+    def _blocks(self, fn, seq_id, what):
+        np = self._np
+        cap = self.num_blocks
+        out = np.empty(cap, dtype=np.int32)
+        n = self._rc(fn(self._h, int(seq_id), out.ctypes.data, cap), what)
+        return out[:n].copy()
+
+    def block_table(self, seq_id: int):
+        return self._blocks(self._lib.pkv_bm_block_table, seq_id, "block_table")
+
+    def swap_out(self, seq_id: int):
+        """Releases the sequence's blocks; returns them (logical order) for the device-to-host copy."""
+        return self._blocks(self._lib.pkv_bm_swap_out, seq_id, "swap_out")
+
+    def swap_in(self, seq_id: int):
+        """Takes fresh blocks for a swapped-out sequence; returns them (logical order)."""
+        return self._blocks(self._lib.pkv_bm_swap_in, seq_id, "swap_in")

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libpkv.so")
 SOURCES = ["pkv_api.cu", "pkv_cache_ops.cu", "pkv_decode.cu", "pkv_decode_balanced.cu", "pkv_decode_fp8.cu",
-           "pkv_static_ws.cu"]
+           "pkv_static_ws.cu", "pkv_block_manager.cpp"]
 HEADERS = ["pkv_internal.h", "pkv_device.cuh", "pkv_fp8.cuh", os.path.join("..", "..", "include", "pkv.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -48,7 +48,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")  # .cpp: host code through nvcc
         cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

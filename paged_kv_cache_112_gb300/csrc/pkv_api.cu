@@ -745,6 +745,7 @@ const char* pkv_status_string(pkv_status s) {
     case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
     case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
     case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+    case PKV_ERR_OUT_OF_BLOCKS: return "PKV_ERR_OUT_OF_BLOCKS";
   }
   return "PKV_ERR_UNKNOWN";
 }

@@ -1,0 +1,335 @@
+// Host block manager of the paged KV cache: the allocator the decode path
+// serves.  Host code only (no CUDA), part of libpkv's C ABI (pkv_bm_*).
+//
+// What it does, from the pages:
+//  * a free list of interchangeable blocks and per-block reference counts
+//    ("KV Cache & PagedAttention", section 4: alloc pops the free list, a
+//    fork bumps the refcount, the last free returns the block);
+//  * prefix sharing keyed by a chained hash: a full block is immutable and
+//    is keyed by the hash of its tokens together with the hash of the block
+//    before it (and the request's extra key: adapter identity, multimodal
+//    inputs), so a hit certifies an identical token history; on admission
+//    every hit is a refcount bump instead of prefill and allocation
+//    ("gpu_paged_kv_cache", "Prefix sharing, reference counts, and
+//    copy-on-write"; "PagedAttention internals", section 04).  A hit is
+//    also checked token for token, so a hash collision cannot share a block;
+//  * copy-on-write: appending into a block whose refcount exceeds one
+//    allocates a fresh block, reports the (old, new) pair for the device
+//    copy, drops a reference to the old block and repoints the table;
+//  * eviction: blocks nobody references but whose contents are cached stay
+//    reusable until allocation needs them, least recently used first;
+//    referenced blocks are never evicted ("PagedAttention internals",
+//    section 04);
+//  * a watermark of blocks admissions may not take, so that running
+//    sequences can always append ("gpu_paged_kv_cache", "Reclaiming memory:
+//    swap versus recompute"), and swap bookkeeping (release a sequence's
+//    blocks to the host, take fresh ones on resume).
+#include <cstdint>
+#include <cstring>
+#include <list>
+#include <mutex>
+#include <unordered_map>
+#include <vector>
+
+#include "pkv.h"
+
+namespace pkv {
+namespace {
+
+// splitmix64's output function (Vigna), used as the mixing step of the chain.
+uint64_t mix64(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+constexpr uint64_t kGolden = 0x9E3779B97F4A7C15ull;
+
+// Hash of a full block: its tokens chained onto the previous block's hash.
+uint64_t block_hash(uint64_t parent, const int32_t* tokens, int n) {
+  uint64_t h = mix64(parent + kGolden);
+  for (int i = 0; i < n; ++i) h = mix64(h ^ (static_cast<uint64_t>(static_cast<uint32_t>(tokens[i])) + kGolden * (i + 1)));
+  return h;
+}
+
+// The chain's start for a request's extra key.
+uint64_t chain_root(uint64_t extra_key) { return mix64(extra_key ^ kGolden); }
+
+struct Block {
+  int ref = 0;
+  bool cached = false;        // registered in the prefix cache (full, immutable)
+  uint64_t hash = 0;
+  uint64_t parent_hash = 0;
+  std::vector<int32_t> tokens;  // of a cached block, for the exact check on a hit
+  std::list<int>::iterator lru;  // position in the evictable list when ref == 0 and cached
+};
+
+struct Sequence {
+  std::vector<int> table;       // physical blocks, logical order
+  std::vector<int32_t> tokens;  // the whole history
+  uint64_t root = 0;            // chain root (extra key)
+  std::vector<uint64_t> hashes; // hash of each full block
+  bool swapped = false;
+};
+
+}  // namespace
+}  // namespace pkv
+
+struct pkv_bm {
+  std::mutex mu;
+  int num_blocks = 0, block_size = 0, watermark = 0;
+  std::vector<pkv::Block> blocks;
+  std::vector<int> free_list;             // ref == 0 and not cached
+  std::list<int> evictable;               // ref == 0 and cached; front = least recently used
+  std::unordered_map<uint64_t, int> cache;  // block hash -> block
+  std::unordered_map<int64_t, pkv::Sequence> seqs;
+};
+
+namespace pkv {
+namespace {
+
+int available(const pkv_bm* m) { return static_cast<int>(m->free_list.size() + m->evictable.size()); }
+
+// Takes one block for new contents: from the free list, else the least
+// recently used evictable cached block (dropped from the cache).  -1 if none.
+int take_block(pkv_bm* m) {
+  int b;
+  if (!m->free_list.empty()) {
+    b = m->free_list.back();
+    m->free_list.pop_back();
+  } else if (!m->evictable.empty()) {
+    b = m->evictable.front();
+    m->evictable.pop_front();
+    Block& blk = m->blocks[b];
+    m->cache.erase(blk.hash);
+    blk.cached = false;
+    blk.tokens.clear();
+  } else {
+    return -1;
+  }
+  m->blocks[b].ref = 1;
+  return b;
+}
+
+// One more reference to block b (a cache hit or a fork).
+void add_ref(pkv_bm* m, int b) {
+  Block& blk = m->blocks[b];
+  if (blk.ref == 0 && blk.cached) m->evictable.erase(blk.lru);
+  ++blk.ref;
+}
+
+// One reference fewer; at zero a cached block becomes evictable (most
+// recently used), any other block returns to the free list.
+void drop_ref(pkv_bm* m, int b) {
+  Block& blk = m->blocks[b];
+  if (--blk.ref > 0) return;
+  if (blk.cached) {
+    m->evictable.push_back(b);
+    blk.lru = std::prev(m->evictable.end());
+  } else {
+    m->free_list.push_back(b);
+  }
+}
+
+// Registers full block `b` (logical index i of s) in the prefix cache under
+// its chained hash, unless an identical block is already there.
+void register_full(pkv_bm* m, Sequence& s, int i) {
+  const int B = m->block_size;
+  const uint64_t parent = i == 0 ? s.root : s.hashes[i - 1];
+  const uint64_t h = block_hash(parent, s.tokens.data() + static_cast<size_t>(i) * B, B);
+  if (static_cast<int>(s.hashes.size()) == i) s.hashes.push_back(h);
+  const int b = s.table[i];
+  Block& blk = m->blocks[b];
+  if (blk.cached || m->cache.count(h)) return;
+  blk.cached = true;
+  blk.hash = h;
+  blk.parent_hash = parent;
+  blk.tokens.assign(s.tokens.begin() + static_cast<size_t>(i) * B, s.tokens.begin() + static_cast<size_t>(i + 1) * B);
+  m->cache.emplace(h, b);
+}
+
+// A cached block with this history, or -1 (the tokens are compared, so a
+// hash collision never shares a block).
+int lookup(const pkv_bm* m, uint64_t h, uint64_t parent, const int32_t* tokens) {
+  const auto it = m->cache.find(h);
+  if (it == m->cache.end()) return -1;
+  const Block& blk = m->blocks[it->second];
+  if (blk.parent_hash != parent ||
+      std::memcmp(blk.tokens.data(), tokens, sizeof(int32_t) * static_cast<size_t>(m->block_size)) != 0)
+    return -1;
+  return it->second;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+pkv_bm* pkv_bm_create(int num_blocks, int block_size, int watermark_blocks) {
+  if (num_blocks <= 0 || block_size <= 0 || watermark_blocks < 0 || watermark_blocks > num_blocks) return nullptr;
+  pkv_bm* m = new pkv_bm();
+  m->num_blocks = num_blocks;
+  m->block_size = block_size;
+  m->watermark = watermark_blocks;
+  m->blocks.resize(num_blocks);
+  m->free_list.reserve(num_blocks);
+  for (int b = num_blocks - 1; b >= 0; --b) m->free_list.push_back(b);  // block 0 first
+  return m;
+}
+
+void pkv_bm_destroy(pkv_bm* m) { delete m; }
+
+int pkv_bm_available_blocks(pkv_bm* m) {
+  std::lock_guard<std::mutex> lock(m->mu);
+  return available(m);
+}
+
+int pkv_bm_cached_blocks(pkv_bm* m) {
+  std::lock_guard<std::mutex> lock(m->mu);
+  return static_cast<int>(m->cache.size());
+}
+
+int pkv_bm_block_refcount(pkv_bm* m, int block) {
+  std::lock_guard<std::mutex> lock(m->mu);
+  if (block < 0 || block >= m->num_blocks) return -PKV_ERR_INVALID_ARG;
+  return m->blocks[block].ref;
+}
+
+int pkv_bm_add_sequence(pkv_bm* m, int64_t seq_id, const int32_t* tokens, int num_tokens, uint64_t extra_key,
+                        int32_t* slots) {
+  std::lock_guard<std::mutex> lock(m->mu);
+  if (num_tokens < 0 || (num_tokens > 0 && (!tokens || !slots)) || m->seqs.count(seq_id)) return -PKV_ERR_INVALID_ARG;
+  const int B = m->block_size;
+  Sequence s;
+  s.root = chain_root(extra_key);
+  s.tokens.assign(tokens, tokens + num_tokens);
+  // Cached prefix: whole blocks from position 0 whose chained hash hits.
+  std::vector<int> hits;
+  uint64_t parent = s.root;
+  for (int i = 0; (i + 1) * B <= num_tokens; ++i) {
+    const uint64_t h = block_hash(parent, tokens + static_cast<size_t>(i) * B, B);
+    const int b = lookup(m, h, parent, tokens + static_cast<size_t>(i) * B);
+    if (b < 0) break;
+    hits.push_back(b);
+    s.hashes.push_back(h);
+    parent = h;
+  }
+  const int need = (num_tokens + B - 1) / B - static_cast<int>(hits.size());
+  // Blocks a hit takes out of the evictable list are not available either.
+  int hit_evictable = 0;
+  for (int b : hits) hit_evictable += m->blocks[b].ref == 0 ? 1 : 0;
+  if (need > available(m) - hit_evictable - m->watermark) return -PKV_ERR_OUT_OF_BLOCKS;
+  for (int b : hits) {
+    add_ref(m, b);
+    s.table.push_back(b);
+  }
+  for (int i = 0; i < need; ++i) s.table.push_back(take_block(m));
+  const int cached_tokens = static_cast<int>(hits.size()) * B;
+  for (int t = 0; t < num_tokens; ++t)
+    slots[t] = t < cached_tokens ? -1 : s.table[t / B] * B + t % B;
+  // The prompt's new full blocks become cacheable once written.
+  for (int i = static_cast<int>(hits.size()); (i + 1) * B <= num_tokens; ++i) register_full(m, s, i);
+  m->seqs.emplace(seq_id, std::move(s));
+  return cached_tokens;
+}
+
+int pkv_bm_fork(pkv_bm* m, int64_t parent, int64_t child) {
+  std::lock_guard<std::mutex> lock(m->mu);
+  const auto it = m->seqs.find(parent);
+  if (it == m->seqs.end() || it->second.swapped || m->seqs.count(child)) return -PKV_ERR_INVALID_ARG;
+  Sequence c = it->second;
+  for (int b : c.table) add_ref(m, b);
+  m->seqs.emplace(child, std::move(c));
+  return PKV_OK;
+}
+
+int pkv_bm_append(pkv_bm* m, int64_t seq_id, int32_t token, int32_t* slot, int32_t* cow_src, int32_t* cow_dst) {
+  std::lock_guard<std::mutex> lock(m->mu);
+  const auto it = m->seqs.find(seq_id);
+  if (it == m->seqs.end() || it->second.swapped || !slot || !cow_src || !cow_dst) return -PKV_ERR_INVALID_ARG;
+  Sequence& s = it->second;
+  const int B = m->block_size;
+  const int pos = static_cast<int>(s.tokens.size());
+  *cow_src = *cow_dst = -1;
+  if (pos % B == 0) {  // the tail is full (or there is none): a fresh block
+    const int b = take_block(m);
+    if (b < 0) return -PKV_ERR_OUT_OF_BLOCKS;
+    s.table.push_back(b);
+  } else {
+    const int tail = s.table[pos / B];
+    if (m->blocks[tail].ref > 1) {  // shared tail: copy-on-write
+      const int b = take_block(m);
+      if (b < 0) return -PKV_ERR_OUT_OF_BLOCKS;
+      drop_ref(m, tail);
+      s.table[pos / B] = b;
+      *cow_src = tail;
+      *cow_dst = b;
+    }
+  }
+  s.tokens.push_back(token);
+  *slot = s.table[pos / B] * B + pos % B;
+  if ((pos + 1) % B == 0) register_full(m, s, pos / B);
+  return PKV_OK;
+}
+
+int pkv_bm_free_sequence(pkv_bm* m, int64_t seq_id) {
+  std::lock_guard<std::mutex> lock(m->mu);
+  const auto it = m->seqs.find(seq_id);
+  if (it == m->seqs.end()) return -PKV_ERR_INVALID_ARG;
+  if (!it->second.swapped)
+    for (auto b = it->second.table.rbegin(); b != it->second.table.rend(); ++b) drop_ref(m, *b);
+  m->seqs.erase(it);
+  return PKV_OK;
+}
+
+int pkv_bm_seq_len(pkv_bm* m, int64_t seq_id) {
+  std::lock_guard<std::mutex> lock(m->mu);
+  const auto it = m->seqs.find(seq_id);
+  return it == m->seqs.end() ? -PKV_ERR_INVALID_ARG : static_cast<int>(it->second.tokens.size());
+}
+
+int pkv_bm_block_table(pkv_bm* m, int64_t seq_id, int32_t* out, int capacity) {
+  std::lock_guard<std::mutex> lock(m->mu);
+  const auto it = m->seqs.find(seq_id);
+  if (it == m->seqs.end() || it->second.swapped) return -PKV_ERR_INVALID_ARG;
+  const int n = static_cast<int>(it->second.table.size());
+  if (n > capacity || (n > 0 && !out)) return -PKV_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) out[i] = it->second.table[i];
+  return n;
+}
+
+int pkv_bm_swap_out(pkv_bm* m, int64_t seq_id, int32_t* blocks, int capacity) {
+  std::lock_guard<std::mutex> lock(m->mu);
+  const auto it = m->seqs.find(seq_id);
+  if (it == m->seqs.end() || it->second.swapped) return -PKV_ERR_INVALID_ARG;
+  Sequence& s = it->second;
+  const int n = static_cast<int>(s.table.size());
+  if (n > capacity || (n > 0 && !blocks)) return -PKV_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) blocks[i] = s.table[i];
+  for (int i = n - 1; i >= 0; --i) drop_ref(m, s.table[i]);
+  s.table.clear();
+  s.swapped = true;
+  return n;
+}
+
+int pkv_bm_swap_in(pkv_bm* m, int64_t seq_id, int32_t* blocks, int capacity) {
+  std::lock_guard<std::mutex> lock(m->mu);
+  const auto it = m->seqs.find(seq_id);
+  if (it == m->seqs.end() || !it->second.swapped) return -PKV_ERR_INVALID_ARG;
+  Sequence& s = it->second;
+  const int B = m->block_size;
+  const int n = (static_cast<int>(s.tokens.size()) + B - 1) / B;
+  if (n > capacity || (n > 0 && !blocks)) return -PKV_ERR_INVALID_ARG;
+  if (n > available(m) - m->watermark) return -PKV_ERR_OUT_OF_BLOCKS;  // resuming is an admission
+  for (int i = 0; i < n; ++i) {
+    blocks[i] = take_block(m);
+    s.table.push_back(blocks[i]);
+  }
+  s.swapped = false;
+  for (int i = 0; (i + 1) * B <= static_cast<int>(s.tokens.size()); ++i) register_full(m, s, i);
+  return n;
+}
+
+}  // extern "C"

@@ -1,0 +1,298 @@
+"""The native host block manager (pkv_bm_*) against a plain Python model of
+the pages' allocator, on random operation sequences (CPU only):
+
+* free list and reference counts ("KV Cache & PagedAttention", section 4);
+* prefix sharing of whole blocks from position 0, keyed here by the exact
+  token history itself (the native one keys by a chained hash and checks
+  the tokens: the two must agree) ("gpu_paged_kv_cache", "Prefix sharing,
+  reference counts, and copy-on-write"; "PagedAttention internals", 04);
+* copy-on-write of a shared tail; LRU eviction of unreferenced cached
+  blocks, referenced blocks never evicted (section 04); a watermark of
+  blocks admissions may not take; swap out / in bookkeeping
+  ("gpu_paged_kv_cache", "Reclaiming memory: swap versus recompute")."""
+import numpy as np
+import pytest
+
+import paged_kv_cache_112_gb300 as pkv
+from paged_kv_cache_112_gb300 import build as pkv_build
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    try:
+        pkv_build.build()
+    except RuntimeError as e:  # no nvcc on this machine
+        pytest.skip(str(e))
+    pkv.load()
+
+
+class Model:
+    """Reference allocator, written for clarity: the same policy as the native
+    one (free list popped from the end, freed blocks pushed there; evictable
+    cached blocks in least-recently-released order)."""
+
+    def __init__(self, nb, bs, wm):
+        self.nb, self.bs, self.wm = nb, bs, wm
+        self.ref = [0] * nb
+        self.key = [None] * nb          # cached block -> its history key
+        self.free = list(range(nb - 1, -1, -1))
+        self.evictable = []             # front = least recently released
+        self.cache = {}                 # history key -> block
+        self.seqs = {}                  # id -> dict(table, tokens, extra, swapped)
+
+    def avail(self):
+        return len(self.free) + len(self.evictable)
+
+    def _take(self):
+        if self.free:
+            b = self.free.pop()
+        elif self.evictable:
+            b = self.evictable.pop(0)
+            del self.cache[self.key[b]]
+            self.key[b] = None
+        else:
+            return None
+        self.ref[b] = 1
+        return b
+
+    def _add_ref(self, b):
+        if self.ref[b] == 0 and self.key[b] is not None:
+            self.evictable.remove(b)
+        self.ref[b] += 1
+
+    def _drop_ref(self, b):
+        self.ref[b] -= 1
+        if self.ref[b] == 0:
+            (self.evictable if self.key[b] is not None else self.free).append(b)
+
+    def _register(self, s, i):
+        key = (s["extra"], tuple(s["tokens"][: (i + 1) * self.bs]))
+        b = s["table"][i]
+        if self.key[b] is not None or key in self.cache:
+            return
+        self.key[b] = key
+        self.cache[key] = b
+
+    def add(self, sid, tokens, extra):
+        if sid in self.seqs:
+            return "invalid", None
+        B = self.bs
+        hits = []
+        for i in range(len(tokens) // B):
+            b = self.cache.get((extra, tuple(tokens[: (i + 1) * B])))
+            if b is None:
+                break
+            hits.append(b)
+        need = -(-len(tokens) // B) - len(hits)
+        hit_evictable = sum(1 for b in hits if self.ref[b] == 0)
+        if need > self.avail() - hit_evictable - self.wm:
+            return "oob", None
+        s = dict(table=[], tokens=list(tokens), extra=extra, swapped=False)
+        for b in hits:
+            self._add_ref(b)
+            s["table"].append(b)
+        for _ in range(need):
+            s["table"].append(self._take())
+        cached = len(hits) * B
+        slots = [-1 if t < cached else s["table"][t // B] * B + t % B for t in range(len(tokens))]
+        for i in range(len(hits), len(tokens) // B):
+            self._register(s, i)
+        self.seqs[sid] = s
+        return cached, slots
+
+    def fork(self, parent, child):
+        if parent not in self.seqs or self.seqs[parent]["swapped"] or child in self.seqs:
+            return "invalid"
+        p = self.seqs[parent]
+        for b in p["table"]:
+            self._add_ref(b)
+        self.seqs[child] = dict(table=list(p["table"]), tokens=list(p["tokens"]), extra=p["extra"], swapped=False)
+        return "ok"
+
+    def append(self, sid, tok):
+        s = self.seqs.get(sid)
+        if s is None or s["swapped"]:
+            return "invalid"
+        B, pos = self.bs, len(s["tokens"])
+        cow = None
+        if pos % B == 0:
+            b = self._take()
+            if b is None:
+                return "oob"
+            s["table"].append(b)
+        else:
+            tail = s["table"][pos // B]
+            if self.ref[tail] > 1:
+                b = self._take()
+                if b is None:
+                    return "oob"
+                self._drop_ref(tail)
+                s["table"][pos // B] = b
+                cow = (tail, b)
+        s["tokens"].append(tok)
+        slot = s["table"][pos // B] * B + pos % B
+        if (pos + 1) % B == 0:
+            self._register(s, pos // B)
+        return slot, cow
+
+    def free_seq(self, sid):
+        s = self.seqs.pop(sid, None)
+        if s is None:
+            return "invalid"
+        if not s["swapped"]:
+            for b in reversed(s["table"]):
+                self._drop_ref(b)
+        return "ok"
+
+    def swap_out(self, sid):
+        s = self.seqs.get(sid)
+        if s is None or s["swapped"]:
+            return "invalid"
+        blocks = list(s["table"])
+        for b in reversed(blocks):
+            self._drop_ref(b)
+        s["table"], s["swapped"] = [], True
+        return blocks
+
+    def swap_in(self, sid):
+        s = self.seqs.get(sid)
+        if s is None or not s["swapped"]:
+            return "invalid"
+        n = -(-len(s["tokens"]) // self.bs)
+        if n > self.avail() - self.wm:
+            return "oob"
+        s["table"] = [self._take() for _ in range(n)]
+        s["swapped"] = False
+        for i in range(len(s["tokens"]) // self.bs):
+            self._register(s, i)
+        return s["table"]
+
+
+def _same_state(bm, m):
+    assert bm.available_blocks == m.avail()
+    assert bm.cached_blocks == len(m.cache)
+    assert [bm.refcount(b) for b in range(m.nb)] == m.ref
+    for sid, s in m.seqs.items():
+        assert bm.seq_len(sid) == len(s["tokens"])
+        if not s["swapped"]:
+            assert bm.block_table(sid).tolist() == s["table"]
+    # conservation: every reference is a table entry of a resident sequence
+    assert sum(m.ref) == sum(len(s["table"]) for s in m.seqs.values())
+    live = {b for b in range(m.nb) if m.ref[b] > 0}
+    assert live.isdisjoint(m.free) and live.isdisjoint(m.evictable)
+    assert len(live) + len(m.free) + len(m.evictable) == m.nb
+
+
+def _call(fn, *a):
+    try:
+        return fn(*a)
+    except pkv.OutOfBlocks:
+        return "oob"
+    except pkv.PkvError:
+        return "invalid"
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_operations_match_the_model(seed):
+    rng = np.random.default_rng(seed)
+    nb, bs, wm = int(rng.choice([24, 40])), int(rng.choice([4, 8, 16])), int(rng.integers(0, 4))
+    bm, m = pkv.BlockManager(nb, bs, wm), Model(nb, bs, wm)
+    system = [int(x) for x in rng.integers(0, 50, size=3 * bs)]  # a shared "system prompt"
+    next_id = 0
+    for _ in range(400):
+        op = rng.choice(["add", "add", "append", "append", "append", "fork", "free", "swap_out", "swap_in", "bad"])
+        ids = list(m.seqs)
+        if op == "add":
+            n_sys = int(rng.integers(0, 4)) * bs - int(rng.integers(0, 2))
+            tail = [int(x) for x in rng.integers(0, 50, size=int(rng.integers(0, 2 * bs)))]
+            toks = system[: max(0, n_sys)] + tail
+            extra = int(rng.integers(0, 2))
+            want = m.add(next_id, toks, extra)
+            got = _call(bm.add_sequence, next_id, toks, extra)
+            if isinstance(want[0], str):
+                assert got == want[0]
+                m.seqs.pop(next_id, None)
+            else:
+                assert got[0] == want[0] and got[1].tolist() == want[1]
+            next_id += 1
+        elif op == "append" and ids:
+            sid = int(rng.choice(ids))
+            tok = int(rng.integers(0, 50))
+            want = m.append(sid, tok)
+            got = _call(bm.append, sid, tok)
+            assert got == want, (got, want)
+        elif op == "fork" and ids:
+            parent = int(rng.choice(ids))
+            want = m.fork(parent, next_id)
+            got = _call(bm.fork, parent, next_id)
+            assert (got is None and want == "ok") or got == want
+            next_id += 1
+        elif op == "free" and ids:
+            sid = int(rng.choice(ids))
+            assert _call(bm.free, sid) is None and m.free_seq(sid) == "ok"
+        elif op == "swap_out" and ids:
+            sid = int(rng.choice(ids))
+            want = m.swap_out(sid)
+            got = _call(bm.swap_out, sid)
+            assert (got == want) if isinstance(want, str) else got.tolist() == want
+        elif op == "swap_in" and ids:
+            sid = int(rng.choice(ids))
+            want = m.swap_in(sid)
+            got = _call(bm.swap_in, sid)
+            assert (got == want) if isinstance(want, str) else got.tolist() == want
+        elif op == "bad":
+            assert _call(bm.append, 10 ** 9, 1) == "invalid"
+            assert _call(bm.fork, 10 ** 9, 10 ** 9 + 1) == "invalid"
+        _same_state(bm, m)
+
+
+def test_prefix_hit_needs_the_same_history_and_key():
+    B = 4
+    bm = pkv.BlockManager(16, B)
+    a = list(range(10))
+    assert bm.add_sequence(1, a)[0] == 0
+    cached, slots = bm.add_sequence(2, a[:9])  # two whole blocks of the same history
+    assert cached == 8 and (slots[:8] == -1).all() and slots[8] >= 0
+    assert bm.block_table(2)[:2].tolist() == bm.block_table(1)[:2].tolist()
+    assert bm.add_sequence(3, a, extra_key=7)[0] == 0          # another adapter: no sharing
+    assert bm.add_sequence(4, [99] + a[1:])[0] == 0             # differs in block 0: nothing shared
+    assert bm.add_sequence(5, a[:4] + [77, 5, 6, 7, 8])[0] == 4  # block 1 differs: only block 0 shared
+    assert bm.add_sequence(6, a[4:])[0] == 0                   # same tokens, not from position 0
+
+
+def test_copy_on_write_of_a_forked_tail():
+    B = 4
+    bm = pkv.BlockManager(8, B)
+    bm.add_sequence(1, [1, 2, 3, 4, 5, 6])  # block 1 half full
+    bm.fork(1, 2)
+    t1 = bm.block_table(1)
+    assert bm.refcount(int(t1[1])) == 2
+    slot, cow = bm.append(2, 9)  # the child writes first: it copies
+    t2 = bm.block_table(2)
+    assert cow == (int(t1[1]), int(t2[1])) and slot == t2[1] * B + 2
+    assert bm.refcount(int(t1[1])) == 1 and bm.refcount(int(t2[1])) == 1
+    slot, cow = bm.append(1, 8)  # the parent's block is its own again: no copy
+    assert cow is None and slot == t1[1] * B + 2
+
+
+def test_lru_eviction_spares_referenced_blocks():
+    B = 4
+    bm = pkv.BlockManager(6, B)
+    bm.add_sequence(1, [1] * 8)          # blocks for [1]*4, [1]*8 cached
+    bm.add_sequence(2, [2] * 8)
+    bm.free(1)                           # sequence 1's blocks: evictable, released first
+    assert bm.available_blocks == 4 and bm.cached_blocks == 4
+    bm.add_sequence(3, [3] * 12)         # needs 3: takes the 2 free ones, then evicts sequence 1's oldest
+    assert bm.cached_blocks == 4 + 3 - 1
+    assert bm.add_sequence(4, [2] * 8)[0] == 8  # sequence 2's blocks were referenced: still cached
+    with pytest.raises(pkv.OutOfBlocks):
+        bm.add_sequence(5, [5] * 20)
+
+
+def test_watermark_reserves_blocks_for_appends():
+    B = 4
+    bm = pkv.BlockManager(4, B, watermark_blocks=1)
+    bm.add_sequence(1, [1] * 12)  # 3 blocks: all but the watermark
+    with pytest.raises(pkv.OutOfBlocks):
+        bm.add_sequence(2, [2])
+    assert bm.append(1, 5)[0] == bm.block_table(1)[3] * B  # an append may take the reserve
