@@ -53,6 +53,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode paged-attention KV GB/s and % of GB300 HBM peak; sequences·layers/sec"
+E2E_BLOCK = 16  # end-to-end steps per captured graph
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -215,14 +216,17 @@ def run_gpu(args):
         host_stage[offs[name]:offs[name] + arr.nbytes].copy_(torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).reshape(-1)))
     dev_stage = host_stage.to(dev)
 
-    def view(name):
-        arr, tdt = next((a, t) for n, a, t in step_inputs if n == name)
-        t = dev_stage[offs[name]:offs[name] + arr.nbytes].view(tdt if tdt in (torch.int32,) else torch.int16)
-        t = t.view(arr.shape)
-        return t.view(dt) if tdt is dt else t
+    def views(stage):
+        """The step's inputs as views of one device staging buffer."""
+        def view(name):
+            arr, tdt = next((a, t) for n, a, t in step_inputs if n == name)
+            t = stage[offs[name]:offs[name] + arr.nbytes].view(tdt if tdt in (torch.int32,) else torch.int16)
+            t = t.view(arr.shape)
+            return t.view(dt) if tdt is dt else t
+        return {name: view(name) for name in ("q", "k_new", "v_new", "bt", "cl", "sm", "pairs")}
 
-    q, k_new, v_new = view("q"), view("k_new"), view("v_new")
-    bt, cl, sm, pairs = view("bt"), view("cl"), view("sm"), view("pairs")
+    io0 = views(dev_stage)
+    pairs = io0["pairs"]
     fp8 = args.kv == "fp8"
     if fp8:  # e4m3 codes + per-(block, KV head) scales; the write path quantises the new rows
         f8 = P.make_fp8_pools(wl, poison=False)
@@ -232,7 +236,7 @@ def run_gpu(args):
         k0 = torch.from_numpy(wl.k_pool.view(np.int16)).to(dev).view(dt)
         v0 = torch.from_numpy(wl.v_pool.view(np.int16)).to(dev).view(dt)
         ks0 = vs0 = None
-    out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    io0["out"] = torch.empty(io0["q"].shape, dtype=torch.float32, device=dev)
     ws_bytes = pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, wl.max_context_len, ps)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -246,10 +250,11 @@ def run_gpu(args):
     separate_write = (not args.fused) if fp8 else args.unfused
     n_launch = (1 if separate_write else 0) + 1 + (1 if ws_bytes else 0) + (1 if pairs.shape[0] else 0)
 
-    def step_fp8(i, ev=None):
+    def step_fp8(i, ev, io):
         kp, vp, ksp, vsp = pools[i % replicas]
-        if pairs.shape[0]:
-            pkv.copy_blocks_fp8(kp, vp, ksp, vsp, pairs, status=status)
+        q, k_new, v_new, bt, cl, sm, out = (io[k] for k in ("q", "k_new", "v_new", "bt", "cl", "sm", "out"))
+        if io["pairs"].shape[0]:
+            pkv.copy_blocks_fp8(kp, vp, ksp, vsp, io["pairs"], status=status)
         if not args.fused:
             pkv.write_cache_fp8(k_new, v_new, kp, vp, ksp, vsp, sm, status=status)
         if ev is not None:
@@ -268,12 +273,13 @@ def run_gpu(args):
                               head_dim=wl.head_dim, partition_size=ps, max_context_len=max_len, workspace=ws,
                               status=status)
 
-    def step(i, ev=None):
+    def step(i, ev=None, io=io0):
         if fp8:
-            return step_fp8(i, ev)
+            return step_fp8(i, ev, io)
         kp, vp = pools[i % replicas][:2]
-        if pairs.shape[0]:
-            pkv.copy_blocks(kp, vp, pairs, status=status)
+        q, k_new, v_new, bt, cl, sm, out = (io[k] for k in ("q", "k_new", "v_new", "bt", "cl", "sm", "out"))
+        if io["pairs"].shape[0]:
+            pkv.copy_blocks(kp, vp, io["pairs"], status=status)
         if not args.unfused:  # the new token's write fused into the partition kernel
             if ev is not None:
                 ev[0].record()
@@ -330,30 +336,71 @@ def run_gpu(args):
     if st != 0:
         raise RuntimeError(f"device status {st} after the timed steps")
 
-    # end to end through the public API: pinned host inputs in, host output out, every step
+    # End to end through the public API: every step uploads its inputs from pinned host memory
+    # (one copy) and reads its output back, double-buffered as a serving loop runs it: step i's
+    # inputs go up on one copy stream while step i-1 computes, and step i's output comes down on
+    # another while step i+1 computes.  A block of E2E_BLOCK such steps is captured once as a
+    # CUDA graph and replayed, so the host's per-call cost does not pace the loop.
     e2e = None
     if rank == 0 or world > 1:
-        host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        up_stream, down_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        dev_stages = [dev_stage, torch.empty_like(dev_stage)]
+        ios = [io0, views(dev_stages[1])]
+        ios[1]["out"] = torch.empty_like(io0["out"])
+        host_outs = [torch.empty(io0["out"].shape, dtype=io0["out"].dtype).pin_memory() for _ in range(2)]
         h2d = int(total)
-        d2h = host_out.numel() * host_out.element_size()
-        Ke = max(1, min(K, args.e2e_steps))
-        for i in range(2):
-            dev_stage.copy_(host_stage, non_blocking=True)
-            step(i)
-            host_out.copy_(out, non_blocking=True)
+        d2h = host_outs[0].numel() * host_outs[0].element_size()
+        block = E2E_BLOCK
+        Ke = max(block, min(K, args.e2e_steps) // block * block)
+
+        def e2e_block(n):
+            comp = torch.cuda.current_stream()
+            up = [torch.cuda.Event() for _ in range(2)]
+            done = [torch.cuda.Event() for _ in range(2)]
+            down = [torch.cuda.Event() for _ in range(2)]
+            up_stream.wait_stream(comp)
+            down_stream.wait_stream(comp)
+            for i in range(n):
+                b = i % 2
+                if i >= 2:
+                    up_stream.wait_event(done[b])    # step i-2 has finished reading this staging buffer
+                    comp.wait_event(down[b])         # and its output has been read back
+                with torch.cuda.stream(up_stream):
+                    dev_stages[b].copy_(host_stage, non_blocking=True)
+                    up[b].record(up_stream)
+                comp.wait_event(up[b])
+                step(i, io=ios[b])
+                done[b].record(comp)
+                down_stream.wait_event(done[b])
+                with torch.cuda.stream(down_stream):
+                    host_outs[b].copy_(ios[b]["out"], non_blocking=True)
+                    down[b].record(down_stream)
+            comp.wait_stream(up_stream)
+            comp.wait_stream(down_stream)
+
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            e2e_block(block)  # eager warm-up of the same work
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            e2e_block(block)
+        for _ in range(2):
+            graph.replay()
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for i in range(Ke):
-            dev_stage.copy_(host_stage, non_blocking=True)
-            step(i)
-            host_out.copy_(out, non_blocking=True)
+        for _ in range(Ke // block):
+            graph.replay()
         e1.record()
         barrier()
         e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
         e2e = {"value": round(job_gbs(nb["step"], world, Ke, e_ms), 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": Ke,
-               "ms_per_step": round(e_ms / Ke, 5)}
+               "ms_per_step": round(e_ms / Ke, 5),
+               "overlap": f"double-buffered (inputs up / outputs down on two copy streams beside the step), "
+                          f"{block} steps per CUDA graph replay"}
 
     if rank != 0:
         if world > 1:

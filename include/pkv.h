@@ -32,7 +32,9 @@
  *         num_kv_heads * head_dim.
  *     Any other block_stride >= the dense one and a multiple of 8 elements
  *     works too.  Pool pointers are 16-byte aligned.
- *   - block_size must be 16 [P1 "Fixed-size blocks"; P2 section 02].
+ *   - block_size is 8, 16, 32 or 64 tokens; 16 is the common default [P1
+ *     "Fixed-size blocks"; P2 section 02].  FP8 pools and the balanced
+ *     split take 16 only.
  *   - Elements are IEEE binary16 (PKV_F16) or bfloat16 (PKV_BF16).  Queries
  *     have the pools' type.
  *   - dev_status, when not NULL, is a device int32 into which kernels OR the
@@ -54,7 +56,7 @@ extern "C" {
 typedef enum pkv_status {
   PKV_OK = 0,
   PKV_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned pointer */
-  PKV_ERR_UNSUPPORTED = 2,   /* block_size != 16, head_dim not 64/128, group > 8 ... */
+  PKV_ERR_UNSUPPORTED = 2,   /* block_size not 8/16/32/64, head_dim not 64/128, group > 8 ... */
   PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than pkv_decode_workspace_bytes */
   PKV_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
   PKV_ERR_OUT_OF_BLOCKS = 5  /* block manager: not enough free blocks (pool exhausted) */
@@ -191,7 +193,8 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, i
  *   workspace    : device scratch of at least pkv_decode_workspace_bytes()
  *                  bytes, 16-byte aligned (may be NULL when that is 0).  Its
  *                  contents need no initialisation.
- * Supported: head_dim 64 or 128, block_size 16, 1 <= G <= 8.
+ * Supported: head_dim 64 or 128, block_size 8, 16, 32 or 64 (16 only for
+ * PKV_PARTITION_BALANCED), 1 <= G <= 8.
  * The two kernels run back to back on `stream`; pkv_decode_partitions and
  * pkv_decode_reduce below expose them separately.
  */
