@@ -8,6 +8,8 @@ never imports it.
 Contents
   write_cache      -- the slot-mapping scatter, a byte copy per token.
   copy_blocks      -- the copy-on-write block copy, a byte copy per pair.
+  swap_blocks      -- block lists moved between two pools (device and host;
+                      swap out / in), a byte copy per pair.
   decode_attention -- fp64 single-query grouped attention through block
                       tables (C++ in csrc/pkv_oracle.cpp, threaded over rows).
   brute            -- a pure-Python restatement used to pin the C++ one.
@@ -26,7 +28,11 @@ Sources (four web pages on paged KV caches):
     the whole source block into a fresh block, device to device.
   * "PagedAttention internals" section 02 and "tm_paged_attention" (aicassindra)
     "The architecture" / "End-to-end flow": the table translation and the
-    decode step attending over the full history.
+    decode step attending over the full history (any block size: the block
+    is the pools' second axis).
+  * "gpu_paged_kv_cache", "Reclaiming memory: swap versus recompute", and
+    "PagedAttention internals" section 05: a preempted sequence's blocks go
+    to pinned host memory and come back to whatever blocks are free.
   * "PagedAttention internals" section 06, "Blocks as quantization groups":
     the 16-token block as the quantization group, its scales riding with the
     block, including across copy-on-write; and "KV Cache & PagedAttention"
