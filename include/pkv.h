@@ -428,8 +428,9 @@ pkv_status pkv_decode_step_partitions_fp8(void* out, const void* q, const void* 
  * pairs.  Calls on one manager are serialised by an internal lock.
  *
  * Functions returning int return a count (>= 0) on success or a negative
- * pkv_status: -PKV_ERR_INVALID_ARG (unknown or duplicate sequence, null or
- * short buffer, wrong state) or -PKV_ERR_OUT_OF_BLOCKS (nothing was changed).
+ * pkv_status: -PKV_ERR_INVALID_ARG (null manager, unknown or duplicate
+ * sequence, null or short buffer, wrong state) or -PKV_ERR_OUT_OF_BLOCKS
+ * (nothing was changed).
  *
  * Prefix cache: a full block (block_size tokens) is keyed by a hash of its
  * tokens chained onto the previous block's key, starting from the

@@ -182,16 +182,19 @@ pkv_bm* pkv_bm_create(int num_blocks, int block_size, int watermark_blocks) {
 void pkv_bm_destroy(pkv_bm* m) { delete m; }
 
 int pkv_bm_available_blocks(pkv_bm* m) {
+  if (!m) return -PKV_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(m->mu);
   return available(m);
 }
 
 int pkv_bm_cached_blocks(pkv_bm* m) {
+  if (!m) return -PKV_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(m->mu);
   return static_cast<int>(m->cache.size());
 }
 
 int pkv_bm_block_refcount(pkv_bm* m, int block) {
+  if (!m) return -PKV_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(m->mu);
   if (block < 0 || block >= m->num_blocks) return -PKV_ERR_INVALID_ARG;
   return m->blocks[block].ref;
@@ -199,6 +202,7 @@ int pkv_bm_block_refcount(pkv_bm* m, int block) {
 
 int pkv_bm_add_sequence(pkv_bm* m, int64_t seq_id, const int32_t* tokens, int num_tokens, uint64_t extra_key,
                         int32_t* slots) {
+  if (!m) return -PKV_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(m->mu);
   if (num_tokens < 0 || (num_tokens > 0 && (!tokens || !slots)) || m->seqs.count(seq_id)) return -PKV_ERR_INVALID_ARG;
   const int B = m->block_size;
@@ -236,6 +240,7 @@ int pkv_bm_add_sequence(pkv_bm* m, int64_t seq_id, const int32_t* tokens, int nu
 }
 
 int pkv_bm_fork(pkv_bm* m, int64_t parent, int64_t child) {
+  if (!m) return -PKV_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(m->mu);
   const auto it = m->seqs.find(parent);
   if (it == m->seqs.end() || it->second.swapped || m->seqs.count(child)) return -PKV_ERR_INVALID_ARG;
@@ -246,6 +251,7 @@ int pkv_bm_fork(pkv_bm* m, int64_t parent, int64_t child) {
 }
 
 int pkv_bm_append(pkv_bm* m, int64_t seq_id, int32_t token, int32_t* slot, int32_t* cow_src, int32_t* cow_dst) {
+  if (!m) return -PKV_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(m->mu);
   const auto it = m->seqs.find(seq_id);
   if (it == m->seqs.end() || it->second.swapped || !slot || !cow_src || !cow_dst) return -PKV_ERR_INVALID_ARG;
@@ -275,6 +281,7 @@ int pkv_bm_append(pkv_bm* m, int64_t seq_id, int32_t token, int32_t* slot, int32
 }
 
 int pkv_bm_free_sequence(pkv_bm* m, int64_t seq_id) {
+  if (!m) return -PKV_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(m->mu);
   const auto it = m->seqs.find(seq_id);
   if (it == m->seqs.end()) return -PKV_ERR_INVALID_ARG;
@@ -285,12 +292,14 @@ int pkv_bm_free_sequence(pkv_bm* m, int64_t seq_id) {
 }
 
 int pkv_bm_seq_len(pkv_bm* m, int64_t seq_id) {
+  if (!m) return -PKV_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(m->mu);
   const auto it = m->seqs.find(seq_id);
   return it == m->seqs.end() ? -PKV_ERR_INVALID_ARG : static_cast<int>(it->second.tokens.size());
 }
 
 int pkv_bm_block_table(pkv_bm* m, int64_t seq_id, int32_t* out, int capacity) {
+  if (!m) return -PKV_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(m->mu);
   const auto it = m->seqs.find(seq_id);
   if (it == m->seqs.end() || it->second.swapped) return -PKV_ERR_INVALID_ARG;
@@ -301,6 +310,7 @@ int pkv_bm_block_table(pkv_bm* m, int64_t seq_id, int32_t* out, int capacity) {
 }
 
 int pkv_bm_swap_out(pkv_bm* m, int64_t seq_id, int32_t* blocks, int capacity) {
+  if (!m) return -PKV_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(m->mu);
   const auto it = m->seqs.find(seq_id);
   if (it == m->seqs.end() || it->second.swapped) return -PKV_ERR_INVALID_ARG;
@@ -315,6 +325,7 @@ int pkv_bm_swap_out(pkv_bm* m, int64_t seq_id, int32_t* blocks, int capacity) {
 }
 
 int pkv_bm_swap_in(pkv_bm* m, int64_t seq_id, int32_t* blocks, int capacity) {
+  if (!m) return -PKV_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(m->mu);
   const auto it = m->seqs.find(seq_id);
   if (it == m->seqs.end() || !it->second.swapped) return -PKV_ERR_INVALID_ARG;

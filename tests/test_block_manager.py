@@ -296,3 +296,22 @@ def test_watermark_reserves_blocks_for_appends():
     with pytest.raises(pkv.OutOfBlocks):
         bm.add_sequence(2, [2])
     assert bm.append(1, 5)[0] == bm.block_table(1)[3] * B  # an append may take the reserve
+
+
+def test_c_abi_guards():
+    lib = pkv.load()
+    assert not lib.pkv_bm_create(0, 16, 0) and not lib.pkv_bm_create(8, 16, 9)
+    assert lib.pkv_bm_available_blocks(None) == -pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_bm_free_sequence(None, 1) == -pkv.PKV_ERR_INVALID_ARG
+    bm = pkv.BlockManager(4, 16)
+    with pytest.raises(pkv.PkvError):
+        bm.add_sequence(1, [1, 2])
+        bm.add_sequence(1, [3])  # duplicate id
+    with pytest.raises(pkv.PkvError):
+        bm.swap_in(1)  # not swapped out
+    with pytest.raises(pkv.PkvError):
+        bm.block_table(99)
+    bm.swap_out(1)
+    with pytest.raises(pkv.PkvError):
+        bm.append(1, 5)  # swapped out: no appends until swap_in
+    assert bm.swap_in(1).size == 1 and bm.append(1, 5)[0] >= 0
