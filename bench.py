@@ -691,10 +691,26 @@ def run_swap(args):
             "pages_figure": "1.25 GiB over PCIe 4.0 x16 at ~25 GB/s: ~50 ms each way"}
 
 
+def kernel_source_hash(paths) -> str:
+    """First 16 hex digits of a sha256 over the given sources with comments
+    and whitespace removed: any change to the code changes it, a change to a
+    comment does not."""
+    import hashlib
+    import re
+
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(re.sub(r"\s+", "", text).encode())
+    return h.hexdigest()[:16]
+
+
 def _recorded_traffic(cfg, kernel):
     """DRAM bytes per launch of the partition kernel from the committed ncu
     summary, if it was taken on the current kernel sources; else None."""
-    import hashlib
 
     sources = {"decode_partitions_kernel": ("decode_partitions", "pkv_decode.cu"),
                "decode_partitions_fp8_kernel": ("decode_partitions_fp8", "pkv_decode_fp8.cu")}
@@ -711,11 +727,7 @@ def _recorded_traffic(cfg, kernel):
             if "=" in line and not line.lstrip().startswith("#"):
                 k, v = line.split("=", 1)
                 vals[k.strip()] = v.strip()
-    h = hashlib.sha256()
-    for p in srcs:
-        with open(p, "rb") as f:
-            h.update(f.read())
-    if vals.get("kernel_source_sha256_16") != h.hexdigest()[:16]:
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash(srcs):
         return None
     try:
         return int(float(vals["dram_bytes_per_launch"]))

@@ -11,16 +11,17 @@
 // kernel (the split-K restructuring of flash-decoding).
 //
 // Mapping onto GB300:
-//  * Work unit = (KV head g, sequence s, partition p), one warp each.  A CTA
-//    is NW warps on consecutive KV heads of the same (s, p), so it reads
-//    neighbouring head rows of every token row of a block.  A warp serves
-//    all G <= 8 query heads of its KV head: every K/V byte is read once.
-//  * Data movement: TMA (cp.async.bulk.tensor.3d, 128-byte swizzle) copies
-//    one (block, head) tile of K and of V per stage into a per-warp ring of
-//    NST stages completing on mbarriers.  Six 2-warp CTAs per SM (12 warps
-//    at D = 128, 2 stages each) keep 24 tiles = 192 KB in flight per SM.
-//    CTA widths that divide H_kv keep a CTA's warps on units of one (s, p):
-//    wider CTAs mixing unit sizes hold shared memory for their slowest warp.
+//  * Work unit = (KV head g, sequence s, partition p), served by one warp
+//    (a CTA's two warps take neighbouring KV heads of the same (s, p), so
+//    they read neighbouring head rows of every token row) or by both warps
+//    of a CTA (see partition_unit).  A warp serves all G <= 8 query heads
+//    of its KV head: every K/V byte is read once.
+//  * Data movement: TMA (cp.async.bulk.tensor.4d over {element line, head
+//    line, row in block, block}, 128-byte swizzle) copies one 16-token tile
+//    of K and of V per stage into a per-warp ring of NST stages completing
+//    on mbarriers.  A tile is 16 rows of one block (blocks of >= 16 tokens)
+//    or two 8-token blocks.  Six 2-warp CTAs per SM (12 warps at D = 128,
+//    2 stages each) keep 24 tiles = 192 KB in flight per SM.
 //  * Math: tensor-core mma.sync (see WarpAttention in pkv_device.cuh).
 //  * Waits are bounded by %globaltimer; on timeout a warp drains its copies,
 //    sets PKV_DEV_ERR_TIMEOUT and returns.  Table entries are range-checked;

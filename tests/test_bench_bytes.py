@@ -19,3 +19,13 @@ def test_step_bytes_16bit_and_fp8():
     assert nb8["write"] == 2 * T * wl.num_kv_heads * wl.head_dim * 3 + T * wl.num_kv_heads * 8 + T * 4
     for d in (nb, nb8):
         assert d["step"] == d["attention"] + d["write"] + d["copy"]
+
+
+def test_kernel_source_hash_ignores_comments_not_code(tmp_path):
+    a = tmp_path / "a.cu"
+    a.write_text("// header\n__global__ void k(int* p) {\n  p[0] = 1;  // store\n}\n/* block */\n")
+    h0 = bench.kernel_source_hash([str(a)])
+    a.write_text("// a different header\n__global__ void k(int* p) {\n    p[0] = 1;\n}\n")
+    assert bench.kernel_source_hash([str(a)]) == h0
+    a.write_text("__global__ void k(int* p) {\n  p[0] = 2;\n}\n")
+    assert bench.kernel_source_hash([str(a)]) != h0
