@@ -318,6 +318,18 @@ pkv_status pkv_decode_attention_static_workspace(
  * The library never chooses a scale: the caller sets a block's scales when
  * it allocates the block (e.g. from a calibrated per-layer amax) and the
  * write path quantises new rows with them.  Pool pointers 16-byte aligned.
+ *
+ * num_layers (1..4096) selects the all-layer layout, one allocation per
+ * pool holding every layer's rows of a block together:
+ *   codes  [num_blocks][num_layers][16][num_kv_heads][head_dim],
+ *   scales [num_blocks][num_layers][num_kv_heads].
+ * pkv_write_cache_fp8 and the decode entry points then take layer l's base
+ * pointers (codes + l * 16 * num_kv_heads * head_dim bytes, scales +
+ * l * num_kv_heads floats): block b of the layer starts num_layers times
+ * further apart than in a one-layer pool.  pkv_copy_blocks_fp8 takes the
+ * whole pools and copies a block's rows and scales of every layer.
+ * num_layers = 1 is the per-layer layout above.  Out of range:
+ * PKV_ERR_INVALID_ARG.
  */
 
 /*
@@ -333,18 +345,19 @@ pkv_status pkv_decode_attention_static_workspace(
 pkv_status pkv_write_cache_fp8(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
                                const float* k_scale, const float* v_scale, const int32_t* slot_mapping,
                                int num_tokens, int64_t new_row_stride, int num_kv_heads, int head_dim,
-                               int block_size, int num_blocks, pkv_dtype new_dtype, int32_t* dev_status,
-                               void* stream);
+                               int block_size, int num_blocks, int num_layers, pkv_dtype new_dtype,
+                               int32_t* dev_status, void* stream);
 
 /*
  * pkv_copy_blocks_fp8 -- copy-on-write over FP8 pools: for each pair, block
  * dst := block src in both pools (bytes), and k_scale[dst][:] :=
- * k_scale[src][:], v_scale likewise.  Pair rules and errors as
- * pkv_copy_blocks.
+ * k_scale[src][:], v_scale likewise (every layer's, with num_layers > 1).
+ * Pair rules and errors as pkv_copy_blocks.
  */
 pkv_status pkv_copy_blocks_fp8(void* k_pool, void* v_pool, float* k_scale, float* v_scale,
-                               const int32_t* pairs, int num_pairs, int num_kv_heads, int head_dim,
-                               int block_size, int num_blocks, int32_t* dev_status, void* stream);
+                               const int32_t* pairs, int num_pairs, int num_layers, int num_kv_heads,
+                               int head_dim, int block_size, int num_blocks, int32_t* dev_status,
+                               void* stream);
 
 /*
  * pkv_decode_attention_fp8 -- pkv_decode_attention over FP8 pools:
@@ -361,7 +374,7 @@ pkv_status pkv_decode_attention_fp8(void* out, const void* q, const void* k_pool
                                     const int32_t* block_tables, int max_blocks_per_seq,
                                     const int32_t* context_lens, int num_seqs, int num_q_heads,
                                     int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                                    float scale, int partition_size, int max_context_len,
+                                    int num_layers, float scale, int partition_size, int max_context_len,
                                     void* workspace, size_t workspace_bytes, pkv_dtype q_dtype,
                                     pkv_dtype out_dtype, int32_t* dev_status, void* stream);
 
@@ -375,7 +388,7 @@ pkv_status pkv_decode_partitions_fp8(void* out, const void* q, const void* k_poo
                                      const int32_t* block_tables, int max_blocks_per_seq,
                                      const int32_t* context_lens, int num_seqs, int num_q_heads,
                                      int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                                     float scale, int partition_size, int max_context_len,
+                                     int num_layers, float scale, int partition_size, int max_context_len,
                                      void* workspace, size_t workspace_bytes, pkv_dtype q_dtype,
                                      pkv_dtype out_dtype, int32_t* dev_status, void* stream);
 
@@ -399,7 +412,7 @@ pkv_status pkv_decode_step_fp8(void* out, const void* q, const void* k_new, cons
                                int max_blocks_per_seq, const int32_t* context_lens,
                                const int32_t* slot_mapping, int num_seqs, int num_q_heads,
                                int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                               float scale, int partition_size, int max_context_len, void* workspace,
+                               int num_layers, float scale, int partition_size, int max_context_len, void* workspace,
                                size_t workspace_bytes, pkv_dtype q_dtype, pkv_dtype out_dtype,
                                int32_t* dev_status, void* stream);
 
@@ -409,8 +422,8 @@ pkv_status pkv_decode_step_partitions_fp8(void* out, const void* q, const void* 
                                           const int32_t* block_tables, int max_blocks_per_seq,
                                           const int32_t* context_lens, const int32_t* slot_mapping,
                                           int num_seqs, int num_q_heads, int num_kv_heads,
-                                          int head_dim, int block_size, int num_blocks, float scale,
-                                          int partition_size, int max_context_len, void* workspace,
+                                          int head_dim, int block_size, int num_blocks, int num_layers,
+                                          float scale, int partition_size, int max_context_len, void* workspace,
                                           size_t workspace_bytes, pkv_dtype q_dtype,
                                           pkv_dtype out_dtype, int32_t* dev_status, void* stream);
 

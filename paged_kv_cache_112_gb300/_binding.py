@@ -41,9 +41,9 @@ _SIGS["pkv_decode_step"] = ([_c_void_p] * 4 + [_c_int64] + [_c_void_p] * 2 + [_c
                             [_c_void_p] * 2 + [_c_int] * 6 + [_c_float, _c_int, _c_int, _c_void_p, _c_size_t, _c_int,
                                                               _c_int, _c_void_p, _c_void_p])
 _SIGS["pkv_decode_step_partitions"] = _SIGS["pkv_decode_step"]
-_SIGS["pkv_write_cache_fp8"] = [_c_void_p] * 7 + [_c_int, _c_int64] + [_c_int] * 5 + [_c_void_p, _c_void_p]
-_SIGS["pkv_copy_blocks_fp8"] = [_c_void_p] * 5 + [_c_int] * 5 + [_c_void_p, _c_void_p]
-_SIGS["pkv_decode_attention_fp8"] = ([_c_void_p] * 7 + [_c_int, _c_void_p] + [_c_int] * 6 +
+_SIGS["pkv_write_cache_fp8"] = [_c_void_p] * 7 + [_c_int, _c_int64] + [_c_int] * 6 + [_c_void_p, _c_void_p]
+_SIGS["pkv_copy_blocks_fp8"] = [_c_void_p] * 5 + [_c_int] * 6 + [_c_void_p, _c_void_p]
+_SIGS["pkv_decode_attention_fp8"] = ([_c_void_p] * 7 + [_c_int, _c_void_p] + [_c_int] * 7 +
                                      [_c_float, _c_int, _c_int, _c_void_p, _c_size_t, _c_int, _c_int, _c_void_p,
                                       _c_void_p])
 _SIGS["pkv_decode_partitions_fp8"] = _SIGS["pkv_decode_attention_fp8"]
@@ -51,7 +51,7 @@ _SIGS["pkv_swap_blocks"] = ([_c_void_p] * 2 + [_c_int64, _c_int] + [_c_void_p] *
                                                                                      _c_void_p, _c_int, _c_void_p,
                                                                                      _c_void_p])
 _SIGS["pkv_decode_step_fp8"] = ([_c_void_p] * 4 + [_c_int64] + [_c_void_p] * 5 + [_c_int] + [_c_void_p] * 2 +
-                                [_c_int] * 6 + [_c_float, _c_int, _c_int, _c_void_p, _c_size_t, _c_int, _c_int,
+                                [_c_int] * 7 + [_c_float, _c_int, _c_int, _c_void_p, _c_size_t, _c_int, _c_int,
                                                 _c_void_p, _c_void_p])
 _SIGS["pkv_decode_step_partitions_fp8"] = _SIGS["pkv_decode_step_fp8"]
 
@@ -270,23 +270,39 @@ def decode_step_partitions(out, q, k_new, v_new, k_pool, v_pool, block_tables, c
 
 # ------------------------------------------------------------------ FP8 pools
 # Pools are uint8 [NB, 16, H_kv, D] tensors of e4m3 codes; scales float32
-# [NB, H_kv] (one per block and KV head, for K and for V).
+# [NB, H_kv] (one per block and KV head, for K and for V).  Either per-layer
+# tensors, or one layer's views of all-layer pools [NB, layers, 16, H_kv, D]
+# and scales [NB, layers, H_kv] (pool[:, layer], scale[:, layer]).
 
 
 def _fp8_pools(k_pool, v_pool, k_scale, v_scale):
-    _need_cuda(k_pool, v_pool, k_scale, v_scale)
-    if k_pool.dtype != torch.uint8 or v_pool.dtype != torch.uint8 or v_pool.shape != k_pool.shape:
+    """(NB, 16, H_kv, D, layers) of FP8 pools given as per-layer tensors or
+    layer views of all-layer pools; the layer count comes from the strides."""
+    for t in (k_pool, v_pool, k_scale, v_scale):
+        if not t.is_cuda or t.dim() not in (2, 4):
+            raise PkvError("FP8 pools must be CUDA [NB, 16, H_kv, D] and scales CUDA [NB, H_kv]")
+    if k_pool.dtype != torch.uint8 or v_pool.dtype != torch.uint8 or v_pool.shape != k_pool.shape or \
+            k_pool.dim() != 4:
         raise PkvError("FP8 pools must be uint8 tensors of one shape [NB, 16, H_kv, D]")
     NB, B, Hkv, D = k_pool.shape
+    block = B * Hkv * D
+    for t in (k_pool, v_pool):
+        if t.stride(3) != 1 or t.stride(2) != D or t.stride(1) != Hkv * D or t.stride(0) % block or \
+                t.stride(0) < block:
+            raise PkvError("FP8 pool blocks must be dense [16, H_kv, D] slices, layers x 16 rows apart")
+    layers = int(k_pool.stride(0)) // block
     for sc in (k_scale, v_scale):
-        if sc.dtype != torch.float32 or tuple(sc.shape) != (NB, Hkv):
-            raise PkvError("scales must be float32 [NB, H_kv]")
-    return NB, B, Hkv, D
+        if sc.dtype != torch.float32 or tuple(sc.shape) != (NB, Hkv) or sc.stride(1) != 1 or \
+                sc.stride(0) != layers * Hkv:
+            raise PkvError("scales must be float32 [NB, H_kv] with the pools' layer count")
+    if v_pool.stride(0) != k_pool.stride(0):
+        raise PkvError("k_pool and v_pool must share a block stride")
+    return NB, B, Hkv, D, layers
 
 
 def write_cache_fp8(k_new, v_new, k_pool, v_pool, k_scale, v_scale, slot_mapping, *, status=None, stream=None):
     """pkv_write_cache_fp8: k_new/v_new f16/bf16 [T, H_kv, D] quantised into the FP8 pools."""
-    NB, B, Hkv, D = _fp8_pools(k_pool, v_pool, k_scale, v_scale)
+    NB, B, Hkv, D, layers = _fp8_pools(k_pool, v_pool, k_scale, v_scale)
     _need_cuda(slot_mapping, status)
     T = k_new.shape[0]
     for t in (k_new, v_new):
@@ -296,21 +312,31 @@ def write_cache_fp8(k_new, v_new, k_pool, v_pool, k_scale, v_scale, slot_mapping
         raise PkvError("k_new and v_new must share a row stride and a dtype")
     _check(load().pkv_write_cache_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
                                       _ptr(v_scale), _ptr(slot_mapping), T, int(k_new.stride(0)), Hkv, D, B, NB,
-                                      _kv_dtype(k_new), _ptr(status), _stream(stream)), "pkv_write_cache_fp8")
+                                      layers, _kv_dtype(k_new), _ptr(status), _stream(stream)), "pkv_write_cache_fp8")
 
 
 def copy_blocks_fp8(k_pool, v_pool, k_scale, v_scale, pairs, *, status=None, stream=None):
-    """pkv_copy_blocks_fp8: pairs int32 [P, 2] (src, dst); codes and scales move together."""
-    NB, B, Hkv, D = _fp8_pools(k_pool, v_pool, k_scale, v_scale)
-    _need_cuda(pairs, status)
+    """pkv_copy_blocks_fp8: pairs int32 [P, 2] (src, dst); codes and scales move together.  Pools
+    and scales are contiguous per-layer tensors ([NB, 16, H_kv, D], [NB, H_kv]) or whole
+    all-layer ones ([NB, layers, 16, H_kv, D], [NB, layers, H_kv]), copied with every layer."""
+    _need_cuda(k_pool, v_pool, k_scale, v_scale, pairs, status)
+    if k_pool.dtype != torch.uint8 or v_pool.dtype != torch.uint8 or v_pool.shape != k_pool.shape or \
+            k_pool.dim() not in (4, 5):
+        raise PkvError("FP8 pools must be uint8 [NB, 16, H_kv, D] or [NB, layers, 16, H_kv, D], K and V alike")
+    layers = 1 if k_pool.dim() == 4 else int(k_pool.shape[1])
+    NB, B, Hkv, D = k_pool.shape[0], k_pool.shape[-3], k_pool.shape[-2], k_pool.shape[-1]
+    want = (NB, Hkv) if k_pool.dim() == 4 else (NB, layers, Hkv)
+    for sc in (k_scale, v_scale):
+        if sc.dtype != torch.float32 or tuple(sc.shape) != want:
+            raise PkvError(f"scales must be float32 {list(want)}")
     _check(load().pkv_copy_blocks_fp8(_ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(pairs),
-                                      int(pairs.shape[0]), Hkv, D, B, NB, _ptr(status), _stream(stream)),
+                                      int(pairs.shape[0]), layers, Hkv, D, B, NB, _ptr(status), _stream(stream)),
            "pkv_copy_blocks_fp8")
 
 
 def _decode_fp8_args(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, context_lens, scale, partition_size,
                      max_context_len, workspace, status, stream):
-    NB, B, Hkv, D = _fp8_pools(k_pool, v_pool, k_scale, v_scale)
+    NB, B, Hkv, D, layers = _fp8_pools(k_pool, v_pool, k_scale, v_scale)
     _need_cuda(out, q, block_tables, context_lens, workspace, status)
     S, Hq, Dq = q.shape
     if Dq != D or out.shape != q.shape or out.dtype not in _DTYPES:
@@ -319,7 +345,8 @@ def _decode_fp8_args(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, con
         raise PkvError("block_tables and context_lens must be int32")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     return (_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
-            int(block_tables.shape[1]), _ptr(context_lens), S, Hq, Hkv, D, B, NB, float(scale), int(partition_size),
+            int(block_tables.shape[1]), _ptr(context_lens), S, Hq, Hkv, D, B, NB, layers, float(scale),
+            int(partition_size),
             int(max_context_len), _ptr(workspace), ws_bytes, _kv_dtype(q), _DTYPES[out.dtype], _ptr(status),
             _stream(stream))
 
@@ -355,9 +382,9 @@ def _step_fp8_args(out, q, k_new, v_new, k_pool, v_pool, k_scale, v_scale, block
         raise PkvError("k_new and v_new must share a row stride and the queries' dtype")
     if slot_mapping.dtype != torch.int32 or slot_mapping.shape != (q.shape[0],):
         raise PkvError("slot_mapping must be int32 [S]")
-    (o, qp, kp, vp, ksp, vsp, bt, maxb, cl, S, Hq, Hkv_, D_, B_, NB_, sc, ps, mcl, ws, wsb, qd, od, st, strm) = base
+    (o, qp, kp, vp, ksp, vsp, bt, maxb, cl, S, Hq, Hkv_, D_, B_, NB_, L, sc, ps, mcl, ws, wsb, qd, od, st, strm) = base
     return (o, qp, _ptr(k_new), _ptr(v_new), int(k_new.stride(0)), kp, vp, ksp, vsp, bt, maxb, cl, _ptr(slot_mapping),
-            S, Hq, Hkv_, D_, B_, NB_, sc, ps, mcl, ws, wsb, qd, od, st, strm)
+            S, Hq, Hkv_, D_, B_, NB_, L, sc, ps, mcl, ws, wsb, qd, od, st, strm)
 
 
 def decode_step_fp8(out, q, k_new, v_new, k_pool, v_pool, k_scale, v_scale, block_tables, context_lens, slot_mapping,

@@ -501,9 +501,10 @@ pkv_status pkv_decode_attention(void* out, const void* q, const void* k_pool, co
 pkv_status pkv_write_cache_fp8(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
                                const float* k_scale, const float* v_scale, const int32_t* slot_mapping,
                                int num_tokens, int64_t new_row_stride, int num_kv_heads, int head_dim,
-                               int block_size, int num_blocks, pkv_dtype new_dtype, int32_t* dev_status,
-                               void* stream) {
-  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || new_row_stride < 0)
+                               int block_size, int num_blocks, int num_layers, pkv_dtype new_dtype,
+                               int32_t* dev_status, void* stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || new_row_stride < 0 ||
+      num_layers <= 0 || num_layers > kMaxLayers)
     return PKV_ERR_INVALID_ARG;
   if (!kv_dtype_ok(new_dtype)) return PKV_ERR_INVALID_ARG;
   if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
@@ -527,6 +528,8 @@ pkv_status pkv_write_cache_fp8(const void* k_new, const void* v_new, void* k_poo
   a.dev_status = dev_status;
   a.stride = stride;
   a.num_slots = static_cast<int64_t>(num_blocks) * kBlockSize;
+  a.block_stride = static_cast<int64_t>(num_layers) * kBlockSize * row;
+  a.scale_stride = static_cast<int64_t>(num_layers) * num_kv_heads;
   a.num_tokens = num_tokens;
   a.num_kv_heads = num_kv_heads;
   a.head_dim = head_dim;
@@ -535,9 +538,11 @@ pkv_status pkv_write_cache_fp8(const void* k_new, const void* v_new, void* k_poo
 }
 
 pkv_status pkv_copy_blocks_fp8(void* k_pool, void* v_pool, float* k_scale, float* v_scale, const int32_t* pairs,
-                               int num_pairs, int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                               int32_t* dev_status, void* stream) {
-  if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+                               int num_pairs, int num_layers, int num_kv_heads, int head_dim, int block_size,
+                               int num_blocks, int32_t* dev_status, void* stream) {
+  if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || num_layers <= 0 ||
+      num_layers > kMaxLayers)
+    return PKV_ERR_INVALID_ARG;
   if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
   if (num_pairs == 0) return PKV_OK;
   if (!k_pool || !v_pool || !k_scale || !v_scale || !pairs) return PKV_ERR_INVALID_ARG;
@@ -549,12 +554,13 @@ pkv_status pkv_copy_blocks_fp8(void* k_pool, void* v_pool, float* k_scale, float
   a.v_pool = static_cast<uint16_t*>(v_pool);
   a.pairs = pairs;
   a.dev_status = dev_status;
-  a.block_elems = static_cast<int64_t>(kBlockSize) * num_kv_heads * head_dim / 2;  // 16 * H_kv * D bytes
+  // num_layers * 16 * H_kv * D bytes, counted in 16-bit units
+  a.block_elems = static_cast<int64_t>(num_layers) * kBlockSize * num_kv_heads * head_dim / 2;
   a.num_pairs = num_pairs;
   a.num_blocks = num_blocks;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
-  a.scales_per_block = num_kv_heads;
+  a.scales_per_block = num_layers * num_kv_heads;
   return launch_copy_blocks(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -567,11 +573,15 @@ namespace {
 pkv_status prepare_decode_fp8(DecodeCall* c, void* out, const void* q, const void* k_pool, const void* v_pool,
                               const float* k_scale, const float* v_scale, const int32_t* block_tables,
                               int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads,
-                              int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
-                              int partition_size, int max_context_len, void* workspace, size_t workspace_bytes,
-                              pkv_dtype q_dtype, pkv_dtype out_dtype, int32_t* dev_status) {
+                              int num_kv_heads, int head_dim, int block_size, int num_blocks, int num_layers,
+                              float scale, int partition_size, int max_context_len, void* workspace,
+                              size_t workspace_bytes, pkv_dtype q_dtype, pkv_dtype out_dtype, int32_t* dev_status) {
   if (partition_size == PKV_PARTITION_BALANCED || block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
-  pkv_status st = prepare_decode(c, out, q, k_pool, v_pool, 0, block_tables, max_blocks_per_seq, context_lens,
+  if (num_layers <= 0 || num_layers > kMaxLayers || num_kv_heads <= 0 || head_dim <= 0)
+    return PKV_ERR_INVALID_ARG;
+  // One byte per code: the block stride in codes is the stride in bytes.
+  const int64_t block_bytes = static_cast<int64_t>(num_layers) * kBlockSize * num_kv_heads * head_dim;
+  pkv_status st = prepare_decode(c, out, q, k_pool, v_pool, block_bytes, block_tables, max_blocks_per_seq, context_lens,
                                  num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                                  partition_size, max_context_len, workspace, workspace_bytes, q_dtype, out_dtype,
                                  dev_status, false);
@@ -582,7 +592,7 @@ pkv_status prepare_decode_fp8(DecodeCall* c, void* out, const void* q, const voi
     return PKV_ERR_INVALID_ARG;
   c->args.k_scale = k_scale;
   c->args.v_scale = v_scale;
-  // FP8 pools are dense (one layer): the same block stride, in bytes.
+  c->args.scale_stride = static_cast<int64_t>(num_layers) * num_kv_heads;
   if (!encode_pool_map(&c->tmap_k, k_pool, num_blocks, kBlockSize, num_kv_heads, head_dim, 1, c->args.block_stride) ||
       !encode_pool_map(&c->tmap_v, v_pool, num_blocks, kBlockSize, num_kv_heads, head_dim, 1, c->args.block_stride))
     return PKV_ERR_CUDA;
@@ -598,14 +608,15 @@ pkv_status pkv_decode_partitions_fp8(void* out, const void* q, const void* k_poo
                                      const float* k_scale, const float* v_scale, const int32_t* block_tables,
                                      int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
                                      int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                                     float scale, int partition_size, int max_context_len, void* workspace,
+                                     int num_layers, float scale, int partition_size, int max_context_len, void* workspace,
                                      size_t workspace_bytes, pkv_dtype q_dtype, pkv_dtype out_dtype,
                                      int32_t* dev_status, void* stream) {
   DecodeCall c{};
   const pkv_status st = prepare_decode_fp8(&c, out, q, k_pool, v_pool, k_scale, v_scale, block_tables,
                                            max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
-                                           head_dim, block_size, num_blocks, scale, partition_size, max_context_len,
-                                           workspace, workspace_bytes, q_dtype, out_dtype, dev_status);
+                                           head_dim, block_size, num_blocks, num_layers, scale, partition_size,
+                                           max_context_len, workspace, workspace_bytes, q_dtype, out_dtype,
+                                           dev_status);
   if (st != PKV_OK || num_seqs == 0) return st;
   return launch_decode_partitions_fp8(c.args, c.tmap_k, c.tmap_v, head_dim, q_dtype == PKV_BF16,
                                       static_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -618,14 +629,15 @@ pkv_status pkv_decode_step_partitions_fp8(void* out, const void* q, const void* 
                                           const float* v_scale, const int32_t* block_tables, int max_blocks_per_seq,
                                           const int32_t* context_lens, const int32_t* slot_mapping, int num_seqs,
                                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                                          int num_blocks, float scale, int partition_size, int max_context_len,
+                                          int num_blocks, int num_layers, float scale, int partition_size, int max_context_len,
                                           void* workspace, size_t workspace_bytes, pkv_dtype q_dtype,
                                           pkv_dtype out_dtype, int32_t* dev_status, void* stream) {
   DecodeCall c{};
   const pkv_status st = prepare_decode_fp8(&c, out, q, k_pool, v_pool, k_scale, v_scale, block_tables,
                                            max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
-                                           head_dim, block_size, num_blocks, scale, partition_size, max_context_len,
-                                           workspace, workspace_bytes, q_dtype, out_dtype, dev_status);
+                                           head_dim, block_size, num_blocks, num_layers, scale, partition_size,
+                                           max_context_len, workspace, workspace_bytes, q_dtype, out_dtype,
+                                           dev_status);
   if (st != PKV_OK || num_seqs == 0) return st;
   const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
   const int64_t stride = new_row_stride ? new_row_stride : row;
@@ -650,13 +662,13 @@ pkv_status pkv_decode_step_fp8(void* out, const void* q, const void* k_new, cons
                                const float* v_scale, const int32_t* block_tables, int max_blocks_per_seq,
                                const int32_t* context_lens, const int32_t* slot_mapping, int num_seqs,
                                int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                               float scale, int partition_size, int max_context_len, void* workspace,
+                               int num_layers, float scale, int partition_size, int max_context_len, void* workspace,
                                size_t workspace_bytes, pkv_dtype q_dtype, pkv_dtype out_dtype, int32_t* dev_status,
                                void* stream) {
   const pkv_status st = pkv_decode_step_partitions_fp8(
       out, q, k_new, v_new, new_row_stride, k_pool, v_pool, k_scale, v_scale, block_tables, max_blocks_per_seq,
-      context_lens, slot_mapping, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
-      partition_size, max_context_len, workspace, workspace_bytes, q_dtype, out_dtype, dev_status, stream);
+      context_lens, slot_mapping, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, num_layers,
+      scale, partition_size, max_context_len, workspace, workspace_bytes, q_dtype, out_dtype, dev_status, stream);
   if (st != PKV_OK) return st;
   return pkv_decode_reduce(out, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, partition_size,
                            max_context_len, workspace, workspace_bytes, out_dtype, dev_status, stream);
@@ -666,13 +678,14 @@ pkv_status pkv_decode_attention_fp8(void* out, const void* q, const void* k_pool
                                     const float* k_scale, const float* v_scale, const int32_t* block_tables,
                                     int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
                                     int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                                    float scale, int partition_size, int max_context_len, void* workspace,
+                                    int num_layers, float scale, int partition_size, int max_context_len, void* workspace,
                                     size_t workspace_bytes, pkv_dtype q_dtype, pkv_dtype out_dtype,
                                     int32_t* dev_status, void* stream) {
   pkv_status st = pkv_decode_partitions_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables,
                                             max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
-                                            head_dim, block_size, num_blocks, scale, partition_size, max_context_len,
-                                            workspace, workspace_bytes, q_dtype, out_dtype, dev_status, stream);
+                                            head_dim, block_size, num_blocks, num_layers, scale, partition_size,
+                                            max_context_len, workspace, workspace_bytes, q_dtype, out_dtype,
+                                            dev_status, stream);
   if (st != PKV_OK) return st;
   return pkv_decode_reduce(out, context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, partition_size,
                            max_context_len, workspace, workspace_bytes, out_dtype, dev_status, stream);

@@ -115,12 +115,12 @@ __global__ void __launch_bounds__(256) write_cache_fp8_kernel(WriteCacheFp8Args 
       continue;
     }
     const int g = (v * 16) / a.head_dim;
-    const float sc = (which ? a.v_scale : a.k_scale)[(slot / kBlockSize) * a.num_kv_heads + g];
+    const float sc = (which ? a.v_scale : a.k_scale)[(slot / kBlockSize) * a.scale_stride + g];
     const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
     uint32_t c[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) c[i] = fp8::quantize4(w[2 * i], w[2 * i + 1], sc, bf16);
-    uint8_t* dst = (which ? a.v_pool : a.k_pool) + slot * row;
+    uint8_t* dst = (which ? a.v_pool : a.k_pool) + (slot / kBlockSize) * a.block_stride + (slot % kBlockSize) * row;
     reinterpret_cast<uint4*>(dst)[v] = make_uint4(c[0], c[1], c[2], c[3]);
   }
 }

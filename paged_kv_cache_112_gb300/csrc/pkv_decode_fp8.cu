@@ -372,12 +372,12 @@ __device__ __forceinline__ void partition_unit_fp8(const DecodeArgs& a, const CU
   // Scales of (entry, g); 1 for an entry outside the pool (its tile is masked).
   auto ks_of = [&](int phys) {
     return static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks)
-               ? __ldg(a.k_scale + static_cast<int64_t>(phys) * Hkv + g)
+               ? __ldg(a.k_scale + static_cast<int64_t>(phys) * a.scale_stride + g)
                : 1.f;
   };
   auto vs_of = [&](int phys) {
     return static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks)
-               ? __ldg(a.v_scale + static_cast<int64_t>(phys) * Hkv + g)
+               ? __ldg(a.v_scale + static_cast<int64_t>(phys) * a.scale_stride + g)
                : 1.f;
   };
   // Lane j holds the entry and scales of the warp's tile j of the current

@@ -45,6 +45,8 @@ struct WriteCacheFp8Args {
   int32_t* dev_status;
   int64_t stride;        // elements between consecutive new tokens
   int64_t num_slots;
+  int64_t block_stride;  // pool bytes between consecutive blocks
+  int64_t scale_stride;  // scales (floats) between consecutive blocks' rows
   int num_tokens;
   int num_kv_heads;
   int head_dim;
@@ -116,9 +118,10 @@ struct DecodeArgs {
   const int32_t* slot_mapping;  // [S]: slot of position L-1, or -1
   uint16_t* k_pool_w;
   uint16_t* v_pool_w;
-  // FP8 pools only: per-(block, KV head) scales, [num_blocks][num_kv_heads].
+  // FP8 pools only: per-(block, KV head) scales, block b's row at b * scale_stride.
   const float* k_scale;
   const float* v_scale;
+  int64_t scale_stride;
 };
 
 // Split-K workspace layout (regions 256-byte aligned).  Fixed partitions:
@@ -136,6 +139,10 @@ int current_sm_count(int fallback);
 // Raises a kernel's dynamic shared memory limit to `bytes` on the current
 // device (once per kernel, device and size).
 cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
+
+// Upper bound on the layers an FP8 all-layer pool holds per block (keeps the
+// per-block scale count, layers x H_kv, well inside an int).
+constexpr int kMaxLayers = 4096;
 
 // Balanced split geometry (pkv_decode_balanced.cu).
 constexpr int kBalancedMaxSeqs = 4096;

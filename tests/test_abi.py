@@ -124,11 +124,13 @@ def test_write_and_copy_argument_validation(lib):
 def test_fp8_argument_validation(lib):
     def d(**kw):
         a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, ks=FAKE, vs=FAKE, bt=FAKE, maxb=4, cl=FAKE, S=2, Hq=8, Hkv=2,
-                 D=128, B=16, NB=10, scale=0.1, ps=0, maxlen=64, ws=None, wsb=0, qd=pkv.PKV_BF16, od=pkv.PKV_F32)
+                 D=128, B=16, NB=10, L=1, scale=0.1, ps=0, maxlen=64, ws=None, wsb=0, qd=pkv.PKV_BF16,
+                 od=pkv.PKV_F32)
         a.update(kw)
         return lib.pkv_decode_attention_fp8(a["out"], a["q"], a["k"], a["v"], a["ks"], a["vs"], a["bt"], a["maxb"],
-                                            a["cl"], a["S"], a["Hq"], a["Hkv"], a["D"], a["B"], a["NB"], a["scale"],
-                                            a["ps"], a["maxlen"], a["ws"], a["wsb"], a["qd"], a["od"], None, None)
+                                            a["cl"], a["S"], a["Hq"], a["Hkv"], a["D"], a["B"], a["NB"], a["L"],
+                                            a["scale"], a["ps"], a["maxlen"], a["ws"], a["wsb"], a["qd"], a["od"],
+                                            None, None)
 
     assert d(D=64) == pkv.PKV_ERR_UNSUPPORTED  # FP8 tiles: head_dim 128 only
     assert d(ps=pkv.PARTITION_BALANCED) == pkv.PKV_ERR_UNSUPPORTED
@@ -138,19 +140,24 @@ def test_fp8_argument_validation(lib):
     assert d(q=FAKE + 8) == pkv.PKV_ERR_INVALID_ARG  # q rows are read as 16-byte vectors
     assert d(qd=pkv.PKV_F32) == pkv.PKV_ERR_INVALID_ARG
     assert d(ps=16, maxlen=64) == pkv.PKV_ERR_WORKSPACE
+    assert d(L=0) == pkv.PKV_ERR_INVALID_ARG  # layers per block: 1..4096
+    assert d(L=4097) == pkv.PKV_ERR_INVALID_ARG
     assert d(S=0) == pkv.PKV_OK
+    assert d(S=0, L=32) == pkv.PKV_OK
     w = lambda **kw: lib.pkv_write_cache_fp8(FAKE, FAKE, FAKE, FAKE, kw.get("ks", FAKE), FAKE, FAKE, kw.get("T", 4),
                                              kw.get("stride", 0), 8, kw.get("D", 128), kw.get("B", 16), 100,
-                                             kw.get("dt", pkv.PKV_BF16), None, None)
+                                             kw.get("L", 1), kw.get("dt", pkv.PKV_BF16), None, None)
     assert w(D=72) == pkv.PKV_ERR_UNSUPPORTED  # 16 codes per vector within one head
     assert w(B=32) == pkv.PKV_ERR_UNSUPPORTED
     assert w(ks=None) == pkv.PKV_ERR_INVALID_ARG
     assert w(dt=pkv.PKV_F32) == pkv.PKV_ERR_INVALID_ARG
     assert w(stride=12) == pkv.PKV_ERR_INVALID_ARG
+    assert w(L=0) == pkv.PKV_ERR_INVALID_ARG
     assert w(T=0) == pkv.PKV_OK
-    c = lambda **kw: lib.pkv_copy_blocks_fp8(FAKE, FAKE, kw.get("ks", FAKE), FAKE, FAKE, kw.get("P", 3), 8, 128,
-                                             kw.get("B", 16), 100, None, None)
+    c = lambda **kw: lib.pkv_copy_blocks_fp8(FAKE, FAKE, kw.get("ks", FAKE), FAKE, FAKE, kw.get("P", 3),
+                                             kw.get("L", 1), 8, 128, kw.get("B", 16), 100, None, None)
     assert c(B=8) == pkv.PKV_ERR_UNSUPPORTED
+    assert c(L=0) == pkv.PKV_ERR_INVALID_ARG
     assert c(ks=None) == pkv.PKV_ERR_INVALID_ARG
     assert c(P=0) == pkv.PKV_OK
 
