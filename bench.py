@@ -28,6 +28,10 @@ statement of the same computation) on a bounded sample of the workload.
 `--swap-gib X` times swapping X GiB of a preempted sequence's blocks out to
 pinned host memory and back in (pkv_swap_blocks).
 
+`--op write|copy` times pkv_write_cache (a bulk prefill of --op-tokens
+tokens; --kv fp8: pkv_write_cache_fp8) or pkv_copy_blocks (--op-pairs pairs)
+alone, in GB/s of algorithmic bytes.
+
 `--layers N` times every layer of a decode step over an all-layer pool
 [2][NB][N][16][H_kv][D], the step captured once as a CUDA graph and replayed
 (eager time reported beside it).
@@ -97,6 +101,27 @@ def job_gbs(bytes_per_rank_step: int, world: int, steps: int, elapsed_ms: float)
 
 # ----------------------------------------------------------- byte accounting
 
+def write_bytes(num_tokens, num_kv_heads, head_dim, fp8=False):
+    """Algorithmic bytes of writing `num_tokens` new tokens: read their 16-bit
+    K and V rows and write them into the pool (16-bit rows, or one e4m3 code
+    per element plus the K and V scale read per (token, KV head)), and read
+    the slot mapping."""
+    T, Hkv, D = num_tokens, num_kv_heads, head_dim
+    if fp8:
+        return 2 * T * Hkv * D * (2 + 1) + T * Hkv * 2 * 4 + T * 4
+    return 2 * T * Hkv * D * 2 * 2 + T * 4
+
+
+def copy_bytes(num_pairs, block_size, num_kv_heads, head_dim, fp8=False):
+    """Algorithmic bytes of `num_pairs` copy-on-write block copies: each reads
+    and writes one K and one V block (16-bit, or e4m3 codes plus the block's
+    K and V scales) and reads its (src, dst) pair."""
+    P, B, Hkv, D = num_pairs, block_size, num_kv_heads, head_dim
+    if fp8:
+        return P * (2 * (B * Hkv * D + Hkv * 4) * 2 + 8)
+    return P * (2 * B * Hkv * D * 2 * 2 + 8)
+
+
 def step_bytes(wl, out_bytes_per_elem=4):
     """Algorithmic bytes of one step, split into the partition kernel's share and the rest."""
     S, Hq, Hkv, D = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
@@ -108,9 +133,8 @@ def step_bytes(wl, out_bytes_per_elem=4):
     out = S * Hq * D * out_bytes_per_elem
     lens = S * 4
     attn = kv + tables + q + out + lens
-    T = wl.slot_mapping.shape[0]
-    write = 2 * T * Hkv * D * 2 * 2 + T * 4  # read new rows + write pool rows, K and V; slots
-    cow = wl.copy_pairs.shape[0] * (2 * B * Hkv * D * 2 * 2 + 8)
+    write = write_bytes(wl.slot_mapping.shape[0], Hkv, D)
+    cow = copy_bytes(wl.copy_pairs.shape[0], B, Hkv, D)
     return {"attention": attn, "kv": kv, "write": write, "copy": cow, "step": attn + write + cow}
 
 
@@ -123,9 +147,8 @@ def step_bytes_fp8(wl, out_bytes_per_elem=4):
     blocks = int(np.sum((L + 15) // 16))
     kv = int(L.sum()) * Hkv * D * 2 + blocks * Hkv * 2 * 4
     attn = kv + blocks * 4 + S * Hq * D * 2 + S * Hq * D * out_bytes_per_elem + S * 4
-    T = wl.slot_mapping.shape[0]
-    write = 2 * T * Hkv * D * (2 + 1) + T * Hkv * 2 * 4 + T * 4
-    cow = wl.copy_pairs.shape[0] * (2 * (16 * Hkv * D + Hkv * 4) * 2 + 8)
+    write = write_bytes(wl.slot_mapping.shape[0], Hkv, D, fp8=True)
+    cow = copy_bytes(wl.copy_pairs.shape[0], 16, Hkv, D, fp8=True)
     return {"attention": attn, "kv": kv, "write": write, "copy": cow, "step": attn + write + cow}
 
 
@@ -691,6 +714,126 @@ def run_swap(args):
             "pages_figure": "1.25 GiB over PCIe 4.0 x16 at ~25 GB/s: ~50 ms each way"}
 
 
+def cache_op_sets(op, n, block_size, sets, rng):
+    """Disjoint inputs for `sets` calls of write_cache or copy_blocks.
+    write: n tokens per set filling whole blocks in order, the blocks a random
+    permutation of the pool: slots int32 [sets, n].  copy: n (src, dst) pairs
+    per set, every src and dst block distinct across all sets: pairs int32
+    [sets, n, 2].  Returns (array, blocks the pool needs)."""
+    B = block_size
+    if op == "write":
+        per = -(-n // B)
+        nb = sets * per
+        perm = rng.permutation(nb).astype(np.int64)
+        t = np.arange(n, dtype=np.int64)
+        slots = np.stack([perm[r * per + t // B] * B + t % B for r in range(sets)])
+        return slots.astype(np.int32), nb
+    nb = sets * 2 * n
+    perm = rng.permutation(nb).astype(np.int32).reshape(sets, 2, n)
+    return np.ascontiguousarray(np.stack([perm[:, 0], perm[:, 1]], axis=2)), nb
+
+
+def run_cache_op(args):
+    """pkv_write_cache or pkv_copy_blocks timed alone (--op write | copy), on
+    the recipe's row shape (H_kv, head_dim, dtype; --kv fp8 for the FP8 entry
+    points): a bulk write of --op-tokens new tokens (a prefill fills whole
+    blocks, scattered over the pool; --op-tokens = the batch size gives the
+    decode step's write), or --op-pairs copy-on-write block copies.  GB/s of
+    algorithmic bytes (write_bytes / copy_bytes).  Call i works on input set
+    i mod R, the R sets disjoint in inputs and blocks and together larger
+    than 3x L2."""
+    import torch
+
+    import paged_kv_cache_112_gb300 as pkv
+    import pkv_inputs as P
+
+    _, _, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkv.load()
+    spec = P.CONFIGS[args.config]
+    Hkv, D, dtype = spec["num_kv_heads"], spec["head_dim"], spec["dtype"]
+    fp8 = args.kv == "fp8"
+    if fp8 and args.block_size != 16:
+        raise SystemExit("FP8 pools use 16-token blocks")
+    B = args.block_size
+    n = args.op_tokens if args.op == "write" else args.op_pairs
+    if n <= 0:
+        raise SystemExit("--op-tokens / --op-pairs must be positive")
+    per_call = write_bytes(n, Hkv, D, fp8) if args.op == "write" else copy_bytes(n, B, Hkv, D, fp8)
+    l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    R = max(2, min(4096, math.ceil(3 * l2 / per_call)))
+    sets, NB = cache_op_sets(args.op, n, B, R, np.random.default_rng(args.config))
+    tdt = torch.float16 if dtype == "f16" else torch.bfloat16
+    gen = torch.Generator(device=dev).manual_seed(args.config)
+    shape = (NB, B, Hkv, D)
+    if fp8:
+        k_pool = torch.randint(0, 0x7F, shape, generator=gen, dtype=torch.uint8, device=dev)
+        v_pool = torch.randint(0, 0x7F, shape, generator=gen, dtype=torch.uint8, device=dev)
+        k_scale = torch.rand((NB, Hkv), generator=gen, device=dev) + 0.5
+        v_scale = torch.rand((NB, Hkv), generator=gen, device=dev) + 0.5
+    else:
+        k_pool = torch.randn(shape, generator=gen, device=dev).to(tdt)
+        v_pool = torch.randn(shape, generator=gen, device=dev).to(tdt)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if args.op == "write":
+        k_new = torch.randn((R, n, Hkv, D), generator=gen, device=dev).to(tdt)
+        v_new = torch.randn((R, n, Hkv, D), generator=gen, device=dev).to(tdt)
+        slots = torch.from_numpy(sets).to(dev)
+
+        def call(i):
+            r = i % R
+            if fp8:
+                pkv.write_cache_fp8(k_new[r], v_new[r], k_pool, v_pool, k_scale, v_scale, slots[r], status=status)
+            else:
+                pkv.write_cache(k_new[r], v_new[r], k_pool, v_pool, slots[r], status=status)
+        entry = "pkv_write_cache_fp8" if fp8 else "pkv_write_cache"
+        kernel = "write_cache_fp8_kernel" if fp8 else "write_cache_kernel"
+        what = f"{n} new tokens filling whole {B}-token blocks scattered over a {NB}-block pool"
+    else:
+        pairs = torch.from_numpy(sets).to(dev)
+
+        def call(i):
+            r = i % R
+            if fp8:
+                pkv.copy_blocks_fp8(k_pool, v_pool, k_scale, v_scale, pairs[r], status=status)
+            else:
+                pkv.copy_blocks(k_pool, v_pool, pairs[r], status=status)
+        entry = "pkv_copy_blocks_fp8" if fp8 else "pkv_copy_blocks"
+        kernel = "copy_blocks_kernel"
+        what = f"{n} copy-on-write pairs of {B}-token blocks, distinct blocks of a {NB}-block pool"
+    K, W = args.steps, args.warmup
+    for i in range(W):
+        call(i)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(K):
+        call(W + i)
+    b.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    ms = a.elapsed_time(b) / K
+    gbs = per_call / (ms * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+    return {"metric": f"{entry} alone, GB/s of algorithmic bytes", "value": round(gbs, 2), "unit": "GB/s",
+            "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": f"e4m3 KV, {dtype} new rows" if fp8 else dtype, "data": "synthetic",
+            "config": {"workload": f"{spec['name']}: {what}", "num_kv_heads": Hkv, "head_dim": D,
+                       "block_size": B, "entry": entry, "bytes_per_call": per_call,
+                       "l2": f"inputs larger than L2: {R} disjoint input sets of {per_call / 1e6:.2f} MB rotated "
+                             f"(L2 {l2 / 1e6:.0f} MB)"},
+            "us_per_call": round(ms * 1e3, 3),
+            "roofline": {"bound": "hbm", "kernel": kernel, "achieved": round(gbs, 2), "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": round(gbs / peak, 4), "traffic": None},
+            "clocks": clocks, "gpu_launches": K}
+
+
 def kernel_source_hash(paths) -> str:
     """First 16 hex digits of a sha256 over the given sources with comments
     and whitespace removed: any change to the code changes it, a change to a
@@ -864,6 +1007,13 @@ def main(argv=None):
                     help="time every layer of a decode step (this many) over an all-layer pool, as a CUDA graph")
     ap.add_argument("--fused", action="store_true",
                     help="with --kv fp8: fuse the quantising write into the partition kernel (pkv_decode_step_fp8)")
+    ap.add_argument("--op", default=None, choices=["write", "copy"],
+                    help="time pkv_write_cache (--op-tokens new tokens) or pkv_copy_blocks (--op-pairs pairs) alone")
+    ap.add_argument("--op-tokens", type=int, default=65536,
+                    help="with --op write: tokens per call (default: a 64K-token bulk prefill)")
+    ap.add_argument("--op-pairs", type=int, default=128,
+                    help="with --op copy: copy-on-write pairs per call (default 128, about the prefix-sharing "
+                         "recipe's per-step count)")
     ap.add_argument("--kv", default="16bit", choices=["16bit", "fp8"],
                     help="KV pool format: the workload's 16-bit type, or e4m3 codes with per-(block, KV head) "
                          "scales (copy, write and attention through the *_fp8 entry points)")
@@ -878,6 +1028,8 @@ def main(argv=None):
         line = run_reference(args)
     elif args.swap_gib > 0:
         line = run_swap(args)
+    elif args.op is not None:
+        line = run_cache_op(args)
     elif args.layers > 0:
         line = run_layers(args)
     else:

@@ -29,3 +29,32 @@ def test_kernel_source_hash_ignores_comments_not_code(tmp_path):
     assert bench.kernel_source_hash([str(a)]) == h0
     a.write_text("__global__ void k(int* p) {\n  p[0] = 2;\n}\n")
     assert bench.kernel_source_hash([str(a)]) != h0
+
+
+def test_write_and_copy_bytes_count_rows_and_blocks():
+    # one token of the 8B-class row (8 KV heads x 128): K and V rows read (2 B) and written (2 B), one slot
+    assert bench.write_bytes(1, 8, 128) == 2 * 1024 * 4 + 4
+    # FP8: rows read (2 B), codes written (1 B), the K and V scale of each KV head, one slot
+    assert bench.write_bytes(1, 8, 128, fp8=True) == 2 * 1024 * 3 + 8 * 8 + 4
+    # one pair of 16-token blocks: K and V block read and written, the pair read
+    assert bench.copy_bytes(1, 16, 8, 128) == 2 * 16 * 1024 * 2 * 2 + 8
+    assert bench.copy_bytes(1, 16, 8, 128, fp8=True) == 2 * (16 * 1024 + 32) * 2 + 8
+    wl = P.make_workload(5, num_seqs=8, lens=("prefix", 64, 0, 40))
+    assert wl.copy_pairs.shape[0] > 0
+    nb = bench.step_bytes(wl)
+    assert nb["copy"] == bench.copy_bytes(wl.copy_pairs.shape[0], 16, wl.num_kv_heads, wl.head_dim)
+
+
+def test_cache_op_sets_are_disjoint_whole_blocks():
+    rng = np.random.default_rng(0)
+    slots, nb = bench.cache_op_sets("write", 40, 16, 5, rng)
+    assert slots.shape == (5, 40) and slots.dtype == np.int32 and nb == 5 * 3
+    assert len(np.unique(slots)) == slots.size and slots.min() >= 0 and slots.max() < nb * 16
+    for r in range(5):
+        # tokens fill their blocks in order: offset t % 16 within block t // 16 of the set
+        assert np.array_equal(slots[r] % 16, np.arange(40) % 16)
+        blocks = slots[r] // 16
+        assert np.all(blocks[np.arange(40) // 16 * 16] == blocks)
+    pairs, nb = bench.cache_op_sets("copy", 7, 16, 4, rng)
+    assert pairs.shape == (4, 7, 2) and pairs.dtype == np.int32 and nb == 4 * 2 * 7
+    assert len(np.unique(pairs)) == pairs.size and pairs.min() >= 0 and pairs.max() < nb
