@@ -851,6 +851,10 @@ def kernel_source_hash(paths) -> str:
     return h.hexdigest()[:16]
 
 
+# short names of the workload recipes, as the profile summaries are named
+WORKLOAD_SLUGS = {1: "tiny", 2: "8b_class", 3: "70b_class", 4: "long_context", 5: "prefix_sharing"}
+
+
 def _recorded_traffic(cfg, kernel):
     """DRAM bytes per launch of the partition kernel from the committed ncu
     summary, if it was taken on the current kernel sources; else None."""
@@ -860,7 +864,7 @@ def _recorded_traffic(cfg, kernel):
     if kernel not in sources:
         return None
     stem, src = sources[kernel]
-    summ = os.path.join(ROOT, "profiles", f"{stem}_config{cfg}_traffic.txt")
+    summ = os.path.join(ROOT, "profiles", f"{stem}_{WORKLOAD_SLUGS[cfg]}_traffic.txt")
     srcs = [os.path.join(ROOT, "paged_kv_cache_112_gb300", "csrc", f) for f in (src, "pkv_device.cuh")]
     if not os.path.exists(summ):
         return None
