@@ -456,7 +456,9 @@ pkv_status pkv_decode_step_partitions_fp8(void* out, const void* q, const void* 
 typedef struct pkv_bm pkv_bm;
 
 /* A manager of num_blocks blocks of block_size tokens; watermark_blocks are
- * kept back from admissions (add_sequence, swap_in).  NULL on bad sizes. */
+ * kept back from admissions (add_sequence, swap_in).  NULL on bad sizes
+ * (non-positive, a watermark above num_blocks, or num_blocks * block_size
+ * slots beyond the int32 range). */
 pkv_bm* pkv_bm_create(int num_blocks, int block_size, int watermark_blocks);
 void pkv_bm_destroy(pkv_bm* bm);
 

@@ -169,6 +169,8 @@ extern "C" {
 
 pkv_bm* pkv_bm_create(int num_blocks, int block_size, int watermark_blocks) {
   if (num_blocks <= 0 || block_size <= 0 || watermark_blocks < 0 || watermark_blocks > num_blocks) return nullptr;
+  // slots (block * block_size + offset) are int32
+  if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX) return nullptr;
   pkv_bm* m = new pkv_bm();
   m->num_blocks = num_blocks;
   m->block_size = block_size;

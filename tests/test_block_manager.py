@@ -301,6 +301,10 @@ def test_watermark_reserves_blocks_for_appends():
 def test_c_abi_guards():
     lib = pkv.load()
     assert not lib.pkv_bm_create(0, 16, 0) and not lib.pkv_bm_create(8, 16, 9)
+    assert not lib.pkv_bm_create(2, 2 ** 30, 0)  # 2^31 slots: beyond int32
+    edge = lib.pkv_bm_create(1, 2 ** 31 - 1, 0)  # the largest slot count that fits
+    assert edge
+    lib.pkv_bm_destroy(edge)
     assert lib.pkv_bm_available_blocks(None) == -pkv.PKV_ERR_INVALID_ARG
     assert lib.pkv_bm_free_sequence(None, 1) == -pkv.PKV_ERR_INVALID_ARG
     bm = pkv.BlockManager(4, 16)
