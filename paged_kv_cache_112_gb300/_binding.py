@@ -1,10 +1,12 @@
 """ctypes binding of libpkv (include/pkv.h): argument marshalling only.
 
 Every function takes torch tensors that already live on the GPU, checks
-their dtype, shape, device and contiguity, and forwards raw pointers, sizes
-and the current CUDA stream to the C ABI.  All computation happens in the
-library's kernels; there is no fallback path, and the library must be built
-(see build.py) or calls raise.
+their dtype, shape, strides and that they are CUDA tensors, and forwards raw
+pointers, sizes and the current CUDA stream to the C ABI.  The library
+launches on the current CUDA device, so the tensors must live there (one
+process per GPU; the device index is not checked per tensor).  All
+computation happens in the library's kernels; there is no fallback path,
+and the library must be built (see build.py) or calls raise.
 """
 from __future__ import annotations
 
