@@ -101,6 +101,16 @@ def job_gbs(bytes_per_rank_step: int, world: int, steps: int, elapsed_ms: float)
 
 # ----------------------------------------------------------- byte accounting
 
+def workload_config(wl, fp8=False):
+    """The keys of a JSON line's `config` that describe the workload, the same
+    for the CUDA arm and the oracle's reference arm."""
+    return {"workload": wl.name, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
+            "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
+            "total_context_tokens": int(wl.context_lens.astype(np.int64).sum()), "num_blocks": wl.num_blocks,
+            "cow_pairs": int(wl.copy_pairs.shape[0]),
+            "kv_cache": "e4m3 + per-(block, KV head) f32 scales" if fp8 else wl.dtype}
+
+
 def write_bytes(num_tokens, num_kv_heads, head_dim, fp8=False):
     """Algorithmic bytes of writing `num_tokens` new tokens: read their 16-bit
     K and V rows and write them into the pool (16-bit rows, or one e4m3 code
@@ -444,12 +454,8 @@ def run_gpu(args):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": f"e4m3 KV, {wl.dtype} q" if fp8 else wl.dtype, "data": "synthetic",
-        "config": {"workload": wl.name, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
-                   "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
-                   "partition_size": ps, "max_context_len": max_len, "total_context_tokens":
-                   int(wl.context_lens.astype(np.int64).sum()), "num_blocks": wl.num_blocks,
-                   "cow_pairs": int(wl.copy_pairs.shape[0]), "out_dtype": "f32",
-                   "kv_cache": "e4m3 + per-(block, KV head) f32 scales" if fp8 else wl.dtype,
+        "config": {**workload_config(wl, fp8), "partition_size": ps, "max_context_len": max_len,
+                   "out_dtype": "f32",
                    "entry": (("pkv_decode_step_fp8" if args.fused else
                               "pkv_write_cache_fp8 + pkv_decode_attention_fp8") if fp8 else
                              "pkv_write_cache + pkv_decode_attention" if args.unfused else "pkv_decode_step"),
@@ -754,8 +760,6 @@ def run_cache_op(args):
     spec = P.CONFIGS[args.config]
     Hkv, D, dtype = spec["num_kv_heads"], spec["head_dim"], spec["dtype"]
     fp8 = args.kv == "fp8"
-    if fp8 and args.block_size != 16:
-        raise SystemExit("FP8 pools use 16-token blocks")
     B = args.block_size
     n = args.op_tokens if args.op == "write" else args.op_pairs
     if n <= 0:
@@ -941,7 +945,7 @@ def run_reference(args):
     import oracle
     import pkv_inputs as P
 
-    wl = P.make_workload(args.config, poison=False)
+    wl = P.make_workload(args.config, poison=False, block_size=args.block_size)
     threads = oracle.hardware_threads()
     fp8 = args.kv == "fp8"
     if fp8:
@@ -982,7 +986,8 @@ def run_reference(args):
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "sample_rows": n_rows},
+            "config": {**workload_config(wl, fp8), "entry": "oracle.decode_attention" +
+                       ("_fp8" if fp8 else ""), "sample_rows": n_rows},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -1028,6 +1033,8 @@ def main(argv=None):
         args.warmup = 20 if args.impl == "ours" else 3
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.kv == "fp8" and args.block_size != 16:
+        ap.error("FP8 pools use 16-token blocks")
     if args.impl == "reference":
         line = run_reference(args)
     elif args.swap_gib > 0:

@@ -58,3 +58,22 @@ def test_cache_op_sets_are_disjoint_whole_blocks():
     pairs, nb = bench.cache_op_sets("copy", 7, 16, 4, rng)
     assert pairs.shape == (4, 7, 2) and pairs.dtype == np.int32 and nb == 4 * 2 * 7
     assert len(np.unique(pairs)) == pairs.size and pairs.min() >= 0 and pairs.max() < nb
+
+
+def test_reference_arm_prints_one_contract_line(capsys):
+    """`bench.py --impl reference` (the fp64 oracle on host cores) prints one
+    JSON line with the contract's keys, on the same workload description as
+    the CUDA arm."""
+    import json
+
+    bench.main(["--impl", "reference", "--config", "1", "--steps", "2", "--warmup", "3", "--ref-seconds", "0.5"])
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == "GB/s"
+    assert line["value"] > 0 and line["higher_is_better"] is True and line["steps"] == 2 and line["warmup"] == 3
+    wl = P.make_workload(1)
+    assert {k: line["config"][k] for k in bench.workload_config(wl)} == bench.workload_config(wl)
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
