@@ -58,6 +58,7 @@ if ROOT not in sys.path:
 
 METRIC = "decode paged-attention KV GB/s and % of GB300 HBM peak; sequences·layers/sec"
 E2E_BLOCK = 16  # end-to-end steps per captured graph
+REPS = 5  # repetitions the timed steps are split into (rate of each, and their median, beside the total)
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -342,19 +343,25 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    # Timed region A: exactly K steps, nothing else on the stream (value).
+    # Timed region A: exactly K steps, nothing else on the stream (value).  Events
+    # at the boundaries of REPS equal runs of steps give each repetition's rate.
     sampler = ClockSampler(local) if rank == 0 else None
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = REPS if K >= REPS else 1
+    bounds = [K * r // reps for r in range(reps + 1)]
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
     if sampler:
         sampler.start()
     barrier()
-    t_start.record()
-    for i in range(K):
-        step(W + i)
-    t_end.record()
+    marks[0].record()
+    for r in range(reps):
+        for i in range(bounds[r], bounds[r + 1]):
+            step(W + i)
+        marks[r + 1].record()
     barrier()
     clocks = sampler.stop() if sampler else None
-    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = marks[0].elapsed_time(marks[-1])
+    rep_gbs = [round(nb["step"] * (bounds[r + 1] - bounds[r]) / (marks[r].elapsed_time(marks[r + 1]) * 1e-3) / 1e9,
+                     2) for r in range(reps)]
     # Timed region B: the same K steps with CUDA events around every launch of
     # the partition kernel, for its average launch duration (the events stop
     # consecutive kernels from overlapping, so region A alone gives the step time).
@@ -464,6 +471,8 @@ def run_gpu(args):
         "pct_of_hbm_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_hbm_measured": round(100 * value / world / peak, 2),
         "seq_layers_per_s": round(world * wl.num_seqs / (ms * 1e-3), 1),
+        "repetitions": {"n": len(rep_gbs), "gbs_rank0": rep_gbs, "median_gbs_rank0": statistics.median(rep_gbs),
+                        "note": "the K timed steps in equal runs, one GPU's rate each; value is their total"},
         "kv_bytes_per_step": nb["kv"], "step_bytes": nb["step"],
         "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
