@@ -319,3 +319,92 @@ def test_c_abi_guards():
     with pytest.raises(pkv.PkvError):
         bm.append(1, 5)  # swapped out: no appends until swap_in
     assert bm.swap_in(1).size == 1 and bm.append(1, 5)[0] >= 0
+
+
+def test_concurrent_threads_keep_the_books():
+    """Four threads drive one manager at once (ctypes releases the GIL for
+    each call, so the C++ runs in parallel behind the manager's mutex).  The
+    threads share system prompts, so they hit, share and evict one another's
+    cached blocks.  Afterwards every block's refcount equals the number of
+    table rows that hold it, and the free and evictable lists hold exactly the
+    unreferenced blocks; freeing everything returns the whole pool."""
+    import threading
+
+    B, NB = 16, 96
+    bm = pkv.BlockManager(NB, B, watermark_blocks=2)
+    prompts = [[int(x) for x in np.random.default_rng(p).integers(0, 50, size=3 * B)] for p in range(3)]
+    live = {}
+    errors = []
+
+    def worker(w):
+        rng = np.random.default_rng(1000 + w)
+        mine = {}  # id -> (tokens, swapped)
+        next_id = w * 1_000_000
+        try:
+            for _ in range(1500):
+                op = rng.integers(0, 6)
+                ids = sorted(mine)
+                try:
+                    if op == 0 or not ids:
+                        p = prompts[rng.integers(0, 3)]
+                        toks = p[: rng.integers(1, len(p) + 1)] + [int(x) for x in rng.integers(0, 50, rng.integers(0, 9))]
+                        bm.add_sequence(next_id, toks)
+                        mine[next_id] = (toks, False)
+                        next_id += 1
+                    elif op == 1:
+                        sid = ids[rng.integers(0, len(ids))]
+                        toks, sw = mine[sid]
+                        if not sw:
+                            tok = int(rng.integers(0, 50))
+                            bm.append(sid, tok)
+                            mine[sid] = (toks + [tok], False)
+                    elif op == 2:
+                        sid = ids[rng.integers(0, len(ids))]
+                        toks, sw = mine[sid]
+                        if not sw:
+                            bm.fork(sid, next_id)
+                            mine[next_id] = (list(toks), False)
+                            next_id += 1
+                    elif op == 3:
+                        sid = ids[rng.integers(0, len(ids))]
+                        bm.free(sid)
+                        del mine[sid]
+                    elif op == 4:
+                        sid = ids[rng.integers(0, len(ids))]
+                        toks, sw = mine[sid]
+                        if sw:
+                            bm.swap_in(sid)
+                        else:
+                            bm.swap_out(sid)
+                        mine[sid] = (toks, not sw)
+                    else:
+                        sid = ids[rng.integers(0, len(ids))]
+                        toks, sw = mine[sid]
+                        assert bm.seq_len(sid) == len(toks)
+                        if not sw:
+                            assert len(bm.block_table(sid)) == -(-len(toks) // B)
+                except pkv.OutOfBlocks:
+                    pass
+            live.update(mine)
+        except Exception as e:  # surfaced in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(w,)) for w in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    holders = np.zeros(NB, dtype=np.int64)
+    for sid, (toks, sw) in live.items():
+        assert bm.seq_len(sid) == len(toks)
+        if not sw:
+            table = bm.block_table(sid)
+            assert len(table) == -(-len(toks) // B)
+            np.add.at(holders, table, 1)
+    refs = np.array([bm.refcount(b) for b in range(NB)])
+    assert np.array_equal(refs, holders)
+    assert bm.available_blocks == int(np.sum(refs == 0))
+    for sid in live:
+        bm.free(sid)
+    assert bm.available_blocks == NB
