@@ -493,6 +493,27 @@ int pkv_bm_fork(pkv_bm* bm, int64_t parent, int64_t child);
 int pkv_bm_append(pkv_bm* bm, int64_t seq_id, int32_t token, int32_t* slot, int32_t* cow_src,
                   int32_t* cow_dst);
 
+/*
+ * One decode step's host bookkeeping for a batch, under one lock: appends
+ * tokens[i] to sequence seq_ids[i] for i = 0 .. n-1 in order, exactly as n
+ * calls of pkv_bm_append would, and writes the device step's inputs (host
+ * arrays):
+ *   slot_mapping[i]   the slot of the appended token;
+ *   context_lens[i]   the sequence's length after the append;
+ *   block_tables[i][max_blocks_per_seq]   its table row, padded with pad_value;
+ *   cow_pairs[k][2]   (src, dst) of each copy-on-write, in batch order, for
+ *                     pkv_copy_blocks; room for n pairs.
+ * Returns the number of copy-on-write pairs.  All or nothing: unknown,
+ * swapped-out or repeated sequences, or a table wider than
+ * max_blocks_per_seq after the append, return -PKV_ERR_INVALID_ARG, and too
+ * few blocks for the batch returns -PKV_ERR_OUT_OF_BLOCKS; either way
+ * nothing changes.  A tail shared by several sequences of the batch is
+ * copied by the first that appends; the last holder then owns it.
+ */
+int pkv_bm_decode_step(pkv_bm* bm, const int64_t* seq_ids, const int32_t* tokens, int n,
+                       int32_t* slot_mapping, int32_t* context_lens, int32_t* block_tables,
+                       int max_blocks_per_seq, int32_t pad_value, int32_t* cow_pairs);
+
 /* Releases a sequence (its blocks' references). */
 int pkv_bm_free_sequence(pkv_bm* bm, int64_t seq_id);
 

@@ -68,6 +68,8 @@ _BM_SIGS = {
     "pkv_bm_fork": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64], ctypes.c_int),
     "pkv_bm_append": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32] + [ctypes.POINTER(ctypes.c_int32)] * 3,
                       ctypes.c_int),
+    "pkv_bm_decode_step": ([ctypes.c_void_p] * 3 + [ctypes.c_int] + [ctypes.c_void_p] * 3 +
+                           [ctypes.c_int, ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
     "pkv_bm_free_sequence": ([ctypes.c_void_p, ctypes.c_int64], ctypes.c_int),
     "pkv_bm_seq_len": ([ctypes.c_void_p, ctypes.c_int64], ctypes.c_int),
     "pkv_bm_block_table": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
@@ -520,6 +522,26 @@ class BlockManager:
         self._rc(self._lib.pkv_bm_append(self._h, int(seq_id), int(token), ctypes.byref(slot), ctypes.byref(src),
                                          ctypes.byref(dst)), "append")
         return slot.value, ((src.value, dst.value) if src.value >= 0 else None)
+
+    def decode_step(self, seq_ids, tokens, max_blocks_per_seq: int, pad_value: int = -1):
+        """pkv_bm_decode_step: appends tokens[i] to seq_ids[i] for the whole batch at once and returns
+        the device step's host inputs (slot_mapping int32[n], context_lens int32[n],
+        block_tables int32[n, max_blocks_per_seq], cow_pairs int32[P, 2]).  All or nothing."""
+        np = self._np
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64).reshape(-1)
+        toks = np.ascontiguousarray(tokens, dtype=np.int32).reshape(-1)
+        if ids.size != toks.size:
+            raise PkvError("decode_step: one token per sequence")
+        n, w = ids.size, int(max_blocks_per_seq)
+        slots = np.empty(n, dtype=np.int32)
+        lens = np.empty(n, dtype=np.int32)
+        tables = np.empty((n, w), dtype=np.int32)
+        pairs = np.empty((max(n, 1), 2), dtype=np.int32)
+        rc = self._lib.pkv_bm_decode_step(self._h, ids.ctypes.data, toks.ctypes.data, n, slots.ctypes.data,
+                                          lens.ctypes.data, tables.ctypes.data, w, int(pad_value),
+                                          pairs.ctypes.data)
+        p = self._rc(rc, "decode_step")
+        return slots, lens, tables, pairs[:p].copy()
 
     def free(self, seq_id: int) -> None:
         self._rc(self._lib.pkv_bm_free_sequence(self._h, int(seq_id)), "free_sequence")

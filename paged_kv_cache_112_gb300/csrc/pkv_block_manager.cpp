@@ -29,6 +29,7 @@
 #include <list>
 #include <mutex>
 #include <unordered_map>
+#include <unordered_set>
 #include <vector>
 
 #include "pkv.h"
@@ -160,6 +161,34 @@ int lookup(const pkv_bm* m, uint64_t h, uint64_t parent, const int32_t* tokens) 
   return it->second;
 }
 
+// Appends `token` to s (lock held): a fresh block when the tail is full, a
+// copy-on-write when it is shared.  -PKV_ERR_OUT_OF_BLOCKS (nothing changed)
+// when no block can be taken.
+int append_locked(pkv_bm* m, Sequence& s, int32_t token, int32_t* slot, int32_t* cow_src, int32_t* cow_dst) {
+  const int B = m->block_size;
+  const int pos = static_cast<int>(s.tokens.size());
+  *cow_src = *cow_dst = -1;
+  if (pos % B == 0) {  // the tail is full (or there is none): a fresh block
+    const int b = take_block(m);
+    if (b < 0) return -PKV_ERR_OUT_OF_BLOCKS;
+    s.table.push_back(b);
+  } else {
+    const int tail = s.table[pos / B];
+    if (m->blocks[tail].ref > 1) {  // shared tail: copy-on-write
+      const int b = take_block(m);
+      if (b < 0) return -PKV_ERR_OUT_OF_BLOCKS;
+      drop_ref(m, tail);
+      s.table[pos / B] = b;
+      *cow_src = tail;
+      *cow_dst = b;
+    }
+  }
+  s.tokens.push_back(token);
+  *slot = s.table[pos / B] * B + pos % B;
+  if ((pos + 1) % B == 0) register_full(m, s, pos / B);
+  return PKV_OK;
+}
+
 }  // namespace
 }  // namespace pkv
 
@@ -257,29 +286,68 @@ int pkv_bm_append(pkv_bm* m, int64_t seq_id, int32_t token, int32_t* slot, int32
   std::lock_guard<std::mutex> lock(m->mu);
   const auto it = m->seqs.find(seq_id);
   if (it == m->seqs.end() || it->second.swapped || !slot || !cow_src || !cow_dst) return -PKV_ERR_INVALID_ARG;
-  Sequence& s = it->second;
+  return append_locked(m, it->second, token, slot, cow_src, cow_dst);
+}
+
+int pkv_bm_decode_step(pkv_bm* m, const int64_t* seq_ids, const int32_t* tokens, int n, int32_t* slot_mapping,
+                       int32_t* context_lens, int32_t* block_tables, int max_blocks_per_seq, int32_t pad_value,
+                       int32_t* cow_pairs) {
+  if (!m) return -PKV_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(m->mu);
+  if (n < 0 || max_blocks_per_seq < 0) return -PKV_ERR_INVALID_ARG;
+  if (n == 0) return 0;
+  if (!seq_ids || !tokens || !slot_mapping || !context_lens || !cow_pairs ||
+      (!block_tables && max_blocks_per_seq > 0))
+    return -PKV_ERR_INVALID_ARG;
   const int B = m->block_size;
-  const int pos = static_cast<int>(s.tokens.size());
-  *cow_src = *cow_dst = -1;
-  if (pos % B == 0) {  // the tail is full (or there is none): a fresh block
-    const int b = take_block(m);
-    if (b < 0) return -PKV_ERR_OUT_OF_BLOCKS;
-    s.table.push_back(b);
-  } else {
-    const int tail = s.table[pos / B];
-    if (m->blocks[tail].ref > 1) {  // shared tail: copy-on-write
-      const int b = take_block(m);
-      if (b < 0) return -PKV_ERR_OUT_OF_BLOCKS;
-      drop_ref(m, tail);
-      s.table[pos / B] = b;
-      *cow_src = tail;
-      *cow_dst = b;
+  // Check the whole batch first, so that it either happens entirely or not
+  // at all: known, distinct, resident sequences whose tables fit the row
+  // width after the append, and enough blocks.  A shared tail is copied by
+  // the first of its holders that appends; a later holder finds one
+  // reference fewer, so the references each tail loses are counted as the
+  // batch would drop them.
+  std::vector<Sequence*> seqs(static_cast<size_t>(n));
+  std::unordered_set<int64_t> seen;
+  std::unordered_map<int, int> dropped;  // tail block -> references the batch drops before this point
+  int need = 0;
+  for (int i = 0; i < n; ++i) {
+    const auto it = m->seqs.find(seq_ids[i]);
+    if (it == m->seqs.end() || it->second.swapped || !seen.insert(seq_ids[i]).second) return -PKV_ERR_INVALID_ARG;
+    Sequence& s = it->second;
+    const int pos = static_cast<int>(s.tokens.size());
+    if (pos / B + 1 > max_blocks_per_seq) return -PKV_ERR_INVALID_ARG;
+    if (pos % B == 0) {
+      ++need;
+    } else {
+      const int tail = s.table[pos / B];
+      int& d = dropped[tail];
+      if (m->blocks[tail].ref - d > 1) {
+        ++need;
+        ++d;
+      }
+    }
+    seqs[static_cast<size_t>(i)] = &s;
+  }
+  if (need > available(m)) return -PKV_ERR_OUT_OF_BLOCKS;
+  int pairs = 0;
+  for (int i = 0; i < n; ++i) {
+    int32_t src, dst;
+    // cannot fail: the blocks were counted above
+    append_locked(m, *seqs[static_cast<size_t>(i)], tokens[i], slot_mapping + i, &src, &dst);
+    if (src >= 0) {
+      cow_pairs[2 * pairs] = src;
+      cow_pairs[2 * pairs + 1] = dst;
+      ++pairs;
     }
   }
-  s.tokens.push_back(token);
-  *slot = s.table[pos / B] * B + pos % B;
-  if ((pos + 1) % B == 0) register_full(m, s, pos / B);
-  return PKV_OK;
+  for (int i = 0; i < n; ++i) {
+    const Sequence& s = *seqs[static_cast<size_t>(i)];
+    context_lens[i] = static_cast<int32_t>(s.tokens.size());
+    int32_t* row = block_tables + static_cast<int64_t>(i) * max_blocks_per_seq;
+    const int w = static_cast<int>(s.table.size());
+    for (int j = 0; j < max_blocks_per_seq; ++j) row[j] = j < w ? s.table[j] : pad_value;
+  }
+  return pairs;
 }
 
 int pkv_bm_free_sequence(pkv_bm* m, int64_t seq_id) {

@@ -408,3 +408,95 @@ def test_concurrent_threads_keep_the_books():
     for sid in live:
         bm.free(sid)
     assert bm.available_blocks == NB
+
+
+def _books(bm, ids, nb):
+    """Everything observable about a manager's state for `ids`."""
+    return ([bm.seq_len(i) for i in ids], [bm.block_table(i).tolist() for i in ids],
+            [bm.refcount(b) for b in range(nb)], bm.available_blocks, bm.cached_blocks)
+
+
+def test_decode_step_equals_appends_one_by_one():
+    """pkv_bm_decode_step over a batch gives the slots, copy-on-write pairs,
+    tables and lengths of the same appends made one call at a time, on a twin
+    manager, through admissions with prefix hits, forks (parallel samples
+    whose shared tails get copied) and frees."""
+    B, NB = 16, 200
+    a, b = pkv.BlockManager(NB, B), pkv.BlockManager(NB, B)
+    rng = np.random.default_rng(7)
+    system = [int(x) for x in rng.integers(0, 100, size=2 * B + 5)]
+    live, next_id = [], 0
+    for step in range(120):
+        if step % 10 == 0 and len(live) < 12:  # admit one, fork another
+            toks = system + [int(x) for x in rng.integers(0, 100, size=rng.integers(0, 20))]
+            for m in (a, b):
+                m.add_sequence(next_id, toks)
+            live.append(next_id)
+            parent = live[int(rng.integers(0, len(live)))]
+            for m in (a, b):
+                m.fork(parent, next_id + 1)
+            live.append(next_id + 1)
+            next_id += 2
+        if step % 17 == 16 and len(live) > 4:
+            gone = live.pop(int(rng.integers(0, len(live))))
+            for m in (a, b):
+                m.free(gone)
+        batch = [i for i in live if rng.random() < 0.8]
+        if not batch:
+            continue
+        toks = [int(x) for x in rng.integers(0, 100, size=len(batch))]
+        width = max(-(-(a.seq_len(i) + 1) // B) for i in batch) + int(rng.integers(0, 3))
+        slots, lens, tables, pairs = a.decode_step(batch, toks, width)
+        want_pairs = []
+        for i, (sid, t) in enumerate(zip(batch, toks)):
+            slot, cow = b.append(sid, t)
+            assert slots[i] == slot
+            if cow:
+                want_pairs.append(cow)
+            assert lens[i] == b.seq_len(sid)
+            row = b.block_table(sid)
+            assert tables[i, : len(row)].tolist() == row.tolist() and np.all(tables[i, len(row):] == -1)
+        assert pairs.tolist() == [list(p) for p in want_pairs]
+    assert _books(a, live, NB) == _books(b, live, NB)
+
+
+def test_decode_step_sibling_tails_copy_once():
+    """Two samples forked from one sequence share its partial tail: in one
+    batch the first copies it on write, the second then owns it and appends
+    in place (one pair)."""
+    B = 16
+    bm = pkv.BlockManager(16, B)
+    bm.add_sequence(1, list(range(20)))
+    bm.fork(1, 2)
+    tail = int(bm.block_table(1)[1])
+    slots, lens, tables, pairs = bm.decode_step([1, 2], [5, 6], 2)
+    assert pairs.shape == (1, 2) and pairs[0, 0] == tail and pairs[0, 1] != tail
+    assert tables[0, 1] == pairs[0, 1] and tables[1, 1] == tail
+    assert slots.tolist() == [int(pairs[0, 1]) * B + 4, tail * B + 4] and lens.tolist() == [21, 21]
+    assert bm.refcount(tail) == 1
+
+
+def test_decode_step_is_all_or_nothing():
+    B, NB = 16, 4
+    bm = pkv.BlockManager(NB, B)
+    bm.add_sequence(1, list(range(16)))       # one full block: its next token needs a fresh one
+    bm.add_sequence(2, list(range(100, 132)))  # two full blocks
+    bm.fork(2, 3)
+    before = _books(bm, [1, 2, 3], NB)
+    assert bm.available_blocks == 1
+    with pytest.raises(pkv.OutOfBlocks):  # three fresh blocks wanted, one left
+        bm.decode_step([1, 2, 3], [7, 8, 9], 4)
+    assert _books(bm, [1, 2, 3], NB) == before
+    for bad in (dict(ids=[1, 1], toks=[1, 2], w=4),   # repeated sequence
+                dict(ids=[1, 9], toks=[1, 2], w=4),   # unknown sequence
+                dict(ids=[2], toks=[1], w=2)):        # row too narrow after the append (3 blocks)
+        with pytest.raises(pkv.PkvError):
+            bm.decode_step(bad["ids"], bad["toks"], bad["w"])
+        assert _books(bm, [1, 2, 3], NB) == before
+    bm.swap_out(3)
+    with pytest.raises(pkv.PkvError):  # swapped out
+        bm.decode_step([3], [1], 4)
+    slots, lens, tables, pairs = bm.decode_step([1], [7], 4, pad_value=0)
+    assert lens.tolist() == [17] and pairs.shape == (0, 2) and tables[0, 2:].tolist() == [0, 0]
+    s0, l0, t0, p0 = bm.decode_step([], [], 4)
+    assert s0.size == 0 and p0.shape == (0, 2)
