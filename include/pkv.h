@@ -514,6 +514,41 @@ int pkv_bm_decode_step(pkv_bm* bm, const int64_t* seq_ids, const int32_t* tokens
                        int32_t* slot_mapping, int32_t* context_lens, int32_t* block_tables,
                        int max_blocks_per_seq, int32_t pad_value, int32_t* cow_pairs);
 
+/*
+ * Operating signals of a manager ("gpu_paged_kv_cache", "Operating it": KV
+ * utilisation, preemption rate, prefix hit ratio, blocks per sequence).
+ * Gauges describe the state at the call; counters accumulate from creation.
+ *   blocks_referenced / num_blocks           KV utilisation by blocks;
+ *   slots_holding_tokens / (blocks_referenced * block_size)
+ *                                            fill of the referenced blocks
+ *                                            (1 - internal waste);
+ *   prompt_tokens_cached / prompt_tokens     prefix hit ratio;
+ *   swap_outs, refusals                      preemption pressure;
+ *   table_entries / sequences_resident, max_blocks_per_sequence
+ *                                            blocks per sequence.
+ */
+typedef struct pkv_bm_stats {
+  int64_t num_blocks, block_size;
+  int64_t blocks_free;                /* on the free list */
+  int64_t blocks_cached_unreferenced; /* cached, no reference: reusable, evicted LRU first */
+  int64_t blocks_referenced;          /* held by at least one resident sequence */
+  int64_t blocks_cached;              /* in the prefix cache, referenced or not */
+  int64_t slots_holding_tokens;       /* slots of referenced blocks holding a resident token */
+  int64_t sequences_resident, sequences_swapped;
+  int64_t table_entries;              /* sum of resident sequences' table lengths */
+  int64_t max_blocks_per_sequence;
+  /* counters */
+  int64_t prompt_tokens;              /* admitted prompt tokens */
+  int64_t prompt_tokens_cached;       /* of which found in the prefix cache */
+  int64_t evictions;                  /* cached blocks taken back for new contents */
+  int64_t cow_copies;                 /* copy-on-write pairs handed out */
+  int64_t swap_outs;
+  int64_t refusals;                   /* PKV_ERR_OUT_OF_BLOCKS returns */
+} pkv_bm_stats;
+
+/* Fills *out (host).  PKV_OK, or -PKV_ERR_INVALID_ARG for a NULL argument. */
+int pkv_bm_get_stats(pkv_bm* bm, pkv_bm_stats* out);
+
 /* Releases a sequence (its blocks' references). */
 int pkv_bm_free_sequence(pkv_bm* bm, int64_t seq_id);
 

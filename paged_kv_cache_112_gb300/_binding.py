@@ -57,6 +57,15 @@ _SIGS["pkv_decode_step_fp8"] = ([_c_void_p] * 4 + [_c_int64] + [_c_void_p] * 5 +
                                                 _c_void_p, _c_void_p])
 _SIGS["pkv_decode_step_partitions_fp8"] = _SIGS["pkv_decode_step_fp8"]
 
+class _BmStats(ctypes.Structure):
+    """pkv_bm_stats (include/pkv.h): int64 fields in declaration order."""
+    _fields_ = [(name, ctypes.c_int64) for name in (
+        "num_blocks", "block_size", "blocks_free", "blocks_cached_unreferenced", "blocks_referenced",
+        "blocks_cached", "slots_holding_tokens", "sequences_resident", "sequences_swapped", "table_entries",
+        "max_blocks_per_sequence", "prompt_tokens", "prompt_tokens_cached", "evictions", "cow_copies",
+        "swap_outs", "refusals")]
+
+
 _BM_SIGS = {
     "pkv_bm_create": ([ctypes.c_int] * 3, ctypes.c_void_p),
     "pkv_bm_destroy": ([ctypes.c_void_p], None),
@@ -70,6 +79,7 @@ _BM_SIGS = {
                       ctypes.c_int),
     "pkv_bm_decode_step": ([ctypes.c_void_p] * 3 + [ctypes.c_int] + [ctypes.c_void_p] * 3 +
                            [ctypes.c_int, ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
+    "pkv_bm_get_stats": ([ctypes.c_void_p, ctypes.POINTER(_BmStats)], ctypes.c_int),
     "pkv_bm_free_sequence": ([ctypes.c_void_p, ctypes.c_int64], ctypes.c_int),
     "pkv_bm_seq_len": ([ctypes.c_void_p, ctypes.c_int64], ctypes.c_int),
     "pkv_bm_block_table": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
@@ -542,6 +552,12 @@ class BlockManager:
                                           pairs.ctypes.data)
         p = self._rc(rc, "decode_step")
         return slots, lens, tables, pairs[:p].copy()
+
+    def stats(self) -> dict:
+        """pkv_bm_get_stats as a dict (gauges at the call, counters since creation)."""
+        st = _BmStats()
+        self._rc(self._lib.pkv_bm_get_stats(self._h, ctypes.byref(st)), "get_stats")
+        return {name: int(getattr(st, name)) for name, _ in _BmStats._fields_}
 
     def free(self, seq_id: int) -> None:
         self._rc(self._lib.pkv_bm_free_sequence(self._h, int(seq_id)), "free_sequence")

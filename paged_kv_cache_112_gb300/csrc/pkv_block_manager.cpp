@@ -24,6 +24,7 @@
 //    sequences can always append ("gpu_paged_kv_cache", "Reclaiming memory:
 //    swap versus recompute"), and swap bookkeeping (release a sequence's
 //    blocks to the host, take fresh ones on resume).
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <list>
@@ -79,6 +80,9 @@ struct Sequence {
 struct pkv_bm {
   std::mutex mu;
   int num_blocks = 0, block_size = 0, watermark = 0;
+  // cumulative counters reported by pkv_bm_get_stats
+  int64_t prompt_tokens = 0, prompt_tokens_cached = 0, evictions = 0, cow_copies = 0, swap_outs = 0,
+          refusals = 0;
   std::vector<pkv::Block> blocks;
   std::vector<int> free_list;             // ref == 0 and not cached
   std::list<int> evictable;               // ref == 0 and cached; front = least recently used
@@ -101,6 +105,7 @@ int take_block(pkv_bm* m) {
   } else if (!m->evictable.empty()) {
     b = m->evictable.front();
     m->evictable.pop_front();
+    ++m->evictions;
     Block& blk = m->blocks[b];
     m->cache.erase(blk.hash);
     blk.cached = false;
@@ -181,6 +186,7 @@ int append_locked(pkv_bm* m, Sequence& s, int32_t token, int32_t* slot, int32_t*
       s.table[pos / B] = b;
       *cow_src = tail;
       *cow_dst = b;
+      ++m->cow_copies;
     }
   }
   s.tokens.push_back(token);
@@ -255,13 +261,18 @@ int pkv_bm_add_sequence(pkv_bm* m, int64_t seq_id, const int32_t* tokens, int nu
   // Blocks a hit takes out of the evictable list are not available either.
   int hit_evictable = 0;
   for (int b : hits) hit_evictable += m->blocks[b].ref == 0 ? 1 : 0;
-  if (need > available(m) - hit_evictable - m->watermark) return -PKV_ERR_OUT_OF_BLOCKS;
+  if (need > available(m) - hit_evictable - m->watermark) {
+    ++m->refusals;
+    return -PKV_ERR_OUT_OF_BLOCKS;
+  }
   for (int b : hits) {
     add_ref(m, b);
     s.table.push_back(b);
   }
   for (int i = 0; i < need; ++i) s.table.push_back(take_block(m));
   const int cached_tokens = static_cast<int>(hits.size()) * B;
+  m->prompt_tokens += num_tokens;
+  m->prompt_tokens_cached += cached_tokens;
   for (int t = 0; t < num_tokens; ++t)
     slots[t] = t < cached_tokens ? -1 : s.table[t / B] * B + t % B;
   // The prompt's new full blocks become cacheable once written.
@@ -286,7 +297,9 @@ int pkv_bm_append(pkv_bm* m, int64_t seq_id, int32_t token, int32_t* slot, int32
   std::lock_guard<std::mutex> lock(m->mu);
   const auto it = m->seqs.find(seq_id);
   if (it == m->seqs.end() || it->second.swapped || !slot || !cow_src || !cow_dst) return -PKV_ERR_INVALID_ARG;
-  return append_locked(m, it->second, token, slot, cow_src, cow_dst);
+  const int rc = append_locked(m, it->second, token, slot, cow_src, cow_dst);
+  if (rc == -PKV_ERR_OUT_OF_BLOCKS) ++m->refusals;
+  return rc;
 }
 
 int pkv_bm_decode_step(pkv_bm* m, const int64_t* seq_ids, const int32_t* tokens, int n, int32_t* slot_mapping,
@@ -328,7 +341,10 @@ int pkv_bm_decode_step(pkv_bm* m, const int64_t* seq_ids, const int32_t* tokens,
     }
     seqs[static_cast<size_t>(i)] = &s;
   }
-  if (need > available(m)) return -PKV_ERR_OUT_OF_BLOCKS;
+  if (need > available(m)) {
+    ++m->refusals;
+    return -PKV_ERR_OUT_OF_BLOCKS;
+  }
   int pairs = 0;
   for (int i = 0; i < n; ++i) {
     int32_t src, dst;
@@ -391,6 +407,7 @@ int pkv_bm_swap_out(pkv_bm* m, int64_t seq_id, int32_t* blocks, int capacity) {
   for (int i = n - 1; i >= 0; --i) drop_ref(m, s.table[i]);
   s.table.clear();
   s.swapped = true;
+  ++m->swap_outs;
   return n;
 }
 
@@ -403,7 +420,10 @@ int pkv_bm_swap_in(pkv_bm* m, int64_t seq_id, int32_t* blocks, int capacity) {
   const int B = m->block_size;
   const int n = (static_cast<int>(s.tokens.size()) + B - 1) / B;
   if (n > capacity || (n > 0 && !blocks)) return -PKV_ERR_INVALID_ARG;
-  if (n > available(m) - m->watermark) return -PKV_ERR_OUT_OF_BLOCKS;  // resuming is an admission
+  if (n > available(m) - m->watermark) {  // resuming is an admission
+    ++m->refusals;
+    return -PKV_ERR_OUT_OF_BLOCKS;
+  }
   for (int i = 0; i < n; ++i) {
     blocks[i] = take_block(m);
     s.table.push_back(blocks[i]);
@@ -411,6 +431,48 @@ int pkv_bm_swap_in(pkv_bm* m, int64_t seq_id, int32_t* blocks, int capacity) {
   s.swapped = false;
   for (int i = 0; (i + 1) * B <= static_cast<int>(s.tokens.size()); ++i) register_full(m, s, i);
   return n;
+}
+
+int pkv_bm_get_stats(pkv_bm* m, pkv_bm_stats* out) {
+  if (!m || !out) return -PKV_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(m->mu);
+  const int B = m->block_size;
+  pkv_bm_stats st{};
+  st.num_blocks = m->num_blocks;
+  st.block_size = B;
+  st.blocks_free = static_cast<int64_t>(m->free_list.size());
+  st.blocks_cached_unreferenced = static_cast<int64_t>(m->evictable.size());
+  st.blocks_referenced = m->num_blocks - st.blocks_free - st.blocks_cached_unreferenced;
+  st.blocks_cached = static_cast<int64_t>(m->cache.size());
+  // Slots holding a token: per referenced block, the fill of its fullest
+  // holder (holders of a shared block agree on the rows they share).
+  std::vector<int> fill(static_cast<size_t>(m->num_blocks), 0);
+  for (const auto& kv : m->seqs) {
+    const pkv::Sequence& s = kv.second;
+    if (s.swapped) {
+      ++st.sequences_swapped;
+      continue;
+    }
+    ++st.sequences_resident;
+    const int len = static_cast<int>(s.tokens.size());
+    const int nb = static_cast<int>(s.table.size());
+    st.table_entries += nb;
+    if (nb > st.max_blocks_per_sequence) st.max_blocks_per_sequence = nb;
+    for (int j = 0; j < nb; ++j) {
+      const int f = std::min(B, len - j * B);
+      int& slot_fill = fill[static_cast<size_t>(s.table[static_cast<size_t>(j)])];
+      if (f > slot_fill) slot_fill = f;
+    }
+  }
+  for (int f : fill) st.slots_holding_tokens += f;
+  st.prompt_tokens = m->prompt_tokens;
+  st.prompt_tokens_cached = m->prompt_tokens_cached;
+  st.evictions = m->evictions;
+  st.cow_copies = m->cow_copies;
+  st.swap_outs = m->swap_outs;
+  st.refusals = m->refusals;
+  *out = st;
+  return PKV_OK;
 }
 
 }  // extern "C"

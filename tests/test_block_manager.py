@@ -39,6 +39,8 @@ class Model:
         self.evictable = []             # front = least recently released
         self.cache = {}                 # history key -> block
         self.seqs = {}                  # id -> dict(table, tokens, extra, swapped)
+        self.count = dict(prompt_tokens=0, prompt_tokens_cached=0, evictions=0, cow_copies=0, swap_outs=0,
+                          refusals=0)
 
     def avail(self):
         return len(self.free) + len(self.evictable)
@@ -48,6 +50,7 @@ class Model:
             b = self.free.pop()
         elif self.evictable:
             b = self.evictable.pop(0)
+            self.count["evictions"] += 1
             del self.cache[self.key[b]]
             self.key[b] = None
         else:
@@ -86,6 +89,7 @@ class Model:
         need = -(-len(tokens) // B) - len(hits)
         hit_evictable = sum(1 for b in hits if self.ref[b] == 0)
         if need > self.avail() - hit_evictable - self.wm:
+            self.count["refusals"] += 1
             return "oob", None
         s = dict(table=[], tokens=list(tokens), extra=extra, swapped=False)
         for b in hits:
@@ -94,6 +98,8 @@ class Model:
         for _ in range(need):
             s["table"].append(self._take())
         cached = len(hits) * B
+        self.count["prompt_tokens"] += len(tokens)
+        self.count["prompt_tokens_cached"] += cached
         slots = [-1 if t < cached else s["table"][t // B] * B + t % B for t in range(len(tokens))]
         for i in range(len(hits), len(tokens) // B):
             self._register(s, i)
@@ -118,6 +124,7 @@ class Model:
         if pos % B == 0:
             b = self._take()
             if b is None:
+                self.count["refusals"] += 1
                 return "oob"
             s["table"].append(b)
         else:
@@ -125,10 +132,12 @@ class Model:
             if self.ref[tail] > 1:
                 b = self._take()
                 if b is None:
+                    self.count["refusals"] += 1
                     return "oob"
                 self._drop_ref(tail)
                 s["table"][pos // B] = b
                 cow = (tail, b)
+                self.count["cow_copies"] += 1
         s["tokens"].append(tok)
         slot = s["table"][pos // B] * B + pos % B
         if (pos + 1) % B == 0:
@@ -152,6 +161,7 @@ class Model:
         for b in reversed(blocks):
             self._drop_ref(b)
         s["table"], s["swapped"] = [], True
+        self.count["swap_outs"] += 1
         return blocks
 
     def swap_in(self, sid):
@@ -160,6 +170,7 @@ class Model:
             return "invalid"
         n = -(-len(s["tokens"]) // self.bs)
         if n > self.avail() - self.wm:
+            self.count["refusals"] += 1
             return "oob"
         s["table"] = [self._take() for _ in range(n)]
         s["swapped"] = False
@@ -181,6 +192,18 @@ def _same_state(bm, m):
     live = {b for b in range(m.nb) if m.ref[b] > 0}
     assert live.isdisjoint(m.free) and live.isdisjoint(m.evictable)
     assert len(live) + len(m.free) + len(m.evictable) == m.nb
+    # operating signals: gauges from the model's state, counters kept beside it
+    resident = [s for s in m.seqs.values() if not s["swapped"]]
+    fill = [0] * m.nb
+    for s in resident:
+        for j, b in enumerate(s["table"]):
+            fill[b] = max(fill[b], min(m.bs, len(s["tokens"]) - j * m.bs))
+    want = dict(num_blocks=m.nb, block_size=m.bs, blocks_free=len(m.free), blocks_cached_unreferenced=len(m.evictable),
+                blocks_referenced=len(live), blocks_cached=len(m.cache), slots_holding_tokens=sum(fill),
+                sequences_resident=len(resident), sequences_swapped=len(m.seqs) - len(resident),
+                table_entries=sum(len(s["table"]) for s in resident),
+                max_blocks_per_sequence=max((len(s["table"]) for s in resident), default=0), **m.count)
+    assert bm.stats() == want
 
 
 def _call(fn, *a):
@@ -487,6 +510,7 @@ def test_decode_step_is_all_or_nothing():
     with pytest.raises(pkv.OutOfBlocks):  # three fresh blocks wanted, one left
         bm.decode_step([1, 2, 3], [7, 8, 9], 4)
     assert _books(bm, [1, 2, 3], NB) == before
+    assert bm.stats()["refusals"] == 1
     for bad in (dict(ids=[1, 1], toks=[1, 2], w=4),   # repeated sequence
                 dict(ids=[1, 9], toks=[1, 2], w=4),   # unknown sequence
                 dict(ids=[2], toks=[1], w=2)):        # row too narrow after the append (3 blocks)
