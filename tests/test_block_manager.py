@@ -330,7 +330,12 @@ def test_c_abi_guards():
     lib.pkv_bm_destroy(edge)
     assert lib.pkv_bm_available_blocks(None) == -pkv.PKV_ERR_INVALID_ARG
     assert lib.pkv_bm_free_sequence(None, 1) == -pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_bm_get_stats(None, None) == -pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_bm_decode_step(None, None, None, 1, None, None, None, 4, -1, None) == -pkv.PKV_ERR_INVALID_ARG
     bm = pkv.BlockManager(4, 16)
+    assert lib.pkv_bm_get_stats(bm._h, None) == -pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_bm_decode_step(bm._h, None, None, 0, None, None, None, 0, -1, None) == 0  # empty batch
+    assert lib.pkv_bm_decode_step(bm._h, None, None, 1, None, None, None, 4, -1, None) == -pkv.PKV_ERR_INVALID_ARG
     with pytest.raises(pkv.PkvError):
         bm.add_sequence(1, [1, 2])
         bm.add_sequence(1, [3])  # duplicate id
