@@ -438,7 +438,9 @@ pkv_status pkv_decode_step_partitions_fp8(void* out, const void* q, const void* 
  * watermark of blocks admissions may not take and swap bookkeeping [P1
  * "Reclaiming memory: swap versus recompute"].  It produces what the device
  * entry points consume: block-table rows, slot mappings and copy-on-write
- * pairs.  Calls on one manager are serialised by an internal lock.
+ * pairs, for a whole batch at once with pkv_bm_decode_step; and the
+ * operating signals of [P1 "Operating it"] with pkv_bm_get_stats.  Calls on
+ * one manager are serialised by an internal lock.
  *
  * Functions returning int return a count (>= 0) on success or a negative
  * pkv_status: -PKV_ERR_INVALID_ARG (null manager, unknown or duplicate
