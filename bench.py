@@ -482,7 +482,7 @@ def run_gpu(args):
         "clocks": clocks,
         "e2e": e2e,
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:  # the oracle's host-core baseline: one GPU runs only
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds, f8 if fp8 else None)
     if world > 1:
         dist.destroy_process_group()
