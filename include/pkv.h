@@ -569,6 +569,19 @@ int pkv_bm_block_table(pkv_bm* bm, int64_t seq_id, int32_t* out, int capacity);
 int pkv_bm_swap_out(pkv_bm* bm, int64_t seq_id, int32_t* blocks, int capacity);
 int pkv_bm_swap_in(pkv_bm* bm, int64_t seq_id, int32_t* blocks, int capacity);
 
+/*
+ * pkv_bm_swap_in with the prefix cache: the sequence's full blocks from
+ * position 0 whose contents are still cached (by the admission rule, up to
+ * the first miss) are shared again with a reference bump instead of being
+ * copied back; the rest take fresh blocks.  blocks[i] receives logical
+ * block i and from_host[i] is 1 when host block i must be moved there, 0
+ * when the block already holds it.  Returns the number of blocks.  Swap-out
+ * still moves every block: a shared block may be evicted before the
+ * resume, and the host copy is then the only one.
+ */
+int pkv_bm_swap_in_cached(pkv_bm* bm, int64_t seq_id, int32_t* blocks, int32_t* from_host,
+                          int capacity);
+
 /* Static string naming a status code.  Host function. */
 const char* pkv_status_string(pkv_status status);
 

@@ -85,6 +85,8 @@ _BM_SIGS = {
     "pkv_bm_block_table": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
     "pkv_bm_swap_out": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
     "pkv_bm_swap_in": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
+    "pkv_bm_swap_in_cached": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int],
+                              ctypes.c_int),
 }
 
 _LIB = None
@@ -582,3 +584,14 @@ class BlockManager:
     def swap_in(self, seq_id: int):
         """Takes fresh blocks for a swapped-out sequence; returns them (logical order)."""
         return self._blocks(self._lib.pkv_bm_swap_in, seq_id, "swap_in")
+
+    def swap_in_cached(self, seq_id: int):
+        """swap_in reusing still-cached prefix blocks: returns (blocks, from_host) int32 arrays in
+        logical order; from_host[i] == 1 where host block i must be moved to blocks[i]."""
+        np = self._np
+        cap = self.num_blocks
+        blocks = np.empty(cap, dtype=np.int32)
+        from_host = np.empty(cap, dtype=np.int32)
+        n = self._rc(self._lib.pkv_bm_swap_in_cached(self._h, int(seq_id), blocks.ctypes.data,
+                                                     from_host.ctypes.data, cap), "swap_in_cached")
+        return blocks[:n].copy(), from_host[:n].copy()

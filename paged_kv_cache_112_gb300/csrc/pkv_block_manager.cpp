@@ -433,6 +433,46 @@ int pkv_bm_swap_in(pkv_bm* m, int64_t seq_id, int32_t* blocks, int capacity) {
   return n;
 }
 
+int pkv_bm_swap_in_cached(pkv_bm* m, int64_t seq_id, int32_t* blocks, int32_t* from_host, int capacity) {
+  if (!m) return -PKV_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(m->mu);
+  const auto it = m->seqs.find(seq_id);
+  if (it == m->seqs.end() || !it->second.swapped) return -PKV_ERR_INVALID_ARG;
+  Sequence& s = it->second;
+  const int B = m->block_size;
+  const int len = static_cast<int>(s.tokens.size());
+  const int n = (len + B - 1) / B;
+  if (n > capacity || (n > 0 && (!blocks || !from_host))) return -PKV_ERR_INVALID_ARG;
+  // Full blocks from position 0 whose contents are still cached (the
+  // admission rule: chained hash and tokens, up to the first miss).
+  std::vector<int> hits;
+  for (int i = 0; (i + 1) * B <= len; ++i) {
+    const uint64_t parent = i == 0 ? s.root : s.hashes[static_cast<size_t>(i) - 1];
+    const int b = lookup(m, s.hashes[static_cast<size_t>(i)], parent, s.tokens.data() + static_cast<size_t>(i) * B);
+    if (b < 0) break;
+    hits.push_back(b);
+  }
+  const int need = n - static_cast<int>(hits.size());
+  int hit_evictable = 0;
+  for (int b : hits) hit_evictable += m->blocks[b].ref == 0 ? 1 : 0;
+  if (need > available(m) - hit_evictable - m->watermark) {  // resuming is an admission
+    ++m->refusals;
+    return -PKV_ERR_OUT_OF_BLOCKS;
+  }
+  for (size_t i = 0; i < hits.size(); ++i) {
+    add_ref(m, hits[i]);
+    s.table.push_back(hits[i]);
+  }
+  while (static_cast<int>(s.table.size()) < n) s.table.push_back(take_block(m));
+  for (int i = 0; i < n; ++i) {
+    blocks[i] = s.table[static_cast<size_t>(i)];
+    from_host[i] = i < static_cast<int>(hits.size()) ? 0 : 1;
+  }
+  s.swapped = false;
+  for (int i = static_cast<int>(hits.size()); (i + 1) * B <= len; ++i) register_full(m, s, i);
+  return n;
+}
+
 int pkv_bm_get_stats(pkv_bm* m, pkv_bm_stats* out) {
   if (!m || !out) return -PKV_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(m->mu);

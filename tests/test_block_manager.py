@@ -178,6 +178,30 @@ class Model:
             self._register(s, i)
         return s["table"]
 
+    def swap_in_cached(self, sid):
+        s = self.seqs.get(sid)
+        if s is None or not s["swapped"]:
+            return "invalid"
+        B = self.bs
+        hits = []
+        for i in range(len(s["tokens"]) // B):
+            b = self.cache.get((s["extra"], tuple(s["tokens"][: (i + 1) * B])))
+            if b is None:
+                break
+            hits.append(b)
+        n = -(-len(s["tokens"]) // B)
+        need = n - len(hits)
+        if need > self.avail() - sum(1 for b in hits if self.ref[b] == 0) - self.wm:
+            self.count["refusals"] += 1
+            return "oob"
+        for b in hits:
+            self._add_ref(b)
+        s["table"] = hits + [self._take() for _ in range(need)]
+        s["swapped"] = False
+        for i in range(len(hits), len(s["tokens"]) // B):
+            self._register(s, i)
+        return s["table"], [0] * len(hits) + [1] * need
+
 
 def _same_state(bm, m):
     assert bm.available_blocks == m.avail()
@@ -223,7 +247,8 @@ def test_random_operations_match_the_model(seed):
     system = [int(x) for x in rng.integers(0, 50, size=3 * bs)]  # a shared "system prompt"
     next_id = 0
     for _ in range(400):
-        op = rng.choice(["add", "add", "append", "append", "append", "fork", "free", "swap_out", "swap_in", "bad"])
+        op = rng.choice(["add", "add", "append", "append", "append", "fork", "free", "swap_out", "swap_in",
+                         "swap_in_cached", "bad"])
         ids = list(m.seqs)
         if op == "add":
             n_sys = int(rng.integers(0, 4)) * bs - int(rng.integers(0, 2))
@@ -263,6 +288,14 @@ def test_random_operations_match_the_model(seed):
             want = m.swap_in(sid)
             got = _call(bm.swap_in, sid)
             assert (got == want) if isinstance(want, str) else got.tolist() == want
+        elif op == "swap_in_cached" and ids:
+            sid = int(rng.choice(ids))
+            want = m.swap_in_cached(sid)
+            got = _call(bm.swap_in_cached, sid)
+            if isinstance(want, str):
+                assert got == want
+            else:
+                assert got[0].tolist() == want[0] and got[1].tolist() == want[1]
         elif op == "bad":
             assert _call(bm.append, 10 ** 9, 1) == "invalid"
             assert _call(bm.fork, 10 ** 9, 10 ** 9 + 1) == "invalid"
@@ -529,3 +562,38 @@ def test_decode_step_is_all_or_nothing():
     assert lens.tolist() == [17] and pairs.shape == (0, 2) and tables[0, 2:].tolist() == [0, 0]
     s0, l0, t0, p0 = bm.decode_step([], [], 4)
     assert s0.size == 0 and p0.shape == (0, 2)
+
+
+def test_swap_in_reuses_cached_prefix_blocks():
+    """A preempted sequence sharing a system prompt: on resume its prompt
+    blocks are still cached (another sequence holds them), so only its
+    private blocks come back from the host; once nobody holds the prompt and
+    its blocks are evicted, everything comes back from the host."""
+    B = 16
+    bm = pkv.BlockManager(12, B)
+    system = list(range(1000, 1000 + 3 * B))
+    bm.add_sequence(1, system + [1, 2, 3])
+    bm.add_sequence(2, system + [4, 5, 6, 7])
+    shared = bm.block_table(2)[:3].tolist()
+    out = bm.swap_out(2)
+    assert out.tolist()[:3] == shared and len(out) == 4
+    blocks, from_host = bm.swap_in_cached(2)
+    assert blocks[:3].tolist() == shared and from_host.tolist() == [0, 0, 0, 1]
+    assert [bm.refcount(b) for b in shared] == [2, 2, 2]
+    # nobody else holds the prompt and the pool is reused.  free(1) releases its table back to front,
+    # so prompt block 0 is the most recently released: taking 11 of the 12 blocks evicts blocks 2 and
+    # 1 of the prompt but not block 0, which is still a hit; the chain stops at block 1's miss.
+    bm.swap_out(2)
+    bm.free(1)
+    bm.add_sequence(3, list(range(5000, 5000 + 11 * B)))
+    bm.free(3)
+    blocks, from_host = bm.swap_in_cached(2)
+    assert blocks[0] == shared[0] and from_host.tolist() == [0, 1, 1, 1]
+    # all twelve blocks taken: nothing of the prompt is left, everything comes from the host
+    bm.swap_out(2)
+    bm.add_sequence(4, list(range(7000, 7000 + 12 * B)))
+    bm.free(4)
+    blocks, from_host = bm.swap_in_cached(2)
+    assert from_host.tolist() == [1, 1, 1, 1]
+    st = bm.stats()
+    assert st["swap_outs"] == 3 and st["evictions"] >= 3
