@@ -20,7 +20,7 @@ PROGRAM = r"""
 int main(void) {
   int32_t toks[20], slots[20], slots2[17], table[4], slot, src, dst, i, n, cached;
   int64_t batch[2] = {1, 2};
-  int32_t btoks[2] = {5, 6}, bslots[2], blens[2], btables[2][4], bpairs[2][2];
+  int32_t btoks[2] = {5, 6}, bslots[2], blens[2], btables[2][4], bpairs[2][2], sblocks[4], shost[4];
   pkv_bm* bm;
   if (strlen(pkv_status_string(PKV_OK)) == 0) return 1;
   /* one sequence, 1024 tokens, partitions of 512: f32 partial records exist */
@@ -44,6 +44,10 @@ int main(void) {
   /* one batched decode step: sequence 1 (tail of 4 shared with nobody now) and 2 (17 tokens) */
   n = pkv_bm_decode_step(bm, batch, btoks, 2, bslots, blens, &btables[0][0], 4, -1, &bpairs[0][0]);
   printf("step_pairs %d lens %d %d pad %d\n", n, blens[0], blens[1], btables[0][3]);
+  /* preempt sequence 2 and resume it: its first block is still cached (sequence 1 holds it) */
+  if (pkv_bm_swap_out(bm, 2, sblocks, 4) != 2) return 5;
+  n = pkv_bm_swap_in_cached(bm, 2, sblocks, shost, 4);
+  printf("resume %d from_host %d %d first_shared %d\n", n, shost[0], shost[1], sblocks[0] == table[0]);
   pkv_bm_free_sequence(bm, 1);
   pkv_bm_free_sequence(bm, 2);
   pkv_bm_free_sequence(bm, 3);
@@ -77,4 +81,5 @@ def test_header_compiles_as_c11_and_host_calls_run(tmp_path):
     assert got["blocks1"] == "2 refcount0 2"
     assert got["cow_src_is_tail"] == "1 cow_dst_fresh 1 slot_in_dst 1"
     assert got["step_pairs"] == "0 lens 21 18 pad -1"
+    assert got["resume"] == "2 from_host 0 1 first_shared 1"
     assert got["available"] == "8"
