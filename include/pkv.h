@@ -457,6 +457,19 @@ pkv_status pkv_decode_step_partitions_fp8(void* out, const void* q, const void* 
  */
 typedef struct pkv_bm pkv_bm;
 
+/*
+ * Blocks of a pool that fit kv_bytes of memory ("gpu_paged_kv_cache",
+ * "Sizing the pool": the KV budget over the bytes of one block):
+ *   floor(kv_bytes / (2 * num_layers * num_kv_heads * (block_size * head_dim
+ *         * elem_bytes + (with_scales ? 4 : 0))))
+ * -- K and V rows of every layer for block_size tokens, plus for FP8 pools
+ * (elem_bytes 1, with_scales 1) a float K and V scale per layer and KV
+ * head.  Pass num_layers = 1 for one layer's pool.  -1 on a non-positive
+ * size.  Host function.
+ */
+int64_t pkv_pool_blocks(uint64_t kv_bytes, int num_layers, int block_size, int num_kv_heads, int head_dim,
+                        int elem_bytes, int with_scales);
+
 /* A manager of num_blocks blocks of block_size tokens; watermark_blocks are
  * kept back from admissions (add_sequence, swap_in).  NULL on bad sizes
  * (non-positive, a watermark above num_blocks, or num_blocks * block_size

@@ -67,6 +67,7 @@ class _BmStats(ctypes.Structure):
 
 
 _BM_SIGS = {
+    "pkv_pool_blocks": ([ctypes.c_uint64] + [ctypes.c_int] * 6, ctypes.c_int64),
     "pkv_bm_create": ([ctypes.c_int] * 3, ctypes.c_void_p),
     "pkv_bm_destroy": ([ctypes.c_void_p], None),
     "pkv_bm_available_blocks": ([ctypes.c_void_p], ctypes.c_int),
@@ -469,6 +470,16 @@ def swap_blocks(dst_k, dst_v, src_k, src_v, pairs, *, status=None, stream=None):
 
 class OutOfBlocks(PkvError):
     """The block manager has not enough free blocks (nothing was changed)."""
+
+
+def pool_blocks(kv_bytes: int, num_layers: int, block_size: int, num_kv_heads: int, head_dim: int,
+                elem_bytes: int = 2, with_scales: bool = False) -> int:
+    """pkv_pool_blocks: how many blocks fit kv_bytes (all layers of a block, K and V; FP8 scales optional)."""
+    n = load().pkv_pool_blocks(int(kv_bytes), int(num_layers), int(block_size), int(num_kv_heads), int(head_dim),
+                               int(elem_bytes), int(bool(with_scales)))
+    if n < 0:
+        raise PkvError("pool_blocks: sizes must be positive")
+    return int(n)
 
 
 class BlockManager:

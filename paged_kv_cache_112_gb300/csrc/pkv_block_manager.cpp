@@ -202,6 +202,18 @@ using namespace pkv;
 
 extern "C" {
 
+int64_t pkv_pool_blocks(uint64_t kv_bytes, int num_layers, int block_size, int num_kv_heads, int head_dim,
+                        int elem_bytes, int with_scales) {
+  if (num_layers <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 || elem_bytes <= 0) return -1;
+  // K and V rows of every layer for block_size tokens, plus (FP8 pools) a K
+  // and a V float scale per layer and KV head.
+  const uint64_t rows = 2ull * static_cast<uint64_t>(num_layers) * static_cast<uint64_t>(num_kv_heads);
+  const uint64_t per_block = rows * static_cast<uint64_t>(block_size) * static_cast<uint64_t>(head_dim) *
+                                 static_cast<uint64_t>(elem_bytes) +
+                             (with_scales ? rows * 4ull : 0ull);
+  return static_cast<int64_t>(kv_bytes / per_block);
+}
+
 pkv_bm* pkv_bm_create(int num_blocks, int block_size, int watermark_blocks) {
   if (num_blocks <= 0 || block_size <= 0 || watermark_blocks < 0 || watermark_blocks > num_blocks) return nullptr;
   // slots (block * block_size + offset) are int32

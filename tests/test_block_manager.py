@@ -597,3 +597,26 @@ def test_swap_in_reuses_cached_prefix_blocks():
     assert from_host.tolist() == [1, 1, 1, 1]
     st = bm.stats()
     assert st["swap_outs"] == 3 and st["evictions"] >= 3
+
+
+def test_pool_blocks_matches_the_pages_sizing():
+    """pkv_pool_blocks against the pages' printed pool ("PagedAttention
+    internals", 05: an 8B-class model, 32 layers x 8 KV heads x 128 x fp16,
+    2 MiB blocks of 16 tokens, 54 GiB of KV -> 27,648 blocks) and against the
+    oracle's closed forms on drawn sizes; FP8 pools add a K and a V scale per
+    layer and KV head."""
+    import oracle.sizing as Z
+
+    GiB = 2 ** 30
+    assert pkv.pool_blocks(54 * GiB, 32, 16, 8, 128) == 27648
+    assert pkv.pool_blocks(2 * 2 ** 20 - 1, 32, 16, 8, 128) == 0
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        L, B, H, D, eb = (int(rng.integers(1, 100)), int(rng.choice([8, 16, 32, 64])), int(rng.integers(1, 17)),
+                          int(rng.choice([64, 128, 256])), int(rng.choice([1, 2, 4])))
+        budget = int(rng.integers(0, 300 * GiB))
+        assert pkv.pool_blocks(budget, L, B, H, D, eb) == Z.pool_blocks(budget, Z.block_bytes(L, H, D, eb, B))
+    # FP8: one-layer pool of the 8B-class row, 16-token blocks: 32 KiB of codes + 8 heads x 2 scales x 4 B
+    assert pkv.pool_blocks(10 * (32768 + 64), 1, 16, 8, 128, elem_bytes=1, with_scales=True) == 10
+    with pytest.raises(pkv.PkvError):
+        pkv.pool_blocks(GiB, 0, 16, 8, 128)
