@@ -571,6 +571,9 @@ int pkv_bm_free_sequence(pkv_bm* bm, int64_t seq_id);
  * number of blocks). */
 int pkv_bm_seq_len(pkv_bm* bm, int64_t seq_id);
 int pkv_bm_block_table(pkv_bm* bm, int64_t seq_id, int32_t* out, int capacity);
+/* A sequence's token history (swapped out or not) into out[capacity];
+ * returns its length. */
+int pkv_bm_seq_tokens(pkv_bm* bm, int64_t seq_id, int32_t* out, int capacity);
 
 /*
  * Swap: pkv_bm_swap_out lists the sequence's blocks in blocks[] (logical
@@ -591,6 +594,13 @@ int pkv_bm_swap_in(pkv_bm* bm, int64_t seq_id, int32_t* blocks, int capacity);
  * when the block already holds it.  Returns the number of blocks.  Swap-out
  * still moves every block: a shared block may be evicted before the
  * resume, and the host copy is then the only one.
+ *
+ * Preemption by recompute ("gpu_paged_kv_cache", "Reclaiming memory: swap
+ * versus recompute") is the same pair of calls without the copies: skip the
+ * move at pkv_bm_swap_out, and at the resume recompute (prefill) the K/V of
+ * the tokens in the blocks whose from_host is 1 -- token t of logical block
+ * i goes to slot blocks[i] * block_size + t % block_size -- from the history
+ * pkv_bm_seq_tokens returns.  Cached prefix blocks need neither.
  */
 int pkv_bm_swap_in_cached(pkv_bm* bm, int64_t seq_id, int32_t* blocks, int32_t* from_host,
                           int capacity);

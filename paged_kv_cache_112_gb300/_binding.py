@@ -84,6 +84,7 @@ _BM_SIGS = {
     "pkv_bm_free_sequence": ([ctypes.c_void_p, ctypes.c_int64], ctypes.c_int),
     "pkv_bm_seq_len": ([ctypes.c_void_p, ctypes.c_int64], ctypes.c_int),
     "pkv_bm_block_table": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
+    "pkv_bm_seq_tokens": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
     "pkv_bm_swap_out": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
     "pkv_bm_swap_in": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
     "pkv_bm_swap_in_cached": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int],
@@ -584,6 +585,14 @@ class BlockManager:
         out = np.empty(cap, dtype=np.int32)
         n = self._rc(fn(self._h, int(seq_id), out.ctypes.data, cap), what)
         return out[:n].copy()
+
+    def tokens(self, seq_id: int):
+        """pkv_bm_seq_tokens: the sequence's token history (int32)."""
+        np = self._np
+        n = self.seq_len(seq_id)
+        out = np.empty(max(n, 1), dtype=np.int32)
+        m = self._rc(self._lib.pkv_bm_seq_tokens(self._h, int(seq_id), out.ctypes.data, n), "seq_tokens")
+        return out[:m].copy()
 
     def block_table(self, seq_id: int):
         return self._blocks(self._lib.pkv_bm_block_table, seq_id, "block_table")

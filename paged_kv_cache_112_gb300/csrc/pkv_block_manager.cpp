@@ -396,6 +396,18 @@ int pkv_bm_seq_len(pkv_bm* m, int64_t seq_id) {
   return it == m->seqs.end() ? -PKV_ERR_INVALID_ARG : static_cast<int>(it->second.tokens.size());
 }
 
+int pkv_bm_seq_tokens(pkv_bm* m, int64_t seq_id, int32_t* out, int capacity) {
+  if (!m) return -PKV_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(m->mu);
+  const auto it = m->seqs.find(seq_id);
+  if (it == m->seqs.end()) return -PKV_ERR_INVALID_ARG;
+  const std::vector<int32_t>& t = it->second.tokens;
+  const int n = static_cast<int>(t.size());
+  if (n > capacity || (n > 0 && !out)) return -PKV_ERR_INVALID_ARG;
+  if (n > 0) std::memcpy(out, t.data(), sizeof(int32_t) * static_cast<size_t>(n));
+  return n;
+}
+
 int pkv_bm_block_table(pkv_bm* m, int64_t seq_id, int32_t* out, int capacity) {
   if (!m) return -PKV_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(m->mu);

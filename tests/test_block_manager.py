@@ -620,3 +620,31 @@ def test_pool_blocks_matches_the_pages_sizing():
     assert pkv.pool_blocks(10 * (32768 + 64), 1, 16, 8, 128, elem_bytes=1, with_scales=True) == 10
     with pytest.raises(pkv.PkvError):
         pkv.pool_blocks(GiB, 0, 16, 8, 128)
+
+
+def test_recompute_preemption_with_the_history():
+    """Preemption by recompute: swap out without moving anything, resume with
+    swap_in_cached, and recompute exactly the tokens of the from_host blocks
+    (their slots from the new table) from the kept history; the shared prompt
+    blocks come back from the prefix cache."""
+    B = 16
+    bm = pkv.BlockManager(16, B)
+    system = list(range(500, 500 + 2 * B))
+    bm.add_sequence(1, system)
+    toks = system + [1, 2, 3, 4, 5]
+    bm.add_sequence(2, toks)
+    for t in (6, 7):
+        bm.append(2, t)
+    history = toks + [6, 7]
+    assert bm.tokens(2).tolist() == history
+    bm.swap_out(2)  # recompute: nothing is copied
+    assert bm.tokens(2).tolist() == history  # kept while swapped out
+    blocks, from_host = bm.swap_in_cached(2)
+    assert from_host.tolist() == [0, 0, 1]
+    redo = [t for t in range(len(history)) if from_host[t // B]]
+    slots = [int(blocks[t // B]) * B + t % B for t in redo]
+    assert redo == list(range(2 * B, len(history))) and len(set(slots)) == len(slots)
+    assert bm.block_table(2).tolist() == blocks.tolist()
+    assert bm.tokens(1).tolist() == system
+    with pytest.raises(pkv.PkvError):
+        bm.tokens(99)
