@@ -223,8 +223,8 @@ pkv_status pkv_decode_partitions(void* out, const void* q, const void* k_pool, c
 
 /*
  * pkv_decode_reduce -- the second kernel: merges the partial softmax states of
- * every (sequence, query head) row that was split ("the cheap reduction" of
- * [P1 "Inside the paged attention kernel"]):  M = max_p m_p,
+ * every (sequence, query head) row that was split (the small merge step that
+ * follows split-K in [P1 "Inside the paged attention kernel"]):  M = max_p m_p,
  *     out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p.
  * Arguments as in pkv_decode_attention; it must follow pkv_decode_partitions
  * with the same sizes, workspace and stream, on the same device.  A no-op

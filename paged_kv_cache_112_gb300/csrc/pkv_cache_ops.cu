@@ -1,13 +1,16 @@
 // Write path and copy-on-write block copy.
 //
-//  * write_cache: "a small scatter kernel copies the new K and V into the
-//    pool, driven by a slot mapping ... block_index x B + offset"; head_dim
-//    innermost "so each store stays vectorized despite scattered
-//    destinations" ("gpu_paged_kv_cache", section "The write path: slot
+//  * write_cache: each new token's K and V rows go to the pool row named by
+//    its slot (block number times the block size plus the offset inside the
+//    block).  Because head_dim is the innermost axis of a pool row, a row
+//    moves as whole 16-byte vectors even though consecutive tokens land in
+//    unrelated blocks ("gpu_paged_kv_cache", section "The write path: slot
 //    mapping and scatter").
-//  * copy_blocks: copy-on-write "allocate a fresh block, device-to-device copy
-//    it" (same page, "Prefix sharing, reference counts, and copy-on-write";
-//    "PagedAttention internals", section 03).
+//  * copy_blocks: before a sequence appends into a block it shares, the
+//    block's contents are duplicated into a block of its own, which the
+//    sequence's table then points to ("gpu_paged_kv_cache", section "Prefix
+//    sharing, reference counts, and copy-on-write"; "PagedAttention
+//    internals", section 03).
 //
 // Both are pure byte movers: every thread moves one 16-byte vector, adjacent
 // threads move adjacent vectors of the same row (coalesced 128-byte lines on

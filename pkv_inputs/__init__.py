@@ -3,7 +3,7 @@
 This module is shared by the CUDA path's tests/bench and by the oracle's tests.
 It holds no arithmetic of the method itself (no attention, no gather, no copy):
 it draws context lengths and values, and it runs a small host-side block
-manager (free list, reference counts, copy-on-write decision) to build block
+pool (block stack, reference counts, copy-on-write decision) to build block
 tables, the slot mapping of the new tokens and the copy-on-write pairs -- the
 bookkeeping a scheduler does on the host each step.
 
@@ -87,34 +87,55 @@ def bits_to_f32(b: np.ndarray, dtype: str) -> np.ndarray:
     raise ValueError(dtype)
 
 
-class BlockManager:
-    """Host block manager: a free list of interchangeable blocks plus refcounts.
+class BlockPool:
+    """Host-side block pool: per-block reference counts in an int32 array and
+    the unreferenced blocks on a stack (an int32 array and its fill level).
 
-    The free list starts as a random permutation of the pool, so consecutive
-    allocations land on scattered physical blocks.
+    The stack starts as a random permutation of the pool, so consecutive
+    takes land on scattered physical blocks.  take() returns -1 when no block
+    is left; callers turn that into their own error.
     """
 
     def __init__(self, num_blocks: int, rng: np.random.Generator):
         self.num_blocks = num_blocks
-        self.free = [int(b) for b in rng.permutation(num_blocks)]
-        self.refcount: dict[int, int] = {}
+        self.counts = np.zeros(num_blocks, dtype=np.int32)
+        self._stack = rng.permutation(num_blocks).astype(np.int32)
+        self._depth = num_blocks
 
-    def alloc(self) -> int:
-        if not self.free:
-            raise MemoryError("KV pool exhausted")
-        b = self.free.pop()
-        self.refcount[b] = 1
+    def take(self) -> int:
+        """A block with one reference, or -1 when the pool is empty."""
+        if self._depth == 0:
+            return -1
+        self._depth -= 1
+        b = int(self._stack[self._depth])
+        self.counts[b] = 1
         return b
 
-    def share(self, b: int) -> int:
-        self.refcount[b] += 1
+    def ref(self, b: int) -> int:
+        """One more reference to a held block; returns b."""
+        assert self.counts[b] > 0, f"block {b} is not held"
+        self.counts[b] += 1
         return b
 
-    def release(self, b: int) -> None:
-        self.refcount[b] -= 1
-        if self.refcount[b] == 0:
-            del self.refcount[b]
-            self.free.append(b)
+    def unref(self, b: int) -> None:
+        """Drops one reference; the block goes back on the stack at zero."""
+        assert self.counts[b] > 0, f"block {b} is not held"
+        self.counts[b] -= 1
+        if self.counts[b] == 0:
+            self._stack[self._depth] = b
+            self._depth += 1
+
+    def held(self) -> dict:
+        """{block: references} of every held block."""
+        idx = np.flatnonzero(self.counts)
+        return {int(b): int(self.counts[b]) for b in idx}
+
+
+def _take(pool: BlockPool) -> int:
+    b = pool.take()
+    if b < 0:
+        raise RuntimeError(f"workload recipe needs more than the {pool.num_blocks} blocks of its pool")
+    return b
 
 
 @dataclass
@@ -123,22 +144,22 @@ class SeqState:
     length: int = 0
 
 
-def append_token(bm: BlockManager, seq: SeqState, block_size: int = BLOCK_SIZE):
+def append_token(pool: BlockPool, seq: SeqState, block_size: int = BLOCK_SIZE):
     """Reserve the slot of one new token.
 
-    Allocates a block only when the tail block is full; if the tail block is
-    shared (refcount > 1) it is replaced by a fresh block and a copy pair is
-    returned.  Returns (slot, cow_pair_or_None).
+    Takes a block only when the tail block is full; if the tail block is
+    shared (more than one reference) it is replaced by a fresh block and a
+    copy pair is returned.  Returns (slot, cow_pair_or_None).
     """
     pair = None
     if seq.length % block_size == 0:
-        seq.table.append(bm.alloc())
+        seq.table.append(_take(pool))
     else:
         tail = seq.table[-1]
-        if bm.refcount[tail] > 1:
-            fresh = bm.alloc()
+        if pool.counts[tail] > 1:
+            fresh = _take(pool)
             pair = (tail, fresh)
-            bm.release(tail)
+            pool.unref(tail)
             seq.table[-1] = fresh
     slot = seq.table[seq.length // block_size] * block_size + seq.length % block_size
     seq.length += 1
@@ -261,29 +282,29 @@ def make_workload(cfg: int, *, poison: bool = False, seed: int | None = None, **
         NB = int(math.ceil(spec.get("pool_factor", 1.25) * needed))
     assert NB >= needed, (NB, needed)
 
-    bm = BlockManager(NB, rng)
+    bm = BlockPool(NB, rng)
     seqs = [SeqState() for _ in range(S)]
     slots, pairs = [], []
     protected = set()
     if prefix_len:
         assert prefix_len % B == 0, "shared prefix is whole blocks"
-        prefix_blocks = [bm.alloc() for _ in range(prefix_len // B)]
+        prefix_blocks = [_take(bm) for _ in range(prefix_len // B)]
         protected.update(prefix_blocks)
         for i, sq in enumerate(seqs):
-            sq.table = [bm.share(b) if i else b for b in prefix_blocks]
+            sq.table = [bm.ref(b) if i else b for b in prefix_blocks]
             sq.length = prefix_len
             for _ in range(math.ceil(int(suffix[i]) / B)):
-                sq.table.append(bm.alloc())
+                sq.table.append(_take(bm))
             sq.length += int(suffix[i])
             if sq.length % B:
                 # the partial tail block also belongs to a forked parent
-                bm.share(sq.table[-1])
+                bm.ref(sq.table[-1])
                 protected.add(sq.table[-1])
     else:
         for sq, L in zip(seqs, lens):
             hist = int(L) - 1
             for _ in range(math.ceil(hist / B)):
-                sq.table.append(bm.alloc())
+                sq.table.append(_take(bm))
             sq.length = hist
     # Slots holding a token cached before this step (history), from the
     # tables as they stand before the append (a CoW source is still live).
@@ -330,7 +351,7 @@ def make_workload(cfg: int, *, poison: bool = False, seed: int | None = None, **
         slot_mapping=np.asarray(slots, dtype=np.int32).reshape(-1),
         copy_pairs=np.asarray(pairs, dtype=np.int32).reshape(-1, 2),
         q=q, k_new=k_new, v_new=v_new, k_pool=k_pool, v_pool=v_pool,
-        refcount=dict(bm.refcount), protected_blocks=np.asarray(sorted(protected), dtype=np.int32),
+        refcount=bm.held(), protected_blocks=np.asarray(sorted(protected), dtype=np.int32),
         poisoned=poison, live=live,
     )
 

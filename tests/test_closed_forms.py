@@ -4,7 +4,7 @@ import os
 import pytest
 
 from oracle import sizing as Z
-from pkv_inputs import BlockManager, SeqState, append_token
+from pkv_inputs import BlockPool, SeqState, append_token
 
 import numpy as np
 
@@ -96,7 +96,7 @@ def test_fleet_waste_256_sequences():
 
 def test_worked_decode_example_300_tokens():
     """300-token prompt -> 19 blocks; token 301 lands in logical block 18, no new block."""
-    bm = BlockManager(64, np.random.default_rng(0))
+    bm = BlockPool(64, np.random.default_rng(0))
     seq = SeqState()
     for _ in range(300):
         append_token(bm, seq)
