@@ -606,6 +606,21 @@ int pkv_bm_swap_in_cached(pkv_bm* bm, int64_t seq_id, int32_t* blocks, int32_t* 
                           int capacity);
 
 /* Static string naming a status code.  Host function. */
+/*
+ * pkv_check_bounded_wait -- exercises the decode kernels' error path for a
+ * tile copy that never lands, without any copy in flight.  One warp sets up
+ * the partition kernel's shared-memory tile ring and waits on its first
+ * stage, which nothing arms, with the same bounded wait (%globaltimer) the
+ * decode kernels use, but for timeout_ns instead of their fixed 2 s.  When
+ * the wait runs out the warp drains its (zero) outstanding copies, ORs
+ * PKV_DEV_ERR_TIMEOUT into *dev_status and returns, leaving the context
+ * usable.  A diagnostic: lets a test (or a deployment's health check) see
+ * that a stuck copy turns into a status bit rather than a hung kernel.
+ * timeout_ns in [0, 2e9]; dev_status is required (device int32).  The pages
+ * have no counterpart of this call.
+ */
+pkv_status pkv_check_bounded_wait(int64_t timeout_ns, int32_t* dev_status, void* stream);
+
 const char* pkv_status_string(pkv_status status);
 
 /* Library version, major * 10000 + minor * 100 + patch.  Host function. */

@@ -56,6 +56,7 @@ _SIGS["pkv_decode_step_fp8"] = ([_c_void_p] * 4 + [_c_int64] + [_c_void_p] * 5 +
                                 [_c_int] * 7 + [_c_float, _c_int, _c_int, _c_void_p, _c_size_t, _c_int, _c_int,
                                                 _c_void_p, _c_void_p])
 _SIGS["pkv_decode_step_partitions_fp8"] = _SIGS["pkv_decode_step_fp8"]
+_SIGS["pkv_check_bounded_wait"] = [_c_int64, _c_void_p, _c_void_p]
 
 class _BmStats(ctypes.Structure):
     """pkv_bm_stats (include/pkv.h): int64 fields in declaration order."""
@@ -164,6 +165,15 @@ def _pool_stride(k_pool, v_pool) -> int:
     if k_pool.stride(0) != v_pool.stride(0) or k_pool.shape != v_pool.shape:
         raise PkvError("k_pool and v_pool must share shape and block stride")
     return int(k_pool.stride(0))
+
+
+def check_bounded_wait(timeout_ns: int, status, *, stream=None):
+    """pkv_check_bounded_wait: one warp waits on a tile barrier nothing arms for
+    timeout_ns, then ORs DEV_ERR_TIMEOUT into `status` (a CUDA int32 tensor)."""
+    _need_cuda(status)
+    if status is None or status.dtype != torch.int32:
+        raise PkvError("status must be a CUDA int32 tensor")
+    _check(load().pkv_check_bounded_wait(int(timeout_ns), _ptr(status), _stream(stream)), "pkv_check_bounded_wait")
 
 
 def _kv_dtype(t) -> int:

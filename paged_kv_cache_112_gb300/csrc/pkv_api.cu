@@ -2,6 +2,7 @@
 // encoding and kernel launches.  No allocation, no device synchronisation.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -15,21 +16,54 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 }  // namespace
 
 int current_sm_count(int fallback) {
-  static int cache[256] = {};
+  // Filled once per device; readers see either 0 (not yet known) or the
+  // count, never a torn value.
+  static std::atomic<int> cache[256];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) {
     cudaGetLastError();
     return fallback;
   }
-  if (cache[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
-      cudaGetLastError();
-      return fallback;
-    }
-    cache[dev] = n;
+  int n = cache[dev].load(std::memory_order_acquire);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return fallback;
   }
-  return cache[dev];
+  cache[dev].store(n, std::memory_order_release);
+  return n;
+}
+
+int resident_warp_slots(const void* kernel, int threads, size_t smem) {
+  struct Entry {
+    const void* kernel;
+    int dev, threads;
+    size_t smem;
+    int slots;
+  };
+  static Entry table[32];
+  static int used = 0;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = -1;
+  }
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+      if (table[i].kernel == kernel && table[i].dev == dev && table[i].threads == threads && table[i].smem == smem)
+        return table[i].slots;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm <= 0) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  const int slots = current_sm_count(1) * per_sm * (threads / 32);
+  std::lock_guard<std::mutex> lock(mu);
+  if (used < 32) table[used++] = Entry{kernel, dev, threads, smem, slots};
+  return slots;
 }
 
 cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
@@ -749,6 +783,14 @@ pkv_status pkv_swap_blocks(void* dst_k, void* dst_v, int64_t dst_block_stride, i
   a.dst_num_blocks = dst_num_blocks;
   a.src_num_blocks = src_num_blocks;
   return launch_swap_blocks(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_check_bounded_wait(int64_t timeout_ns, int32_t* dev_status, void* stream) {
+  if (timeout_ns < 0 || timeout_ns > kWaitTimeoutNs || !dev_status || !aligned(dev_status, 4))
+    return PKV_ERR_INVALID_ARG;
+  return launch_bounded_wait_check(dev_status, timeout_ns, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
 }
 
 const char* pkv_status_string(pkv_status s) {

@@ -270,35 +270,30 @@ __global__ void __launch_bounds__(kLongReduceWarps * 32, 2) decode_reduce_long_k
   }
 }
 
+// ------------------------------------------------------- bounded-wait check
+
+// One warp sets up the partition kernel's tile ring (the same WarpRing, the
+// same bounded wait and drain) but issues no copy, so the first wait can
+// only end by running out of time.  It then takes the decode kernels' error
+// path: drain (nothing is in flight), set PKV_DEV_ERR_TIMEOUT, return.
+// Nothing in flight ever targets this CTA's shared memory.
+__global__ void __launch_bounds__(32) bounded_wait_check_kernel(int32_t* status, long long timeout_ns) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  using Geom = TileGeom<128>;
+  constexpr int NST = 2;
+  const int lane = threadIdx.x & 31;
+  WarpRing<128, NST> ring{smem_u32(smem), smem_u32(smem + NST * Geom::kStageBytes)};
+  ring.init(lane);
+  const int issued = 0;
+  if (!__all_sync(kFull, ring.wait(0, timeout_ns))) {
+    ring.drain(0, issued, timeout_ns);
+    if (lane == 0) flag(status, 16u);
+  }
+}
+
 // ------------------------------------------------------------------ launchers
 
 constexpr int kStages = 2;
-
-// Warp slots of the partition kernel on the current device (SMs x resident
-// CTAs x 2 warps), cached per kernel.
-int partition_warp_slots(const void* kern, size_t smem) {
-  static const void* cached_kern[16] = {};
-  static int cached_slots[16] = {};
-  static int cached_dev[16] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  for (int i = 0; i < 16; ++i)
-    if (cached_kern[i] == kern && cached_dev[i] == dev) return cached_slots[i];
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 64, smem) != cudaSuccess || per_sm <= 0) {
-    cudaGetLastError();
-    per_sm = 1;
-  }
-  const int slots = current_sm_count(1) * per_sm * 2;
-  for (int i = 0; i < 16; ++i)
-    if (!cached_kern[i]) {
-      cached_kern[i] = kern;
-      cached_dev[i] = dev;
-      cached_slots[i] = slots;
-      break;
-    }
-  return slots;
-}
 
 template <int D, bool BF16, bool FUSED, bool B8>
 cudaError_t launch_partitions_t(const DecodeArgs& a_in, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -318,7 +313,7 @@ cudaError_t launch_partitions_t(const DecodeArgs& a_in, const CUtensorMap& tk, c
   // from the start.  (The host does not see the lengths; estimating the
   // unit count on the device cost more than it gained on the benchmarked
   // batches.)
-  const int slots = partition_warp_slots(reinterpret_cast<const void*>(kern), smem);
+  const int slots = resident_warp_slots(reinterpret_cast<const void*>(kern), 64, smem);
   a.unit_warps = static_cast<int64_t>(a.num_kv_heads) * a.num_seqs > slots ? 2 : 1;
   const int64_t ctas = a.unit_warps == 1 ? (units + 1) / 2 : units;
   return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(64), smem, stream, a, tk, tv);
@@ -345,6 +340,14 @@ cudaError_t launch_decode_partitions(const DecodeArgs& a, const CUtensorMap& tma
     return kv_bf16 ? launch_partitions_f<64, true>(a, tmap_k, tmap_v, stream)
                    : launch_partitions_f<64, false>(a, tmap_k, tmap_v, stream);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bounded_wait_check(int32_t* status, long long timeout_ns, cudaStream_t stream) {
+  constexpr size_t smem = 2 * TileGeom<128>::kStageBytes + 2 * 8;
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(bounded_wait_check_kernel), smem);
+  if (e != cudaSuccess) return e;
+  bounded_wait_check_kernel<<<1, 32, smem, stream>>>(status, timeout_ns);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t stream) {

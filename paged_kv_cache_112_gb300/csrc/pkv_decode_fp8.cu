@@ -528,31 +528,6 @@ __global__ void __launch_bounds__(64, 6) decode_partitions_fp8_kernel(
   }
 }
 
-// Warp slots of the kernel on the current device (SMs x resident CTAs x 2).
-int fp8_warp_slots(const void* kern, size_t smem) {
-  static const void* cached_kern[4] = {};
-  static int cached_slots[4] = {};
-  static int cached_dev[4] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  for (int i = 0; i < 4; ++i)
-    if (cached_kern[i] == kern && cached_dev[i] == dev) return cached_slots[i];
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 64, smem) != cudaSuccess || per_sm <= 0) {
-    cudaGetLastError();
-    per_sm = 1;
-  }
-  const int slots = current_sm_count(1) * per_sm * 2;
-  for (int i = 0; i < 4; ++i)
-    if (!cached_kern[i]) {
-      cached_kern[i] = kern;
-      cached_dev[i] = dev;
-      cached_slots[i] = slots;
-      break;
-    }
-  return slots;
-}
-
 template <int D, bool QBF16, bool FUSED>
 cudaError_t launch_fp8_t(const DecodeArgs& a_in, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
   using Geom = TileGeom<D, 1>;
@@ -565,7 +540,7 @@ cudaError_t launch_fp8_t(const DecodeArgs& a_in, const CUtensorMap& tk, const CU
   const int64_t units = static_cast<int64_t>(a.num_kv_heads) * a.num_seqs * a.max_parts;
   if (units == 0) return cudaSuccess;
   // Warps per unit: the 16-bit kernel's rule.
-  const int slots = fp8_warp_slots(reinterpret_cast<const void*>(kern), smem);
+  const int slots = resident_warp_slots(reinterpret_cast<const void*>(kern), 64, smem);
   a.unit_warps = static_cast<int64_t>(a.num_kv_heads) * a.num_seqs > slots ? 2 : 1;
   const int64_t ctas = a.unit_warps == 1 ? (units + 1) / 2 : units;
   return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(64), smem, stream, a, tk, tv);

@@ -136,6 +136,11 @@ WorkspaceLayout balanced_workspace_layout(int num_seqs, int num_q_heads, int hea
 // SM count of the current device, cached per device; `fallback` when no
 // device answers.
 int current_sm_count(int fallback);
+// Warps of `kernel` (launched with `threads` threads and `smem` bytes of
+// dynamic shared memory) that the current device holds at once: SMs x
+// resident CTAs x warps per CTA.  Cached per kernel, device and shape;
+// safe to call from several host threads.
+int resident_warp_slots(const void* kernel, int threads, size_t smem);
 // Raises a kernel's dynamic shared memory limit to `bytes` on the current
 // device (once per kernel, device and size).
 cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
@@ -175,6 +180,9 @@ cudaError_t launch_decode_partitions(const DecodeArgs& a, const CUtensorMap& tma
                                      const CUtensorMap& tmap_v, int head_dim, int kv_bf16,
                                      cudaStream_t stream);  // fuses the write when a.k_new is set
 cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t stream);
+// One warp waits on a tile barrier that no copy arms, for timeout_ns, and
+// sets PKV_DEV_ERR_TIMEOUT in *status (pkv_check_bounded_wait).
+cudaError_t launch_bounded_wait_check(int32_t* status, long long timeout_ns, cudaStream_t stream);
 // FP8 pools (pkv_decode_fp8.cu): tensor maps describe the uint8 pools;
 // q_bf16: 0 = f16 queries, 1 = bf16.
 cudaError_t launch_decode_partitions_fp8(const DecodeArgs& a, const CUtensorMap& tmap_k,

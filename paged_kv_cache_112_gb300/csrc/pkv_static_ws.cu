@@ -12,10 +12,13 @@
 // The array is a file-scope __device__ variable of PKV_STATIC_WORKSPACE_BYTES
 // bytes.  Every GPU on which the library's module is loaded holds that much
 // memory until the process exits.  Host code cannot use the array's name as a
-// device address (on the host it names a stand-in object), so the first call
-// on each device, with that device current, asks the runtime for the real
-// device address with cudaGetSymbolAddress and keeps it.  Because that first
-// call does this set-up, it should come before any stream capture.
+// device address (on the host it names a stand-in object), so each call made
+// outside stream capture, with its device current, asks the runtime for the
+// real device address with cudaGetSymbolAddress and keeps it for that device.
+// A call inside stream capture uses the kept address, so the first call on a
+// device must come before any stream capture (a captured first call returns
+// PKV_ERR_CUDA).  cudaDeviceReset unloads the module; the next uncaptured
+// call looks the address up again.
 //
 // All calls share the one array, and it keeps whatever the last call left in
 // it.  Nothing in it has to start at zero: every partial result the reduce
@@ -39,15 +42,23 @@ constexpr int kMaxDevices = 256;
 void* g_workspace_addr[kMaxDevices] = {};
 std::mutex g_workspace_mutex;
 
-// Device address of the array on the current device (set up once per device).
-pkv_status static_workspace_address(void** addr) {
+// Device address of the array on the current device.  The address is looked
+// up again on every call made outside stream capture, so a module reloaded
+// after cudaDeviceReset is picked up; during capture (where the lookup is not
+// wanted) the address from the device's last uncaptured call is used, and a
+// device that has had no uncaptured call yet is refused.
+pkv_status static_workspace_address(cudaStream_t stream, void** addr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return PKV_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_workspace_mutex);
-  if (!g_workspace_addr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_pkv_static_workspace) != cudaSuccess || p == nullptr) return PKV_ERR_CUDA;
     g_workspace_addr[dev] = p;
+  } else if (!g_workspace_addr[dev]) {
+    return PKV_ERR_CUDA;
   }
   *addr = g_workspace_addr[dev];
   return PKV_OK;
@@ -65,7 +76,7 @@ extern "C" pkv_status pkv_decode_attention_static_workspace(
   if (need > static_cast<size_t>(PKV_STATIC_WORKSPACE_BYTES)) return PKV_ERR_WORKSPACE;
   void* ws = nullptr;
   if (need > 0) {
-    const pkv_status st = static_workspace_address(&ws);
+    const pkv_status st = static_workspace_address(static_cast<cudaStream_t>(stream), &ws);
     if (st != PKV_OK) return st;
   }
   return pkv_decode_attention(out, q, k_pool, v_pool, block_stride, block_tables, max_blocks_per_seq, context_lens,

@@ -187,3 +187,13 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_binding._build, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(pkv.PkvError):
         _binding.load()
+
+
+def test_bounded_wait_check_argument_validation(lib):
+    """Rejected before any launch: negative or over-long limits, a missing or
+    misaligned status word."""
+    fake = 256
+    assert lib.pkv_check_bounded_wait(-1, fake, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_check_bounded_wait(2_000_000_001, fake, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_check_bounded_wait(1000, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_check_bounded_wait(1000, fake + 2, None) == pkv.PKV_ERR_INVALID_ARG

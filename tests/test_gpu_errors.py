@@ -2,6 +2,8 @@
 every table entry, slot, copy pair and length, skip the bad element and OR a
 PKV_DEV_ERR_* bit into the caller's status word.  Everything else is still
 computed correctly."""
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -78,3 +80,38 @@ def test_length_beyond_bound_is_clamped_and_flagged(ps):
     others = [s for s in range(wl.num_seqs) if s != 1]
     assert float(np.max(np.abs(out[others] - ref[others]))) <= ATOL
     assert np.all(np.isfinite(out))
+
+
+@pytest.mark.parametrize("limit_ms", [2, 20])
+def test_timed_out_wait_sets_the_status_bit_and_the_context_stays_usable(limit_ms):
+    """A tile wait that nothing completes ends after its limit with
+    PKV_DEV_ERR_TIMEOUT (the decode kernels' bounded wait and drain, run with
+    a short limit and no copy in flight); the same context then runs a normal
+    decode step that matches the oracle."""
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record()
+    pkv.check_bounded_wait(limit_ms * 1_000_000, status)
+    e1.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    assert int(status.item()) == pkv.DEV_ERR_TIMEOUT
+    waited_ms = e0.elapsed_time(e1)
+    assert 0.5 * limit_ms <= waited_ms < limit_ms + 500, waited_ms
+    assert wall < 5.0
+    wl = P.make_workload(2, num_seqs=5, poison=True)
+    _, _, ref = oracle.apply_step(wl)
+    ds = DeviceStep(wl, partition_size=64)
+    out = ds.step().cpu().numpy()
+    assert ds.status_bits() == 0
+    assert float(np.max(np.abs(out - ref))) <= ATOL
+
+
+def test_bounded_wait_check_rejects_bad_arguments():
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(pkv.PkvError):
+        pkv.check_bounded_wait(-1, status)
+    with pytest.raises(pkv.PkvError):
+        pkv.check_bounded_wait(3_000_000_000, status)
+    assert pkv.load().pkv_check_bounded_wait(1000, None, None) == pkv.PKV_ERR_INVALID_ARG

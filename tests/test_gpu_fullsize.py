@@ -1,8 +1,7 @@
 """Parity at the benchmark's full sizes, in the launch configuration bench.py
 times (its partition size, fp32 output, one write token per sequence, the
-recipe's copy-on-write pairs).  Pools are compared bit for bit in full;
-attention is compared on sampled (sequence, head) rows that the oracle
-computes one by one, always including the shortest and longest sequences."""
+recipe's copy-on-write pairs).  Pools are compared bit for bit in full and
+every (sequence, query head) output row is compared with the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -22,14 +21,6 @@ def _lib():
     pkv.load(build_if_missing=True)
 
 
-def _rows(wl, n, rng):
-    S, Hq = wl.num_seqs, wl.num_q_heads
-    picks = {(int(s), int(h)) for s, h in zip(rng.integers(0, S, n), rng.integers(0, Hq, n))}
-    for s in (int(np.argmin(wl.context_lens)), int(np.argmax(wl.context_lens))):
-        picks.update({(s, 0), (s, Hq - 1), (s, Hq // 2)})
-    return sorted(picks)
-
-
 @pytest.mark.parametrize("cfg,ps", [(2, None), (3, None), (4, None), (5, None),
                                     (2, pkv.PARTITION_BALANCED), (3, pkv.PARTITION_BALANCED),
                                     (5, pkv.PARTITION_BALANCED)])
@@ -43,11 +34,8 @@ def test_full_size_step(cfg, ps):
     oracle.write_cache(k_ref, v_ref, wl.k_new, wl.v_new, wl.slot_mapping)
     assert np.array_equal(to_bits(ds.k_pool), k_ref)
     assert np.array_equal(to_bits(ds.v_pool), v_ref)
-    rows = _rows(wl, 48, np.random.default_rng(cfg))
-    ref = oracle.decode_attention(wl.q, k_ref, v_ref, wl.block_tables, wl.context_lens, wl.scale, wl.dtype,
-                                  rows=rows)
-    got = np.stack([out[s, h] for s, h in rows])
-    err = float(np.max(np.abs(got.astype(np.float64) - ref)))
+    ref = oracle.decode_attention(wl.q, k_ref, v_ref, wl.block_tables, wl.context_lens, wl.scale, wl.dtype)
+    err = float(np.max(np.abs(out.astype(np.float64) - ref)))
     assert err <= ATOL, err
     # every row is finite (NaN poison in unowned slots never leaks)
     assert np.all(np.isfinite(out))

@@ -101,6 +101,35 @@ class Loop:
                         torch.from_numpy(bt).cuda(), torch.from_numpy(cl).cuda(),
                         torch.tensor(slots, dtype=torch.int32).cuda(), SCALE, partition_size=ps,
                         max_context_len=int(cl.max()), workspace=ws, status=self.status)
+        return self._check(sids, q, out)
+
+    def decode_batch(self, rng, sids):
+        """The same step with the whole batch's bookkeeping in one call
+        (pkv_bm_decode_step: slots, lengths, padded tables and copy pairs)."""
+        toks = [int(x) for x in rng.integers(0, 1000, size=len(sids))]
+        width = max(-(-(self.bm.seq_len(s) + 1) // B) for s in sids)
+        slots, cl, bt, pairs = self.bm.decode_step(sids, toks, width)
+        knew, vnew = [], []
+        for sid, tok in zip(sids, toks):
+            self.tokens[sid].append(tok)
+            k, v = kv_row(self.tokens[sid])
+            knew.append(k)
+            vnew.append(v)
+        if len(pairs):
+            pkv.copy_blocks(self.k, self.v, torch.from_numpy(np.ascontiguousarray(pairs, np.int32)).cuda(),
+                            status=self.status)
+        q = P.f32_to_bits(rng.standard_normal((len(sids), HQ, D)).astype(np.float32), DT)
+        out = torch.empty((len(sids), HQ, D), dtype=torch.float32, device="cuda")
+        ps = 32
+        nb = pkv.decode_workspace_bytes(len(sids), HQ, D, int(cl.max()), ps)
+        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
+        pkv.decode_step(out, dev16(q), dev16(np.stack(knew)), dev16(np.stack(vnew)), self.k, self.v,
+                        torch.from_numpy(np.ascontiguousarray(bt)).cuda(), torch.from_numpy(cl).cuda(),
+                        torch.from_numpy(slots).cuda(), SCALE, partition_size=ps, max_context_len=int(cl.max()),
+                        workspace=ws, status=self.status)
+        return self._check(sids, q, out)
+
+    def _check(self, sids, q, out):
         torch.cuda.synchronize()
         assert int(self.status.item()) == 0
         got = out.cpu().numpy()
@@ -149,3 +178,39 @@ def test_serving_loop_with_prefix_cache_fork_cow_and_swap():
     for sid in (1, 2, 3, 4, 5):
         loop.bm.free(sid)
     assert loop.bm.available_blocks == NB
+
+
+def test_serving_loop_with_batched_bookkeeping_and_cached_swap_in():
+    """Decode steps whose bookkeeping comes from pkv_bm_decode_step, and a
+    resume through swap_in_cached: full blocks still in the prefix cache are
+    shared again, only the others come back from the host."""
+    rng = np.random.default_rng(77)
+    loop = Loop()
+    system = [int(x) for x in rng.integers(0, 1000, size=3 * B)]  # 3 whole blocks
+    loop.admit(1, system + [int(x) for x in rng.integers(0, 1000, size=B + 5)])
+    assert loop.admit(2, system + [int(x) for x in rng.integers(0, 1000, size=9)]) == 3 * B
+    loop.fork(2, 3)  # forked tail: the next batch step copies it once
+    for _ in range(3):
+        loop.decode_batch(rng, [1, 2, 3])
+    # preempt sequence 1: every block goes to the host, the blocks are released
+    blocks = loop.bm.swap_out(1)
+    hk = torch.empty((len(blocks), B, HKV, D), dtype=torch.float16).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    pkv.swap_blocks(hk, hv, loop.k, loop.v, torch.tensor(np.stack([blocks, np.arange(len(blocks))], 1),
+                                                         dtype=torch.int32).cuda(), status=loop.status)
+    torch.cuda.synchronize()
+    loop.decode_batch(rng, [2, 3])
+    new, from_host = loop.bm.swap_in_cached(1)
+    assert len(new) == len(blocks)
+    # the system prompt's blocks (held by sequences 2 and 3) and sequence 1's own full
+    # prompt block (released to the prefix cache, not evicted) are shared again; only
+    # the partial tail block, which is never cached, comes back from the host
+    assert list(from_host) == [0, 0, 0, 0, 1]
+    assert np.array_equal(new[:3], loop.bm.block_table(2)[:3])
+    idx = np.flatnonzero(from_host)
+    pkv.swap_blocks(loop.k, loop.v, hk, hv, torch.tensor(np.stack([idx, new[idx]], 1), dtype=torch.int32).cuda(),
+                    status=loop.status)
+    for _ in range(2):
+        loop.decode_batch(rng, [1, 2, 3])
+    for sid in (1, 2, 3):
+        loop.bm.free(sid)

@@ -15,7 +15,7 @@ import torch
 
 import paged_kv_cache_112_gb300 as pkv
 import pkv_inputs as P
-from tests.gpu_util import ATOL, DeviceStep
+from tests.gpu_util import DeviceStep
 
 pytestmark = pytest.mark.gpu
 
@@ -64,7 +64,8 @@ def test_static_workspace_matches_workspace_entry_point(entry, first, second):
         torch.cuda.synchronize()
         assert int(ds.status.item()) == 0
         assert torch.isfinite(out).all()
-        assert float((out - ds.out).abs().max()) <= ATOL
+        # the same kernels on the same inputs: only where the partials live differs
+        assert torch.equal(out, ds.out)
 
 
 def test_static_workspace_rejects_oversized_calls(entry):
