@@ -4,10 +4,17 @@ A step = the whole hot path over one batch: copy-on-write block copies (when
 the workload has any), the write of one new token per sequence and decode
 attention (partition kernel + reduce kernel).  By default the write is fused
 into the partition kernel (pkv_decode_step); --unfused runs pkv_write_cache
-and pkv_decode_attention as separate calls.  Default workload: the 8B-class
-GQA decode layer (64 sequences, 32 query / 8 KV heads, head_dim 128, bf16,
-context lengths uniform in [128, 2048], blocks scattered over a pool 1.25x
-the need).  Inputs are synthetic, seeded, N(0,1).
+and pkv_decode_attention as separate calls.
+
+Default line: the long-context layer (8 sequences, 32 query / 8 KV heads,
+head_dim 128, bf16, context lengths uniform in [32768, 131072], split-K
+partitions of 512 tokens) is the headline; the 8B-class layer (64 sequences,
+lengths in [128, 2048]), the 70B-class layer (256 sequences, 64 query heads,
+lognormal lengths) and the prefix-sharing step (128 sequences over one
+2048-token prefix, copy-on-write tails) are measured the same way under
+`per_config`.  `--config N` measures one recipe alone.  Blocks are scattered
+over a pool 1.25x the need; inputs are synthetic, seeded, N(0,1).  The timed
+steps are CUDA graph replays, so the device time is not paced by the host.
 
 Metric: decode KV bytes per second (GB/s) over the step, its fraction of the
 HBM peak, and sequences*layers per second.  `value` counts the algorithmic
@@ -216,21 +223,46 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU arm
 
-def run_gpu(args):
+def unique_kv_bytes(wl, elem_bytes=2):
+    """K+V bytes of the distinct pool slots a step reads: a slot referenced by
+    several sequences (a shared prefix) counts once."""
+    B = wl.block_size
+    slots = []
+    for s in range(wl.num_seqs):
+        L = int(wl.context_lens[s])
+        t = np.arange(L, dtype=np.int64)
+        slots.append(wl.block_tables[s, t // B].astype(np.int64) * B + t % B)
+    n = int(np.unique(np.concatenate(slots)).size) if slots else 0
+    return n * wl.num_kv_heads * wl.head_dim * 2 * elem_bytes
+
+
+def graph_blocks(K, replicas):
+    """Steps per captured graph for a timed region of exactly K steps: a
+    multiple of the pool replica count (so replays continue the rotation),
+    about K / REPS so the region splits into REPS repetitions.  Returns
+    (steps per graph, full replays, remainder steps)."""
+    b = max(replicas, (max(1, K // REPS) // replicas) * replicas)
+    b = min(b, max(replicas, 64 // replicas * replicas))
+    return b, K // b, K % b
+
+
+def measure_workload(args, cfg, ctx, want_cpu_baseline):
+    """One workload's bench line (rank 0; None on other ranks).
+
+    Timed region A (value): exactly K steps, captured as CUDA graphs of a
+    fixed number of steps and replayed back to back between two events, so
+    the host's launch rate cannot pace the device.  Region B: the same steps
+    launched eagerly with events around every partition-kernel launch (its
+    average duration: the roofline's `achieved`).  e2e: the same step through
+    the public API with every step's inputs copied up from pinned host memory
+    and its output copied back."""
     import torch
-    import torch.distributed as dist
 
     import paged_kv_cache_112_gb300 as pkv
     import pkv_inputs as P
 
-    rank, world, local = _dist()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
-    pkv.load()
-
-    wl = P.make_workload(args.config, poison=False, block_size=args.block_size)
+    dist, dev, rank, world, local = ctx["dist"], ctx["dev"], ctx["rank"], ctx["world"], ctx["local"]
+    wl = P.make_workload(cfg, poison=False, block_size=args.block_size)
     ps = wl.partition_size if args.partition_size is None else args.partition_size
     dt = {"f16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
 
@@ -247,7 +279,8 @@ def run_gpu(args):
         total += (arr.nbytes + 255) // 256 * 256
     host_stage = torch.empty(max(total, 256), dtype=torch.uint8).pin_memory()
     for name, arr, _ in step_inputs:
-        host_stage[offs[name]:offs[name] + arr.nbytes].copy_(torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).reshape(-1)))
+        host_stage[offs[name]:offs[name] + arr.nbytes].copy_(
+            torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).reshape(-1)))
     dev_stage = host_stage.to(dev)
 
     def views(stage):
@@ -262,6 +295,7 @@ def run_gpu(args):
     io0 = views(dev_stage)
     pairs = io0["pairs"]
     fp8 = args.kv == "fp8"
+    f8 = None
     if fp8:  # e4m3 codes + per-(block, KV head) scales; the write path quantises the new rows
         f8 = P.make_fp8_pools(wl, poison=False)
         k0, v0 = torch.from_numpy(f8.k8).to(dev), torch.from_numpy(f8.v8).to(dev)
@@ -272,7 +306,7 @@ def run_gpu(args):
         ks0 = vs0 = None
     io0["out"] = torch.empty(io0["q"].shape, dtype=torch.float32, device=dev)
     ws_bytes = pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, wl.max_context_len, ps)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -334,43 +368,67 @@ def run_gpu(args):
 
     nb = step_bytes_fp8(wl) if fp8 else step_bytes(wl)
     K, W = args.steps, args.warmup
-    for i in range(W):
-        step(i)
-    torch.cuda.synchronize()
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
 
-    # Timed region A: exactly K steps, nothing else on the stream (value).  Events
-    # at the boundaries of REPS equal runs of steps give each repetition's rate.
+    def capture(n):
+        """A CUDA graph of steps 0..n-1 (pool replica i % replicas for step i)."""
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for i in range(n):
+                step(i)  # eager run of the same work on the capture stream first
+        torch.cuda.current_stream().wait_stream(side)
+        with torch.cuda.graph(g):
+            for i in range(n):
+                step(i)
+        return g
+
+    b, n_full, rem = graph_blocks(K, replicas)
+    g_full = capture(b)
+    g_rem = capture(rem) if rem else None
     sampler = ClockSampler(local) if rank == 0 else None
-    reps = REPS if K >= REPS else 1
-    bounds = [K * r // reps for r in range(reps + 1)]
-    marks = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
     if sampler:
-        sampler.start()
+        sampler.start()  # sampling starts before the warm-up: no idle gap before the timed region
+    for i in range(W):
+        step(i)
+    g_full.replay()
+    torch.cuda.synchronize()
+
+    # Timed region A: exactly K steps (n_full replays of b steps, then the
+    # remainder), nothing else on the stream.  Events between replays split it
+    # into repetitions.
+    groups = min(n_full, REPS)
+    bounds = [n_full * r // groups for r in range(groups + 1)] if groups else [0]
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(len(bounds) + (1 if g_rem else 0))]
     barrier()
     marks[0].record()
-    for r in range(reps):
-        for i in range(bounds[r], bounds[r + 1]):
-            step(W + i)
+    for r in range(groups):
+        for _ in range(bounds[r + 1] - bounds[r]):
+            g_full.replay()
         marks[r + 1].record()
+    if g_rem is not None:
+        g_rem.replay()
+        marks[-1].record()
     barrier()
     clocks = sampler.stop() if sampler else None
     elapsed_ms = marks[0].elapsed_time(marks[-1])
-    rep_gbs = [round(nb["step"] * (bounds[r + 1] - bounds[r]) / (marks[r].elapsed_time(marks[r + 1]) * 1e-3) / 1e9,
-                     2) for r in range(reps)]
-    # Timed region B: the same K steps with CUDA events around every launch of
-    # the partition kernel, for its average launch duration (the events stop
-    # consecutive kernels from overlapping, so region A alone gives the step time).
+    rep_gbs = [round(nb["step"] * b * (bounds[r + 1] - bounds[r]) / (marks[r].elapsed_time(marks[r + 1]) * 1e-3)
+                     / 1e9, 2) for r in range(groups)]
+    # Timed region B: the same K steps launched eagerly with CUDA events around
+    # every launch of the partition kernel (its average launch duration; the
+    # events stop consecutive kernels from overlapping, so region A alone
+    # gives the step time).
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     barrier()
     for i in range(K):
-        step(W + i, evs[i])
+        step(i, evs[i])
     barrier()
-    kern_ms = [a.elapsed_time(b) for a, b in evs]
+    kern_ms = [x.elapsed_time(y) for x, y in evs]
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
     st = int(status.item())
     if st != 0:
@@ -381,70 +439,68 @@ def run_gpu(args):
     # inputs go up on one copy stream while step i-1 computes, and step i's output comes down on
     # another while step i+1 computes.  A block of E2E_BLOCK such steps is captured once as a
     # CUDA graph and replayed, so the host's per-call cost does not pace the loop.
-    e2e = None
-    if rank == 0 or world > 1:
-        up_stream, down_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-        dev_stages = [dev_stage, torch.empty_like(dev_stage)]
-        ios = [io0, views(dev_stages[1])]
-        ios[1]["out"] = torch.empty_like(io0["out"])
-        host_outs = [torch.empty(io0["out"].shape, dtype=io0["out"].dtype).pin_memory() for _ in range(2)]
-        h2d = int(total)
-        d2h = host_outs[0].numel() * host_outs[0].element_size()
-        block = E2E_BLOCK
-        Ke = max(block, min(K, args.e2e_steps) // block * block)
+    up_stream, down_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    dev_stages = [dev_stage, torch.empty_like(dev_stage)]
+    ios = [io0, views(dev_stages[1])]
+    ios[1]["out"] = torch.empty_like(io0["out"])
+    host_outs = [torch.empty(io0["out"].shape, dtype=io0["out"].dtype).pin_memory() for _ in range(2)]
+    h2d = int(total)
+    d2h = host_outs[0].numel() * host_outs[0].element_size()
+    block = E2E_BLOCK
+    Ke = max(block, min(K, args.e2e_steps) // block * block)
 
-        def e2e_block(n):
-            comp = torch.cuda.current_stream()
-            up = [torch.cuda.Event() for _ in range(2)]
-            done = [torch.cuda.Event() for _ in range(2)]
-            down = [torch.cuda.Event() for _ in range(2)]
-            up_stream.wait_stream(comp)
-            down_stream.wait_stream(comp)
-            for i in range(n):
-                b = i % 2
-                if i >= 2:
-                    up_stream.wait_event(done[b])    # step i-2 has finished reading this staging buffer
-                    comp.wait_event(down[b])         # and its output has been read back
-                with torch.cuda.stream(up_stream):
-                    dev_stages[b].copy_(host_stage, non_blocking=True)
-                    up[b].record(up_stream)
-                comp.wait_event(up[b])
-                step(i, io=ios[b])
-                done[b].record(comp)
-                down_stream.wait_event(done[b])
-                with torch.cuda.stream(down_stream):
-                    host_outs[b].copy_(ios[b]["out"], non_blocking=True)
-                    down[b].record(down_stream)
-            comp.wait_stream(up_stream)
-            comp.wait_stream(down_stream)
+    def e2e_block(n):
+        comp = torch.cuda.current_stream()
+        up = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+        down = [torch.cuda.Event() for _ in range(2)]
+        up_stream.wait_stream(comp)
+        down_stream.wait_stream(comp)
+        for i in range(n):
+            bb = i % 2
+            if i >= 2:
+                up_stream.wait_event(done[bb])    # step i-2 has finished reading this staging buffer
+                comp.wait_event(down[bb])         # and its output has been read back
+            with torch.cuda.stream(up_stream):
+                dev_stages[bb].copy_(host_stage, non_blocking=True)
+                up[bb].record(up_stream)
+            comp.wait_event(up[bb])
+            step(i, io=ios[bb])
+            done[bb].record(comp)
+            down_stream.wait_event(done[bb])
+            with torch.cuda.stream(down_stream):
+                host_outs[bb].copy_(ios[bb]["out"], non_blocking=True)
+                down[bb].record(down_stream)
+        comp.wait_stream(up_stream)
+        comp.wait_stream(down_stream)
 
-        side = torch.cuda.Stream(device=dev)
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            e2e_block(block)  # eager warm-up of the same work
-        torch.cuda.current_stream().wait_stream(side)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            e2e_block(block)
-        for _ in range(2):
-            graph.replay()
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(Ke // block):
-            graph.replay()
-        e1.record()
-        barrier()
-        e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
-        e2e = {"value": round(job_gbs(nb["step"], world, Ke, e_ms), 2), "unit": "GB/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": Ke,
-               "ms_per_step": round(e_ms / Ke, 5),
-               "overlap": f"double-buffered (inputs up / outputs down on two copy streams beside the step), "
-                          f"{block} steps per CUDA graph replay"}
-
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        e2e_block(block)  # eager warm-up of the same work
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        e2e_block(block)
+    for _ in range(2):
+        graph.replay()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(Ke // block):
+        graph.replay()
+    e1.record()
+    barrier()
+    e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after the end-to-end steps")
+    e2e = {"value": round(job_gbs(nb["step"], world, Ke, e_ms), 2), "unit": "GB/s",
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": Ke,
+           "ms_per_step": round(e_ms / Ke, 5),
+           "overlap": f"double-buffered (inputs up / outputs down on two copy streams beside the step), "
+                      f"{block} steps per CUDA graph replay"}
+    del graph, g_full, g_rem
     if rank != 0:
-        if world > 1:
-            dist.destroy_process_group()
         return None
 
     peak, peak_kind = _peaks()
@@ -455,8 +511,11 @@ def run_gpu(args):
         kernel_name = "decode_partitions_fp8_kernel"
     else:
         kernel_name = "decode_balanced_kernel" if ps == pkv.PARTITION_BALANCED else "decode_partitions_kernel"
-    traffic = _recorded_traffic(args.config, kernel_name)
+    traffic = _recorded_traffic(cfg, kernel_name)
     achieved = nb["attention"] / (kern_avg_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 2), "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                "bytes_per_launch": nb["attention"], "avg_launch_ms": round(kern_avg_ms, 5)}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -467,23 +526,80 @@ def run_gpu(args):
                               "pkv_write_cache_fp8 + pkv_decode_attention_fp8") if fp8 else
                              "pkv_write_cache + pkv_decode_attention" if args.unfused else "pkv_decode_step"),
                    "l2": f"inputs larger than L2: {replicas} pool replicas of {pool_bytes / 1e6:.0f} MB rotated "
-                         f"(L2 {l2 / 1e6:.0f} MB)", "parallelism": f"replicas x{world}"},
+                         f"(L2 {l2 / 1e6:.0f} MB)", "parallelism": f"replicas x{world}",
+                   "timed_region": f"{n_full} CUDA graph replays of {b} steps" +
+                                   (f" + one of {rem}" if rem else "") + " between two events",
+                   "warmup_graph_replays": 1},
         "pct_of_hbm_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_hbm_measured": round(100 * value / world / peak, 2),
         "seq_layers_per_s": round(world * wl.num_seqs / (ms * 1e-3), 1),
-        "repetitions": {"n": len(rep_gbs), "gbs_rank0": rep_gbs, "median_gbs_rank0": statistics.median(rep_gbs),
-                        "note": "the K timed steps in equal runs, one GPU's rate each; value is their total"},
+        "repetitions": {"n": len(rep_gbs), "gbs_rank0": rep_gbs,
+                        "median_gbs_rank0": statistics.median(rep_gbs) if rep_gbs else None,
+                        "note": "the K timed steps in equal runs of graph replays, one GPU's rate each; "
+                                "value is their total"},
         "kv_bytes_per_step": nb["kv"], "step_bytes": nb["step"],
-        "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 2),
-                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "bytes_per_launch": nb["attention"],
-                     "avg_launch_ms": round(kern_avg_ms, 5)},
+        "roofline": roofline,
         "gpu_launches": n_launch * K,
         "clocks": clocks,
         "e2e": e2e,
     }
-    if not args.no_cpu_baseline and world == 1:  # the oracle's host-core baseline: one GPU runs only
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds, f8 if fp8 else None)
+    if wl.copy_pairs.shape[0] and not fp8:
+        # A shared prefix is read by every sequence but sits in HBM once (and
+        # stays in L2): the HBM roofline counts each distinct slot once.
+        uniq = unique_kv_bytes(wl) + (nb["attention"] - nb["kv"])
+        line["unique_bytes"] = {
+            "note": "the logical bytes above count a shared prefix once per sequence; these count each distinct "
+                    "pool slot once (the HBM roofline of this workload)",
+            "attention_bytes_per_launch": uniq, "kv_bytes_per_step": unique_kv_bytes(wl),
+            "step_gbs": round(job_gbs(uniq + nb["write"] + nb["copy"], world, K, elapsed_ms), 2)}
+        roofline["achieved_logical"] = roofline["achieved"]
+        roofline["frac_logical"] = roofline["frac"]
+        roofline["achieved"] = round(uniq / (kern_avg_ms * 1e-3) / 1e9, 2)
+        roofline["frac"] = round(roofline["achieved"] / peak, 4)
+        roofline["bytes_per_launch"] = uniq
+        roofline["bytes_counted"] = "unique (each distinct pool slot once)"
+    if want_cpu_baseline:  # the oracle's host-core baseline: one GPU runs only
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds, f8)
+    del pools, k0, v0, ws, dev_stage, dev_stages, ios, io0
+    return line
+
+
+# Workloads of the default line: the largest single-GPU configuration (long
+# context, split-K) is the headline; the 8B- and 70B-class layers and the
+# prefix-sharing step ride along under per_config.
+HEADLINE_CONFIG = 4
+PER_CONFIG = (2, 3, 5)
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_112_gb300 as pkv
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    pkv.load()
+    ctx = {"dist": dist, "dev": dev, "rank": rank, "world": world, "local": local}
+    cpu_on = not args.no_cpu_baseline and world == 1
+    if args.config is not None:
+        line = measure_workload(args, args.config, ctx, cpu_on)
+    else:
+        line = measure_workload(args, HEADLINE_CONFIG, ctx, cpu_on)
+        per = {}
+        for cfg in PER_CONFIG:
+            torch.cuda.empty_cache()
+            per[str(cfg)] = measure_workload(args, cfg, ctx, False)
+        if line is not None:
+            keep = ("value", "unit", "ms_per_step", "pct_of_hbm_nominal_8tbs", "pct_of_hbm_measured",
+                    "seq_layers_per_s", "repetitions", "roofline", "unique_bytes", "clocks", "e2e", "config",
+                    "step_bytes", "gpu_launches")
+            line["per_config"] = {k: {f: v[f] for f in keep if f in v} for k, v in per.items()}
+            line["gpu_launches"] += sum(v["gpu_launches"] for v in per.values())
+            line["config"]["per_config_workloads"] = [per[str(c)]["config"]["workload"] for c in PER_CONFIG]
     if world > 1:
         dist.destroy_process_group()
     return line
@@ -528,7 +644,7 @@ def run_layers(args):
     out = torch.empty((n_layers, S, Hq, D), dtype=torch.float32, device=dev)
     max_len = wl.max_context_len
     ws_bytes = pkv.decode_workspace_bytes(S, Hq, D, max_len, ps)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def step(evs=None):
@@ -1007,7 +1123,9 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=None, choices=[1, 2, 3, 4, 5],
+                    help="one workload recipe; default: the long-context layer (4) as the headline with the 8B-class "
+                         "(2), 70B-class (3) and prefix-sharing (5) layers under per_config")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--partition-size", type=int, default=None)
     ap.add_argument("--replicas", type=int, default=0)
@@ -1042,6 +1160,9 @@ def main(argv=None):
         args.warmup = 20 if args.impl == "ours" else 3
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.config is None and (args.impl == "reference" or args.layers > 0 or args.op is not None):
+        # the reference arm times the headline workload; the single-purpose modes default to the 8B-class layer
+        args.config = HEADLINE_CONFIG if args.impl == "reference" else 2
     if args.kv == "fp8" and args.block_size != 16:
         ap.error("FP8 pools use 16-token blocks")
     if args.impl == "reference":

@@ -161,15 +161,19 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, i
  * pkv_decode_attention -- single-query (decode) grouped-query attention
  * through block tables [P1 "Inside the paged attention kernel"; P2 section
  * 02; P3 "End-to-end flow"].  For each sequence s and query head h, with
- * G = num_q_heads / num_kv_heads, g = h / G (contiguous groups: each KV head
- * serves its group of query heads [P2 section 02]) and L = context_lens[s]
+ * G = num_q_heads / num_kv_heads, g = h / G (contiguous groups: a KV head is
+ * shared by G consecutive query heads [P2 section 02]) and L = context_lens[s]
  * (the history including the token written this step [P3]):
  *     k_t = k_pool[block_tables[s][t / 16]][t % 16][g],  v_t likewise,
  *     out[s][h] = sum_t softmax_t(scale * q[s][h] . k_t) v_t,  t in [0, L).
  * L == 0 gives a zero row.  Sequences longer than partition_size tokens
- * are split into partitions of partition_size tokens that run on separate
- * thread blocks and are merged by a second reduce kernel (the split-K
- * restructuring of [P1 "Inside the paged attention kernel"]).
+ * are split into partitions of partition_size tokens that are computed
+ * independently and merged by a second reduce kernel (the split-K
+ * restructuring of [P1 "Inside the paged attention kernel"]).  Split calls
+ * with blocks of 16 tokens or more and num_seqs <= 1024 run on one
+ * persistent CTA per SM that takes (sequence, KV head, partition) units
+ * from a queue in the workspace, longest first; the others on a grid of
+ * small CTAs.  Both give the same results.
  *   out          : [num_seqs][num_q_heads][head_dim], out_dtype F32/F16/BF16.
  *   q            : [num_seqs][num_q_heads][head_dim], kv_dtype, 4-byte aligned.
  *   k_pool, v_pool, block_stride : pools as above (one layer).
@@ -191,8 +195,12 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, i
  *                  on the host).  Longer sequences set PKV_DEV_ERR_LENGTH and
  *                  are truncated.
  *   workspace    : device scratch of at least pkv_decode_workspace_bytes()
- *                  bytes, 16-byte aligned (may be NULL when that is 0).  Its
- *                  contents need no initialisation.
+ *                  bytes, 16-byte aligned (may be NULL when that is 0).
+ *                  Zero-fill it once after allocating it (cudaMemset): its
+ *                  first 256 bytes hold the work queue's control words, which
+ *                  must read zero when a call starts; every call leaves them
+ *                  zero again.  The rest needs no initialisation.  Calls
+ *                  that share a workspace must not overlap on the GPU.
  * Supported: head_dim 64 or 128, block_size 8, 16, 32 or 64 (16 only for
  * PKV_PARTITION_BALANCED), 1 <= G <= 8.
  * The two kernels run back to back on `stream`; pkv_decode_partitions and
@@ -288,11 +296,17 @@ pkv_status pkv_decode_step_partitions(void* out, const void* q, const void* k_ne
  *     library is loaded, until the process exits.  A call whose
  *     pkv_decode_workspace_bytes() exceeds it returns PKV_ERR_WORKSPACE and
  *     launches nothing.
- *   - The first call on a device (with that device current) looks up the
- *     array's device address; make that first call before any stream capture.
- *   - Every call shares the array and it keeps the last call's contents;
- *     nothing in it needs to start at zero.  Calls whose kernels overlap on
- *     the GPU race on it: order them (one stream, or explicit events).
+ *   - A call made outside stream capture (with its device current) looks up
+ *     the array's device address and keeps it for that device; a call inside
+ *     stream capture uses the kept address.  So make the first call on a
+ *     device before any stream capture (a captured first call returns
+ *     PKV_ERR_CUDA).  After cudaDeviceReset the next uncaptured call looks
+ *     the address up again.
+ *   - Every call shares the array and it keeps the last call's contents.
+ *     Only its first 256 bytes (the work queue's control words) must read
+ *     zero when a call starts: they are zero when the library is loaded and
+ *     every call leaves them zero.  Calls whose kernels overlap on the GPU
+ *     race on it: order them (one stream, or explicit events).
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  */
 #define PKV_STATIC_WORKSPACE_BYTES (16u << 20)
@@ -622,6 +636,16 @@ int pkv_bm_swap_in_cached(pkv_bm* bm, int64_t seq_id, int32_t* blocks, int32_t* 
 pkv_status pkv_check_bounded_wait(int64_t timeout_ns, int32_t* dev_status, void* stream);
 
 const char* pkv_status_string(pkv_status status);
+
+/*
+ * The CUDA error behind the calling thread's most recent PKV_ERR_CUDA
+ * return: a cudaError_t value, or minus the CUresult of a failed
+ * cuTensorMapEncodeTiled; 0 when this thread has had none.  Thread-local,
+ * so concurrent callers each see their own.  pkv_cuda_error_name() names a
+ * value returned here.
+ */
+int pkv_last_cuda_error(void);
+const char* pkv_cuda_error_name(int code);
 
 /* Library version, major * 10000 + minor * 100 + patch.  Host function. */
 int pkv_version(void);

@@ -57,6 +57,8 @@ _SIGS["pkv_decode_step_fp8"] = ([_c_void_p] * 4 + [_c_int64] + [_c_void_p] * 5 +
                                                 _c_void_p, _c_void_p])
 _SIGS["pkv_decode_step_partitions_fp8"] = _SIGS["pkv_decode_step_fp8"]
 _SIGS["pkv_check_bounded_wait"] = [_c_int64, _c_void_p, _c_void_p]
+_SIGS["pkv_last_cuda_error"] = []
+_SIGS["pkv_cuda_error_name"] = [_c_int]
 
 class _BmStats(ctypes.Structure):
     """pkv_bm_stats (include/pkv.h): int64 fields in declaration order."""
@@ -118,7 +120,7 @@ def load(build_if_missing: bool = False):
         fn = getattr(lib, name)
         fn.argtypes = argtypes
         fn.restype = ctypes.c_size_t if name == "pkv_decode_workspace_bytes" else (
-            ctypes.c_char_p if name == "pkv_status_string" else ctypes.c_int)
+            ctypes.c_char_p if name in ("pkv_status_string", "pkv_cuda_error_name") else ctypes.c_int)
     for name, (argtypes, restype) in _BM_SIGS.items():
         fn = getattr(lib, name)
         fn.argtypes = argtypes
@@ -133,7 +135,12 @@ def status_string(code: int) -> str:
 
 def _check(code: int, what: str):
     if code != PKV_OK:
-        raise PkvError(f"{what}: {status_string(code)}")
+        detail = ""
+        if code == PKV_ERR_CUDA:
+            lib = load()
+            err = int(lib.pkv_last_cuda_error())
+            detail = f" ({lib.pkv_cuda_error_name(err).decode()}, code {err})"
+        raise PkvError(f"{what}: {status_string(code)}{detail}")
 
 
 def _stream(stream) -> int:

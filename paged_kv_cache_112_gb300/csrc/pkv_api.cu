@@ -15,6 +15,22 @@ namespace {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 }  // namespace
 
+// The CUDA error behind the calling thread's last PKV_ERR_CUDA (0: none yet):
+// a cudaError_t, or minus a CUresult when descriptor encoding failed.
+thread_local int t_last_cuda_error = 0;
+
+pkv_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return PKV_OK;
+  t_last_cuda_error = static_cast<int>(e);
+  cudaGetLastError();  // a launch error is not sticky: clear it for the next call on this thread
+  return PKV_ERR_CUDA;
+}
+
+pkv_status cuda_status_fail(int code) {
+  t_last_cuda_error = code;
+  return PKV_ERR_CUDA;
+}
+
 int current_sm_count(int fallback) {
   // Filled once per device; readers see either 0 (not yet known) or the
   // count, never a torn value.
@@ -92,12 +108,16 @@ cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
   return cudaSuccess;
 }
 
+// Every layout starts with the kCtlBytes control block (offset 0, written
+// only by the SM-streaming kernel, which leaves it zero), so a workspace
+// keeps its control words in place whatever the sizes of the calls using it.
 WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_parts) {
   WorkspaceLayout w{};
   if (max_parts <= 1) return w;
   const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_parts;
-  w.acc_offset = 0;
-  w.ml_offset = align256(rows * head_dim * sizeof(float));
+  w.ctl_offset = 0;
+  w.acc_offset = kCtlBytes;
+  w.ml_offset = w.acc_offset + align256(rows * head_dim * sizeof(float));
   w.meta_offset = w.ml_offset + align256(rows * 2 * sizeof(float));
   w.total = w.meta_offset;
   return w;
@@ -107,8 +127,9 @@ WorkspaceLayout balanced_workspace_layout(int num_seqs, int num_q_heads, int hea
   WorkspaceLayout w{};
   const size_t heads = static_cast<size_t>(num_q_heads < 8 ? num_q_heads : 8);  // group size bound
   const size_t recs = static_cast<size_t>(warps) * 2 * heads;
-  w.acc_offset = 0;
-  w.ml_offset = align256(recs * head_dim * sizeof(float));
+  w.ctl_offset = 0;
+  w.acc_offset = kCtlBytes;
+  w.ml_offset = w.acc_offset + align256(recs * head_dim * sizeof(float));
   w.meta_offset = w.ml_offset + align256(recs * 2 * sizeof(float));
   w.total = w.meta_offset + align256(static_cast<size_t>(num_seqs) * num_q_heads * 2 * sizeof(int));
   return w;
@@ -146,7 +167,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 bool encode_pool_map_uncached(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int num_kv_heads,
                               int head_dim, int eb, int64_t block_stride) {
   auto fn = encode_fn();
-  if (!fn) return false;
+  if (!fn) {
+    t_last_cuda_error = static_cast<int>(cudaErrorSymbolNotFound);
+    return false;
+  }
   const cuuint32_t line = 128 / eb;  // elements per 128-byte line
   const cuuint64_t dims[4] = {line, static_cast<cuuint64_t>(num_kv_heads) * (head_dim / line),
                               static_cast<cuuint64_t>(block_size), static_cast<cuuint64_t>(num_blocks)};
@@ -160,6 +184,7 @@ bool encode_pool_map_uncached(CUtensorMap* map, const void* pool, int num_blocks
                         CU_TENSOR_MAP_SWIZZLE_128B,
                         head_dim * eb >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) t_last_cuda_error = -static_cast<int>(r);
   return r == CUDA_SUCCESS;
 }
 
@@ -272,7 +297,7 @@ pkv_status prepare_decode(DecodeCall* c, void* out, const void* q, const void* k
   const int64_t bstride = resolve_block_stride(block_stride, block_size, num_kv_heads, head_dim);
   if (bstride < 0) return PKV_ERR_INVALID_ARG;
   const int sms = balanced ? current_sm_count(0) : 0;
-  if (balanced && sms <= 0) return PKV_ERR_CUDA;
+  if (balanced && sms <= 0) return cuda_status_fail(static_cast<int>(cudaErrorNoDevice));
   int max_parts = 1, ps = 0;
   const WorkspaceLayout ws =
       decode_layout(num_seqs, num_q_heads, head_dim, max_context_len, partition_size, sms, &max_parts);
@@ -290,6 +315,7 @@ pkv_status prepare_decode(DecodeCall* c, void* out, const void* q, const void* k
   a.ws_acc = ws.total ? reinterpret_cast<float*>(wsb + ws.acc_offset) : nullptr;
   a.ws_ml = ws.total ? reinterpret_cast<float2*>(wsb + ws.ml_offset) : nullptr;
   a.ws_meta = (ws.total && balanced) ? reinterpret_cast<int2*>(wsb + ws.meta_offset) : nullptr;
+  a.ctl = (ws.total && !balanced) ? reinterpret_cast<int*>(wsb + ws.ctl_offset) : nullptr;
   a.balanced_ctas = balanced ? sms : 0;
   a.dev_status = dev_status;
   a.num_seqs = num_seqs;
@@ -355,7 +381,7 @@ pkv_status pkv_write_cache(const void* k_new, const void* v_new, void* k_pool, v
   a.block_shift = shift;
   a.num_tokens = num_tokens;
   a.row_elems = row;
-  return launch_write_cache(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return cuda_status(launch_write_cache(a, static_cast<cudaStream_t>(stream)));
 }
 
 pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int num_pairs, int num_layers,
@@ -377,7 +403,7 @@ pkv_status pkv_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int
   a.block_elems = static_cast<int64_t>(num_layers) * block_size * num_kv_heads * head_dim;
   a.num_pairs = num_pairs;
   a.num_blocks = num_blocks;
-  return launch_copy_blocks(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return cuda_status(launch_copy_blocks(a, static_cast<cudaStream_t>(stream)));
 }
 
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_context_len,
@@ -411,7 +437,7 @@ pkv_status pkv_decode_partitions(void* out, const void* q, const void* k_pool, c
                                                      static_cast<cudaStream_t>(stream))
                             : launch_decode_partitions(c.args, c.tmap_k, c.tmap_v, head_dim, kv_dtype == PKV_BF16,
                                                        static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return cuda_status(e);
 }
 
 pkv_status pkv_decode_reduce(void* out, const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
@@ -426,7 +452,7 @@ pkv_status pkv_decode_reduce(void* out, const int32_t* context_lens, int num_seq
   if (!balanced && partition_size % kTile != 0) return PKV_ERR_UNSUPPORTED;
   if (out_dtype != PKV_F32 && out_dtype != PKV_F16 && out_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
   const int sms = balanced ? current_sm_count(0) : 0;
-  if (balanced && sms <= 0) return PKV_ERR_CUDA;
+  if (balanced && sms <= 0) return cuda_status_fail(static_cast<int>(cudaErrorNoDevice));
   int max_parts = 1, ps = 0;
   const WorkspaceLayout ws =
       decode_layout(num_seqs, num_q_heads, head_dim, max_context_len, partition_size, sms, &max_parts);
@@ -457,7 +483,7 @@ pkv_status pkv_decode_reduce(void* out, const int32_t* context_lens, int num_seq
   a.balanced_ctas = balanced ? sms : 0;
   const cudaError_t e = balanced ? launch_decode_reduce_balanced(a, head_dim, static_cast<cudaStream_t>(stream))
                                  : launch_decode_reduce(a, head_dim, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return cuda_status(e);
 }
 
 pkv_status pkv_decode_step_partitions(void* out, const void* q, const void* k_new, const void* v_new,
@@ -492,7 +518,7 @@ pkv_status pkv_decode_step_partitions(void* out, const void* q, const void* k_ne
                                         : launch_decode_partitions(a, c.tmap_k, c.tmap_v, head_dim,
                                                                    kv_dtype == PKV_BF16,
                                                                    static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return cuda_status(e);
 }
 
 pkv_status pkv_decode_step(void* out, const void* q, const void* k_new, const void* v_new, int64_t new_row_stride,
@@ -568,7 +594,7 @@ pkv_status pkv_write_cache_fp8(const void* k_new, const void* v_new, void* k_poo
   a.num_kv_heads = num_kv_heads;
   a.head_dim = head_dim;
   a.new_bf16 = new_dtype == PKV_BF16;
-  return launch_write_cache_fp8(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return cuda_status(launch_write_cache_fp8(a, static_cast<cudaStream_t>(stream)));
 }
 
 pkv_status pkv_copy_blocks_fp8(void* k_pool, void* v_pool, float* k_scale, float* v_scale, const int32_t* pairs,
@@ -595,7 +621,7 @@ pkv_status pkv_copy_blocks_fp8(void* k_pool, void* v_pool, float* k_scale, float
   a.k_scale = k_scale;
   a.v_scale = v_scale;
   a.scales_per_block = num_layers * num_kv_heads;
-  return launch_copy_blocks(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return cuda_status(launch_copy_blocks(a, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"
@@ -652,10 +678,8 @@ pkv_status pkv_decode_partitions_fp8(void* out, const void* q, const void* k_poo
                                            max_context_len, workspace, workspace_bytes, q_dtype, out_dtype,
                                            dev_status);
   if (st != PKV_OK || num_seqs == 0) return st;
-  return launch_decode_partitions_fp8(c.args, c.tmap_k, c.tmap_v, head_dim, q_dtype == PKV_BF16,
-                                      static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? PKV_OK
-             : PKV_ERR_CUDA;
+  return cuda_status(launch_decode_partitions_fp8(c.args, c.tmap_k, c.tmap_v, head_dim, q_dtype == PKV_BF16,
+                                      static_cast<cudaStream_t>(stream)));
 }
 
 pkv_status pkv_decode_step_partitions_fp8(void* out, const void* q, const void* k_new, const void* v_new,
@@ -685,10 +709,8 @@ pkv_status pkv_decode_step_partitions_fp8(void* out, const void* q, const void* 
   a.slot_mapping = slot_mapping;
   a.k_pool_w = static_cast<uint16_t*>(k_pool);  // written as bytes by the FP8 kernel
   a.v_pool_w = static_cast<uint16_t*>(v_pool);
-  return launch_decode_partitions_fp8(a, c.tmap_k, c.tmap_v, head_dim, q_dtype == PKV_BF16,
-                                      static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? PKV_OK
-             : PKV_ERR_CUDA;
+  return cuda_status(launch_decode_partitions_fp8(a, c.tmap_k, c.tmap_v, head_dim, q_dtype == PKV_BF16,
+                                      static_cast<cudaStream_t>(stream)));
 }
 
 pkv_status pkv_decode_step_fp8(void* out, const void* q, const void* k_new, const void* v_new,
@@ -782,15 +804,13 @@ pkv_status pkv_swap_blocks(void* dst_k, void* dst_v, int64_t dst_block_stride, i
   a.num_pairs = num_pairs;
   a.dst_num_blocks = dst_num_blocks;
   a.src_num_blocks = src_num_blocks;
-  return launch_swap_blocks(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return cuda_status(launch_swap_blocks(a, static_cast<cudaStream_t>(stream)));
 }
 
 pkv_status pkv_check_bounded_wait(int64_t timeout_ns, int32_t* dev_status, void* stream) {
   if (timeout_ns < 0 || timeout_ns > kWaitTimeoutNs || !dev_status || !aligned(dev_status, 4))
     return PKV_ERR_INVALID_ARG;
-  return launch_bounded_wait_check(dev_status, timeout_ns, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? PKV_OK
-             : PKV_ERR_CUDA;
+  return cuda_status(launch_bounded_wait_check(dev_status, timeout_ns, static_cast<cudaStream_t>(stream)));
 }
 
 const char* pkv_status_string(pkv_status s) {
@@ -806,5 +826,12 @@ const char* pkv_status_string(pkv_status s) {
 }
 
 int pkv_version(void) { return 100; }
+
+int pkv_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char* pkv_cuda_error_name(int code) {
+  if (code >= 0) return cudaGetErrorName(static_cast<cudaError_t>(code));
+  return "CUresult from cuTensorMapEncodeTiled (negated)";
+}
 
 }  // extern "C"

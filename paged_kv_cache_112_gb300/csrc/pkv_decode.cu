@@ -333,6 +333,13 @@ cudaError_t launch_partitions_f(const DecodeArgs& a, const CUtensorMap& tk, cons
 
 cudaError_t launch_decode_partitions(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                      int head_dim, int kv_bf16, cudaStream_t stream) {
+  // Split calls whose plan fits the SM-streaming kernel run there; the grid
+  // kernel takes unsplit calls (no workspace), 8-token blocks and very large
+  // batches.
+  if (a.ctl && a.max_parts > 1 && a.block_shift >= 4 && a.num_seqs <= kStreamMaxSeqs &&
+      (head_dim == 64 || head_dim == 128) &&
+      static_cast<int64_t>(a.max_parts) * a.num_seqs * a.num_kv_heads < (int64_t{1} << 30))
+    return launch_decode_stream(a, tmap_k, tmap_v, head_dim, kv_bf16, stream);
   if (head_dim == 128)
     return kv_bf16 ? launch_partitions_f<128, true>(a, tmap_k, tmap_v, stream)
                    : launch_partitions_f<128, false>(a, tmap_k, tmap_v, stream);

@@ -40,7 +40,7 @@ class DeviceStep:
         self.out = torch.empty(wl.q.shape, dtype=out_dtype, device=device)
         nbytes = pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, self.max_context_len,
                                             self.partition_size)
-        self.workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device) if nbytes else None
+        self.workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device) if nbytes else None
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
 
     def copy(self):
@@ -106,7 +106,7 @@ class DeviceStepFp8:
         wl = self.wl
         nbytes = pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, max_context_len,
                                             self.partition_size)
-        self.workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=self.q.device) if nbytes else None
+        self.workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=self.q.device) if nbytes else None
 
     def copy(self):
         if self.pairs.shape[0]:

@@ -52,12 +52,13 @@ def test_workspace_bytes(lib):
     # no split -> nothing needed
     assert pkv.decode_workspace_bytes(64, 32, 128, 2048, 0) == 0
     assert pkv.decode_workspace_bytes(64, 32, 128, 512, 512) == 0
-    # 8 seqs x 32 heads x 256 partitions: acc fp32 [.., 128] + (m, l) pairs, each 256-B aligned
+    # 8 seqs x 32 heads x 256 partitions: acc fp32 [.., 128] + (m, l) pairs, each 256-B aligned,
+    # then the 256-byte control block of the work queue
     rows = 8 * 32 * 256
     acc = rows * 128 * 4
     ml = rows * 8
     up = lambda x: (x + 255) // 256 * 256
-    assert pkv.decode_workspace_bytes(8, 32, 128, 131072, 512) == up(acc) + up(ml)
+    assert pkv.decode_workspace_bytes(8, 32, 128, 131072, 512) == up(acc) + up(ml) + 256
     assert pkv.decode_workspace_bytes(8, 32, 128, 100, 24) == 0  # not a multiple of 16 -> invalid
     # balanced split: per-pair metadata + 2 partial records per warp (group <= 8 heads); without a
     # device the SM count defaults to 256, else the device's

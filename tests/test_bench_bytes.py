@@ -77,3 +77,23 @@ def test_reference_arm_prints_one_contract_line(capsys):
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_unique_bytes_count_a_shared_prefix_once():
+    """Prefix-sharing recipe: every sequence reads the same 2048-token prefix
+    blocks; the distinct slots are the prefix once plus each private suffix
+    (copy-on-write tails land in fresh blocks, so they are distinct too)."""
+    wl = P.make_workload(5, num_seqs=24)
+    L = wl.context_lens.astype(np.int64)
+    row = wl.num_kv_heads * wl.head_dim * 2 * 2
+    assert bench.unique_kv_bytes(wl) == (2048 + int((L - 2048).sum())) * row
+    wl2 = P.make_workload(2, num_seqs=8)  # no sharing: unique == logical
+    assert bench.unique_kv_bytes(wl2) == bench.step_bytes(wl2)["kv"]
+
+
+def test_graph_blocks_time_exactly_k_steps():
+    for K in (1, 3, 5, 20, 21, 64, 5000, 4999):
+        for R in (1, 2, 3):
+            b, full, rem = bench.graph_blocks(K, R)
+            assert b * full + rem == K and b % R == 0 and b >= 1
+            assert rem < b

@@ -95,7 +95,7 @@ def test_block_size_all_layer_view():
     out = torch.empty((L,) + wl.q.shape, dtype=torch.float32, device="cuda")
     bt, cl, sm = (torch.from_numpy(x).cuda() for x in (wl.block_tables, wl.context_lens, wl.slot_mapping))
     nb = pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, wl.max_context_len, 64)
-    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     q, kn, vn = dev(ld.q), dev(ld.k_new), dev(ld.v_new)
     for layer in range(L):

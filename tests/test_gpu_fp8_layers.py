@@ -53,7 +53,7 @@ def test_fp8_all_layer_step_matches_oracle(case, fused):
     out = torch.empty((L,) + wl.q.shape, dtype=torch.float32, device="cuda")
     nb = pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, wl.max_context_len,
                                     wl.partition_size)
-    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     if pairs.shape[0]:
         pkv.copy_blocks_fp8(dk, dv, dks, dvs, pairs, status=status)  # every layer at once

@@ -55,7 +55,7 @@ class LayeredStep:
         self.out = torch.empty(ld.q.shape, dtype=torch.float32, device="cuda")
         self.max_len = max_len or wl.max_context_len
         nb = pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, self.max_len, wl.partition_size)
-        self.ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda") if nb else None
+        self.ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device="cuda") if nb else None
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
 
     def layer_pools(self, layer):

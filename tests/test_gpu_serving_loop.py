@@ -96,7 +96,7 @@ class Loop:
         out = torch.empty((len(sids), HQ, D), dtype=torch.float32, device="cuda")
         ps = 32
         nb = pkv.decode_workspace_bytes(len(sids), HQ, D, int(cl.max()), ps)
-        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device="cuda")
         pkv.decode_step(out, dev16(q), dev16(np.stack(knew)), dev16(np.stack(vnew)), self.k, self.v,
                         torch.from_numpy(bt).cuda(), torch.from_numpy(cl).cuda(),
                         torch.tensor(slots, dtype=torch.int32).cuda(), SCALE, partition_size=ps,
@@ -122,7 +122,7 @@ class Loop:
         out = torch.empty((len(sids), HQ, D), dtype=torch.float32, device="cuda")
         ps = 32
         nb = pkv.decode_workspace_bytes(len(sids), HQ, D, int(cl.max()), ps)
-        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device="cuda")
         pkv.decode_step(out, dev16(q), dev16(np.stack(knew)), dev16(np.stack(vnew)), self.k, self.v,
                         torch.from_numpy(np.ascontiguousarray(bt)).cuda(), torch.from_numpy(cl).cuda(),
                         torch.from_numpy(slots).cuda(), SCALE, partition_size=ps, max_context_len=int(cl.max()),
