@@ -169,11 +169,7 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, i
  * L == 0 gives a zero row.  Sequences longer than partition_size tokens
  * are split into partitions of partition_size tokens that are computed
  * independently and merged by a second reduce kernel (the split-K
- * restructuring of [P1 "Inside the paged attention kernel"]).  Split calls
- * with blocks of 16 tokens or more and num_seqs <= 1024 run on one
- * persistent CTA per SM that takes (sequence, KV head, partition) units
- * from a queue in the workspace, longest first; the others on a grid of
- * small CTAs.  Both give the same results.
+ * restructuring of [P1 "Inside the paged attention kernel"]).
  *   out          : [num_seqs][num_q_heads][head_dim], out_dtype F32/F16/BF16.
  *   q            : [num_seqs][num_q_heads][head_dim], kv_dtype, 4-byte aligned.
  *   k_pool, v_pool, block_stride : pools as above (one layer).
@@ -195,12 +191,9 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, i
  *                  on the host).  Longer sequences set PKV_DEV_ERR_LENGTH and
  *                  are truncated.
  *   workspace    : device scratch of at least pkv_decode_workspace_bytes()
- *                  bytes, 16-byte aligned (may be NULL when that is 0).
- *                  Zero-fill it once after allocating it (cudaMemset): its
- *                  first 256 bytes hold the work queue's control words, which
- *                  must read zero when a call starts; every call leaves them
- *                  zero again.  The rest needs no initialisation.  Calls
- *                  that share a workspace must not overlap on the GPU.
+ *                  bytes, 16-byte aligned (may be NULL when that is 0).  Its
+ *                  contents need no initialisation.  Calls that share a
+ *                  workspace must not overlap on the GPU.
  * Supported: head_dim 64 or 128, block_size 8, 16, 32 or 64 (16 only for
  * PKV_PARTITION_BALANCED), 1 <= G <= 8.
  * The two kernels run back to back on `stream`; pkv_decode_partitions and
@@ -302,11 +295,9 @@ pkv_status pkv_decode_step_partitions(void* out, const void* q, const void* k_ne
  *     device before any stream capture (a captured first call returns
  *     PKV_ERR_CUDA).  After cudaDeviceReset the next uncaptured call looks
  *     the address up again.
- *   - Every call shares the array and it keeps the last call's contents.
- *     Only its first 256 bytes (the work queue's control words) must read
- *     zero when a call starts: they are zero when the library is loaded and
- *     every call leaves them zero.  Calls whose kernels overlap on the GPU
- *     race on it: order them (one stream, or explicit events).
+ *   - Every call shares the array and it keeps the last call's contents;
+ *     nothing in it needs to start at zero.  Calls whose kernels overlap on
+ *     the GPU race on it: order them (one stream, or explicit events).
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  */
 #define PKV_STATIC_WORKSPACE_BYTES (16u << 20)

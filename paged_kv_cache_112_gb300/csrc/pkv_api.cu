@@ -108,16 +108,12 @@ cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
   return cudaSuccess;
 }
 
-// Every layout starts with the kCtlBytes control block (offset 0, written
-// only by the SM-streaming kernel, which leaves it zero), so a workspace
-// keeps its control words in place whatever the sizes of the calls using it.
 WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_parts) {
   WorkspaceLayout w{};
   if (max_parts <= 1) return w;
   const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_parts;
-  w.ctl_offset = 0;
-  w.acc_offset = kCtlBytes;
-  w.ml_offset = w.acc_offset + align256(rows * head_dim * sizeof(float));
+  w.acc_offset = 0;
+  w.ml_offset = align256(rows * head_dim * sizeof(float));
   w.meta_offset = w.ml_offset + align256(rows * 2 * sizeof(float));
   w.total = w.meta_offset;
   return w;
@@ -127,9 +123,8 @@ WorkspaceLayout balanced_workspace_layout(int num_seqs, int num_q_heads, int hea
   WorkspaceLayout w{};
   const size_t heads = static_cast<size_t>(num_q_heads < 8 ? num_q_heads : 8);  // group size bound
   const size_t recs = static_cast<size_t>(warps) * 2 * heads;
-  w.ctl_offset = 0;
-  w.acc_offset = kCtlBytes;
-  w.ml_offset = w.acc_offset + align256(recs * head_dim * sizeof(float));
+  w.acc_offset = 0;
+  w.ml_offset = align256(recs * head_dim * sizeof(float));
   w.meta_offset = w.ml_offset + align256(recs * 2 * sizeof(float));
   w.total = w.meta_offset + align256(static_cast<size_t>(num_seqs) * num_q_heads * 2 * sizeof(int));
   return w;
@@ -157,13 +152,45 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// cuTensorMapEncodeTiled needs a current context.  A host thread that has
+// made no CUDA runtime call yet has none; the runtime would bind the
+// device's primary context at its first launch, so do the same here (a
+// thread that already has a context, primary or its own, keeps it).
+bool bind_context_if_none() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+  });
+  CUcontext ctx = nullptr;
+  if (get_current && get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr) return true;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) {
+    t_last_cuda_error = static_cast<int>(cudaGetLastError());
+    return false;
+  }
+  return true;
+}
+
 // Describes a pool of `eb`-byte elements, blocks `block_stride` elements
-// apart, as [num_blocks][16 rows][num_kv_heads * head_dim * eb / 128 lines]
-// [128 bytes], so that one box {128 bytes, 1, 16, 1} is the 16 token rows
-// of one 128-byte line of one head of one block: a (block, head) tile is
-// head_dim * eb / 128 boxes (16-bit: 2 at head_dim 128, 1 at 64; FP8: 1 at
-// head_dim 128).  A block stride above 16 rows is a layer slice of a pool
-// that keeps all layers of a block together.
+// apart, for TMA tile loads in the 128-byte swizzle (a 128-byte line is the
+// widest a swizzled box row may be).  A head's row of head_dim * eb bytes is
+// head_dim * eb / 128 lines.
+//  * Blocks of 16 tokens or more: dimensions {element in line, row in block,
+//    line (head * lines per head + line), block}, with the rows (stride
+//    num_kv_heads * head_dim * eb) before the lines (stride 128).  One box
+//    {128 bytes, 16 rows, lines per head, 1} is a whole (block, head) tile,
+//    landing in shared memory as [line][16 rows][128 bytes]: one copy per K
+//    or V tile, whatever head_dim is.
+//  * 8-token blocks: {element in line, line, row in block, block}; a box
+//    {128 bytes, 1, 8, 1} is one line of one head's 8 rows (a 16-row tile is
+//    two blocks, so lines per head x 2 boxes).
+// A block stride above one block's rows is a layer slice of a pool that
+// keeps all layers of a block together.
 bool encode_pool_map_uncached(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int num_kv_heads,
                               int head_dim, int eb, int64_t block_stride) {
   auto fn = encode_fn();
@@ -171,13 +198,19 @@ bool encode_pool_map_uncached(CUtensorMap* map, const void* pool, int num_blocks
     t_last_cuda_error = static_cast<int>(cudaErrorSymbolNotFound);
     return false;
   }
+  if (!bind_context_if_none()) return false;
   const cuuint32_t line = 128 / eb;  // elements per 128-byte line
-  const cuuint64_t dims[4] = {line, static_cast<cuuint64_t>(num_kv_heads) * (head_dim / line),
-                              static_cast<cuuint64_t>(block_size), static_cast<cuuint64_t>(num_blocks)};
-  const cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(num_kv_heads) * head_dim * eb,
+  const cuuint64_t lines = static_cast<cuuint64_t>(num_kv_heads) * (head_dim / line);
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(num_kv_heads) * head_dim * eb;
+  const bool whole_head = block_size >= kTile;
+  const cuuint64_t dims[4] = {line, whole_head ? static_cast<cuuint64_t>(block_size) : lines,
+                              whole_head ? lines : static_cast<cuuint64_t>(block_size),
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[3] = {whole_head ? row_bytes : 128, whole_head ? 128 : row_bytes,
                                  static_cast<cuuint64_t>(block_stride) * eb};
-  // A box is one 16-row tile, or one 8-token block (two boxes per tile).
-  const cuuint32_t box[4] = {line, 1, static_cast<cuuint32_t>(block_size < kTile ? block_size : kTile), 1};
+  const cuuint32_t box[4] = {line, whole_head ? static_cast<cuuint32_t>(kTile) : 1u,
+                             whole_head ? static_cast<cuuint32_t>(head_dim * eb / 128) : static_cast<cuuint32_t>(block_size),
+                             1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = fn(map, eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
                         const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -315,7 +348,6 @@ pkv_status prepare_decode(DecodeCall* c, void* out, const void* q, const void* k
   a.ws_acc = ws.total ? reinterpret_cast<float*>(wsb + ws.acc_offset) : nullptr;
   a.ws_ml = ws.total ? reinterpret_cast<float2*>(wsb + ws.ml_offset) : nullptr;
   a.ws_meta = (ws.total && balanced) ? reinterpret_cast<int2*>(wsb + ws.meta_offset) : nullptr;
-  a.ctl = (ws.total && !balanced) ? reinterpret_cast<int*>(wsb + ws.ctl_offset) : nullptr;
   a.balanced_ctas = balanced ? sms : 0;
   a.dev_status = dev_status;
   a.num_seqs = num_seqs;

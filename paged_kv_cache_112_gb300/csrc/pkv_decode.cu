@@ -142,11 +142,15 @@ __device__ __forceinline__ void partition_unit(const DecodeArgs& a, const CUtens
     const int st = i % NST;
     const int nv = ((bad_stage >> st) & 1) ? 0 : min(kTile, ntok - t * kTile);
     const uint32_t sK = ring.k_tile(i);
-    if (owns_new && t == nblk - 1 && nt.commit(a, g, lane)) nt.patch(sK, sK + Geom::kTileBytes, lane);
+    const bool patched = owns_new && t == nblk - 1 && nt.commit(a, g, lane);
+    if (patched) nt.patch(sK, sK + Geom::kTileBytes, lane);
     at.tile(sK, sK + Geom::kTileBytes, nv, a.scale_log2, lane);
     __syncwarp();
     if (i + NST < cnt) {
-      fence_proxy_async_smem();
+      // The stage's reads are complete (their values are in registers); only
+      // a generic-proxy write (the patched new token) must be ordered before
+      // the next copy into it.
+      if (patched) fence_proxy_async_smem();
       issue(i + NST);
     }
   }
@@ -333,13 +337,6 @@ cudaError_t launch_partitions_f(const DecodeArgs& a, const CUtensorMap& tk, cons
 
 cudaError_t launch_decode_partitions(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                      int head_dim, int kv_bf16, cudaStream_t stream) {
-  // Split calls whose plan fits the SM-streaming kernel run there; the grid
-  // kernel takes unsplit calls (no workspace), 8-token blocks and very large
-  // batches.
-  if (a.ctl && a.max_parts > 1 && a.block_shift >= 4 && a.num_seqs <= kStreamMaxSeqs &&
-      (head_dim == 64 || head_dim == 128) &&
-      static_cast<int64_t>(a.max_parts) * a.num_seqs * a.num_kv_heads < (int64_t{1} << 30))
-    return launch_decode_stream(a, tmap_k, tmap_v, head_dim, kv_bf16, stream);
   if (head_dim == 128)
     return kv_bf16 ? launch_partitions_f<128, true>(a, tmap_k, tmap_v, stream)
                    : launch_partitions_f<128, false>(a, tmap_k, tmap_v, stream);

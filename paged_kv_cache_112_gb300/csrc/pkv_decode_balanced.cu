@@ -210,11 +210,12 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     const int st = i % NST;
     const int nv = ((bad_stage >> st) & 1) ? 0 : min(kBlockSize, len[cc.s] - cc.t * kBlockSize);
     const uint32_t sK = ring.k_tile(i);
-    if (FUSED && cc.t == cc.n - 1 && nt.commit(a, cc.g, lane)) nt.patch(sK, sK + Geom::kTileBytes, lane);
+    const bool patched = FUSED && cc.t == cc.n - 1 && nt.commit(a, cc.g, lane);
+    if (patched) nt.patch(sK, sK + Geom::kTileBytes, lane);
     at.tile(sK, sK + Geom::kTileBytes, nv, a.scale_log2, lane);
     __syncwarp();
     if (i + NST < count) {
-      fence_proxy_async_smem();
+      if (patched) fence_proxy_async_smem();  // only the patched new token is a generic write to the stage
       issue(i + NST);
     }
     if (cc.t == cc.n - 1 || i == count - 1) {  // end of a segment

@@ -478,7 +478,7 @@ __device__ __forceinline__ void partition_unit_fp8(const DecodeArgs& a, const CU
     at.template tiles<2>(sK, nv, sl2k, pv, lane);
     __syncwarp();
     if (i + NST < cnt) {
-      fence_proxy_async_smem();
+      if (owns_new) fence_proxy_async_smem();  // only the new token's patch writes a stage
       issue(i + NST);
       if (i + 1 + NST < cnt) issue(i + 1 + NST);
     }

@@ -201,6 +201,16 @@ struct TileGeom {
   static constexpr int kStageBytes = 2 * kTileBytes;
 };
 
+// One (block, head) tile of K or V, rows [row0, row0 + 16) of block phys,
+// head g, from a pool map of blocks >= 16 tokens (dimensions {element in
+// line, row, line, block}): a single copy of the whole head row, landing as
+// [line][16 rows][128 bytes] with 16-byte chunk c of row r at c ^ (r & 7).
+template <int D, int EB = 2>
+__device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap* map, int row0, int g, int phys,
+                                         uint32_t bar) {
+  tma_load_4d(dst, map, 0, row0, g * TileGeom<D, EB>::kHalves, phys, bar);
+}
+
 // A warp's private ring of NST stages, each completing on its own mbarrier.
 template <int D, int NST, int EB = 2>
 struct WarpRing {
@@ -218,11 +228,11 @@ struct WarpRing {
   }
 
   // Lane 0 issues the K and V copies of tile number j (stage j % NST), KV
-  // head g (tensor maps: {element line, head line, row in block, block}):
-  // rows [row0, row0 + 16) of block `phys` (blocks of >= 16 tokens; box of
-  // 16 rows), or, when phys2 >= 0 (8-token blocks; box of 8 rows), block
-  // phys then block phys2, the second landing 8 rows (1024 bytes) further,
-  // in the same swizzle phase as a 16-row box.
+  // head g: rows [row0, row0 + 16) of block `phys` (blocks of >= 16 tokens;
+  // one whole-head box per tensor, see tma_tile), or, when phys2 >= 0
+  // (8-token blocks; tensor maps {element, line, row in block, block}, a box
+  // is one line of 8 rows), block phys then block phys2, the second landing
+  // 8 rows (1024 bytes) further, in the same swizzle phase as a 16-row box.
   __device__ __forceinline__ void issue(int j, int phys, int phys2, int row0, int g, const CUtensorMap* tk,
                                         const CUtensorMap* tv, int lane) const {
     if (lane != 0) return;
@@ -230,14 +240,17 @@ struct WarpRing {
     const uint32_t b = bar + 8 * st;
     const uint32_t dst = buf + st * Geom::kStageBytes;
     mbar_arrive_expect_tx(b, Geom::kStageBytes);
+    if (phys2 < 0) {
+      tma_tile<D, EB>(dst, tk, row0, g, phys, b);
+      tma_tile<D, EB>(dst + Geom::kTileBytes, tv, row0, g, phys, b);
+      return;
+    }
 #pragma unroll
     for (int h = 0; h < Geom::kHalves; ++h) {
       tma_load_4d(dst + h * 2048, tk, 0, g * Geom::kHalves + h, row0, phys, b);
       tma_load_4d(dst + Geom::kTileBytes + h * 2048, tv, 0, g * Geom::kHalves + h, row0, phys, b);
-      if (phys2 >= 0) {
-        tma_load_4d(dst + h * 2048 + 1024, tk, 0, g * Geom::kHalves + h, 0, phys2, b);
-        tma_load_4d(dst + Geom::kTileBytes + h * 2048 + 1024, tv, 0, g * Geom::kHalves + h, 0, phys2, b);
-      }
+      tma_load_4d(dst + h * 2048 + 1024, tk, 0, g * Geom::kHalves + h, 0, phys2, b);
+      tma_load_4d(dst + Geom::kTileBytes + h * 2048 + 1024, tv, 0, g * Geom::kHalves + h, 0, phys2, b);
     }
   }
 

@@ -93,8 +93,6 @@ struct DecodeArgs {
   float* ws_acc;     // partial records [..][D]: unnormalised partial outputs
   float2* ws_ml;     // partial records: (running max in log2 units, running sum)
   int2* ws_meta;     // balanced split: per (s, g) pair (first warp, 2 * pieces + its slot)
-  int* ctl;          // fixed partitions: the SM-streaming kernel's control words (queue, CTAs done);
-                     // zero before a call, zero again after it
   int32_t* dev_status;
   int num_seqs;
   int num_q_heads;
@@ -130,13 +128,8 @@ struct DecodeArgs {
 // records [S][H_q][max_parts].  Balanced split: per-pair metadata [S][<=H_q]
 // then records [W warps][2 slots][<= 8 heads].
 struct WorkspaceLayout {
-  size_t acc_offset, ml_offset, meta_offset, ctl_offset, total;
+  size_t acc_offset, ml_offset, meta_offset, total;
 };
-// Bytes of the control block at the end of a fixed-partition workspace.
-constexpr size_t kCtlBytes = 256;
-// Sequences the SM-streaming partition kernel plans for in shared memory;
-// larger batches use the grid kernel.
-constexpr int kStreamMaxSeqs = 1024;
 WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_parts);
 WorkspaceLayout balanced_workspace_layout(int num_seqs, int num_q_heads, int head_dim, int64_t warps);
 
@@ -187,12 +180,6 @@ cudaError_t launch_decode_partitions(const DecodeArgs& a, const CUtensorMap& tma
                                      const CUtensorMap& tmap_v, int head_dim, int kv_bf16,
                                      cudaStream_t stream);  // fuses the write when a.k_new is set
 cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t stream);
-// SM-streaming partition kernel (pkv_decode_stream.cu): one persistent CTA
-// per SM, a device-wide longest-first unit queue in a.ctl.  Same outputs and
-// partial records as launch_decode_partitions; 16-bit pools, blocks of 16
-// tokens or more, num_seqs <= kStreamMaxSeqs.
-cudaError_t launch_decode_stream(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                                 int head_dim, int kv_bf16, cudaStream_t stream);
 // One warp waits on a tile barrier that no copy arms, for timeout_ns, and
 // sets PKV_DEV_ERR_TIMEOUT in *status (pkv_check_bounded_wait).
 cudaError_t launch_bounded_wait_check(int32_t* status, long long timeout_ns, cudaStream_t stream);

@@ -58,7 +58,7 @@ def test_workspace_bytes(lib):
     acc = rows * 128 * 4
     ml = rows * 8
     up = lambda x: (x + 255) // 256 * 256
-    assert pkv.decode_workspace_bytes(8, 32, 128, 131072, 512) == up(acc) + up(ml) + 256
+    assert pkv.decode_workspace_bytes(8, 32, 128, 131072, 512) == up(acc) + up(ml)
     assert pkv.decode_workspace_bytes(8, 32, 128, 100, 24) == 0  # not a multiple of 16 -> invalid
     # balanced split: per-pair metadata + 2 partial records per warp (group <= 8 heads); without a
     # device the SM count defaults to 256, else the device's

@@ -1,14 +1,12 @@
-"""The grid partition kernel (used for batches of more than 1024 sequences
-and for 8-token blocks; smaller split batches run on the SM-streaming
-kernel) serves a unit (sequence, KV head, partition) with one warp, or with
-two warps that split its blocks and merge their softmax states through
-shared memory.  The host picks two when the sequences alone (H_kv x S, a
-unit each at least) overfill one wave of warp slots, else one.  These cases
-take each path on a GB300 (152 SMs x 6 CTAs x 2 warps = 1824 warp slots)
-with short sequences the oracle finishes quickly, including a one-warp batch
-whose partition-indexed grid is mostly empty and one whose units exceed a
-wave; on another GPU the paths may differ but every result must still
-match."""
+"""The partition kernel serves a unit (sequence, KV head, partition) with one
+warp, or with two warps that split its blocks and merge their softmax states
+through shared memory.  The host picks two when the sequences alone
+(H_kv x S, a unit each at least) overfill one wave of warp slots, else one.
+These cases take each path on a GB300 (152 SMs x 6 CTAs x 2 warps = 1824
+warp slots) with short sequences the oracle finishes quickly, including a
+one-warp batch whose partition-indexed grid is mostly empty and one whose
+units exceed a wave; on another GPU the paths may differ but every result
+must still match."""
 import numpy as np
 import pytest
 import torch
@@ -29,24 +27,19 @@ def _lib():
 
 
 CASES = {
-    # 1100 x 8 = 8800 sequence-heads > 1824 slots: two warps per unit.
-    "two_warps": dict(cfg=3, num_seqs=1100, lens=("uniform", 1, 90), ps=32, max_len=None),
-    # 1100 x 1 sequence-heads: one warp; a bound of 16 partitions per sequence
+    # 256 x 8 = 2048 sequence-heads > 1824 slots: two warps per unit.
+    "two_warps": dict(cfg=3, num_seqs=256, lens=("uniform", 1, 90), ps=32, max_len=None),
+    # 64 x 8 = 512 sequence-heads: one warp; a bound of 16 partitions per sequence
     # while the lengths need at most 2 leaves most of the grid empty.
-    "one_warp_sparse": dict(cfg=2, num_seqs=1100, num_q_heads=8, num_kv_heads=1, lens=("uniform", 1, 30), ps=16,
-                            max_len=256),
-    # same shape, lengths near the bound: 1100 x ~15 units, several waves of one-warp units.
-    "one_warp_waves": dict(cfg=2, num_seqs=1100, num_q_heads=8, num_kv_heads=1, lens=("uniform", 224, 255), ps=16,
-                           max_len=256),
+    "one_warp_sparse": dict(cfg=2, num_seqs=64, lens=("uniform", 1, 30), ps=16, max_len=256),
+    # same shape, lengths near the bound: 64 x 8 x ~15 units, several waves of one-warp units.
+    "one_warp_waves": dict(cfg=2, num_seqs=64, lens=("uniform", 224, 255), ps=16, max_len=256),
 }
 
 
 def _workload(case, dtype=None):
     c = CASES[case]
     kw = dict(num_seqs=c["num_seqs"], lens=c["lens"], partition_size=c["ps"])
-    for key in ("num_q_heads", "num_kv_heads"):
-        if key in c:
-            kw[key] = c[key]
     if dtype:
         kw["dtype"] = dtype
     return P.make_workload(c["cfg"], **kw), c["max_len"]
@@ -61,7 +54,7 @@ def test_unit_warps_match_oracle(case, dtype):
     if max_len:
         ds.max_context_len = max_len
         nbytes = pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, max_len, ds.partition_size)
-        ds.workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+        ds.workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
     out = ds.step().cpu().numpy()
     assert ds.status_bits() == 0
     assert float(np.max(np.abs(out - ref))) <= ATOL
@@ -76,7 +69,7 @@ def test_unit_warps_fused_step_equals_write_then_attend(case):
         if max_len:
             ds.max_context_len = max_len
             nbytes = pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim, max_len, ds.partition_size)
-            ds.workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+            ds.workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
     out_a = a.step().clone()
     out_b = b.fused_step().clone()
     assert a.status_bits() == 0 and b.status_bits() == 0
