@@ -59,7 +59,7 @@ CONFIGS = {
             lens=("uniform", 32768, 131072), pool_factor=1.25, partition_size=512),
     5: dict(name="prefix sharing + copy-on-write: S=128 32q/4kv D=128 f16 2048 shared + U[0,512] private",
             dtype="f16", num_seqs=128, num_q_heads=32, num_kv_heads=4, head_dim=128,
-            lens=("prefix", 2048, 0, 512), pool_factor=1.25, partition_size=1024),
+            lens=("prefix", 2048, 0, 512), pool_factor=1.25, partition_size=768),
 }
 
 
