@@ -65,6 +65,7 @@ if ROOT not in sys.path:
 
 METRIC = "decode paged-attention KV GB/s and % of GB300 HBM peak; sequences·layers/sec"
 E2E_BLOCK = 16  # end-to-end steps per captured graph
+WARMUP_GRAPH_MS = 30.0  # graph replays after the eager warm-up steps, before the timed region
 REPS = 5  # repetitions the timed steps are split into (rate of each, and their median, beside the total)
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
@@ -223,17 +224,20 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU arm
 
-def unique_kv_bytes(wl, elem_bytes=2):
+def unique_kv_bytes(wl, elem_bytes=2, scale_bytes=0):
     """K+V bytes of the distinct pool slots a step reads: a slot referenced by
-    several sequences (a shared prefix) counts once."""
+    several sequences (a shared prefix) counts once.  With `scale_bytes`, each
+    distinct block also contributes its K and V scale per KV head (FP8 pools)."""
     B = wl.block_size
     slots = []
     for s in range(wl.num_seqs):
         L = int(wl.context_lens[s])
         t = np.arange(L, dtype=np.int64)
         slots.append(wl.block_tables[s, t // B].astype(np.int64) * B + t % B)
-    n = int(np.unique(np.concatenate(slots)).size) if slots else 0
-    return n * wl.num_kv_heads * wl.head_dim * 2 * elem_bytes
+    uniq = np.unique(np.concatenate(slots)) if slots else np.zeros(0, np.int64)
+    n_blocks = int(np.unique(uniq // B).size)
+    return (int(uniq.size) * wl.num_kv_heads * wl.head_dim * 2 * elem_bytes
+            + n_blocks * wl.num_kv_heads * 2 * scale_bytes)
 
 
 def graph_blocks(K, replicas):
@@ -388,6 +392,50 @@ def measure_workload(args, cfg, ctx, want_cpu_baseline):
                 step(i)
         return g
 
+    def graph_warmup(g):
+        """Replays g until at least WARMUP_GRAPH_MS of replays have run (one
+        at least); returns the number of replays."""
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        more = max(0, math.ceil(WARMUP_GRAPH_MS / max(e0.elapsed_time(e1), 1e-3)) - 1)
+        for _ in range(more):
+            g.replay()
+        torch.cuda.synchronize()
+        return 1 + more
+
+    def timed_launches(n_steps, per_graph):
+        """Durations (ms) of the partition-kernel launches of steps 0..n_steps-1
+        and how they were timed."""
+        try:
+            evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                    torch.cuda.Event(enable_timing=True, external=True)) for _ in range(per_graph)]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(per_graph):
+                    step(i, evs[i])
+        except (TypeError, RuntimeError):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n_steps)]
+            barrier()
+            for i in range(n_steps):
+                step(i, evs[i])
+            barrier()
+            return [x.elapsed_time(y) for x, y in evs], "eager launches, events around each"
+        g.replay()  # warm-up replay, not timed
+        barrier()
+        out = []
+        while len(out) < n_steps:
+            g.replay()
+            torch.cuda.synchronize()
+            out += [x.elapsed_time(y) for x, y in evs][:n_steps - len(out)]
+        del g
+        if not all(t > 0 for t in out):
+            raise RuntimeError("non-positive kernel duration from graph-recorded events")
+        return out, f"CUDA graph replays of {per_graph} steps, event nodes around each launch"
+
     b, n_full, rem = graph_blocks(K, replicas)
     g_full = capture(b)
     g_rem = capture(rem) if rem else None
@@ -396,8 +444,7 @@ def measure_workload(args, cfg, ctx, want_cpu_baseline):
         sampler.start()  # sampling starts before the warm-up: no idle gap before the timed region
     for i in range(W):
         step(i)
-    g_full.replay()
-    torch.cuda.synchronize()
+    warm_replays = graph_warmup(g_full)
 
     # Timed region A: exactly K steps (n_full replays of b steps, then the
     # remainder), nothing else on the stream.  Events between replays split it
@@ -406,6 +453,10 @@ def measure_workload(args, cfg, ctx, want_cpu_baseline):
     bounds = [n_full * r // groups for r in range(groups + 1)] if groups else [0]
     marks = [torch.cuda.Event(enable_timing=True) for _ in range(len(bounds) + (1 if g_rem else 0))]
     barrier()
+    # One untimed replay is already running when the first event is recorded,
+    # so the timed replays queue behind it: the region starts on a busy GPU,
+    # as every step of a serving loop does, not with a launch from idle.
+    g_full.replay()
     marks[0].record()
     for r in range(groups):
         for _ in range(bounds[r + 1] - bounds[r]):
@@ -419,16 +470,13 @@ def measure_workload(args, cfg, ctx, want_cpu_baseline):
     elapsed_ms = marks[0].elapsed_time(marks[-1])
     rep_gbs = [round(nb["step"] * b * (bounds[r + 1] - bounds[r]) / (marks[r].elapsed_time(marks[r + 1]) * 1e-3)
                      / 1e9, 2) for r in range(groups)]
-    # Timed region B: the same K steps launched eagerly with CUDA events around
-    # every launch of the partition kernel (its average launch duration; the
-    # events stop consecutive kernels from overlapping, so region A alone
-    # gives the step time).
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    barrier()
-    for i in range(K):
-        step(i, evs[i])
-    barrier()
-    kern_ms = [x.elapsed_time(y) for x, y in evs]
+    # Timed region B: the same K steps with CUDA events around every launch of
+    # the partition kernel (its average launch duration; the events stop
+    # consecutive kernels from overlapping, so region A alone gives the step
+    # time).  The events are recorded by nodes of a captured graph where torch
+    # can capture them, so the host's launch rate does not stretch the short
+    # launches; otherwise the steps are launched eagerly.
+    kern_ms, kern_timing = timed_launches(K, b)
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
     st = int(status.item())
     if st != 0:
@@ -486,6 +534,7 @@ def measure_workload(args, cfg, ctx, want_cpu_baseline):
         graph.replay()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    graph.replay()  # untimed, in flight when the region starts (as in region A)
     e0.record()
     for _ in range(Ke // block):
         graph.replay()
@@ -515,7 +564,8 @@ def measure_workload(args, cfg, ctx, want_cpu_baseline):
     achieved = nb["attention"] / (kern_avg_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 2), "peak": peak,
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                "bytes_per_launch": nb["attention"], "avg_launch_ms": round(kern_avg_ms, 5)}
+                "bytes_per_launch": nb["attention"], "avg_launch_ms": round(kern_avg_ms, 5),
+                "launch_timing": kern_timing}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -529,7 +579,7 @@ def measure_workload(args, cfg, ctx, want_cpu_baseline):
                          f"(L2 {l2 / 1e6:.0f} MB)", "parallelism": f"replicas x{world}",
                    "timed_region": f"{n_full} CUDA graph replays of {b} steps" +
                                    (f" + one of {rem}" if rem else "") + " between two events",
-                   "warmup_graph_replays": 1},
+                   "warmup_graph_replays": warm_replays + 1},
         "pct_of_hbm_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_hbm_measured": round(100 * value / world / peak, 2),
         "seq_layers_per_s": round(world * wl.num_seqs / (ms * 1e-3), 1),
@@ -543,14 +593,15 @@ def measure_workload(args, cfg, ctx, want_cpu_baseline):
         "clocks": clocks,
         "e2e": e2e,
     }
-    if wl.copy_pairs.shape[0] and not fp8:
+    if wl.copy_pairs.shape[0]:
         # A shared prefix is read by every sequence but sits in HBM once (and
         # stays in L2): the HBM roofline counts each distinct slot once.
-        uniq = unique_kv_bytes(wl) + (nb["attention"] - nb["kv"])
+        ukv = unique_kv_bytes(wl, 1, 4) if fp8 else unique_kv_bytes(wl)
+        uniq = ukv + (nb["attention"] - nb["kv"])
         line["unique_bytes"] = {
             "note": "the logical bytes above count a shared prefix once per sequence; these count each distinct "
                     "pool slot once (the HBM roofline of this workload)",
-            "attention_bytes_per_launch": uniq, "kv_bytes_per_step": unique_kv_bytes(wl),
+            "attention_bytes_per_launch": uniq, "kv_bytes_per_step": ukv,
             "step_gbs": round(job_gbs(uniq + nb["write"] + nb["copy"], world, K, elapsed_ms), 2)}
         roofline["achieved_logical"] = roofline["achieved"]
         roofline["frac_logical"] = roofline["frac"]

@@ -91,6 +91,18 @@ def test_unique_bytes_count_a_shared_prefix_once():
     assert bench.unique_kv_bytes(wl2) == bench.step_bytes(wl2)["kv"]
 
 
+def test_unique_bytes_fp8_count_codes_and_block_scales_once():
+    """FP8 pools: one byte per element, plus a K and a V scale per KV head of
+    each distinct block.  Without sharing this is the step's own K/V count."""
+    wl = P.make_workload(5, num_seqs=24)
+    L = wl.context_lens.astype(np.int64)
+    hd = wl.num_kv_heads * wl.head_dim
+    blocks = 2048 // 16 + int(np.sum((L - 2048 + 15) // 16))  # prefix blocks once, then each private tail
+    assert bench.unique_kv_bytes(wl, 1, 4) == (2048 + int((L - 2048).sum())) * hd * 2 + blocks * wl.num_kv_heads * 8
+    wl2 = P.make_workload(2, num_seqs=8)
+    assert bench.unique_kv_bytes(wl2, 1, 4) == bench.step_bytes_fp8(wl2)["kv"]
+
+
 def test_graph_blocks_time_exactly_k_steps():
     for K in (1, 3, 5, 20, 21, 64, 5000, 4999):
         for R in (1, 2, 3):
