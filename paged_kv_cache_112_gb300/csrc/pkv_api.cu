@@ -668,7 +668,7 @@ pkv_status prepare_decode_fp8(DecodeCall* c, void* out, const void* q, const voi
                               int num_kv_heads, int head_dim, int block_size, int num_blocks, int num_layers,
                               float scale, int partition_size, int max_context_len, void* workspace,
                               size_t workspace_bytes, pkv_dtype q_dtype, pkv_dtype out_dtype, int32_t* dev_status) {
-  if (partition_size == PKV_PARTITION_BALANCED || block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
   if (num_layers <= 0 || num_layers > kMaxLayers || num_kv_heads <= 0 || head_dim <= 0)
     return PKV_ERR_INVALID_ARG;
   // One byte per code: the block stride in codes is the stride in bytes.
@@ -710,6 +710,9 @@ pkv_status pkv_decode_partitions_fp8(void* out, const void* q, const void* k_poo
                                            max_context_len, workspace, workspace_bytes, q_dtype, out_dtype,
                                            dev_status);
   if (st != PKV_OK || num_seqs == 0) return st;
+  if (c.args.balanced_ctas)
+    return cuda_status(launch_decode_balanced_fp8(c.args, c.tmap_k, c.tmap_v, head_dim, q_dtype == PKV_BF16,
+                                                  static_cast<cudaStream_t>(stream)));
   return cuda_status(launch_decode_partitions_fp8(c.args, c.tmap_k, c.tmap_v, head_dim, q_dtype == PKV_BF16,
                                       static_cast<cudaStream_t>(stream)));
 }
@@ -722,6 +725,7 @@ pkv_status pkv_decode_step_partitions_fp8(void* out, const void* q, const void* 
                                           int num_blocks, int num_layers, float scale, int partition_size, int max_context_len,
                                           void* workspace, size_t workspace_bytes, pkv_dtype q_dtype,
                                           pkv_dtype out_dtype, int32_t* dev_status, void* stream) {
+  if (partition_size == PKV_PARTITION_BALANCED) return PKV_ERR_UNSUPPORTED;  // the fused write needs fixed partitions
   DecodeCall c{};
   const pkv_status st = prepare_decode_fp8(&c, out, q, k_pool, v_pool, k_scale, v_scale, block_tables,
                                            max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,

@@ -38,7 +38,7 @@
 //    table entries, one chunk of 32 tiles at a time.
 //  * The accumulator is rescaled only in tiles where some head's running
 //    max grows (a warp-uniform branch).
-#include "pkv_device.cuh"
+#include "pkv_balanced.cuh"
 #include "pkv_fp8.cuh"
 
 namespace pkv {
@@ -266,6 +266,11 @@ struct WarpAttentionFp8 : SoftmaxState<D / 16> {
 // 2^e for an integer e in [-126, 127], exactly.
 __device__ __forceinline__ float exp2i(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
 
+// The factor 2^(from - to) that moves the accumulator from unit 2^from to
+// unit 2^to (to > from), exactly, down to the f32 subnormals and 0 (the
+// first unit of a pair starts at 2^-126, so the gap can exceed 126).
+__device__ __forceinline__ float unit_change(int from, int to) { return ldexpf(1.f, from - to); }
+
 // The accumulator's unit for a chunk of tiles: 2^-e with 2^e <= the
 // largest V scale of the chunk (over the warp) < 2^(e+1), so P * scale /
 // unit stays below 2 and well inside the f16 range.
@@ -450,7 +455,7 @@ __device__ __forceinline__ void partition_unit_fp8(const DecodeArgs& a, const CU
       vexp_chunk = i >> 5;
       const int e = chunk_exponent(vs_cur);
       if (e > vexp) {
-        at.scale_acc(exp2i(vexp - e));
+        at.scale_acc(unit_change(vexp, e));
         vexp = e;
         inv_unit = exp2i(-e);
       }
@@ -528,6 +533,235 @@ __global__ void __launch_bounds__(64, 6) decode_partitions_fp8_kernel(
   }
 }
 
+// ------------------------------------------------------------ balanced split
+//
+// PKV_PARTITION_BALANCED over FP8 pools: the work order and equal shares of
+// the 16-bit balanced kernel (pkv_balanced.cuh) with this file's tile math.
+// One CTA of NW warps per SM; each warp's 4-stage ring of 4 KB tiles runs on
+// across the (s, g) pairs of its share.
+//  * Issue side: the table entries of three chunks (a chunk is up to 32
+//    consecutive tiles of one pair; lane j holds tile j's entry) and the K/V
+//    scales of the first two, so a chunk's scales are loaded one chunk
+//    before its tiles are issued, from entries loaded one chunk before that.
+//    Each issued tile's two scales are stored beside its stage, where the
+//    compute side reads them with the tile.
+//  * Compute side: two consecutive tiles of one pair share a softmax step;
+//    a pair's last odd tile goes alone.  The accumulator's unit (a power of
+//    two at least the largest V scale seen, as in the partition kernel)
+//    starts afresh with each pair.
+//  * Output: as the 16-bit balanced kernel (final rows for pairs a warp
+//    covers whole, two partial-state slots per warp, pair metadata for the
+//    balanced reduce).
+template <int D, bool QBF16, int NW, int NST>
+__global__ void __launch_bounds__(NW * 32, 1) decode_balanced_fp8_kernel(
+    const DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
+    const __grid_constant__ CUtensorMap tmap_v) {
+  using Geom = TileGeom<D, 1>;
+  using Att = WarpAttentionFp8<D>;
+  static_assert(NST % 2 == 0 && NST <= 32, "tile pairs take whole pairs of stages");
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const size_t ring_bytes = static_cast<size_t>(NW) * NST * Geom::kStageBytes;
+  const uint32_t bars = smem_u32(smem + ring_bytes);
+  float2* stage_scale = reinterpret_cast<float2*>(smem + ring_bytes + NW * NST * 8);  // [NW][NST]: (k, v)
+  int* pre = reinterpret_cast<int*>(smem + ring_bytes + NW * NST * 16);  // [S + 1] tile prefix
+  int* len = pre + a.num_seqs + 1;                                        // [S] clamped lengths
+  int* warp_tot = len + a.num_seqs;                                       // [32] scan scratch
+
+  griddep_wait();  // every input may come from the previous kernel on the stream
+  griddep_launch_dependents();
+  if (smem_misaligned(smem, a.dev_status)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = a.num_seqs, Hkv = a.num_kv_heads, G = a.group;
+
+  for (int i = threadIdx.x; i < S; i += blockDim.x) {
+    const int L = clamped_len(a, i, blockIdx.x == 0);
+    len[i] = L;
+    pre[i + 1] = (L + kBlockSize - 1) / kBlockSize;
+  }
+  if (threadIdx.x == 0) pre[0] = 0;
+  __syncthreads();
+  block_inclusive_scan(pre + 1, S, warp_tot);
+
+  const int64_t T = static_cast<int64_t>(Hkv) * pre[S];
+  const int64_t W = min(static_cast<int64_t>(gridDim.x) * NW, T);  // no warp gets an empty range
+  const int64_t w = static_cast<int64_t>(blockIdx.x) * NW + warp;
+  WarpRing<D, NST, 1> ring{smem_u32(smem + static_cast<size_t>(warp) * NST * Geom::kStageBytes),
+                           bars + 8 * NST * warp};
+  ring.init(lane);
+  if (w >= W) return;
+  const int64_t x0 = w * T / W, x1 = (w + 1) * T / W;
+  const int count = static_cast<int>(x1 - x0);
+  float2* my_scale = stage_scale + warp * NST;
+
+  // Locate tile x0: the last sequence s with Hkv * pre[s] <= x0 has tiles.
+  int lo = 0, hi = S - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (static_cast<int64_t>(Hkv) * pre[mid] <= x0) lo = mid; else hi = mid - 1;
+  }
+  Cursor start;
+  start.s = lo;
+  start.n = pre[lo + 1] - pre[lo];
+  {
+    const int off = static_cast<int>(x0 - static_cast<int64_t>(Hkv) * pre[lo]);
+    start.g = off / start.n;
+    start.t = off % start.n;
+  }
+
+  // ---- issue side
+  struct Chunk {
+    int s, g, base;
+  };
+  auto chunk_after = [&](const Chunk& c) -> Chunk {
+    if (c.s >= S) return c;  // past the last pair: nothing follows
+    const int n = pre[c.s + 1] - pre[c.s];
+    if (c.base + 32 < n) return Chunk{c.s, c.g, c.base + 32};
+    Cursor q{c.s, c.g, 0, n};
+    next_pair(q, pre, S, Hkv);
+    return Chunk{q.s, q.g, 0};
+  };
+  auto entry_of = [&](const Chunk& c) -> int {
+    if (c.s >= S) return 0;
+    const int t = c.base + lane;
+    return t < pre[c.s + 1] - pre[c.s] ? __ldg(a.block_tables + static_cast<int64_t>(c.s) * a.max_blocks_per_seq + t)
+                                       : 0;
+  };
+  // Scales of (entry, g); 1 for an entry outside the pool (its tile is masked).
+  auto scale_of = [&](const float* sc, int phys, int g) {
+    return static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks)
+               ? __ldg(sc + static_cast<int64_t>(phys) * a.scale_stride + g)
+               : 1.f;
+  };
+  Cursor ic = start;
+  Chunk cur{ic.s, ic.g, ic.t};
+  Chunk nxt = chunk_after(cur);
+  Chunk nxt2 = chunk_after(nxt);
+  int phys_cur = entry_of(cur), phys_nxt = entry_of(nxt), phys_nxt2 = entry_of(nxt2);
+  float ks_cur = scale_of(a.k_scale, phys_cur, cur.g), vs_cur = scale_of(a.v_scale, phys_cur, cur.g);
+  float ks_nxt = scale_of(a.k_scale, phys_nxt, nxt.g), vs_nxt = scale_of(a.v_scale, phys_nxt, nxt.g);
+  uint32_t bad_stage = 0;
+
+  auto issue = [&](int j) {  // tile j of this warp's range, at cursor ic; all lanes call
+    if (ic.s != cur.s || ic.g != cur.g || ic.t >= cur.base + 32) {
+      cur = nxt;
+      phys_cur = phys_nxt;
+      ks_cur = ks_nxt;
+      vs_cur = vs_nxt;
+      nxt = nxt2;
+      phys_nxt = phys_nxt2;
+      ks_nxt = scale_of(a.k_scale, phys_nxt, nxt.g);
+      vs_nxt = scale_of(a.v_scale, phys_nxt, nxt.g);
+      nxt2 = chunk_after(nxt);
+      phys_nxt2 = entry_of(nxt2);
+    }
+    const int st = j % NST;
+    const int idx = ic.t - cur.base;
+    int phys = __shfl_sync(kFull, phys_cur, idx);
+    const float ksc = __shfl_sync(kFull, ks_cur, idx), vsc = __shfl_sync(kFull, vs_cur, idx);
+    if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
+      if (lane == 0) flag(a.dev_status, 4u);  // PKV_DEV_ERR_BLOCK
+      phys = 0;
+      bad_stage |= 1u << st;
+    } else {
+      bad_stage &= ~(1u << st);
+    }
+    if (lane == 0) my_scale[st] = make_float2(ksc, vsc);
+    ring.issue(j, phys, -1, 0, ic.g, &tmap_k, &tmap_v, lane);
+    advance(ic, pre, S, Hkv);
+  };
+
+  for (int j = 0; j < min(count, NST); ++j) issue(j);
+  __syncwarp();  // the stage scales written by lane 0 before any lane reads them
+
+  // ---- compute side
+  Cursor cc = start;
+  Att at;
+  int seg_t0 = cc.t, seg_idx = 0;
+  int vexp = -126;  // the accumulator holds (sum of P V) * 2^-vexp
+  float inv_unit = exp2i(126);
+  at.reset();
+  float sl2q = a.scale_log2 *
+               at.template load_q<QBF16>(a.q + (static_cast<int64_t>(cc.s) * a.num_q_heads + cc.g * G) * D, G, lane);
+  for (int i = 0; i < count;) {
+    if (i > 0 && cc.t == 0) {  // a new (s, g) pair starts here
+      seg_t0 = 0;
+      at.reset();
+      vexp = -126;
+      inv_unit = exp2i(126);
+      sl2q = a.scale_log2 *
+             at.template load_q<QBF16>(a.q + (static_cast<int64_t>(cc.s) * a.num_q_heads + cc.g * G) * D, G, lane);
+    }
+    const bool two = i + 1 < count && cc.t + 1 < cc.n;
+    const bool ok = ring.wait(i, a.timeout_ns) && (!two || ring.wait(i + 1, a.timeout_ns));
+    if (!__all_sync(kFull, ok)) {
+      ring.drain(i, min(count, i + NST), a.timeout_ns);
+      if (lane == 0) flag(a.dev_status, 16u);  // PKV_DEV_ERR_TIMEOUT; the output is undefined
+      return;
+    }
+    uint32_t sK[2];
+    int nv[2];
+    float sl2k[2], vsc[2], pv[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int j = two ? i + u : i;  // a missing second tile reuses the first one's stage, no valid token
+      const int st = j % NST;
+      const float2 sc = my_scale[st];
+      nv[u] = (u == 1 && !two) || ((bad_stage >> st) & 1) ? 0
+                                                          : min(kBlockSize, len[cc.s] - (cc.t + u) * kBlockSize);
+      sK[u] = ring.k_tile(j);
+      sl2k[u] = sl2q * sc.x;
+      vsc[u] = (u == 1 && !two) ? 0.f : sc.y;
+    }
+    {
+      const float vmax = fmaxf(vsc[0], vsc[1]);
+      const int e = min(max(static_cast<int>((__float_as_uint(vmax) >> 23) & 0xff) - 127, -126), 126);
+      if (e > vexp) {
+        at.scale_acc(unit_change(vexp, e));
+        vexp = e;
+        inv_unit = exp2i(-e);
+      }
+    }
+    pv[0] = vsc[0] * inv_unit;
+    pv[1] = vsc[1] * inv_unit;
+    at.template tiles<2>(sK, nv, sl2k, pv, lane);
+    __syncwarp();
+    const int used = two ? 2 : 1;
+    for (int k = 0; k < used; ++k)
+      if (i + k + NST < count) issue(i + k + NST);
+    if (two) advance(cc, pre, S, Hkv);  // to the second tile (same pair)
+    if (cc.t == cc.n - 1 || i + used == count) {  // end of a segment
+      at.scale_acc(exp2i(vexp));
+      at.finish_sums();
+      const bool whole = seg_t0 == 0 && cc.t == cc.n - 1;
+      const int64_t head0 = static_cast<int64_t>(cc.s) * a.num_q_heads + cc.g * G;
+      const int slot = seg_idx == 0 ? 0 : 1;
+      if (whole)
+        at.store_final(a.out, head0, G, a.out_dtype, lane);
+      else
+        at.store_partial(a.ws_acc, a.ws_ml, (w * 2 + slot) * G, 1, G, lane);
+      if (seg_t0 == 0 && lane == 0) {  // this warp holds the pair's first tile
+        int pieces = 0;
+        if (!whole) {
+          const int64_t pair_end = static_cast<int64_t>(Hkv) * pre[cc.s] + static_cast<int64_t>(cc.g + 1) * cc.n;
+          pieces = static_cast<int>((pair_end * W - 1) / T - w + 1);
+        }
+        a.ws_meta[static_cast<int64_t>(cc.s) * Hkv + cc.g] = make_int2(static_cast<int>(w), pieces * 2 + slot);
+      }
+      ++seg_idx;
+    }
+    advance(cc, pre, S, Hkv);
+    i += used;
+  }
+}
+
+constexpr int kFp8BalancedWarps = 12;  // 12 x 4 stages x 4 KB = 192 KB of tiles; 170 registers a thread
+
+size_t balanced_fp8_smem(int num_seqs) {
+  using Geom = TileGeom<128, 1>;
+  return static_cast<size_t>(kFp8BalancedWarps) * kFp8Stages * (Geom::kStageBytes + 16) +
+         (2 * static_cast<size_t>(num_seqs) + 1 + 32) * sizeof(int);
+}
+
 template <int D, bool QBF16, bool FUSED>
 cudaError_t launch_fp8_t(const DecodeArgs& a_in, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
   using Geom = TileGeom<D, 1>;
@@ -546,7 +780,28 @@ cudaError_t launch_fp8_t(const DecodeArgs& a_in, const CUtensorMap& tk, const CU
   return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(64), smem, stream, a, tk, tv);
 }
 
+template <int D, bool QBF16>
+cudaError_t launch_balanced_fp8_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                                  cudaStream_t stream) {
+  auto kern = decode_balanced_fp8_kernel<D, QBF16, kFp8BalancedWarps, kFp8Stages>;
+  const size_t smem = balanced_fp8_smem(a.num_seqs);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(a.balanced_ctas)), dim3(kFp8BalancedWarps * 32), smem, stream,
+                    a, tk, tv);
+}
+
 }  // namespace
+
+cudaError_t launch_decode_balanced_fp8(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                       int head_dim, int q_bf16, cudaStream_t stream) {
+  if (head_dim != 128 || a.k_new) return cudaErrorInvalidValue;
+  if (a.balanced_ctas <= 0) return cudaSuccess;
+  return q_bf16 ? launch_balanced_fp8_t<128, true>(a, tmap_k, tmap_v, stream)
+                : launch_balanced_fp8_t<128, false>(a, tmap_k, tmap_v, stream);
+}
+
+int balanced_fp8_warps_per_cta() { return kFp8BalancedWarps; }
 
 cudaError_t launch_decode_partitions_fp8(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                          int head_dim, int q_bf16, cudaStream_t stream) {

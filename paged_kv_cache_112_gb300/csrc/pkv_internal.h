@@ -188,6 +188,11 @@ cudaError_t launch_bounded_wait_check(int32_t* status, long long timeout_ns, cud
 cudaError_t launch_decode_partitions_fp8(const DecodeArgs& a, const CUtensorMap& tmap_k,
                                          const CUtensorMap& tmap_v, int head_dim, int q_bf16,
                                          cudaStream_t stream);
+// PKV_PARTITION_BALANCED over FP8 pools (head_dim 128, no fused write): one
+// CTA of balanced_fp8_warps_per_cta() warps per SM (a.balanced_ctas CTAs).
+cudaError_t launch_decode_balanced_fp8(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                       int head_dim, int q_bf16, cudaStream_t stream);
+int balanced_fp8_warps_per_cta();
 cudaError_t launch_write_cache_fp8(const WriteCacheFp8Args& a, cudaStream_t stream);
 cudaError_t launch_swap_blocks(const SwapBlocksArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_balanced(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,

@@ -134,13 +134,18 @@ def test_fp8_argument_validation(lib):
                                             None, None)
 
     assert d(D=64) == pkv.PKV_ERR_UNSUPPORTED  # FP8 tiles: head_dim 128 only
-    assert d(ps=pkv.PARTITION_BALANCED) == pkv.PKV_ERR_UNSUPPORTED
+    # balanced split: needs its workspace (no device here: the SM-count query fails first)
+    assert d(ps=pkv.PARTITION_BALANCED) in (pkv.PKV_ERR_WORKSPACE, pkv.PKV_ERR_CUDA)
     assert d(B=8) == pkv.PKV_ERR_UNSUPPORTED
     assert d(ks=None) == pkv.PKV_ERR_INVALID_ARG
     assert d(vs=FAKE + 2) == pkv.PKV_ERR_INVALID_ARG
     assert d(q=FAKE + 8) == pkv.PKV_ERR_INVALID_ARG  # q rows are read as 16-byte vectors
     assert d(qd=pkv.PKV_F32) == pkv.PKV_ERR_INVALID_ARG
     assert d(ps=16, maxlen=64) == pkv.PKV_ERR_WORKSPACE
+    # the fused FP8 step needs fixed partitions (the balanced split has no fused write)
+    assert lib.pkv_decode_step_fp8(FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 2, 8, 2,
+                                   128, 16, 10, 1, 0.1, pkv.PARTITION_BALANCED, 64, None, 0, pkv.PKV_BF16,
+                                   pkv.PKV_F32, None, None) == pkv.PKV_ERR_UNSUPPORTED
     assert d(L=0) == pkv.PKV_ERR_INVALID_ARG  # layers per block: 1..4096
     assert d(L=4097) == pkv.PKV_ERR_INVALID_ARG
     assert d(S=0) == pkv.PKV_OK
