@@ -557,7 +557,13 @@ def measure_workload(args, cfg, ctx, want_cpu_baseline):
     value = job_gbs(nb["step"], world, K, elapsed_ms)
     kern_avg_ms = statistics.mean(kern_ms)
     if fp8:
-        kernel_name = "decode_partitions_fp8_kernel"
+        # the library's rule: write-then-attend over fixed partitions with H_kv % 4 == 0 and at most one
+        # wave of the partition kernel's warp slots (6 two-warp CTAs per SM) runs the head-group grid
+        slots = 12 * torch.cuda.get_device_properties(dev).multi_processor_count
+        hg = (not args.fused and ps != pkv.PARTITION_BALANCED and wl.num_kv_heads % 4 == 0
+              and wl.num_kv_heads * wl.num_seqs <= slots)
+        kernel_name = ("decode_balanced_fp8_kernel" if ps == pkv.PARTITION_BALANCED else
+                       "decode_partitions_fp8_hg_kernel" if hg else "decode_partitions_fp8_kernel")
     else:
         kernel_name = "decode_balanced_kernel" if ps == pkv.PARTITION_BALANCED else "decode_partitions_kernel"
     traffic = _recorded_traffic(cfg, kernel_name)
@@ -1062,7 +1068,8 @@ def _recorded_traffic(cfg, kernel):
     summary, if it was taken on the current kernel sources; else None."""
 
     sources = {"decode_partitions_kernel": ("decode_partitions", "pkv_decode.cu"),
-               "decode_partitions_fp8_kernel": ("decode_partitions_fp8", "pkv_decode_fp8.cu")}
+               "decode_partitions_fp8_kernel": ("decode_partitions_fp8", "pkv_decode_fp8.cu"),
+               "decode_partitions_fp8_hg_kernel": ("decode_partitions_fp8", "pkv_decode_fp8.cu")}
     if kernel not in sources:
         return None
     stem, src = sources[kernel]

@@ -370,9 +370,10 @@ pkv_status pkv_copy_blocks_fp8(void* k_pool, void* v_pool, float* k_scale, float
  * v_t likewise, the rest as pkv_decode_attention (same workspace size from
  * pkv_decode_workspace_bytes, same split-K partials and reduce kernel).
  * q has q_dtype (PKV_F16 or PKV_BF16) and must be 16-byte aligned.
- * Supported: head_dim 128, fixed partitions (partition_size >= 0; the
- * balanced split returns PKV_ERR_UNSUPPORTED).  Rows of tokens >= L in a
- * sequence's last block, NaN codes included, are never used.
+ * Supported: head_dim 128; fixed partitions (partition_size >= 0) or
+ * PKV_PARTITION_BALANCED (the same equal tile shares per warp as for 16-bit
+ * pools, num_seqs <= 4096).  Rows of tokens >= L in a sequence's last
+ * block, NaN codes included, are never used.
  */
 pkv_status pkv_decode_attention_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
                                     const float* k_scale, const float* v_scale,
@@ -409,7 +410,9 @@ pkv_status pkv_decode_partitions_fp8(void* out, const void* q, const void* k_poo
  * is not written.  k_new, v_new have q_dtype, [num_seqs][num_kv_heads][128],
  * rows 16-byte aligned, new_row_stride as in pkv_decode_step.
  * pkv_decode_step_partitions_fp8 is its first kernel alone (follow it with
- * pkv_decode_reduce).
+ * pkv_decode_reduce).  Fixed partitions only: PKV_PARTITION_BALANCED returns
+ * PKV_ERR_UNSUPPORTED (write with pkv_write_cache_fp8 and attend with
+ * pkv_decode_attention_fp8 instead).
  */
 pkv_status pkv_decode_step_fp8(void* out, const void* q, const void* k_new, const void* v_new,
                                int64_t new_row_stride, void* k_pool, void* v_pool, const float* k_scale,

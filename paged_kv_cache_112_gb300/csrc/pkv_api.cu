@@ -192,7 +192,7 @@ bool bind_context_if_none() {
 // A block stride above one block's rows is a layer slice of a pool that
 // keeps all layers of a block together.
 bool encode_pool_map_uncached(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int num_kv_heads,
-                              int head_dim, int eb, int64_t block_stride) {
+                              int head_dim, int eb, int64_t block_stride, int heads_per_box) {
   auto fn = encode_fn();
   if (!fn) {
     t_last_cuda_error = static_cast<int>(cudaErrorSymbolNotFound);
@@ -209,7 +209,8 @@ bool encode_pool_map_uncached(CUtensorMap* map, const void* pool, int num_blocks
   const cuuint64_t strides[3] = {whole_head ? row_bytes : 128, whole_head ? 128 : row_bytes,
                                  static_cast<cuuint64_t>(block_stride) * eb};
   const cuuint32_t box[4] = {line, whole_head ? static_cast<cuuint32_t>(kTile) : 1u,
-                             whole_head ? static_cast<cuuint32_t>(head_dim * eb / 128) : static_cast<cuuint32_t>(block_size),
+                             whole_head ? static_cast<cuuint32_t>(head_dim * eb / 128 * heads_per_box)
+                                        : static_cast<cuuint32_t>(block_size),
                              1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = fn(map, eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
@@ -223,11 +224,13 @@ bool encode_pool_map_uncached(CUtensorMap* map, const void* pool, int num_blocks
 
 // Descriptors depend only on the pool address and geometry, so recent ones
 // are kept (a small round-robin cache) instead of re-encoded every call.
+// heads_per_box > 1 (blocks of >= 16 tokens): one box holds that many
+// adjacent KV heads' tiles of a block, one after the other.
 bool encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int num_kv_heads,
-                     int head_dim, int eb, int64_t block_stride) {
+                     int head_dim, int eb, int64_t block_stride, int heads_per_box = 1) {
   struct Entry {
     const void* pool;
-    int num_blocks, block_size, num_kv_heads, head_dim, eb;
+    int num_blocks, block_size, num_kv_heads, head_dim, eb, heads_per_box;
     int64_t block_stride;
     CUtensorMap map;
   };
@@ -238,15 +241,17 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int blo
     std::lock_guard<std::mutex> lock(mu);
     for (const Entry& e : cache)
       if (e.pool == pool && e.num_blocks == num_blocks && e.block_size == block_size &&
-          e.num_kv_heads == num_kv_heads && e.head_dim == head_dim && e.eb == eb && e.block_stride == block_stride) {
+          e.num_kv_heads == num_kv_heads && e.head_dim == head_dim && e.eb == eb && e.block_stride == block_stride &&
+          e.heads_per_box == heads_per_box) {
         *map = e.map;
         return true;
       }
   }
-  if (!encode_pool_map_uncached(map, pool, num_blocks, block_size, num_kv_heads, head_dim, eb, block_stride))
+  if (!encode_pool_map_uncached(map, pool, num_blocks, block_size, num_kv_heads, head_dim, eb, block_stride,
+                                heads_per_box))
     return false;
   std::lock_guard<std::mutex> lock(mu);
-  cache[next] = Entry{pool, num_blocks, block_size, num_kv_heads, head_dim, eb, block_stride, *map};
+  cache[next] = Entry{pool, num_blocks, block_size, num_kv_heads, head_dim, eb, heads_per_box, block_stride, *map};
   next = (next + 1) % 64;
   return true;
 }
@@ -667,7 +672,8 @@ pkv_status prepare_decode_fp8(DecodeCall* c, void* out, const void* q, const voi
                               int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads,
                               int num_kv_heads, int head_dim, int block_size, int num_blocks, int num_layers,
                               float scale, int partition_size, int max_context_len, void* workspace,
-                              size_t workspace_bytes, pkv_dtype q_dtype, pkv_dtype out_dtype, int32_t* dev_status) {
+                              size_t workspace_bytes, pkv_dtype q_dtype, pkv_dtype out_dtype, int32_t* dev_status,
+                              bool fused) {
   if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
   if (num_layers <= 0 || num_layers > kMaxLayers || num_kv_heads <= 0 || head_dim <= 0)
     return PKV_ERR_INVALID_ARG;
@@ -685,8 +691,13 @@ pkv_status prepare_decode_fp8(DecodeCall* c, void* out, const void* q, const voi
   c->args.k_scale = k_scale;
   c->args.v_scale = v_scale;
   c->args.scale_stride = static_cast<int64_t>(num_layers) * num_kv_heads;
-  if (!encode_pool_map(&c->tmap_k, k_pool, num_blocks, kBlockSize, num_kv_heads, head_dim, 1, c->args.block_stride) ||
-      !encode_pool_map(&c->tmap_v, v_pool, num_blocks, kBlockSize, num_kv_heads, head_dim, 1, c->args.block_stride))
+  // The launch picks its kernel by the same rule, so the boxes match it.
+  const int hpb = fp8_heads_per_box(num_kv_heads, num_seqs, fused, partition_size == PKV_PARTITION_BALANCED);
+  c->args.heads_per_box = hpb;
+  if (!encode_pool_map(&c->tmap_k, k_pool, num_blocks, kBlockSize, num_kv_heads, head_dim, 1, c->args.block_stride,
+                       hpb) ||
+      !encode_pool_map(&c->tmap_v, v_pool, num_blocks, kBlockSize, num_kv_heads, head_dim, 1, c->args.block_stride,
+                       hpb))
     return PKV_ERR_CUDA;
   return PKV_OK;
 }
@@ -708,7 +719,7 @@ pkv_status pkv_decode_partitions_fp8(void* out, const void* q, const void* k_poo
                                            max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
                                            head_dim, block_size, num_blocks, num_layers, scale, partition_size,
                                            max_context_len, workspace, workspace_bytes, q_dtype, out_dtype,
-                                           dev_status);
+                                           dev_status, false);
   if (st != PKV_OK || num_seqs == 0) return st;
   if (c.args.balanced_ctas)
     return cuda_status(launch_decode_balanced_fp8(c.args, c.tmap_k, c.tmap_v, head_dim, q_dtype == PKV_BF16,
@@ -731,7 +742,7 @@ pkv_status pkv_decode_step_partitions_fp8(void* out, const void* q, const void* 
                                            max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
                                            head_dim, block_size, num_blocks, num_layers, scale, partition_size,
                                            max_context_len, workspace, workspace_bytes, q_dtype, out_dtype,
-                                           dev_status);
+                                           dev_status, true);
   if (st != PKV_OK || num_seqs == 0) return st;
   const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
   const int64_t stride = new_row_stride ? new_row_stride : row;

@@ -123,11 +123,11 @@ struct WarpAttentionFp8 : SoftmaxState<D / 16> {
   }
 
   // NT tiles at once (independent chains interleave; one softmax update for
-  // all of them).  Tile t: K at sK[t], V at sK[t] + 2048, nv[t] valid
+  // all of them).  Tile t: K at sK[t], V at sK[t] + VOFF, nv[t] valid
   // tokens (rows >= nv are masked, whatever they hold), sl2k[t] = log2(e) *
   // softmax scale * q prescale * K scale, pv[t] = V scale in the
   // accumulator's unit (a power of two chosen per chunk of tiles).
-  template <int NT>
+  template <int NT, int VOFF = 2048>
   __device__ __forceinline__ void tiles(const uint32_t (&sK)[NT], const int (&nv)[NT], const float (&sl2k)[NT],
                                         const float (&pv)[NT], int lane) {
     const int gr = lane >> 2, tq = lane & 3;
@@ -167,7 +167,7 @@ struct WarpAttentionFp8 : SoftmaxState<D / 16> {
 #pragma unroll
     for (int t = 0; t < NT; ++t)
 #pragma unroll
-      for (int r = 0; r < 4; ++r) lds128(vw[t][r], sK[t] + 2048 + voff[r]);
+      for (int r = 0; r < 4; ++r) lds128(vw[t][r], sK[t] + VOFF + voff[r]);
 
     float sc[4 * NT], p[4 * NT];
 #pragma unroll
@@ -533,6 +533,174 @@ __global__ void __launch_bounds__(64, 6) decode_partitions_fp8_kernel(
   }
 }
 
+// ------------------------------------------------------ head-group partitions
+//
+// Fixed partitions, HP KV heads per CTA: one CTA serves (sequence s,
+// partition p) for KV heads [gi * HP, gi * HP + HP), one warp per head.  A
+// block's codes for HP adjacent heads are adjacent 128-byte lines of each
+// row, so one TMA box of (128 bytes, 16 rows, HP lines) brings the K tiles
+// of all HP heads at once, and another their V tiles: two copies per block
+// for the CTA instead of two per head.  An FP8 tile is only 2 KB, and one
+// copy per 2 KB, issued per warp, is about as many copies as an SM's TMA
+// unit accepts at full HBM rate; this way the copies carry HP * 2 KB.
+//  * The HP warps share one ring of NST stages ([K: HP heads][V: HP heads]),
+//    filled by lane 0 of warp 0.  Every warp waits on a stage's barrier,
+//    reads its own head's K and V tile and keeps its own softmax state and
+//    scales; after each step __syncthreads_or() both frees the step's
+//    stages for the next copies and makes a timed-out wait a decision of the
+//    whole CTA.
+//  * Work per warp, tile math and outputs are the one-warp-per-unit
+//    partition kernel's (fused write excluded: the head-group grid serves
+//    write-then-attend calls).
+template <int D, bool QBF16, int HP, int NST>
+__global__ void __launch_bounds__(HP * 32, 12 / HP) decode_partitions_fp8_hg_kernel(
+    const DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v) {
+  using Att = WarpAttentionFp8<D>;
+  static_assert(D == 128 && NST % 2 == 0, "FP8 tiles are one 128-byte line per head row; tile pairs");
+  constexpr uint32_t kHeadTile = kBlockSize * 128;  // one head's 16 rows of codes
+  constexpr uint32_t kKBytes = HP * kHeadTile;      // the group's K tiles of one block
+  constexpr uint32_t kStage = 2 * kKBytes;          // then its V tiles
+  extern __shared__ __align__(1024) uint8_t smem[];
+  griddep_wait();  // every input may come from the previous kernel on the stream
+  griddep_launch_dependents();
+  if (smem_misaligned(smem, a.dev_status)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int groups = a.num_kv_heads / HP;
+  const int64_t unit = blockIdx.x;  // partition-major: ((p * S) + s) * groups + gi
+  const int gi = static_cast<int>(unit % groups);
+  const int64_t rest = unit / groups;
+  const int s = static_cast<int>(rest % a.num_seqs);
+  const int part = static_cast<int>(rest / a.num_seqs);
+  const int g = gi * HP + warp;
+  const int PS = a.partition_size, G = a.group;
+  const int tiles_per_part = PS / kBlockSize;
+  const int32_t* tbl = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq;
+  const int first = lane < tiles_per_part && part * tiles_per_part + lane < a.max_blocks_per_seq
+                        ? __ldg(tbl + part * tiles_per_part + lane)
+                        : 0;
+  const int L = clamp_len(a, a.context_lens[s], part == 0 && gi == 0 && warp == 0 && lane == 0);
+  const int nparts = L > 0 ? (L + PS - 1) / PS : 1;
+  if (part >= nparts) return;  // the same for every warp of the CTA
+  const int tok0 = part * PS;
+  const int ntok = max(0, min(L - tok0, PS));
+  const int cnt = (ntok + kBlockSize - 1) / kBlockSize;
+  tbl += tok0 / kBlockSize;
+  auto entry = [&](int i) { return i < cnt ? __ldg(tbl + i) : 0; };
+  auto ks_of = [&](int phys) {
+    return static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks)
+               ? __ldg(a.k_scale + static_cast<int64_t>(phys) * a.scale_stride + g)
+               : 1.f;
+  };
+  auto vs_of = [&](int phys) {
+    return static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks)
+               ? __ldg(a.v_scale + static_cast<int64_t>(phys) * a.scale_stride + g)
+               : 1.f;
+  };
+
+  const uint32_t ring = smem_u32(smem);
+  const uint32_t bars = ring + NST * kStage;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < NST; ++st) mbar_init(bars + 8 * st, 1);
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+
+  // Entries and this head's scales, 32 tiles a chunk (as the partition kernel).
+  int phys_cur = first;
+  int phys_next = entry(32 + lane);
+  float ks_cur = lane < cnt ? ks_of(first) : 0.f, vs_cur = lane < cnt ? vs_of(first) : 0.f;
+  float ks_prev = 0.f, vs_prev = 0.f;
+  int chunk_cur = 0;
+  int vexp = -126, vexp_chunk = -1;
+  float inv_unit = exp2i(126);
+  uint32_t bad_stage = 0;
+
+  auto issue = [&](int j) {  // every lane of every warp calls; lane 0 of warp 0 copies
+    if ((j & 31) == 0 && j > 0) {
+      phys_cur = phys_next;
+      phys_next = entry(j + 32 + lane);
+      ks_prev = ks_cur;
+      vs_prev = vs_cur;
+      const bool mine = j + lane < cnt;
+      ks_cur = mine ? ks_of(phys_cur) : 0.f;
+      vs_cur = mine ? vs_of(phys_cur) : 0.f;
+      chunk_cur = j >> 5;
+    }
+    const int st = j % NST;
+    int phys = __shfl_sync(kFull, phys_cur, j & 31);
+    if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
+      if (warp == 0 && lane == 0) flag(a.dev_status, 4u);  // PKV_DEV_ERR_BLOCK
+      phys = 0;
+      bad_stage |= 1u << st;
+    } else {
+      bad_stage &= ~(1u << st);
+    }
+    if (warp == 0 && lane == 0) {
+      const uint32_t bar = bars + 8 * st;
+      const uint32_t dst = ring + st * kStage;
+      mbar_arrive_expect_tx(bar, kStage);
+      tma_load_4d(dst, &tmap_k, 0, 0, gi * HP, phys, bar);
+      tma_load_4d(dst + kKBytes, &tmap_v, 0, 0, gi * HP, phys, bar);
+    }
+  };
+  auto wait = [&](int j) { return mbar_wait_bounded(bars + 8 * (j % NST), (j / NST) & 1, a.timeout_ns); };
+
+  Att at;
+  at.reset();
+  for (int j = 0; j < min(cnt, NST); ++j) issue(j);
+  const float sl2q =
+      a.scale_log2 * at.template load_q<QBF16>(a.q + (static_cast<int64_t>(s) * a.num_q_heads + g * G) * D, G, lane);
+
+  for (int i = 0; i < cnt; i += 2) {
+    const bool two = i + 1 < cnt;
+    const bool ok = __all_sync(kFull, wait(i) && (!two || wait(i + 1)));
+    if (ok) {
+      if ((i >> 5) != vexp_chunk) {  // first pair of a chunk (its scales arrived NST tiles ago)
+        vexp_chunk = i >> 5;
+        const int e = chunk_exponent(vs_cur);
+        if (e > vexp) {
+          at.scale_acc(unit_change(vexp, e));
+          vexp = e;
+          inv_unit = exp2i(-e);
+        }
+      }
+      const bool cur = (i >> 5) == chunk_cur;
+      const float ksel = cur ? ks_cur : ks_prev, vsel = cur ? vs_cur : vs_prev;
+      uint32_t sK[2];
+      int nv[2];
+      float sl2k[2], pv[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int j = two ? i + u : i;  // a missing second tile reuses the first one's stage, no valid token
+        const int st = j % NST;
+        nv[u] = (u == 1 && !two) || ((bad_stage >> st) & 1) ? 0 : min(kBlockSize, ntok - j * kBlockSize);
+        sK[u] = ring + st * kStage + warp * kHeadTile;
+        sl2k[u] = sl2q * __shfl_sync(kFull, ksel, j & 31);
+        pv[u] = inv_unit * __shfl_sync(kFull, vsel, j & 31);
+      }
+      at.template tiles<2, kKBytes>(sK, nv, sl2k, pv, lane);
+    }
+    // Every warp is done with this step's stages; a timed-out wait anywhere ends the CTA.
+    if (__syncthreads_or(!ok)) {
+      if (warp == 0)
+        for (int j = i; j < min(cnt, i + NST); ++j) wait(j);  // copies in flight land before the CTA exits
+      if (warp == 0 && lane == 0) flag(a.dev_status, 16u);  // PKV_DEV_ERR_TIMEOUT; the output is undefined
+      return;
+    }
+    if (i + NST < cnt) issue(i + NST);
+    if (i + 1 + NST < cnt) issue(i + 1 + NST);
+  }
+
+  at.scale_acc(exp2i(vexp));
+  at.finish_sums();
+  const int64_t head0 = static_cast<int64_t>(s) * a.num_q_heads + g * G;
+  if (nparts == 1)
+    at.store_final(a.out, head0, G, a.out_dtype, lane);
+  else
+    at.store_partial(a.ws_acc, a.ws_ml, head0 * a.max_parts + part, a.max_parts, G, lane);
+}
+
 // ------------------------------------------------------------ balanced split
 //
 // PKV_PARTITION_BALANCED over FP8 pools: the work order and equal shares of
@@ -780,6 +948,18 @@ cudaError_t launch_fp8_t(const DecodeArgs& a_in, const CUtensorMap& tk, const CU
   return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(64), smem, stream, a, tk, tv);
 }
 
+template <int D, bool QBF16, int HP>
+cudaError_t launch_fp8_hg_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+  constexpr int NST = kFp8Stages;
+  const size_t smem = static_cast<size_t>(NST) * (2 * HP * kBlockSize * 128 + 8);
+  auto kern = decode_partitions_fp8_hg_kernel<D, QBF16, HP, NST>;
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  const int64_t ctas = static_cast<int64_t>(a.num_kv_heads / HP) * a.num_seqs * a.max_parts;
+  if (ctas == 0) return cudaSuccess;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(HP * 32), smem, stream, a, tk, tv);
+}
+
 template <int D, bool QBF16>
 cudaError_t launch_balanced_fp8_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                   cudaStream_t stream) {
@@ -792,6 +972,15 @@ cudaError_t launch_balanced_fp8_t(const DecodeArgs& a, const CUtensorMap& tk, co
 }
 
 }  // namespace
+
+int fp8_heads_per_box(int num_kv_heads, int num_seqs, bool fused, bool balanced) {
+  if (fused || balanced || num_kv_heads % 4 != 0) return 1;
+  using Geom = TileGeom<128, 1>;
+  const size_t smem = 2 * kFp8Stages * Geom::kStageBytes + 2 * kFp8Stages * 8;
+  const int slots = resident_warp_slots(
+      reinterpret_cast<const void*>(decode_partitions_fp8_kernel<128, false, kFp8Stages, false>), 64, smem);
+  return static_cast<int64_t>(num_kv_heads) * num_seqs > slots ? 1 : 4;
+}
 
 cudaError_t launch_decode_balanced_fp8(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                        int head_dim, int q_bf16, cudaStream_t stream) {
@@ -806,6 +995,9 @@ int balanced_fp8_warps_per_cta() { return kFp8BalancedWarps; }
 cudaError_t launch_decode_partitions_fp8(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                          int head_dim, int q_bf16, cudaStream_t stream) {
   if (head_dim != 128) return cudaErrorInvalidValue;
+  if (a.heads_per_box == 4)
+    return q_bf16 ? launch_fp8_hg_t<128, true, 4>(a, tmap_k, tmap_v, stream)
+                  : launch_fp8_hg_t<128, false, 4>(a, tmap_k, tmap_v, stream);
   if (a.k_new)
     return q_bf16 ? launch_fp8_t<128, true, true>(a, tmap_k, tmap_v, stream)
                   : launch_fp8_t<128, false, true>(a, tmap_k, tmap_v, stream);

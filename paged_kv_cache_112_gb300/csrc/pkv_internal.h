@@ -109,6 +109,7 @@ struct DecodeArgs {
   int out_dtype;       // pkv_dtype
   int balanced_ctas;   // balanced split: persistent CTAs (one per SM); 0 otherwise
   int unit_warps;      // fixed partitions: warps per unit (1 or 2)
+  int heads_per_box;   // FP8 pools: KV heads per TMA box, 4 for the head-group kernel, else 1
   long long timeout_ns;
   // Fused decode step only: the token generated this step, written to the
   // pools by the attention kernel itself (null when not fusing).
@@ -188,6 +189,15 @@ cudaError_t launch_bounded_wait_check(int32_t* status, long long timeout_ns, cud
 cudaError_t launch_decode_partitions_fp8(const DecodeArgs& a, const CUtensorMap& tmap_k,
                                          const CUtensorMap& tmap_v, int head_dim, int q_bf16,
                                          cudaStream_t stream);
+// KV heads per TMA box of the FP8 decode kernels (DecodeArgs::heads_per_box):
+// 4, the head-group partition kernel (four heads' tiles of a block per
+// copy), for write-then-attend calls with fixed partitions, a head count
+// divisible by 4, and sequences x KV heads within one wave of the partition
+// kernel's warp slots (where that kernel would give a unit one warp); else
+// 1 (one head's tile per copy: the partition kernel, the fused step, the
+// balanced split).
+int fp8_heads_per_box(int num_kv_heads, int num_seqs, bool fused, bool balanced);
+
 // PKV_PARTITION_BALANCED over FP8 pools (head_dim 128, no fused write): one
 // CTA of balanced_fp8_warps_per_cta() warps per SM (a.balanced_ctas CTAs).
 cudaError_t launch_decode_balanced_fp8(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
