@@ -32,7 +32,7 @@
  *         num_kv_heads * head_dim.
  *     Any other block_stride >= the dense one and a multiple of 8 elements
  *     works too.  Pool pointers are 16-byte aligned.
- *   - block_size is 8, 16, 32 or 64 tokens; 16 is the common default [P1
+ *   - block_size is 8, 16, 32 or 64 tokens; 16 is the usual choice [P1
  *     "Fixed-size blocks"; P2 section 02].  FP8 pools and the balanced
  *     split take 16 only.
  *   - Elements are IEEE binary16 (PKV_F16) or bfloat16 (PKV_BF16).  Queries

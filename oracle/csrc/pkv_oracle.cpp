@@ -7,9 +7,10 @@
 //
 // What it follows (four web pages on paged KV caches):
 //  * "PagedAttention internals" (manishklach), section 02 "Block tables":
-//    token t of a sequence lives in logical block t/16 at offset t%16; the
-//    physical block is block_table[t/16].  Each KV head serves its group of
-//    query heads.
+//    a sequence's position t is found by integer division by the block
+//    size (16): quotient = index into the sequence's table, whose entry is
+//    the physical block; remainder = row inside that block.  A group of
+//    consecutive query heads reads one KV head.
 //  * "gpu_paged_kv_cache" (aicassindra), sections "Fixed-size blocks and the
 //    block-table indirection" and "Inside the paged attention kernel": the
 //    attention reads K and V through the table; paging changes where bytes

@@ -1,11 +1,12 @@
 """Closed forms for paged KV-cache sizing -- TEST INFRASTRUCTURE ONLY.
 
 Stated from:
-  * "gpu_paged_kv_cache" (aicassindra), "Sizing the pool": per token and per
-    layer the cache costs 2 x kv_heads x head_dim x bytes; times layers for a
-    token, times block size for a block; the block count is the KV budget
-    divided by bytes per block.  "Fixed-size blocks ...": one 32-bit table
-    entry per block; internal waste is at most B - 1 tokens per sequence.
+  * "gpu_paged_kv_cache" (aicassindra), "Sizing the pool": K and V of one
+    token in one layer take 2 x kv_heads x head_dim x bytes; a token in all
+    layers multiplies that by the layer count, a block by the block size;
+    a memory budget holds budget // (bytes of a block) blocks.  "Fixed-size
+    blocks ...": a table entry is 32 bits per block; a sequence leaves fewer
+    than B tokens of its last block unused.
   * "PagedAttention internals" (manishklach), sections 01-05: the same
     per-token formula; expected internal waste (B - 1) / 2 tokens; table
     entries and gather-loop iterations = ceil(tokens / B).

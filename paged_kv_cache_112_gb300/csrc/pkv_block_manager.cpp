@@ -13,7 +13,7 @@
 //    ("gpu_paged_kv_cache", "Prefix sharing, reference counts, and
 //    copy-on-write"; "PagedAttention internals", section 04).  A hit is
 //    also checked token for token, so a hash collision cannot share a block;
-//  * copy-on-write: appending into a block whose refcount exceeds one
+//  * copy-on-write: an append that lands in a block held more than once
 //    allocates a fresh block, reports the (old, new) pair for the device
 //    copy, drops a reference to the old block and repoints the table;
 //  * eviction: blocks nobody references but whose contents are cached stay

@@ -14,8 +14,8 @@ Sources (four web pages on paged KV caches):
   * "PagedAttention internals" (manishklach), sections 02 "Block tables" and
     03 "Sharing via copy-on-write".
   * "tm_paged_attention" (aicassindra), section "End-to-end flow": a sequence's
-    context length counts the token generated this step; blocks are allocated
-    only when the tail block is full.
+    context length counts the token generated this step; a new block is
+    taken when the last one has no free row left.
   * "KV Cache & PagedAttention" (lattice-ai-eng), section 4 "Minimal
     implementation": free list, refcount, fork by refcount bump.
 
@@ -147,9 +147,9 @@ class SeqState:
 def append_token(pool: BlockPool, seq: SeqState, block_size: int = BLOCK_SIZE):
     """Reserve the slot of one new token.
 
-    Takes a block only when the tail block is full; if the tail block is
-    shared (more than one reference) it is replaced by a fresh block and a
-    copy pair is returned.  Returns (slot, cow_pair_or_None).
+    A new block is taken when the last one has no free row; a last block
+    held more than once is first swapped for a private copy, and its
+    (source, destination) pair is returned.  Returns (slot, cow_pair_or_None).
     """
     pair = None
     if seq.length % block_size == 0:

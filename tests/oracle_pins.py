@@ -61,8 +61,8 @@ def _rand_problem(rng, lens, Hq, Hkv, D, dtype, nb_extra=5, B=B):
 
 def pin_block_sizes(attn, dtype="bf16"):
     """Blocks of 8, 32 and 64 tokens: torch SDPA in fp64 on the contiguous K/V
-    the pool was built from ("gpu_paged_kv_cache", "Fixed-size blocks": the
-    table, not address arithmetic, resolves position, whatever B is)."""
+    the pool was built from ("gpu_paged_kv_cache", "Fixed-size blocks": a
+    position is found through the table for every block size B)."""
     rng = np.random.default_rng(17)
     lens = [1, 7, 8, 9, 33, 64, 65, 130]
     Hq, Hkv, D = 4, 2, 32

@@ -4,8 +4,8 @@ the prefill's bulk write, a fork for parallel sampling, decode steps with
 copy-on-write pairs fed to pkv_copy_blocks and the fused write + attention,
 and a swap out / in through pinned host memory.  A token's K/V rows are a
 function of its whole history, so identical prefixes hold identical bytes
-("PagedAttention internals", section 04: identical tokens produce identical
-KV by construction); every output is checked against the oracle on the
+("PagedAttention internals", section 04: equal token prefixes give equal K
+and V); every output is checked against the oracle on the
 sequence's contiguous history."""
 import zlib
 
