@@ -613,22 +613,28 @@ int pkv_bm_swap_in(pkv_bm* bm, int64_t seq_id, int32_t* blocks, int capacity);
 int pkv_bm_swap_in_cached(pkv_bm* bm, int64_t seq_id, int32_t* blocks, int32_t* from_host,
                           int capacity);
 
-/* Static string naming a status code.  Host function. */
 /*
  * pkv_check_bounded_wait -- exercises the decode kernels' error path for a
- * tile copy that never lands, without any copy in flight.  One warp sets up
- * the partition kernel's shared-memory tile ring and waits on its first
- * stage, which nothing arms, with the same bounded wait (%globaltimer) the
- * decode kernels use, but for timeout_ns instead of their fixed 2 s.  When
- * the wait runs out the warp drains its (zero) outstanding copies, ORs
- * PKV_DEV_ERR_TIMEOUT into *dev_status and returns, leaving the context
- * usable.  A diagnostic: lets a test (or a deployment's health check) see
- * that a stuck copy turns into a status bit rather than a hung kernel.
+ * tile copy that never lands, without any copy in flight, with the bounded
+ * wait (%globaltimer) the decode kernels use but for timeout_ns instead of
+ * their fixed 2 s.  A diagnostic: lets a test (or a deployment's health
+ * check) see that a stuck copy turns into a status bit rather than a hung
+ * kernel, and that the context stays usable.
+ *   shared_ring = 0: one warp sets up the partition kernel's per-warp tile
+ *     ring and waits on its first stage, which nothing arms; when the wait
+ *     runs out it drains its (zero) outstanding copies, ORs
+ *     PKV_DEV_ERR_TIMEOUT into *dev_status and returns.
+ *   shared_ring = 1: four warps share stage barriers, as the warps of the
+ *     FP8 head-group kernel share one ring; three pass a barrier completed by
+ *     a plain arrival, one waits on a barrier nothing completes until its
+ *     limit runs out, and the CTA-wide vote that follows sends all four out
+ *     with PKV_DEV_ERR_TIMEOUT set.
  * timeout_ns in [0, 2e9]; dev_status is required (device int32).  The pages
  * have no counterpart of this call.
  */
-pkv_status pkv_check_bounded_wait(int64_t timeout_ns, int32_t* dev_status, void* stream);
+pkv_status pkv_check_bounded_wait(int64_t timeout_ns, int shared_ring, int32_t* dev_status, void* stream);
 
+/* Static string naming a status code.  Host function. */
 const char* pkv_status_string(pkv_status status);
 
 /*

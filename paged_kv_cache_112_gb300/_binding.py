@@ -56,7 +56,7 @@ _SIGS["pkv_decode_step_fp8"] = ([_c_void_p] * 4 + [_c_int64] + [_c_void_p] * 5 +
                                 [_c_int] * 7 + [_c_float, _c_int, _c_int, _c_void_p, _c_size_t, _c_int, _c_int,
                                                 _c_void_p, _c_void_p])
 _SIGS["pkv_decode_step_partitions_fp8"] = _SIGS["pkv_decode_step_fp8"]
-_SIGS["pkv_check_bounded_wait"] = [_c_int64, _c_void_p, _c_void_p]
+_SIGS["pkv_check_bounded_wait"] = [_c_int64, _c_int, _c_void_p, _c_void_p]
 _SIGS["pkv_last_cuda_error"] = []
 _SIGS["pkv_cuda_error_name"] = [_c_int]
 
@@ -174,13 +174,16 @@ def _pool_stride(k_pool, v_pool) -> int:
     return int(k_pool.stride(0))
 
 
-def check_bounded_wait(timeout_ns: int, status, *, stream=None):
-    """pkv_check_bounded_wait: one warp waits on a tile barrier nothing arms for
-    timeout_ns, then ORs DEV_ERR_TIMEOUT into `status` (a CUDA int32 tensor)."""
+def check_bounded_wait(timeout_ns: int, status, *, shared_ring=False, stream=None):
+    """pkv_check_bounded_wait: a wait on a tile barrier nothing completes runs
+    out after timeout_ns and ORs DEV_ERR_TIMEOUT into `status` (a CUDA int32
+    tensor); shared_ring: in a CTA whose warps share stages and leave by a
+    CTA-wide vote."""
     _need_cuda(status)
     if status is None or status.dtype != torch.int32:
         raise PkvError("status must be a CUDA int32 tensor")
-    _check(load().pkv_check_bounded_wait(int(timeout_ns), _ptr(status), _stream(stream)), "pkv_check_bounded_wait")
+    _check(load().pkv_check_bounded_wait(int(timeout_ns), int(bool(shared_ring)), _ptr(status), _stream(stream)),
+           "pkv_check_bounded_wait")
 
 
 def _kv_dtype(t) -> int:

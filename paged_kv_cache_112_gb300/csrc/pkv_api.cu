@@ -854,10 +854,13 @@ pkv_status pkv_swap_blocks(void* dst_k, void* dst_v, int64_t dst_block_stride, i
   return cuda_status(launch_swap_blocks(a, static_cast<cudaStream_t>(stream)));
 }
 
-pkv_status pkv_check_bounded_wait(int64_t timeout_ns, int32_t* dev_status, void* stream) {
-  if (timeout_ns < 0 || timeout_ns > kWaitTimeoutNs || !dev_status || !aligned(dev_status, 4))
+pkv_status pkv_check_bounded_wait(int64_t timeout_ns, int shared_ring, int32_t* dev_status, void* stream) {
+  if (timeout_ns < 0 || timeout_ns > kWaitTimeoutNs || (shared_ring != 0 && shared_ring != 1) || !dev_status ||
+      !aligned(dev_status, 4))
     return PKV_ERR_INVALID_ARG;
-  return cuda_status(launch_bounded_wait_check(dev_status, timeout_ns, static_cast<cudaStream_t>(stream)));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(shared_ring ? launch_bounded_wait_vote_check(dev_status, timeout_ns, s)
+                                 : launch_bounded_wait_check(dev_status, timeout_ns, s));
 }
 
 const char* pkv_status_string(pkv_status s) {

@@ -184,6 +184,8 @@ cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t
 // One warp waits on a tile barrier that no copy arms, for timeout_ns, and
 // sets PKV_DEV_ERR_TIMEOUT in *status (pkv_check_bounded_wait).
 cudaError_t launch_bounded_wait_check(int32_t* status, long long timeout_ns, cudaStream_t stream);
+// The shared-ring form: four warps, a CTA-wide vote after the wait (pkv_checks.cu).
+cudaError_t launch_bounded_wait_vote_check(int32_t* status, long long timeout_ns, cudaStream_t stream);
 // FP8 pools (pkv_decode_fp8.cu): tensor maps describe the uint8 pools;
 // q_bf16: 0 = f16 queries, 1 = bf16.
 cudaError_t launch_decode_partitions_fp8(const DecodeArgs& a, const CUtensorMap& tmap_k,

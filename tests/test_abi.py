@@ -199,7 +199,8 @@ def test_bounded_wait_check_argument_validation(lib):
     """Rejected before any launch: negative or over-long limits, a missing or
     misaligned status word."""
     fake = 256
-    assert lib.pkv_check_bounded_wait(-1, fake, None) == pkv.PKV_ERR_INVALID_ARG
-    assert lib.pkv_check_bounded_wait(2_000_000_001, fake, None) == pkv.PKV_ERR_INVALID_ARG
-    assert lib.pkv_check_bounded_wait(1000, None, None) == pkv.PKV_ERR_INVALID_ARG
-    assert lib.pkv_check_bounded_wait(1000, fake + 2, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_check_bounded_wait(-1, 0, fake, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_check_bounded_wait(2_000_000_001, 0, fake, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_check_bounded_wait(1000, 0, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_check_bounded_wait(1000, 0, fake + 2, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_check_bounded_wait(1000, 2, fake, None) == pkv.PKV_ERR_INVALID_ARG

@@ -82,17 +82,20 @@ def test_length_beyond_bound_is_clamped_and_flagged(ps):
     assert np.all(np.isfinite(out))
 
 
+@pytest.mark.parametrize("shared_ring", [False, True])
 @pytest.mark.parametrize("limit_ms", [2, 20])
-def test_timed_out_wait_sets_the_status_bit_and_the_context_stays_usable(limit_ms):
+def test_timed_out_wait_sets_the_status_bit_and_the_context_stays_usable(limit_ms, shared_ring):
     """A tile wait that nothing completes ends after its limit with
     PKV_DEV_ERR_TIMEOUT (the decode kernels' bounded wait and drain, run with
-    a short limit and no copy in flight); the same context then runs a normal
-    decode step that matches the oracle."""
+    a short limit and no copy in flight; with shared_ring, one warp of four
+    times out and the CTA-wide vote of the shared-ring kernels sends all four
+    out); the same context then runs a normal decode step that matches the
+    oracle."""
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
     e0.record()
-    pkv.check_bounded_wait(limit_ms * 1_000_000, status)
+    pkv.check_bounded_wait(limit_ms * 1_000_000, status, shared_ring=shared_ring)
     e1.record()
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
@@ -114,4 +117,5 @@ def test_bounded_wait_check_rejects_bad_arguments():
         pkv.check_bounded_wait(-1, status)
     with pytest.raises(pkv.PkvError):
         pkv.check_bounded_wait(3_000_000_000, status)
-    assert pkv.load().pkv_check_bounded_wait(1000, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert pkv.load().pkv_check_bounded_wait(1000, 0, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert pkv.load().pkv_check_bounded_wait(1000, 3, None, None) == pkv.PKV_ERR_INVALID_ARG
