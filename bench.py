@@ -267,7 +267,10 @@ def measure_workload(args, cfg, ctx, want_cpu_baseline):
 
     dist, dev, rank, world, local = ctx["dist"], ctx["dev"], ctx["rank"], ctx["world"], ctx["local"]
     wl = P.make_workload(cfg, poison=False, block_size=args.block_size)
-    ps = wl.partition_size if args.partition_size is None else args.partition_size
+    if args.partition_size is not None:
+        ps = args.partition_size
+    else:
+        ps = P.fp8_partition_size(cfg) if args.kv == "fp8" else wl.partition_size
     dt = {"f16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
 
     # Per-step inputs live in one device staging buffer (16-byte aligned
@@ -557,11 +560,8 @@ def measure_workload(args, cfg, ctx, want_cpu_baseline):
     value = job_gbs(nb["step"], world, K, elapsed_ms)
     kern_avg_ms = statistics.mean(kern_ms)
     if fp8:
-        # the library's rule: write-then-attend over fixed partitions with H_kv % 4 == 0 and at most one
-        # wave of the partition kernel's warp slots (6 two-warp CTAs per SM) runs the head-group grid
-        slots = 12 * torch.cuda.get_device_properties(dev).multi_processor_count
-        hg = (not args.fused and ps != pkv.PARTITION_BALANCED and wl.num_kv_heads % 4 == 0
-              and wl.num_kv_heads * wl.num_seqs <= slots)
+        # the library's rule: write-then-attend over fixed partitions with H_kv % 4 == 0 runs the head-group grid
+        hg = not args.fused and ps != pkv.PARTITION_BALANCED and wl.num_kv_heads % 4 == 0
         kernel_name = ("decode_balanced_fp8_kernel" if ps == pkv.PARTITION_BALANCED else
                        "decode_partitions_fp8_hg_kernel" if hg else "decode_partitions_fp8_kernel")
     else:

@@ -692,7 +692,7 @@ pkv_status prepare_decode_fp8(DecodeCall* c, void* out, const void* q, const voi
   c->args.v_scale = v_scale;
   c->args.scale_stride = static_cast<int64_t>(num_layers) * num_kv_heads;
   // The launch picks its kernel by the same rule, so the boxes match it.
-  const int hpb = fp8_heads_per_box(num_kv_heads, num_seqs, fused, partition_size == PKV_PARTITION_BALANCED);
+  const int hpb = fp8_heads_per_box(num_kv_heads, fused, partition_size == PKV_PARTITION_BALANCED);
   c->args.heads_per_box = hpb;
   if (!encode_pool_map(&c->tmap_k, k_pool, num_blocks, kBlockSize, num_kv_heads, head_dim, 1, c->args.block_stride,
                        hpb) ||

@@ -973,13 +973,8 @@ cudaError_t launch_balanced_fp8_t(const DecodeArgs& a, const CUtensorMap& tk, co
 
 }  // namespace
 
-int fp8_heads_per_box(int num_kv_heads, int num_seqs, bool fused, bool balanced) {
-  if (fused || balanced || num_kv_heads % 4 != 0) return 1;
-  using Geom = TileGeom<128, 1>;
-  const size_t smem = 2 * kFp8Stages * Geom::kStageBytes + 2 * kFp8Stages * 8;
-  const int slots = resident_warp_slots(
-      reinterpret_cast<const void*>(decode_partitions_fp8_kernel<128, false, kFp8Stages, false>), 64, smem);
-  return static_cast<int64_t>(num_kv_heads) * num_seqs > slots ? 1 : 4;
+int fp8_heads_per_box(int num_kv_heads, bool fused, bool balanced) {
+  return (!fused && !balanced && num_kv_heads % 4 == 0) ? 4 : 1;
 }
 
 cudaError_t launch_decode_balanced_fp8(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,

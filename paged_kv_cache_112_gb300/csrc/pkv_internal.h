@@ -193,12 +193,10 @@ cudaError_t launch_decode_partitions_fp8(const DecodeArgs& a, const CUtensorMap&
                                          cudaStream_t stream);
 // KV heads per TMA box of the FP8 decode kernels (DecodeArgs::heads_per_box):
 // 4, the head-group partition kernel (four heads' tiles of a block per
-// copy), for write-then-attend calls with fixed partitions, a head count
-// divisible by 4, and sequences x KV heads within one wave of the partition
-// kernel's warp slots (where that kernel would give a unit one warp); else
-// 1 (one head's tile per copy: the partition kernel, the fused step, the
-// balanced split).
-int fp8_heads_per_box(int num_kv_heads, int num_seqs, bool fused, bool balanced);
+// copy), for write-then-attend calls with fixed partitions and a head count
+// divisible by 4; else 1 (one head's tile per copy: the partition kernel,
+// used by the fused step, and the balanced split).
+int fp8_heads_per_box(int num_kv_heads, bool fused, bool balanced);
 
 // PKV_PARTITION_BALANCED over FP8 pools (head_dim 128, no fused write): one
 // CTA of balanced_fp8_warps_per_cta() warps per SM (a.balanced_ctas CTAs).

@@ -43,17 +43,19 @@ NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0}
 # Workload recipes.  Lengths are the post-append context length L_s.
 # partition_size is the split-K partition the step runs with: config 4's
 # definition fixes 512; for the others it is the best of a sweep on the
-# bench's step (256 to 2048 tokens).
+# bench's step (256 to 2048 tokens).  partition_size_fp8, where given, is the
+# same choice for FP8 pools (another kernel, a sweep of its own).
 CONFIGS = {
     1: dict(name="tiny: S=4 L={1,17,33,50} 4q/2kv D=64 f16 NB=64",
             dtype="f16", num_seqs=4, num_q_heads=4, num_kv_heads=2, head_dim=64,
             lens=("fixed", [1, 17, 33, 50]), num_blocks=64, partition_size=0),
     2: dict(name="8B-class GQA decode layer: S=64 32q/8kv D=128 bf16 L~U[128,2048]",
             dtype="bf16", num_seqs=64, num_q_heads=32, num_kv_heads=8, head_dim=128,
-            lens=("uniform", 128, 2048), pool_factor=1.25, partition_size=512),
+            lens=("uniform", 128, 2048), pool_factor=1.25, partition_size=512, partition_size_fp8=384),
     3: dict(name="70B-class GQA decode layer: S=256 64q/8kv D=128 f16 L~lognormal(med 300, sigma 1, cap 4096)",
             dtype="f16", num_seqs=256, num_q_heads=64, num_kv_heads=8, head_dim=128,
-            lens=("lognormal", 300.0, 1.0, 4096), pool_factor=1.25, partition_size=768),
+            lens=("lognormal", 300.0, 1.0, 4096), pool_factor=1.25, partition_size=768,
+            partition_size_fp8=448),
     4: dict(name="long-context split-K decode: S=8 32q/8kv D=128 bf16 L~U[32768,131072] partition 512",
             dtype="bf16", num_seqs=8, num_q_heads=32, num_kv_heads=8, head_dim=128,
             lens=("uniform", 32768, 131072), pool_factor=1.25, partition_size=512),
@@ -61,6 +63,12 @@ CONFIGS = {
             dtype="f16", num_seqs=128, num_q_heads=32, num_kv_heads=4, head_dim=128,
             lens=("prefix", 2048, 0, 512), pool_factor=1.25, partition_size=768),
 }
+
+
+def fp8_partition_size(cfg: int) -> int:
+    """The split-K partition of recipe `cfg` over FP8 pools."""
+    spec = CONFIGS[cfg]
+    return int(spec.get("partition_size_fp8", spec.get("partition_size", 0)))
 
 
 def f32_to_bits(x: np.ndarray, dtype: str) -> np.ndarray:

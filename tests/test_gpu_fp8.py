@@ -2,9 +2,10 @@
 against the FP8 oracle: the write path and the copy-on-write copy bit for
 bit (codes and scales), decode attention within ATOL, at sizes the oracle
 finishes in seconds (several partitions, ragged tails, one and two warps per
-unit, both reduce kernels) and at the benchmark's full sizes on sampled
-rows.  Pools are poisoned: NaN codes in every slot no sequence owns and NaN
-scales on blocks nothing references."""
+unit, both reduce kernels, the head-group grid and the one-head-per-copy
+kernel) and at the benchmark's full sizes, every row.  Pools are poisoned:
+NaN codes in every slot no sequence owns and NaN scales on blocks nothing
+references."""
 import numpy as np
 import pytest
 import torch
@@ -51,12 +52,16 @@ SMALL = {
     "c5_prefix": dict(cfg=5, num_seqs=8, lens=("prefix", 64, 0, 40), ps=32),
     # more than 16 partitions per row: the long-row reduce kernel
     "c4_long": dict(cfg=4, num_seqs=2, lens=("uniform", 3000, 5000), ps=128),
+    # KV head counts not divisible by 4: write-then-attend runs the one-head-per-copy partition kernel
+    "hkv2": dict(cfg=2, num_seqs=12, lens=("uniform", 1, 300), ps=64, num_q_heads=8, num_kv_heads=2),
+    "hkv6_two_warps": dict(cfg=3, num_seqs=400, lens=("uniform", 1, 90), ps=32, num_q_heads=24, num_kv_heads=6),
 }
 
 
 def _small(case, dtype=None):
     c = dict(SMALL[case])
     kw = dict(num_seqs=c["num_seqs"], lens=c["lens"], partition_size=c["ps"])
+    kw.update({k: c[k] for k in ("num_q_heads", "num_kv_heads") if k in c})
     if dtype:
         kw["dtype"] = dtype
     wl = P.make_workload(c["cfg"], poison=True, **kw)
@@ -79,18 +84,30 @@ def test_fp8_step_matches_oracle(case, dtype):
     assert err <= ATOL, err
 
 
+def _fused_unit_warps(wl):
+    """Warps per unit of the fused step's partition kernel: 2 when the
+    sequences x KV heads overfill its warp slots (six 2-warp CTAs per SM)."""
+    slots = 12 * torch.cuda.get_device_properties(0).multi_processor_count
+    return 2 if wl.num_seqs * wl.num_kv_heads > slots else 1
+
+
 @pytest.mark.parametrize("case", sorted(SMALL))
 def test_fp8_fused_step_equals_write_then_attend(case):
     """The write fused into the partition kernel stores the same codes and
-    gives the same output, bit for bit, as the write kernel followed by
-    attention."""
+    gives the same output as the write kernel followed by attention: bit for
+    bit where both sum a unit's tiles in the same order (one warp per unit;
+    the head-group grid of write-then-attend keeps that order), else to
+    float32 rounding (two warps per unit merge two halves)."""
     for dtype in (["f16", "bf16"] if case == "c2_ps16" else [None]):
         wl, pools = _small(case, dtype)
         a, b = DeviceStepFp8(wl, pools), DeviceStepFp8(wl, pools)
         out_a = a.step().clone()
         out_b = b.fused_step().clone()
         assert a.status_bits() == 0 and b.status_bits() == 0
-        assert torch.equal(out_a.view(torch.int32), out_b.view(torch.int32))
+        if _fused_unit_warps(wl) == 1 or wl.num_kv_heads % 4 != 0:
+            assert torch.equal(out_a.view(torch.int32), out_b.view(torch.int32))
+        else:
+            assert float((out_a - out_b).abs().max()) <= 1e-5
         assert torch.equal(a.k8, b.k8) and torch.equal(a.v8, b.v8)
         assert torch.equal(a.k_scale.view(torch.int32), b.k_scale.view(torch.int32))
 
@@ -192,29 +209,19 @@ def test_fp8_bad_table_entry_is_flagged():
     assert float(np.max(np.abs(got - ref))) <= ATOL
 
 
-def _rows(wl, n, rng):
-    S, Hq = wl.num_seqs, wl.num_q_heads
-    picks = {(int(s), int(h)) for s, h in zip(rng.integers(0, S, n), rng.integers(0, Hq, n))}
-    for s in (int(np.argmin(wl.context_lens)), int(np.argmax(wl.context_lens))):
-        picks.update({(s, 0), (s, Hq - 1), (s, Hq // 2)})
-    return sorted(picks)
-
-
 @pytest.mark.parametrize("cfg", [2, 3, 4, 5])
 def test_fp8_full_size_step(cfg):
-    """The benchmark's workloads (recipe partition sizes, fp32 output)."""
+    """The benchmark's workloads at the partition sizes the FP8 bench runs
+    (fp32 output), every row against the oracle."""
     wl = P.make_workload(cfg, poison=True)
     pools = P.make_fp8_pools(wl)
-    ds = DeviceStepFp8(wl, pools)
+    ds = DeviceStepFp8(wl, pools, partition_size=P.fp8_partition_size(cfg))
     out = ds.step().cpu().numpy()
     assert ds.status_bits() == 0
     ref_pools = _ref_pools(wl, pools)
     _check_pools(ds, ref_pools)
     k8, v8, ks, vs = ref_pools
-    rows = _rows(wl, 48, np.random.default_rng(cfg))
-    ref = oracle.decode_attention_fp8(wl.q, k8, v8, ks, vs, wl.block_tables, wl.context_lens, wl.scale, wl.dtype,
-                                      rows=rows)
-    got = np.stack([out[s, h] for s, h in rows])
-    err = float(np.max(np.abs(got.astype(np.float64) - ref)))
+    ref = oracle.decode_attention_fp8(wl.q, k8, v8, ks, vs, wl.block_tables, wl.context_lens, wl.scale, wl.dtype)
+    err = float(np.max(np.abs(out.astype(np.float64) - ref)))
     assert err <= ATOL, err
     assert np.all(np.isfinite(out))
