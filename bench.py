@@ -565,7 +565,13 @@ def measure_workload(args, cfg, ctx, want_cpu_baseline):
         kernel_name = ("decode_balanced_fp8_kernel" if ps == pkv.PARTITION_BALANCED else
                        "decode_partitions_fp8_hg_kernel" if hg else "decode_partitions_fp8_kernel")
     else:
-        kernel_name = "decode_balanced_kernel" if ps == pkv.PARTITION_BALANCED else "decode_partitions_kernel"
+        # the library's rule: blocks of >= 16 tokens, an even H_kv and sequences x KV heads within one wave of the
+        # partition kernel's warp slots (6 two-warp CTAs per SM) run the head-pair kernel
+        slots = 12 * torch.cuda.get_device_properties(dev).multi_processor_count
+        hp = (args.block_size >= 16 and ps != pkv.PARTITION_BALANCED and wl.num_kv_heads % 2 == 0
+              and wl.num_kv_heads * wl.num_seqs <= slots)
+        kernel_name = ("decode_balanced_kernel" if ps == pkv.PARTITION_BALANCED else
+                       "decode_partitions_hg_kernel" if hp else "decode_partitions_kernel")
     traffic = _recorded_traffic(cfg, kernel_name)
     achieved = nb["attention"] / (kern_avg_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 2), "peak": peak,
@@ -1068,6 +1074,7 @@ def _recorded_traffic(cfg, kernel):
     summary, if it was taken on the current kernel sources; else None."""
 
     sources = {"decode_partitions_kernel": ("decode_partitions", "pkv_decode.cu"),
+               "decode_partitions_hg_kernel": ("decode_partitions_hg", "pkv_decode_hg.cu"),
                "decode_partitions_fp8_kernel": ("decode_partitions_fp8", "pkv_decode_fp8.cu"),
                "decode_partitions_fp8_hg_kernel": ("decode_partitions_fp8", "pkv_decode_fp8.cu")}
     if kernel not in sources:

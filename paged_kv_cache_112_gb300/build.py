@@ -16,7 +16,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libpkv.so")
-SOURCES = ["pkv_api.cu", "pkv_cache_ops.cu", "pkv_decode.cu", "pkv_decode_balanced.cu", "pkv_decode_fp8.cu",
+SOURCES = ["pkv_api.cu", "pkv_cache_ops.cu", "pkv_decode.cu", "pkv_decode_hg.cu", "pkv_decode_balanced.cu",
+           "pkv_decode_fp8.cu",
            "pkv_static_ws.cu", "pkv_checks.cu", "pkv_block_manager.cpp"]
 HEADERS = ["pkv_internal.h", "pkv_device.cuh", "pkv_balanced.cuh", "pkv_fp8.cuh", os.path.join("..", "..", "include", "pkv.h")]
 

@@ -369,9 +369,14 @@ pkv_status prepare_decode(DecodeCall* c, void* out, const void* q, const void* k
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out_dtype = static_cast<int>(out_dtype);
   a.timeout_ns = kWaitTimeoutNs;
+  a.heads_per_box = 1;
   if (need_maps && num_seqs > 0) {
-    if (!encode_pool_map(&c->tmap_k, k_pool, num_blocks, block_size, num_kv_heads, head_dim, 2, bstride) ||
-        !encode_pool_map(&c->tmap_v, v_pool, num_blocks, block_size, num_kv_heads, head_dim, 2, bstride))
+    // The launch picks its kernel by a.heads_per_box, so the boxes match it.
+    if (!balanced) a.heads_per_box = partitions_heads_per_box(a, head_dim, kv_dtype == PKV_BF16);
+    if (!encode_pool_map(&c->tmap_k, k_pool, num_blocks, block_size, num_kv_heads, head_dim, 2, bstride,
+                         a.heads_per_box) ||
+        !encode_pool_map(&c->tmap_v, v_pool, num_blocks, block_size, num_kv_heads, head_dim, 2, bstride,
+                         a.heads_per_box))
       return PKV_ERR_CUDA;
   }
   return PKV_OK;

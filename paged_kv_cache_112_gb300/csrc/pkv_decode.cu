@@ -333,10 +333,27 @@ cudaError_t launch_partitions_f(const DecodeArgs& a, const CUtensorMap& tk, cons
                  : launch_partitions_t<D, BF16, false, false>(a, tk, tv, stream);
 }
 
+// Warp slots of the partition kernel (the one-warp-per-unit rule's wave).
+template <int D, bool BF16>
+int partition_slots() {
+  using Geom = TileGeom<D>;
+  const size_t smem = 2 * kStages * Geom::kStageBytes + 2 * kStages * 8;
+  return resident_warp_slots(reinterpret_cast<const void*>(decode_partitions_kernel<D, BF16, kStages, false, false>),
+                             64, smem);
+}
+
 }  // namespace
+
+int partitions_heads_per_box(const DecodeArgs& a, int head_dim, int kv_bf16) {
+  if (a.block_shift < 4 || a.num_kv_heads % 2 != 0 || (head_dim != 128 && head_dim != 64)) return 1;
+  const int slots = head_dim == 128 ? (kv_bf16 ? partition_slots<128, true>() : partition_slots<128, false>())
+                                    : (kv_bf16 ? partition_slots<64, true>() : partition_slots<64, false>());
+  return static_cast<int64_t>(a.num_kv_heads) * a.num_seqs > slots ? 1 : 2;
+}
 
 cudaError_t launch_decode_partitions(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                      int head_dim, int kv_bf16, cudaStream_t stream) {
+  if (a.heads_per_box == 2) return launch_decode_partitions_hg(a, tmap_k, tmap_v, head_dim, kv_bf16, stream);
   if (head_dim == 128)
     return kv_bf16 ? launch_partitions_f<128, true>(a, tmap_k, tmap_v, stream)
                    : launch_partitions_f<128, false>(a, tmap_k, tmap_v, stream);

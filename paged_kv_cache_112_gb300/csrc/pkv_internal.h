@@ -109,7 +109,7 @@ struct DecodeArgs {
   int out_dtype;       // pkv_dtype
   int balanced_ctas;   // balanced split: persistent CTAs (one per SM); 0 otherwise
   int unit_warps;      // fixed partitions: warps per unit (1 or 2)
-  int heads_per_box;   // FP8 pools: KV heads per TMA box, 4 for the head-group kernel, else 1
+  int heads_per_box;   // KV heads per TMA box: 2 (16-bit head-pair kernel), 4 (FP8 head-group kernel) or 1
   long long timeout_ns;
   // Fused decode step only: the token generated this step, written to the
   // pools by the attention kernel itself (null when not fusing).
@@ -177,6 +177,14 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 cudaError_t launch_write_cache(const WriteCacheArgs& a, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream);
 // kv_bf16: 0 = f16, 1 = bf16.  Tensor maps describe the K and V pools.
+// KV heads per TMA box of the 16-bit fixed-partition path (DecodeArgs::
+// heads_per_box): 2, the head-pair kernel (pkv_decode_hg.cu), for blocks of
+// >= 16 tokens, an even KV head count and a batch whose sequences x KV heads
+// fit one wave of the partition kernel's warp slots (where it gives every
+// unit one warp); else 1, the partition kernel.
+int partitions_heads_per_box(const DecodeArgs& a, int head_dim, int kv_bf16);
+cudaError_t launch_decode_partitions_hg(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                        int head_dim, int kv_bf16, cudaStream_t stream);
 cudaError_t launch_decode_partitions(const DecodeArgs& a, const CUtensorMap& tmap_k,
                                      const CUtensorMap& tmap_v, int head_dim, int kv_bf16,
                                      cudaStream_t stream);  // fuses the write when a.k_new is set
