@@ -566,7 +566,7 @@ def measure_workload(args, cfg, ctx, want_cpu_baseline):
                        "decode_partitions_fp8_hg_kernel" if hg else "decode_partitions_fp8_kernel")
     else:
         # the library's rule: blocks of >= 16 tokens, an even H_kv and sequences x KV heads within one wave of the
-        # partition kernel's warp slots (6 two-warp CTAs per SM) run the head-pair kernel
+        # partition kernel's warp slots (6 two-warp CTAs per SM) run the head-group kernel (2 or 4 heads a CTA)
         slots = 12 * torch.cuda.get_device_properties(dev).multi_processor_count
         hp = (args.block_size >= 16 and ps != pkv.PARTITION_BALANCED and wl.num_kv_heads % 2 == 0
               and wl.num_kv_heads * wl.num_seqs <= slots)

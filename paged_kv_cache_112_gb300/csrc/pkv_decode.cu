@@ -348,12 +348,18 @@ int partitions_heads_per_box(const DecodeArgs& a, int head_dim, int kv_bf16) {
   if (a.block_shift < 4 || a.num_kv_heads % 2 != 0 || (head_dim != 128 && head_dim != 64)) return 1;
   const int slots = head_dim == 128 ? (kv_bf16 ? partition_slots<128, true>() : partition_slots<128, false>())
                                     : (kv_bf16 ? partition_slots<64, true>() : partition_slots<64, false>());
-  return static_cast<int64_t>(a.num_kv_heads) * a.num_seqs > slots ? 1 : 2;
+  const int64_t seq_heads = static_cast<int64_t>(a.num_kv_heads) * a.num_seqs;
+  if (seq_heads > slots) return 1;
+  // Four heads per copy (1 KB of each block row instead of 512 B) pay on
+  // grids of many waves, whose warps stream long runs of tiles from HBM;
+  // on a grid of about one wave the CTA-wide lockstep of four warps costs
+  // more than the copies it saves.
+  return (a.num_kv_heads % 4 == 0 && seq_heads * a.max_parts > 4LL * slots) ? 4 : 2;
 }
 
 cudaError_t launch_decode_partitions(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                      int head_dim, int kv_bf16, cudaStream_t stream) {
-  if (a.heads_per_box == 2) return launch_decode_partitions_hg(a, tmap_k, tmap_v, head_dim, kv_bf16, stream);
+  if (a.heads_per_box > 1) return launch_decode_partitions_hg(a, tmap_k, tmap_v, head_dim, kv_bf16, stream);
   if (head_dim == 128)
     return kv_bf16 ? launch_partitions_f<128, true>(a, tmap_k, tmap_v, stream)
                    : launch_partitions_f<128, false>(a, tmap_k, tmap_v, stream);

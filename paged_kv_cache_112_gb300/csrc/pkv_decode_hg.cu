@@ -1,4 +1,4 @@
-// Paged decode attention over 16-bit pools for sm_103a: the head-pair
+// Paged decode attention over 16-bit pools for sm_103a: the head-group
 // partition kernel.
 //
 // What is computed: pkv_decode_partitions (and the fused decode step) over
@@ -6,26 +6,28 @@
 // warp per unit ("gpu_paged_kv_cache", "Inside the paged attention kernel";
 // "PagedAttention internals", section 02 "Block tables").
 //
-// Mapping onto GB300: a CTA serves one (sequence s, partition p) for two
-// adjacent KV heads, one warp per head.  A block's rows hold the heads' K
-// (and V) rows side by side, so one TMA box of (128 bytes, 16 rows, 2 heads'
-// lines, 1 block) brings both heads' K tiles of a block, and another box
-// their V tiles: 8 KB per copy at head_dim 128 instead of 4 KB.  Where tiles
-// come from L2 (a prefix many sequences share) an SM's copy issue rate, not
-// HBM, paces the per-head kernel; here it issues half as many copies.
-//  * The two warps share one ring of two stages ([K: head 0, head 1][V: head
-//    0, head 1]), filled by lane 0 of warp 0.  Each warp waits on a stage's
+// Mapping onto GB300: a CTA serves one (sequence s, partition p) for HP (2 or
+// 4) adjacent KV heads, one warp per head.  A block's rows hold the heads' K
+// (and V) rows side by side, so one TMA box of (128 bytes, 16 rows, HP
+// heads' lines, 1 block) brings all HP heads' K tiles of a block, and another
+// box their V tiles: HP x 4 KB per copy at head_dim 128 instead of 4 KB.
+// Where tiles come from L2 (a prefix many sequences share) an SM's copy issue
+// rate, not HBM, paces the per-head kernel; here it issues 1/HP as many.
+//  * The HP warps share one ring of two stages ([K: heads 0..HP-1][V: heads
+//    0..HP-1]), filled by lane 0 of warp 0; shared memory per warp, and so
+//    warps per SM, stay the per-head kernel's.  Each warp waits on a stage's
 //    barrier, reads its own head's tiles and keeps its own softmax state;
 //    after each tile __syncthreads_or() both frees the stage for the next
 //    copy and makes a timed-out wait the whole CTA's decision.
 //  * Fused step: the warp whose head's tile holds position L-1 writes the new
-//    rows to the pool and patches them into its own half of the stage, then
+//    rows to the pool and patches them into its own part of the stage, then
 //    fences them against the next copy before the CTA barrier.
 //  * Tile order, tile math and outputs are the one-warp-per-unit partition
 //    kernel's, so results are bit-identical to it.
-// Used for blocks of 16 tokens or more, an even KV head count, and a batch
-// whose sequences x KV heads fit one wave of the partition kernel's warp
-// slots (where that kernel gives every unit one warp).
+// Used for blocks of 16 tokens or more, a KV head count divisible by HP (4
+// where it divides, else 2), and a batch whose sequences x KV heads fit one
+// wave of the partition kernel's warp slots (where that kernel gives every
+// unit one warp).
 #include "pkv_device.cuh"
 
 namespace pkv {
@@ -35,24 +37,24 @@ using namespace dev;
 
 constexpr int kPairStages = 2;
 
-template <int D, bool BF16, bool FUSED>
-__global__ void __launch_bounds__(64, 6) decode_partitions_hg_kernel(
+template <int D, bool BF16, bool FUSED, int HP>
+__global__ void __launch_bounds__(HP * 32, 12 / HP) decode_partitions_hg_kernel(
     const DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v) {
   using Geom = TileGeom<D>;
   using Att = WarpAttention<D, BF16>;
-  constexpr int HP = 2, NST = kPairStages;
+  constexpr int NST = kPairStages;
   constexpr uint32_t kHeadTile = Geom::kTileBytes;  // one head's 16 rows
-  constexpr uint32_t kKBytes = HP * kHeadTile;       // the pair's K tiles of one block
+  constexpr uint32_t kKBytes = HP * kHeadTile;       // the group's K tiles of one block
   constexpr uint32_t kStage = 2 * kKBytes;           // then its V tiles
   extern __shared__ __align__(1024) uint8_t smem[];
   griddep_wait();  // every input may come from the previous kernel on the stream
   griddep_launch_dependents();
   if (smem_misaligned(smem, a.dev_status)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pairs = a.num_kv_heads / HP;
-  const int64_t unit = blockIdx.x;  // partition-major: ((p * S) + s) * pairs + gi
-  const int gi = static_cast<int>(unit % pairs);
-  const int64_t rest = unit / pairs;
+  const int groups = a.num_kv_heads / HP;
+  const int64_t unit = blockIdx.x;  // partition-major: ((p * S) + s) * groups + gi
+  const int gi = static_cast<int>(unit % groups);
+  const int64_t rest = unit / groups;
   const int s = static_cast<int>(rest % a.num_seqs);
   const int part = static_cast<int>(rest / a.num_seqs);
   const int g = gi * HP + warp;
@@ -61,7 +63,7 @@ __global__ void __launch_bounds__(64, 6) decode_partitions_hg_kernel(
   const int first = lane < tiles_per_part ? tile_entry(a, s, part * tiles_per_part + lane, 0) : 0;
   const int L = clamp_len(a, a.context_lens[s], part == 0 && gi == 0 && warp == 0 && lane == 0);
   const int nparts = L > 0 ? (L + PS - 1) / PS : 1;
-  if (part >= nparts) return;  // the same for both warps
+  if (part >= nparts) return;  // the same for every warp of the CTA
   const int tok0 = part * PS;
   const int ntok = max(0, min(L - tok0, PS));
   const int cnt = (ntok + kTile - 1) / kTile;
@@ -80,7 +82,7 @@ __global__ void __launch_bounds__(64, 6) decode_partitions_hg_kernel(
   int phys_cur = first;
   int phys_next = entry(32 + lane);
   uint32_t bad_stage = 0;
-  auto issue = [&](int j) {  // both warps call (entry bookkeeping); lane 0 of warp 0 copies
+  auto issue = [&](int j) {  // every warp calls (entry bookkeeping); lane 0 of warp 0 copies
     if ((j & 31) == 0 && j > 0) {
       phys_cur = phys_next;
       phys_next = entry(j + 32 + lane);
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(64, 6) decode_partitions_hg_kernel(
     // Only the patched new token is a generic-proxy write to a stage; it is
     // ordered before the next copy into the stage by this fence and the barrier.
     if (patched) fence_proxy_async_smem();
-    // Both warps are done with this tile's stage; a timed-out wait in either ends the CTA.
+    // Every warp is done with this tile's stage; a timed-out wait in any ends the CTA.
     if (__syncthreads_or(!ok)) {
       if (warp == 0)
         for (int j = i; j < min(cnt, i + NST); ++j) wait(j);  // copies in flight land before the CTA exits
@@ -151,35 +153,44 @@ __global__ void __launch_bounds__(64, 6) decode_partitions_hg_kernel(
     at.store_partial(a.ws_acc, a.ws_ml, head0 * a.max_parts + part, a.max_parts, G, lane);
 }
 
-template <int D, bool BF16, bool FUSED>
+template <int D, bool BF16, bool FUSED, int HP>
 cudaError_t launch_hg_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
   using Geom = TileGeom<D>;
-  const size_t smem = static_cast<size_t>(kPairStages) * (4 * Geom::kTileBytes + 8);
-  auto kern = decode_partitions_hg_kernel<D, BF16, FUSED>;
+  const size_t smem = static_cast<size_t>(kPairStages) * (2 * HP * Geom::kTileBytes + 8);
+  auto kern = decode_partitions_hg_kernel<D, BF16, FUSED, HP>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  const int64_t ctas = static_cast<int64_t>(a.num_kv_heads / 2) * a.num_seqs * a.max_parts;
+  const int64_t ctas = static_cast<int64_t>(a.num_kv_heads / HP) * a.num_seqs * a.max_parts;
   if (ctas == 0) return cudaSuccess;
-  return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(64), smem, stream, a, tk, tv);
+  return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(HP * 32), smem, stream, a, tk, tv);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, int HP>
 cudaError_t launch_hg_fused(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-  return a.k_new ? launch_hg_t<D, BF16, true>(a, tk, tv, stream) : launch_hg_t<D, BF16, false>(a, tk, tv, stream);
+  return a.k_new ? launch_hg_t<D, BF16, true, HP>(a, tk, tv, stream)
+                 : launch_hg_t<D, BF16, false, HP>(a, tk, tv, stream);
+}
+
+template <int HP>
+cudaError_t launch_hg_hp(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int head_dim,
+                         int kv_bf16, cudaStream_t stream) {
+  if (head_dim == 128)
+    return kv_bf16 ? launch_hg_fused<128, true, HP>(a, tk, tv, stream)
+                   : launch_hg_fused<128, false, HP>(a, tk, tv, stream);
+  if (head_dim == 64)
+    return kv_bf16 ? launch_hg_fused<64, true, HP>(a, tk, tv, stream)
+                   : launch_hg_fused<64, false, HP>(a, tk, tv, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_decode_partitions_hg(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                         int head_dim, int kv_bf16, cudaStream_t stream) {
-  if (a.num_kv_heads % 2 != 0 || a.block_shift < 4) return cudaErrorInvalidValue;
-  if (head_dim == 128)
-    return kv_bf16 ? launch_hg_fused<128, true>(a, tmap_k, tmap_v, stream)
-                   : launch_hg_fused<128, false>(a, tmap_k, tmap_v, stream);
-  if (head_dim == 64)
-    return kv_bf16 ? launch_hg_fused<64, true>(a, tmap_k, tmap_v, stream)
-                   : launch_hg_fused<64, false>(a, tmap_k, tmap_v, stream);
-  return cudaErrorInvalidValue;
+  const int hp = a.heads_per_box;
+  if ((hp != 2 && hp != 4) || a.num_kv_heads % hp != 0 || a.block_shift < 4) return cudaErrorInvalidValue;
+  return hp == 4 ? launch_hg_hp<4>(a, tmap_k, tmap_v, head_dim, kv_bf16, stream)
+                 : launch_hg_hp<2>(a, tmap_k, tmap_v, head_dim, kv_bf16, stream);
 }
 
 }  // namespace pkv

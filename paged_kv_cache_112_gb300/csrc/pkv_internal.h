@@ -109,7 +109,7 @@ struct DecodeArgs {
   int out_dtype;       // pkv_dtype
   int balanced_ctas;   // balanced split: persistent CTAs (one per SM); 0 otherwise
   int unit_warps;      // fixed partitions: warps per unit (1 or 2)
-  int heads_per_box;   // KV heads per TMA box: 2 (16-bit head-pair kernel), 4 (FP8 head-group kernel) or 1
+  int heads_per_box;   // KV heads per TMA box: 2 or 4 (head-group kernels), or 1
   long long timeout_ns;
   // Fused decode step only: the token generated this step, written to the
   // pools by the attention kernel itself (null when not fusing).
@@ -178,10 +178,12 @@ cudaError_t launch_write_cache(const WriteCacheArgs& a, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream);
 // kv_bf16: 0 = f16, 1 = bf16.  Tensor maps describe the K and V pools.
 // KV heads per TMA box of the 16-bit fixed-partition path (DecodeArgs::
-// heads_per_box): 2, the head-pair kernel (pkv_decode_hg.cu), for blocks of
-// >= 16 tokens, an even KV head count and a batch whose sequences x KV heads
-// fit one wave of the partition kernel's warp slots (where it gives every
-// unit one warp); else 1, the partition kernel.
+// heads_per_box): 2 or 4, the head-group kernel (pkv_decode_hg.cu), for
+// blocks of >= 16 tokens, an even KV head count and a batch whose sequences x
+// KV heads fit one wave of the partition kernel's warp slots (where it gives
+// every unit one warp); 4 when it divides the KV head count and the grid
+// (sequences x KV heads x partitions) spans more than four waves; else 1, the
+// partition kernel.
 int partitions_heads_per_box(const DecodeArgs& a, int head_dim, int kv_bf16);
 cudaError_t launch_decode_partitions_hg(const DecodeArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                         int head_dim, int kv_bf16, cudaStream_t stream);
