@@ -30,6 +30,10 @@ CASES = [  # (recipe, overrides, partition size)
     (2, dict(num_seqs=3, lens=("fixed", [1, 16, 17])), pkv.PARTITION_BALANCED),
     (5, dict(num_seqs=16, lens=("prefix", 64, 0, 70)), 32),
     (5, dict(num_seqs=16, lens=("prefix", 64, 0, 70)), pkv.PARTITION_BALANCED),
+    # a grid of many waves (64 x 4 sequence-heads x 38 partitions): the head-group kernel with four
+    # heads a CTA on a GB300; then the same with 32-token blocks (two tiles per block)
+    (2, dict(num_seqs=64, num_q_heads=16, num_kv_heads=4, lens=("uniform", 300, 600)), 16),
+    (2, dict(num_seqs=64, num_q_heads=16, num_kv_heads=4, lens=("uniform", 300, 600), block_size=32), 16),
 ]
 
 
