@@ -559,19 +559,8 @@ def measure_workload(args, cfg, ctx, want_cpu_baseline):
     ms = elapsed_ms / K
     value = job_gbs(nb["step"], world, K, elapsed_ms)
     kern_avg_ms = statistics.mean(kern_ms)
-    if fp8:
-        # the library's rule: write-then-attend over fixed partitions with H_kv % 4 == 0 runs the head-group grid
-        hg = not args.fused and ps != pkv.PARTITION_BALANCED and wl.num_kv_heads % 4 == 0
-        kernel_name = ("decode_balanced_fp8_kernel" if ps == pkv.PARTITION_BALANCED else
-                       "decode_partitions_fp8_hg_kernel" if hg else "decode_partitions_fp8_kernel")
-    else:
-        # the library's rule: blocks of >= 16 tokens, an even H_kv and sequences x KV heads within one wave of the
-        # partition kernel's warp slots (6 two-warp CTAs per SM) run the head-group kernel (2 or 4 heads a CTA)
-        slots = 12 * torch.cuda.get_device_properties(dev).multi_processor_count
-        hp = (args.block_size >= 16 and ps != pkv.PARTITION_BALANCED and wl.num_kv_heads % 2 == 0
-              and wl.num_kv_heads * wl.num_seqs <= slots)
-        kernel_name = ("decode_balanced_kernel" if ps == pkv.PARTITION_BALANCED else
-                       "decode_partitions_hg_kernel" if hp else "decode_partitions_kernel")
+    kernel_name = partition_kernel_name(wl.num_seqs, wl.num_kv_heads, ps, args.block_size, fp8, bool(args.fused),
+                                        torch.cuda.get_device_properties(dev).multi_processor_count)
     traffic = _recorded_traffic(cfg, kernel_name)
     achieved = nb["attention"] / (kern_avg_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 2), "peak": peak,
@@ -813,7 +802,10 @@ def run_layers(args):
         "seq_layers_per_s": round(world * S * n_layers / (graph_ms / K * 1e-3), 1),
         "eager_ms_per_step": round(eager_ms / K, 5), "graph_ms_per_step": round(graph_ms / K, 5),
         "step_bytes": per_step,
-        "roofline": {"bound": "hbm", "kernel": "decode_partitions_kernel", "achieved": round(achieved, 2),
+        "roofline": {"bound": "hbm",
+                     "kernel": partition_kernel_name(S, Hkv, ps, 16, False, True,
+                                                     torch.cuda.get_device_properties(dev).multi_processor_count),
+                     "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": None, "bytes_per_launch": nb["attention"], "avg_launch_ms": round(kern_avg_ms, 5)},
         "gpu_launches": ((1 if pairs.shape[0] else 0) + n_layers * (1 + (1 if ws_bytes else 0))) * K,
@@ -1063,6 +1055,24 @@ def kernel_source_hash(paths) -> str:
         text = re.sub(r"//[^\n]*", "", text)
         h.update(re.sub(r"\s+", "", text).encode())
     return h.hexdigest()[:16]
+
+
+def partition_kernel_name(num_seqs, num_kv_heads, partition_size, block_size, fp8, fused, sm_count):
+    """The first kernel of a decode call, by the library's rule.  FP8 pools:
+    write-then-attend over fixed partitions with H_kv % 4 == 0 runs the
+    head-group grid.  16-bit pools: blocks of >= 16 tokens, an even H_kv and
+    sequences x KV heads within one wave of the partition kernel's warp slots
+    (six two-warp CTAs per SM) run the head-group kernel (2 or 4 heads a CTA)."""
+    balanced = partition_size == -1
+    if fp8:
+        if balanced:
+            return "decode_balanced_fp8_kernel"
+        return "decode_partitions_fp8_hg_kernel" if not fused and num_kv_heads % 4 == 0 else \
+            "decode_partitions_fp8_kernel"
+    if balanced:
+        return "decode_balanced_kernel"
+    hg = block_size >= 16 and num_kv_heads % 2 == 0 and num_kv_heads * num_seqs <= 12 * sm_count
+    return "decode_partitions_hg_kernel" if hg else "decode_partitions_kernel"
 
 
 # short names of the workload recipes, as the profile summaries are named

@@ -109,3 +109,23 @@ def test_graph_blocks_time_exactly_k_steps():
             b, full, rem = bench.graph_blocks(K, R)
             assert b * full + rem == K and b % R == 0 and b >= 1
             assert rem < b
+
+
+def test_partition_kernel_names_follow_the_library_rule():
+    """The bench names the kernel a recipe runs (its roofline and traffic
+    record are that kernel's): on 152 SMs the 70B-class layer overfills one
+    wave of warp slots and keeps the per-head kernel, the others run the
+    head-group kernel; FP8 write-then-attend runs the FP8 head-group grid."""
+    name = bench.partition_kernel_name
+    for cfg, expect in ((2, "decode_partitions_hg_kernel"), (3, "decode_partitions_kernel"),
+                        (4, "decode_partitions_hg_kernel"), (5, "decode_partitions_hg_kernel")):
+        spec = P.CONFIGS[cfg]
+        assert name(spec["num_seqs"], spec["num_kv_heads"], spec["partition_size"], 16, False, True, 152) == expect
+        assert name(spec["num_seqs"], spec["num_kv_heads"], P.fp8_partition_size(cfg), 16, True, False, 152) == \
+            "decode_partitions_fp8_hg_kernel"
+        assert name(spec["num_seqs"], spec["num_kv_heads"], P.fp8_partition_size(cfg), 16, True, True, 152) == \
+            "decode_partitions_fp8_kernel"
+    assert name(64, 8, -1, 16, False, True, 152) == "decode_balanced_kernel"
+    assert name(64, 8, -1, 16, True, False, 152) == "decode_balanced_fp8_kernel"
+    assert name(64, 8, 512, 8, False, True, 152) == "decode_partitions_kernel"  # 8-token blocks
+    assert name(64, 3, 512, 16, False, True, 152) == "decode_partitions_kernel"  # odd H_kv
